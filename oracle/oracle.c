@@ -1,0 +1,426 @@
+/*
+ * CPU oracle for one paged-attention step. TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
+ * this code. The CUDA library neither links nor calls it, and it shares no
+ * source with the library.
+ *
+ * Everything here is plain and slow on purpose: fp64 arithmetic, an explicit
+ * gather through the block table, and a two-pass softmax (maximum, then
+ * normalised weights, then the weighted sum of V). No tiling, no online
+ * softmax, no reordering.
+ *
+ * Sources (vLLM inference notes, "AI Infra入门干货总结：大模型是如何高效推理的"):
+ *   - §Paged Attention, KV cache layout: per layer and per K/V, the cache is
+ *     [num_blocks, block_size, num_kv_heads, head_dim].
+ *   - §Paged Attention, block_table: [max_num_reqs, max_num_blocks_per_req],
+ *     the physical block of each logical block of a request.
+ *   - §Paged Attention, slot_mapping and address computation:
+ *     slot = block * block_size + offset; block = slot / block_size;
+ *     offset = slot % block_size.
+ *   - §LLM 推理全流程 3, Attention: K/V are [seq_lens, num_kv_heads, head_dim]
+ *     read discretely from the paged cache; Q is [query_lens, num_heads,
+ *     head_dim]; GQA maps one KV head to a group of query heads by index.
+ *   - §Continuous Batching: a request schedules num_tokens - num_computed_tokens
+ *     query tokens, so query i of a chunk sits at absolute position
+ *     (seq_len - query_len) + i and sees keys 0 .. that position (causal).
+ * The plain attention definition softmax(q k^T / sqrt(d)) v is the one the
+ * operators article ("lpnh.cn/news/2669538", §2.1) prints as its naive
+ * reference; here the scale is an argument.
+ *
+ * Readings where the pages are silent (each one is listed with its reason in
+ * the design notes):
+ *   - seq_lens counts every KV token, including this step's new ones.
+ *   - GQA groups are contiguous: kv_head = head / (num_heads / num_kv_heads).
+ *   - slot_mapping is int64; a negative entry means "skip this token".
+ *   - two tokens of one call may not name the same slot.
+ *   - block_table entries past ceil(seq_len / block_size) are never read.
+ *   - the scale is used as the exact double value of the float argument.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_SLOT_RANGE (-2)
+#define ORACLE_ERR_SLOT_DUPLICATE (-3)
+#define ORACLE_ERR_BLOCK_RANGE (-4)
+#define ORACLE_ERR_LENGTHS (-5)
+#define ORACLE_ERR_NOMEM (-6)
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: reshape_and_cache                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For every token t whose slot s = slot_mapping[t] is not negative, copy the
+ * raw bits of key[t, :, :] to key_cache[s / block_size, s % block_size, :, :]
+ * and likewise for value (§Paged Attention: slot_mapping tells the kernel
+ * where to write new KV; address computation).
+ */
+int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
+                             uint16_t *key_cache, uint16_t *value_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int64_t num_blocks)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    if (num_tokens == 0)
+        return ORACLE_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return ORACLE_ERR_ARG;
+
+    const int64_t row = (int64_t)num_kv_heads * head_dim; /* elements per token row */
+    const int64_t num_slots = num_blocks * block_size;
+
+    /* Reject out-of-range or repeated slots before writing anything. */
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s >= num_slots)
+            return ORACLE_ERR_SLOT_RANGE;
+        if (s < 0)
+            continue;
+        for (int64_t u = 0; u < t; ++u)
+            if (slot_mapping[u] == s)
+                return ORACLE_ERR_SLOT_DUPLICATE;
+    }
+
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        int64_t block = s / block_size;
+        int64_t offset = s % block_size;
+        int64_t dst = (block * block_size + offset) * row;
+        for (int64_t e = 0; e < row; ++e) {
+            key_cache[dst + e] = key[t * row + e];
+            value_cache[dst + e] = value[t * row + e];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: attention over the paged cache                                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *q;
+    const uint16_t *key_cache;
+    const uint16_t *value_cache;
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    const int32_t *query_start_loc;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int64_t num_blocks;
+    double scale;
+} problem_t;
+
+static int check_problem(const problem_t *p)
+{
+    if (p->num_seqs < 0 || p->num_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
+        p->block_size <= 0 || p->max_blocks_per_seq < 0 || p->num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    if (p->num_heads % p->num_kv_heads != 0)
+        return ORACLE_ERR_ARG;
+    if (p->query_start_loc[0] != 0)
+        return ORACLE_ERR_LENGTHS;
+    for (int32_t b = 0; b < p->num_seqs; ++b) {
+        int32_t ql = p->query_start_loc[b + 1] - p->query_start_loc[b];
+        int32_t L = p->seq_lens[b];
+        if (ql < 0 || L < ql)
+            return ORACLE_ERR_LENGTHS;
+        if ((int64_t)L > (int64_t)p->max_blocks_per_seq * p->block_size)
+            return ORACLE_ERR_LENGTHS;
+        int32_t nblk = (L + p->block_size - 1) / p->block_size;
+        for (int32_t i = 0; i < nblk; ++i) {
+            int32_t blk = p->block_tables[(int64_t)b * p->max_blocks_per_seq + i];
+            if (blk < 0 || (int64_t)blk >= p->num_blocks)
+                return ORACLE_ERR_BLOCK_RANGE;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Gather the logical K and V rows 0..L-1 of request b, KV head kvh, into
+ * contiguous [L, head_dim] arrays of doubles. Logical token j lives in
+ * physical block block_tables[b][j / block_size] at offset j % block_size.
+ */
+static void gather_request(const problem_t *p, int32_t b, int32_t kvh, double *K, double *V)
+{
+    const int32_t L = p->seq_lens[b];
+    const int32_t D = p->head_dim;
+    for (int32_t j = 0; j < L; ++j) {
+        int32_t logical_block = j / p->block_size;
+        int32_t offset = j % p->block_size;
+        int64_t phys = p->block_tables[(int64_t)b * p->max_blocks_per_seq + logical_block];
+        int64_t slot = phys * p->block_size + offset;
+        int64_t base = (slot * p->num_kv_heads + kvh) * D;
+        for (int32_t d = 0; d < D; ++d) {
+            K[(int64_t)j * D + d] = bf16_to_double(p->key_cache[base + d]);
+            V[(int64_t)j * D + d] = bf16_to_double(p->value_cache[base + d]);
+        }
+    }
+}
+
+/*
+ * Softmax weights of query token (q0 + i), head h, over its visible keys.
+ * Returns the number of visible keys n; w[0..n-1] receives the weights.
+ * Two passes: the maximum score first, then exp(s - max) / sum.
+ */
+static int32_t weights_for_query(const problem_t *p, int32_t b, int32_t i, int32_t h,
+                                 const double *K, double *w)
+{
+    const int32_t D = p->head_dim;
+    const int32_t q0 = p->query_start_loc[b];
+    const int32_t ql = p->query_start_loc[b + 1] - q0;
+    const int32_t L = p->seq_lens[b];
+    const int32_t ctx = L - ql;
+    const int32_t n = ctx + i + 1; /* keys 0 .. ctx + i */
+    const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;
+
+    double qd[1024];
+    double *qv = qd;
+    double *heap = NULL;
+    if (D > 1024) {
+        heap = (double *)malloc(sizeof(double) * D);
+        qv = heap;
+    }
+    for (int32_t d = 0; d < D; ++d)
+        qv[d] = bf16_to_double(qrow[d]);
+
+    for (int32_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int32_t d = 0; d < D; ++d)
+            dot += qv[d] * K[(int64_t)j * D + d];
+        w[j] = p->scale * dot;
+    }
+    free(heap);
+
+    double m = -INFINITY;
+    for (int32_t j = 0; j < n; ++j)
+        if (w[j] > m)
+            m = w[j];
+    double z = 0.0;
+    for (int32_t j = 0; j < n; ++j) {
+        w[j] = exp(w[j] - m);
+        z += w[j];
+    }
+    for (int32_t j = 0; j < n; ++j)
+        w[j] /= z;
+    return n;
+}
+
+/* out[d] = sum_j w[j] * V[j][d] */
+static void weighted_sum(const double *w, int32_t n, const double *V, int32_t D, double *out)
+{
+    for (int32_t d = 0; d < D; ++d)
+        out[d] = 0.0;
+    for (int32_t j = 0; j < n; ++j)
+        for (int32_t d = 0; d < D; ++d)
+            out[d] += w[j] * V[(int64_t)j * D + d];
+}
+
+/* All query rows of request b for head h -> out[(q0 + i), h, :]. */
+static int attend_request_head(const problem_t *p, int32_t b, int32_t h, double *out)
+{
+    const int32_t D = p->head_dim;
+    const int32_t G = p->num_heads / p->num_kv_heads;
+    const int32_t kvh = h / G;
+    const int32_t q0 = p->query_start_loc[b];
+    const int32_t ql = p->query_start_loc[b + 1] - q0;
+    const int32_t L = p->seq_lens[b];
+    if (ql == 0)
+        return ORACLE_OK;
+    double *K = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+    double *V = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+    double *w = (double *)malloc(sizeof(double) * ((size_t)L + 1));
+    if (!K || !V || !w) {
+        free(K); free(V); free(w);
+        return ORACLE_ERR_NOMEM;
+    }
+    gather_request(p, b, kvh, K, V);
+    for (int32_t i = 0; i < ql; ++i) {
+        int32_t n = weights_for_query(p, b, i, h, K, w);
+        weighted_sum(w, n, V, D, out + ((int64_t)(q0 + i) * p->num_heads + h) * D);
+    }
+    free(K); free(V); free(w);
+    return ORACLE_OK;
+}
+
+/* A tiny thread pool over independent (request, head) items. */
+typedef struct {
+    const problem_t *p;
+    double *out;
+    int64_t n_items;
+    int64_t next;
+    pthread_mutex_t lock;
+    int status;
+} pool_t;
+
+static void *pool_worker(void *arg)
+{
+    pool_t *pool = (pool_t *)arg;
+    for (;;) {
+        pthread_mutex_lock(&pool->lock);
+        int64_t it = pool->next++;
+        pthread_mutex_unlock(&pool->lock);
+        if (it >= pool->n_items)
+            break;
+        int32_t b = (int32_t)(it / pool->p->num_heads);
+        int32_t h = (int32_t)(it % pool->p->num_heads);
+        int rc = attend_request_head(pool->p, b, h, pool->out);
+        if (rc != ORACLE_OK) {
+            pthread_mutex_lock(&pool->lock);
+            pool->status = rc;
+            pthread_mutex_unlock(&pool->lock);
+        }
+    }
+    return NULL;
+}
+
+/*
+ * out: [total_q, num_heads, head_dim] doubles. Rows of requests with
+ * query_len 0 are absent (total_q counts only scheduled tokens).
+ */
+int oracle_attention_varlen(const uint16_t *q, const uint16_t *key_cache,
+                            const uint16_t *value_cache, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                            const int32_t *query_start_loc, int32_t num_seqs,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int64_t num_blocks, float scale,
+                            double *out, int32_t num_threads)
+{
+    problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                   query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
+                   block_size, num_blocks, (double)scale};
+    int rc = check_problem(&p);
+    if (rc != ORACLE_OK)
+        return rc;
+    pool_t pool;
+    pool.p = &p;
+    pool.out = out;
+    pool.n_items = (int64_t)num_seqs * num_heads;
+    pool.next = 0;
+    pool.status = ORACLE_OK;
+    pthread_mutex_init(&pool.lock, NULL);
+    if (num_threads < 1)
+        num_threads = 1;
+    if (num_threads == 1) {
+        pool_worker(&pool);
+    } else {
+        pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * num_threads);
+        if (!th)
+            return ORACLE_ERR_NOMEM;
+        for (int32_t t = 0; t < num_threads; ++t)
+            pthread_create(&th[t], NULL, pool_worker, &pool);
+        for (int32_t t = 0; t < num_threads; ++t)
+            pthread_join(th[t], NULL);
+        free(th);
+    }
+    pthread_mutex_destroy(&pool.lock);
+    return pool.status;
+}
+
+/*
+ * The same definition for a chosen list of (query token, head) pairs, so that
+ * full-size problems can be checked at sampled outputs. out: [n_samples, head_dim].
+ */
+int oracle_attention_sampled(const uint16_t *q, const uint16_t *key_cache,
+                             const uint16_t *value_cache, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                             const int32_t *query_start_loc, int32_t num_seqs,
+                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int64_t num_blocks, float scale,
+                             int64_t n_samples, const int64_t *sample_token,
+                             const int32_t *sample_head, double *out)
+{
+    problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                   query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
+                   block_size, num_blocks, (double)scale};
+    int rc = check_problem(&p);
+    if (rc != ORACLE_OK)
+        return rc;
+    const int32_t D = head_dim;
+    const int32_t G = num_heads / num_kv_heads;
+    for (int64_t s = 0; s < n_samples; ++s) {
+        int64_t t = sample_token[s];
+        int32_t h = sample_head[s];
+        if (t < 0 || t >= query_start_loc[num_seqs] || h < 0 || h >= num_heads)
+            return ORACLE_ERR_ARG;
+        int32_t b = 0;
+        while (!(query_start_loc[b] <= t && t < query_start_loc[b + 1]))
+            ++b;
+        int32_t i = (int32_t)(t - query_start_loc[b]);
+        int32_t L = seq_lens[b];
+        double *K = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+        double *V = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+        double *w = (double *)malloc(sizeof(double) * ((size_t)L + 1));
+        if (!K || !V || !w) {
+            free(K); free(V); free(w);
+            return ORACLE_ERR_NOMEM;
+        }
+        gather_request(&p, b, h / G, K, V);
+        int32_t n = weights_for_query(&p, b, i, h, K, w);
+        weighted_sum(w, n, V, D, out + s * D);
+        free(K); free(V); free(w);
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Softmax weights of one (query token, head) pair over its visible keys, for
+ * the tests' checks of the weights themselves. weights: at least seq_len
+ * doubles. Returns the number of visible keys, or a negative error code.
+ */
+int oracle_attention_weights(const uint16_t *q, const uint16_t *key_cache,
+                             const uint16_t *value_cache, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                             const int32_t *query_start_loc, int32_t num_seqs,
+                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int64_t num_blocks, float scale,
+                             int64_t token, int32_t head, double *weights)
+{
+    problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                   query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
+                   block_size, num_blocks, (double)scale};
+    int rc = check_problem(&p);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (token < 0 || token >= query_start_loc[num_seqs] || head < 0 || head >= num_heads)
+        return ORACLE_ERR_ARG;
+    int32_t b = 0;
+    while (!(query_start_loc[b] <= token && token < query_start_loc[b + 1]))
+        ++b;
+    int32_t L = seq_lens[b];
+    const int32_t D = head_dim;
+    double *K = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+    double *V = (double *)malloc(sizeof(double) * ((size_t)L * D + 1));
+    if (!K || !V) {
+        free(K); free(V);
+        return ORACLE_ERR_NOMEM;
+    }
+    gather_request(&p, b, head / (num_heads / num_kv_heads), K, V);
+    int32_t n = weights_for_query(&p, b, (int32_t)(token - query_start_loc[b]), head, K, weights);
+    free(K); free(V);
+    return n;
+}

@@ -1,0 +1,286 @@
+"""Checks that pin the CPU oracle to facts other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on a
+mismatch. ``test_oracle_pins.py`` runs them against the oracle; the mutant test
+runs them against deliberately broken copies of it and expects each copy to
+fail at least one pin.
+
+What pins what:
+  * dense brute force: scaled_dot_product_attention from PyTorch (float64, CPU,
+    explicit causal mask, GQA by repeat-interleave) on contiguous K/V, against
+    the oracle reading the same rows scattered into a shuffled block pool;
+  * closed forms: seq_len 1 gives the V row, constant V gives V, q = 0 gives
+    the mean of the visible V rows, two keys give logistic weights;
+  * invariants: physical block permutation, causal future perturbation, GQA
+    equals MHA with replicated KV heads, weights sum to one;
+  * the slot address formula, from the golden fixture.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+from paged_kv_cache_55_gb300.workloads import bf16_bits_to_f32, f32_to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def read_golden(name: str) -> np.ndarray:
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return np.array(rows, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# A test-local problem builder: dense per-request K/V first, then a paged pool
+# --------------------------------------------------------------------------
+
+class DenseProblem:
+    """Contiguous K/V per request plus the same rows scattered into a shuffled pool."""
+
+    def __init__(self, rng, ctx_lens, q_lens, H, Hkv, D, bs=16, extra_blocks=3, q_scale=1.0,
+                 perm=None):
+        self.H, self.Hkv, self.D, self.bs = H, Hkv, D, bs
+        self.ctx = list(ctx_lens)
+        self.ql = list(q_lens)
+        self.L = [c + q for c, q in zip(self.ctx, self.ql)]
+        B = len(self.L)
+        nblk = [(x + bs - 1) // bs for x in self.L]
+        self.num_blocks = sum(nblk) + extra_blocks
+        self.kd = [f32_to_bf16_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32)) for x in self.L]
+        self.vd = [f32_to_bf16_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32)) for x in self.L]
+        T = sum(self.ql)
+        self.q = f32_to_bf16_bits((q_scale * rng.standard_normal((T, H, D))).astype(np.float32))
+        self.qsl = np.zeros(B + 1, dtype=np.int32)
+        self.qsl[1:] = np.cumsum(self.ql)
+        self.seq_lens = np.array(self.L, dtype=np.int32)
+        self.perm = rng.permutation(self.num_blocks) if perm is None else np.asarray(perm)
+        self.max_blocks = max(nblk + [1]) + 1
+        self.scale = float(np.float32(1.0 / math.sqrt(D)))
+        self.repack()
+
+    def repack(self):
+        """Write the dense rows into a pool whose unowned slots hold NaN."""
+        bs = self.bs
+        self.bt = np.full((len(self.L), self.max_blocks), -7, dtype=np.int32)
+        self.kc = np.full((self.num_blocks, bs, self.Hkv, self.D), 0x7FC0, dtype=np.uint16)
+        self.vc = np.full_like(self.kc, 0x7FC0)
+        cursor = 0
+        for b, L in enumerate(self.L):
+            for i in range((L + bs - 1) // bs):
+                self.bt[b, i] = self.perm[cursor]
+                cursor += 1
+            for j in range(L):
+                blk = self.bt[b, j // bs]
+                self.kc[blk, j % bs] = self.kd[b][j]
+                self.vc[blk, j % bs] = self.vd[b][j]
+
+    def run(self, oracle, num_threads=2):
+        return oracle.attention(self.q, self.kc, self.vc, self.bt, self.seq_lens, self.qsl,
+                                self.H, self.scale, num_threads=num_threads)
+
+    def sdpa(self):
+        """PyTorch SDPA per request in float64 with a bottom-right causal mask."""
+        out = np.zeros((int(self.qsl[-1]), self.H, self.D), dtype=np.float64)
+        for b, L in enumerate(self.L):
+            q0, ql = int(self.qsl[b]), self.ql[b]
+            if ql == 0:
+                continue
+            qb = torch.from_numpy(bf16_bits_to_f32(self.q[q0:q0 + ql]).astype(np.float64)).transpose(0, 1)
+            kb = torch.from_numpy(bf16_bits_to_f32(self.kd[b]).astype(np.float64)).transpose(0, 1)
+            vb = torch.from_numpy(bf16_bits_to_f32(self.vd[b]).astype(np.float64)).transpose(0, 1)
+            i = torch.arange(ql).unsqueeze(1)
+            j = torch.arange(L).unsqueeze(0)
+            mask = j <= (L - ql) + i
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qb.unsqueeze(0), kb.unsqueeze(0), vb.unsqueeze(0), attn_mask=mask,
+                scale=self.scale, enable_gqa=(self.H != self.Hkv))
+            out[q0:q0 + ql] = o[0].transpose(0, 1).numpy()
+        return out
+
+
+# --------------------------------------------------------------------------
+# The pins
+# --------------------------------------------------------------------------
+
+DENSE_CASES = [
+    # (ctx_lens, q_lens, H, Hkv, D, bs)
+    ([0, 6, 15, 32], [1, 1, 1, 1], 4, 1, 64, 16),
+    ([3, 17, 0], [5, 2, 9], 8, 2, 8, 16),
+    ([30, 1], [10, 4], 8, 8, 4, 16),
+    ([12, 0, 21], [3, 0, 7], 16, 2, 8, 8),
+    ([33], [7], 8, 1, 4, 4),
+]
+
+
+def pin_dense_vs_sdpa(oracle):
+    rng = np.random.default_rng(11)
+    for ctx, ql, H, Hkv, D, bs in DENSE_CASES:
+        p = DenseProblem(rng, ctx, ql, H, Hkv, D, bs)
+        got = p.run(oracle)
+        ref = p.sdpa()
+        err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+        assert err <= 1e-12, f"oracle vs SDPA max |diff| {err} for case {(ctx, ql, H, Hkv, D, bs)}"
+
+
+def pin_block_permutation_invariance(oracle):
+    rng = np.random.default_rng(12)
+    p = DenseProblem(rng, [40, 9, 70], [3, 1, 6], 8, 2, 8, bs=16, extra_blocks=5)
+    a = p.run(oracle)
+    p.perm = np.random.default_rng(99).permutation(p.num_blocks)
+    p.repack()
+    b = p.run(oracle)
+    assert np.array_equal(a, b), "output changed under a permutation of physical block ids"
+
+
+def pin_seq_len_one_is_v_row(oracle):
+    rng = np.random.default_rng(13)
+    p = DenseProblem(rng, [0, 0], [1, 1], 4, 2, 64)
+    out = p.run(oracle)
+    for b in range(2):
+        for h in range(4):
+            v = bf16_bits_to_f32(p.vd[b][0, h // 2]).astype(np.float64)
+            assert np.array_equal(out[b, h], v), "seq_len 1 must return the V row exactly"
+
+
+def pin_constant_v(oracle):
+    rng = np.random.default_rng(14)
+    p = DenseProblem(rng, [25, 3], [4, 1], 4, 1, 8)
+    c = f32_to_bf16_bits(rng.standard_normal(8).astype(np.float32))
+    for b in range(2):
+        p.vd[b][:] = c
+    p.repack()
+    out = p.run(oracle)
+    cv = bf16_bits_to_f32(c).astype(np.float64)
+    assert np.max(np.abs(out - cv)) <= 1e-14, "constant V must give V"
+
+
+def pin_zero_q_mean(oracle):
+    rng = np.random.default_rng(15)
+    p = DenseProblem(rng, [19, 5], [3, 2], 4, 2, 8)
+    p.q[:] = 0
+    out = p.run(oracle)
+    for b in range(2):
+        q0, ql, L = int(p.qsl[b]), p.ql[b], p.L[b]
+        for i in range(ql):
+            n = L - ql + i + 1
+            for h in range(4):
+                mean = bf16_bits_to_f32(p.vd[b][:n, h // 2]).astype(np.float64).mean(axis=0)
+                assert np.max(np.abs(out[q0 + i, h] - mean)) <= 1e-14, "q = 0 must average the visible V rows"
+
+
+def pin_two_keys_logistic(oracle):
+    # One head, D = 4, scale 1: scores are q . k exactly (bf16-exact values),
+    # so the weights are the logistic function of the score gap.
+    for a, c in [(1.0, 0.0), (2.5, -1.25), (-3.0, 4.0), (0.0, 0.0), (10.0, -6.0)]:
+        q = f32_to_bf16_bits(np.array([[[1, 0, 0, 0]]], dtype=np.float32))
+        kc = np.full((2, 4, 1, 4), 0x7FC0, dtype=np.uint16)
+        vc = np.full_like(kc, 0x7FC0)
+        kc[1, 0, 0] = f32_to_bf16_bits(np.array([a, 0, 0, 0], dtype=np.float32))
+        kc[1, 1, 0] = f32_to_bf16_bits(np.array([c, 0, 0, 0], dtype=np.float32))
+        vc[1, 0, 0] = f32_to_bf16_bits(np.array([1, 0, 0, 0], dtype=np.float32))
+        vc[1, 1, 0] = f32_to_bf16_bits(np.array([0, 1, 0, 0], dtype=np.float32))
+        bt = np.array([[1, 0]], dtype=np.int32)
+        out = oracle.attention(q, kc, vc, bt, np.array([2], np.int32), np.array([0, 1], np.int32),
+                               1, 1.0, num_threads=1)
+        w0 = 1.0 / (1.0 + math.exp(-(a - c)))
+        assert abs(out[0, 0, 0] - w0) <= 1e-15 and abs(out[0, 0, 1] - (1.0 - w0)) <= 1e-15, \
+            f"two-key weights must be logistic in the score gap ({a}, {c})"
+        assert out[0, 0, 2] == 0.0 and out[0, 0, 3] == 0.0
+
+
+def pin_weights_sum_to_one(oracle):
+    rng = np.random.default_rng(16)
+    p = DenseProblem(rng, [50, 7], [5, 1], 8, 2, 16, q_scale=4.0)
+    for tok in range(int(p.qsl[-1])):
+        for h in (0, 3, 7):
+            w = oracle.attention_weights(p.q, p.kc, p.vc, p.bt, p.seq_lens, p.qsl, p.H, p.scale, tok, h)
+            assert (w >= 0).all()
+            assert abs(w.sum() - 1.0) <= 1e-12, "softmax weights must sum to one"
+    # the number of visible keys follows the causal rule
+    w = oracle.attention_weights(p.q, p.kc, p.vc, p.bt, p.seq_lens, p.qsl, p.H, p.scale, 2, 0)
+    assert w.shape[0] == 50 + 2 + 1
+
+
+def pin_causal_future_perturbation(oracle):
+    rng = np.random.default_rng(17)
+    p = DenseProblem(rng, [20], [8], 4, 2, 8)
+    base = p.run(oracle)
+    i = 3
+    pos = 20 + i  # query i sees keys 0 .. 23
+    p.kd[0][pos + 1:] = f32_to_bf16_bits(rng.standard_normal(p.kd[0][pos + 1:].shape).astype(np.float32))
+    p.vd[0][pos + 1:] = f32_to_bf16_bits(rng.standard_normal(p.vd[0][pos + 1:].shape).astype(np.float32))
+    p.repack()
+    after = p.run(oracle)
+    assert np.array_equal(base[:i + 1], after[:i + 1]), "future keys must not affect a query"
+    assert not np.array_equal(base[i + 1:], after[i + 1:]), "later queries must see the changed keys"
+
+
+def pin_gqa_equals_replicated_mha(oracle):
+    rng = np.random.default_rng(18)
+    G = 4
+    p = DenseProblem(rng, [30, 12], [2, 5], 8, 2, 8)
+    gqa = p.run(oracle)
+    m = DenseProblem(rng, [30, 12], [2, 5], 8, 8, 8, perm=p.perm)
+    m.q = p.q.copy()
+    m.kd = [np.repeat(k, G, axis=1) for k in p.kd]
+    m.vd = [np.repeat(v, G, axis=1) for v in p.vd]
+    m.repack()
+    mha = m.run(oracle)
+    assert np.array_equal(gqa, mha), "GQA must equal MHA with each KV head repeated for its group"
+
+
+def pin_slot_formula_golden(oracle):
+    rows = read_golden("slot_address.txt")
+    for bs, blk, off, slot in rows:
+        nb = blk + 2
+        kc = np.zeros((nb, bs, 1, 8), dtype=np.uint16)
+        vc = np.zeros_like(kc)
+        key = np.arange(1, 9, dtype=np.uint16).reshape(1, 1, 8)
+        val = key + 100
+        oracle.reshape_and_cache(key, val, kc, vc, np.array([slot]), int(bs))
+        assert np.array_equal(kc[blk, off, 0], key[0, 0]) and np.array_equal(vc[blk, off, 0], val[0, 0]), \
+            f"slot {slot} must land in block {blk} offset {off} (block_size {bs})"
+        assert int(np.count_nonzero(kc)) == 8, "exactly one row may change"
+
+
+def pin_reshape_matches_numpy_scatter(oracle):
+    rng = np.random.default_rng(19)
+    nb, bs, hkv, d = 20, 16, 3, 8
+    kc = np.full((nb, bs, hkv, d), 0x7FC0, dtype=np.uint16)
+    vc = kc.copy()
+    T = 37
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[5] = -1
+    slots[30] = -4
+    key = rng.integers(0, 65535, size=(T, hkv, d), dtype=np.uint16)
+    val = rng.integers(0, 65535, size=(T, hkv, d), dtype=np.uint16)
+    ek, ev = kc.copy(), vc.copy()
+    keep = slots >= 0
+    ek.reshape(nb * bs, hkv, d)[slots[keep]] = key[keep]
+    ev.reshape(nb * bs, hkv, d)[slots[keep]] = val[keep]
+    oracle.reshape_and_cache(key, val, kc, vc, slots, bs)
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev), "scatter must match numpy fancy assignment"
+
+
+PINS = [
+    pin_dense_vs_sdpa,
+    pin_block_permutation_invariance,
+    pin_seq_len_one_is_v_row,
+    pin_constant_v,
+    pin_zero_q_mean,
+    pin_two_keys_logistic,
+    pin_weights_sum_to_one,
+    pin_causal_future_perturbation,
+    pin_gqa_equals_replicated_mha,
+    pin_slot_formula_golden,
+    pin_reshape_matches_numpy_scatter,
+]

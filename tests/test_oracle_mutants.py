@@ -1,0 +1,54 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Every mutant is a one-line textual change to a temporary copy of oracle.c that
+keeps all memory accesses in bounds; the copy is compiled and loaded in this
+process, the pins run against it, and at least one must fail.
+"""
+
+import os
+
+import pytest
+
+import oracle as oracle_mod
+from oracle_pins import PINS
+
+MUTANTS = {
+    "gqa_modulo_map": ("const int32_t kvh = h / G;",
+                       "const int32_t kvh = h % p->num_kv_heads;"),
+    "no_causal_mask": ("const int32_t n = ctx + i + 1; /* keys 0 .. ctx + i */",
+                       "const int32_t n = L;"),
+    "mirrored_gather_offset": ("int32_t offset = j % p->block_size;",
+                               "int32_t offset = (p->block_size - 1) - (j % p->block_size);"),
+    "mirrored_scatter_offset": ("int64_t offset = s % block_size;",
+                                "int64_t offset = (block_size - 1) - (s % block_size);"),
+    "scale_dropped": ("w[j] = p->scale * dot;", "w[j] = dot;"),
+    "dot_drops_last_dim": ("for (int32_t d = 0; d < D; ++d)\n            dot += qv[d]",
+                           "for (int32_t d = 0; d < D - 1; ++d)\n            dot += qv[d]"),
+    "unnormalised_weights": ("w[j] /= z;", "w[j] /= 1.0;"),
+    "v_read_from_k_cache": ("V[(int64_t)j * D + d] = bf16_to_double(p->value_cache[base + d]);",
+                            "V[(int64_t)j * D + d] = bf16_to_double(p->key_cache[base + d]);"),
+    "first_query_row_only": ("const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;",
+                             "const uint16_t *qrow = p->q + ((int64_t)(q0) * p->num_heads + h) * D;"),
+    "drops_last_token": ("        if (s < 0)\n            continue;\n        int64_t block",
+                         "        if (s < 0 || t == num_tokens - 1)\n            continue;\n        int64_t block"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    before, after = MUTANTS[name]
+    src = open(oracle_mod.SOURCE).read()
+    assert src.count(before) == 1, f"mutation site for {name} not found exactly once"
+    mutated = src.replace(before, after)
+    path = os.path.join(tmp_path, f"oracle_{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    lib = oracle_mod.compile_oracle(path, os.path.join(tmp_path, f"liboracle_{name}.so"))
+    mutant = oracle_mod.Oracle(lib)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, oracle_mod.OracleError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
