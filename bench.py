@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-attention step (reshape_and_cache + attention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gqa_decode] [--seed 0]
+
+A step is one pass of the whole path over one batch: pa_reshape_and_cache of
+the step's new K/V rows, then pa_attention_varlen (planning, split-KV
+attention, log-sum-exp merge). Inputs are seeded synthetic data resident in
+HBM before timing starts. The KV working set (1.7 GB for the default
+workload) is far larger than the 126 MB L2, so no L2 flush is needed between
+steps. Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload.
+
+Multi-GPU (torchrun): each rank runs its own copy of the workload with its own
+seed (independent batches, no collective on the data path); the timing is the
+max over ranks and the value counts the bytes of all ranks ("weak" scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn KV GB/s & fraction of GB300 HBM peak; decode tokens/s per layer"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "tiny_decode": "tiny decode: 4 requests, seq_lens {1,7,16,33}, H=4, Hkv=1, D=64, bs=16",
+    "mha_decode": "MHA 7B-like decode layer: batch 64, H=Hkv=32, D=128, bs=16, seq_lens U[128,2048]",
+    "gqa_decode": "GQA 8B-like decode layer: batch 256, H=32, Hkv=8, D=128, bs=16, seq_lens lognormal "
+                  "(median 1024, sigma 1.0) clipped [16,8192], reshape_and_cache of 256 new rows",
+    "long_decode": "long-context decode: batch 8, seq_len 32768, H=64, Hkv=8, D=128, bs=16",
+    "mixed_step": "mixed continuous-batching step: 16 prefill chunks x 512 (ctx U[0,4096]) + 240 decode "
+                  "(ctx U[256,4096], 64 share a 64-block prefix), H=32, Hkv=8, D=128, bs=16",
+}
+
+
+# --------------------------------------------------------------------------
+# Byte and FLOP accounting (algorithmic: what the step must move at minimum)
+# --------------------------------------------------------------------------
+
+def step_accounting(w) -> dict:
+    H, Hkv, D, bs = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+    kv_tok = 2 * Hkv * D * 2
+    uniq = w.kv_tokens_unique()
+    logical = w.kv_tokens_logical()
+    T = w.total_q
+    tables = int(sum(-(-int(L) // bs) for L in w.seq_lens)) * 4
+    meta = (2 * w.num_seqs + 1) * 4
+    q_out = 2 * T * H * D * 2
+    reshape = T * (2 * Hkv * D * 2) * 2 + T * 8
+    kv_bytes = uniq * kv_tok
+    flops = 0
+    ql = w.query_lens
+    for b in range(w.num_seqs):
+        L, n = int(w.seq_lens[b]), int(ql[b])
+        visible = n * (L - n) + n * (n + 1) // 2
+        flops += 4 * H * D * visible
+    return {
+        "kv_bytes": kv_bytes,
+        "kv_bytes_logical": logical * kv_tok,
+        "attention_bytes": kv_bytes + q_out + tables + meta,
+        "step_bytes": kv_bytes + q_out + tables + meta + reshape,
+        "flops": flops,
+        "query_tokens": T,
+    }
+
+
+# --------------------------------------------------------------------------
+# Multi-rank helpers (also exercised by the gloo tests)
+# --------------------------------------------------------------------------
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws an independent batch of the same shape."""
+    return seed + 7919 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_rate(total_units: float, max_seconds: float) -> float:
+    return total_units / max_seconds if max_seconds > 0 else float("nan")
+
+
+# --------------------------------------------------------------------------
+# Clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", self.gpu_id], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the CPU baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def sub_workload(w, reqs):
+    """The listed requests of `w` as their own batch (arrays sliced, not recomputed)."""
+    reqs = np.asarray(sorted(reqs))
+    ql = w.query_lens[reqs]
+    qsl = np.zeros(reqs.size + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(ql)
+    rows = np.concatenate([np.arange(w.query_start_loc[b], w.query_start_loc[b + 1]) for b in reqs])
+    return dict(q=w.q[rows], block_tables=w.block_tables[reqs], seq_lens=w.seq_lens[reqs], query_start_loc=qsl)
+
+
+def oracle_rate(w, kc, vc, target_s: float, rng, threads: int):
+    """Time the oracle on random requests until about target_s of CPU work; returns
+    (KV GB/s, query tokens/s, seconds, requests, threads)."""
+    import oracle as oracle_mod
+    orc = oracle_mod.default()
+    kv_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    order = rng.permutation(w.num_seqs)
+    done_bytes = done_tok = 0
+    used = 0
+    t_total = 0.0
+    n = 1
+    while used < w.num_seqs and t_total < target_s:
+        take = order[used:used + n]
+        used += take.size
+        s = sub_workload(w, take)
+        t0 = time.perf_counter()
+        orc.attention(s["q"], kc, vc, s["block_tables"], s["seq_lens"], s["query_start_loc"], w.num_heads,
+                      w.scale, num_threads=threads)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(s["seq_lens"].astype(np.int64).sum()) * kv_tok
+        done_tok += int(s["query_start_loc"][-1])
+        n = min(2 * n, 64)
+    return done_bytes / t_total / 1e9, done_tok / t_total, t_total, used, threads
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# The committed ncu traffic of the timed kernel (valid only for unchanged source)
+# --------------------------------------------------------------------------
+
+KERNEL_SOURCES = ["paged_kv_cache_55_gb300/csrc/attention_splitkv.cu", "paged_kv_cache_55_gb300/csrc/pa_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        data = json.load(open(path))
+    except ValueError:
+        return None
+    rec = data.get(workload)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def run_reference(args, world, rank) -> None:
+    if rank != 0:
+        return
+    from paged_kv_cache_55_gb300 import workloads as W
+    import oracle as oracle_mod
+    kw = {"batch": args.batch} if args.batch else {}
+    w = W.by_name(args.workload, seed=args.seed, **kw)
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    orc = oracle_mod.default()
+    orc.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
+    threads = host_threads()
+    rng = np.random.default_rng(args.seed)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(w, kc, vc, per_step / 4, rng, threads)
+    rates, toks, secs, reqs = [], [], [], []
+    for _ in range(args.steps):
+        r, t, s, n, _ = oracle_rate(w, kc, vc, per_step, rng, threads)
+        rates.append(r)
+        toks.append(t)
+        secs.append(s)
+        reqs.append(n)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(secs)) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "decode_tokens_per_s": float(np.mean(toks)),
+        "config": {"workload": workload_text(args), "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"per step: random requests of the workload (mean {np.mean(reqs):.1f} of "
+                                   f"{w.num_seqs}) for about {per_step:.1f} s of fp64 oracle work"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_text(args) -> str:
+    text = WORKLOAD_TEXT[args.workload]
+    return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
+
+
+def run_ours(args, world, rank, local_rank) -> None:
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_55_gb300 import binding as B
+    from paged_kv_cache_55_gb300 import build as build_mod
+    from paged_kv_cache_55_gb300 import workloads as W
+    from paged_kv_cache_55_gb300.runner import DeviceStep
+
+    build_mod.build()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    kw = {"batch": args.batch} if args.batch else {}
+    w = W.by_name(args.workload, seed=rank_seed(args.seed, rank), **kw)
+    acct = step_accounting(w)
+    st = DeviceStep(w, device=str(device))
+    stream = torch.cuda.current_stream()
+
+    # warm-up (the first call also creates the timing events)
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for a, b in ev_pairs:
+        a.record(stream)
+        b.record(stream)
+    for _ in range(max(args.warmup, 1)):
+        st.run()
+    torch.cuda.synchronize()
+    if B.pa_debug_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    gpu_id = str(torch.cuda.get_device_properties(device).uuid)
+    gpu_id = gpu_id if gpu_id.startswith("GPU-") else f"GPU-{gpu_id}"
+    sampler = ClockSampler(gpu_id)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = B.pa_launch_count()
+    t0.record(stream)
+    for k in range(args.steps):
+        B.pa_attention_set_timing_events(*ev_pairs[k])
+        st.run()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = B.pa_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = t0.elapsed_time(t1) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs)
+
+    max_ms = reduce_max(step_ms, device)
+    total_bytes = reduce_sum(float(acct["step_bytes"]), device)
+    total_tok = reduce_sum(float(acct["query_tokens"]), device)
+    value = aggregate_rate(total_bytes, max_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers: H2D inputs, the step, D2H output
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = {k: pin(getattr(st, k)) for k in ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens",
+                                                "query_start_loc")}
+    host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, t in host_in.items():
+            getattr(st, k).copy_(t, non_blocking=True)
+        st.run()
+        host_out.copy_(st.out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, device)
+    e2e_value = aggregate_rate(total_bytes, e2e_ms * 1e-3) / 1e9
+
+    peaks = load_peaks()
+    kern_achieved = acct["attention_bytes"] / (kern_ms * 1e-3) / 1e9
+    traffic = committed_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "hbm_frac": value / peaks["hbm_gbs"],
+        "decode_tokens_per_s": total_tok / (max_ms * 1e-3),
+        "config": {"workload": workload_text(args), "seed": args.seed,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "no flush: KV working set per step is larger than L2",
+                   "step": "pa_reshape_and_cache + pa_attention_varlen (plan, split-KV, merge)",
+                   "step_bytes": acct["step_bytes"], "kv_bytes": acct["kv_bytes"],
+                   "kv_bytes_logical": acct["kv_bytes_logical"], "flops": acct["flops"]},
+        "roofline": {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kern_achieved / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "kernel_ms": kern_ms,
+                     "algorithmic_bytes_per_launch": acct["attention_bytes"], "traffic": traffic},
+        "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kc = w.key_cache.copy()
+        vc = w.value_cache.copy()
+        import oracle as oracle_mod
+        oracle_mod.default().reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
+        r, _, secs, n, threads = oracle_rate(w, kc, vc, args.cpu_seconds, np.random.default_rng(1), host_threads())
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{n} random requests of the workload, {secs:.1f} s of fp64 oracle "
+                                          f"attention (KV bytes of the sampled requests / time)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="gqa_decode")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's number of requests (small profiling cases only)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, world, rank, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * pagedattn.h - C ABI of libpagedattn.so: one batched attention step over a
+ * paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the vLLM inference notes ("AI Infra入门干货总结：大模型是
+ * 如何高效推理的"):
+ *   - §Paged Attention: the per-layer cache is [num_blocks, block_size,
+ *     num_kv_heads, head_dim] for K and for V; block_table[b][i] is the
+ *     physical block of logical block i of request b; slot_mapping tells the
+ *     kernel where to write each new token's K/V; slot = block * block_size +
+ *     offset, block = slot / block_size, offset = slot % block_size.
+ *   - §LLM 推理全流程 3 (Attention): K/V are read discretely from the paged
+ *     cache; Q is [query_lens, num_heads, head_dim]; GQA maps one KV head to a
+ *     group of query heads by index, without copies; FlashAttention-style
+ *     fusion with online softmax keeps S and P out of HBM.
+ *   - §Continuous Batching: one step mixes requests; each schedules
+ *     num_tokens - num_computed_tokens query tokens (decode tokens and
+ *     chunked-prefill chunks alike).
+ *
+ * Conventions shared by every call:
+ *   - Pointers marked (device) are CUDA device pointers on the current device;
+ *     (host) are host pointers. The caller owns every buffer; the library
+ *     allocates no device memory and frees nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls enqueue work on it and return without synchronising.
+ *   - Element data is bf16 (dtype PA_BF16). Indices are int32, except
+ *     slot_mapping, which is int64.
+ *   - Errors the host can see (null pointers, bad sizes, unsupported shapes,
+ *     misalignment, small workspace) are returned before anything is
+ *     launched. Errors only the device can see (a block id or slot out of
+ *     range, lengths that contradict the host bounds) make the kernels skip
+ *     the offending work and set bits in a device status word, which
+ *     pa_debug_status() reads; outputs of the offending request are then
+ *     undefined.
+ *   - Supported now: head_dim 64 or 128; block_size 16; num_heads a multiple
+ *     of num_kv_heads with group size 1, 2, 4 or 8.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,          /* a required pointer is NULL */
+    PA_ERR_DIMS = -2,          /* a size is negative or sizes contradict each other */
+    PA_ERR_UNSUPPORTED = -3,   /* dtype, head_dim, block_size or group size not built */
+    PA_ERR_ALIGN = -4,         /* a pointer or stride breaks 16-byte vector alignment */
+    PA_ERR_WORKSPACE = -5,     /* workspace NULL or smaller than pa_attention_workspace_size() */
+    PA_ERR_LAUNCH = -6,        /* a kernel launch failed (the CUDA error is sticky or the config invalid) */
+    PA_ERR_DEVICE_BOUNDS = -7, /* pa_debug_status: a kernel met an out-of-range index */
+    PA_ERR_CUDA = -8           /* another CUDA runtime call failed */
+} pa_status;
+
+enum { PA_BF16 = 0 };
+
+/* Bits of the device status word (pa_debug_status). */
+enum {
+    PA_FLAG_SLOT_RANGE = 1u << 0,   /* reshape_and_cache: slot >= num_blocks * block_size */
+    PA_FLAG_BLOCK_RANGE = 1u << 1,  /* a block_tables entry that must be read is outside [0, num_blocks) */
+    PA_FLAG_LENGTHS = 1u << 2,      /* seq_len < query_len, seq_len > max_seq_len, query_len > max_query_len,
+                                       or seq_len > max_blocks_per_seq * block_size */
+    PA_FLAG_QUERY_LOC = 1u << 3     /* query_start_loc not non-decreasing from 0 to total_q_tokens */
+};
+
+/*
+ * Step 1 - reshape_and_cache: write this step's new K/V rows into the cache.
+ *
+ * For every token t in [0, num_tokens) with s = slot_mapping[t] >= 0:
+ *   key_cache[s / block_size][s % block_size][:][:]   = key[t][:][:]
+ *   value_cache[s / block_size][s % block_size][:][:] = value[t][:][:]
+ * A negative slot means "padding token, write nothing". Two tokens of one
+ * call must not name the same slot (which write wins is then unspecified).
+ *
+ *   key, value         (device) bf16, token t starts at key + t * key_token_stride
+ *                      elements and holds [num_kv_heads, head_dim] contiguous
+ *                      elements (so key may be a slice of a fused QKV output).
+ *   key_token_stride,  elements between consecutive tokens (>= num_kv_heads * head_dim,
+ *   value_token_stride a multiple of 8).
+ *   key_cache,         (device) bf16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *   value_cache        contiguous, updated in place.
+ *   slot_mapping       (device) int64 [num_tokens].
+ * All data pointers must be 16-byte aligned (PA_ERR_ALIGN otherwise).
+ * A slot >= num_blocks * block_size is skipped and sets PA_FLAG_SLOT_RANGE.
+ * num_tokens == 0 launches nothing.
+ */
+pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               int64_t key_token_stride, int64_t value_token_stride,
+                               void *key_cache, void *value_cache,
+                               const int64_t *slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks,
+                               int32_t dtype, void *stream);
+
+/*
+ * Bytes of device workspace pa_attention_varlen needs for these host-side
+ * bounds (0 if the arguments are invalid). Pure host arithmetic; no CUDA call.
+ * The workspace holds the work plan and the split-KV partial results.
+ */
+size_t pa_attention_workspace_size(int32_t num_seqs, int32_t total_q_tokens,
+                                   int32_t max_query_len, int32_t max_seq_len,
+                                   int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size);
+
+/*
+ * How pa_attention_varlen will split KV for these bounds: the partition size
+ * in tokens and the largest number of partitions of one request. Host only.
+ */
+pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len,
+                                 int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t *partition_tokens, int32_t *max_partitions);
+
+/*
+ * Step 2 - attention over the paged cache, for a batch that may mix decode
+ * tokens and chunked-prefill chunks.
+ *
+ * Request b owns query tokens [query_start_loc[b], query_start_loc[b+1]) and
+ * has seq_len = seq_lens[b] KV tokens, which include its new tokens (run
+ * pa_reshape_and_cache first, on the same stream). With
+ * query_len = query_start_loc[b+1] - query_start_loc[b] and
+ * ctx = seq_len - query_len, query i of the request sits at position ctx + i
+ * and attends to keys 0 .. ctx + i (causal, bottom-right aligned; a decode
+ * token sees the whole sequence). Query head h reads KV head
+ * h / (num_heads / num_kv_heads). Logical key j of request b lives at
+ * block_tables[b * max_blocks_per_seq + j / block_size], row j % block_size.
+ *
+ *   out[t][h][:] = bf16( sum_j softmax_j(scale * q[t][h] . K[j]) * V[j] )
+ *
+ *   q                (device) bf16; token t at q + t * q_token_stride elements,
+ *                    [num_heads, head_dim] contiguous; q_token_stride even.
+ *   key_cache,       (device) bf16 [num_blocks, block_size, num_kv_heads, head_dim].
+ *   value_cache
+ *   block_tables     (device) int32 [num_seqs, max_blocks_per_seq]; entries past
+ *                    ceil(seq_len / block_size) are never read.
+ *   seq_lens         (device) int32 [num_seqs].
+ *   query_start_loc  (device) int32 [num_seqs + 1], starts at 0, non-decreasing,
+ *                    ends at total_q_tokens.
+ *   max_query_len,   (host) upper bounds of query_len and seq_len over the batch;
+ *   max_seq_len      they size the launch and the workspace without a device read.
+ *   scale            softmax scale (usually 1/sqrt(head_dim)).
+ *   out              (device) bf16 [total_q_tokens, num_heads, head_dim], contiguous.
+ *   workspace        (device) at least pa_attention_workspace_size(...) bytes,
+ *                    256-byte aligned; contents need no initialisation and are
+ *                    scratch after the call.
+ * Requests with query_len 0 are allowed and produce nothing. All work is
+ * enqueued on `stream`: a planning kernel, the split-KV attention kernel and,
+ * when some request is split, the log-sum-exp merge kernel.
+ */
+pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
+                              const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, const int32_t *query_start_loc,
+                              int32_t num_seqs, int32_t total_q_tokens,
+                              int32_t max_query_len, int32_t max_seq_len,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int64_t num_blocks, float scale,
+                              void *out, void *workspace, size_t workspace_bytes,
+                              int32_t dtype, void *stream);
+
+/*
+ * Block-table addressing on its own: copy the seq_len logical K/V rows of one
+ * request, read through its block-table row, into contiguous
+ * [seq_len, num_kv_heads, head_dim] buffers (device, 16-byte aligned).
+ * block_table_row is a device pointer to that request's row. Used to check
+ * the addressing bit for bit.
+ */
+pa_status pa_gather_kv(const void *key_cache, const void *value_cache,
+                       const int32_t *block_table_row, int32_t seq_len,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int64_t num_blocks, void *key_out, void *value_out,
+                       int32_t dtype, void *stream);
+
+/* Human-readable name of a pa_status value (static string). */
+const char *pa_status_string(int32_t status);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * *flags_out (host, may be NULL) receives the PA_FLAG_* bits that were set.
+ * Returns PA_ERR_DEVICE_BOUNDS if any bit was set, PA_ERR_CUDA if the
+ * synchronisation failed, PA_OK otherwise.
+ */
+pa_status pa_debug_status(void *stream, uint32_t *flags_out);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pa_launch_count(void);
+
+/*
+ * Measurement hook: the next pa_attention_varlen call made by this host
+ * thread records `start` (a cudaEvent_t) just before its split-KV attention
+ * kernel and `stop` just after it, on the call's stream, then forgets them.
+ * Pass NULL, NULL to cancel.
+ */
+pa_status pa_attention_set_timing_events(void *start, void *stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,181 @@
+"""Thin ctypes binding of libpagedattn.so with the C ABI's names.
+
+Argument marshalling only: torch tensors become device pointers, shapes become
+sizes, the current torch stream becomes the ``stream`` argument. Every step of
+the computation runs in the library's CUDA kernels; there is no fallback. If
+the library has not been built, importing the functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libpagedattn.so")
+
+PA_BF16 = 0
+STATUS = {
+    0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_DIMS", -3: "PA_ERR_UNSUPPORTED", -4: "PA_ERR_ALIGN",
+    -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_LAUNCH", -7: "PA_ERR_DEVICE_BOUNDS", -8: "PA_ERR_CUDA",
+}
+FLAG_SLOT_RANGE, FLAG_BLOCK_RANGE, FLAG_LENGTHS, FLAG_QUERY_LOC = 1, 2, 4, 8
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_lib().pa_status_string(status).decode()})")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+SIGNATURES = {
+    "pa_reshape_and_cache": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, _I32, _P], ctypes.c_int),
+    "pa_attention_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
+    "pa_attention_plan_info": ([_I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+    "pa_attention_varlen": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                             _I32, _I64, ctypes.c_float, _P, _P, _SZ, _I32, _P], ctypes.c_int),
+    "pa_gather_kv": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P, _P, _I32, _P], ctypes.c_int),
+    "pa_status_string": ([_I32], ctypes.c_char_p),
+    "pa_debug_status": ([_P, _P], ctypes.c_int),
+    "pa_launch_count": ([], ctypes.c_uint64),
+    "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
+}
+
+
+def load_library(path: str = LIBRARY) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m paged_kv_cache_55_gb300.build` "
+                           "(the CUDA path has no fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = load_library()
+    return _LIB
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise PagedAttnError(status, what)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """key/value [T, Hkv, D] bf16 (token stride free), caches [NB, bs, Hkv, D] bf16, slots int64 [T]."""
+    for t, n in ((key, "key"), (value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache")):
+        _need(t, n, torch.bfloat16)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T, hkv, d = key.shape
+    if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
+        raise ValueError("each token row of key/value must be [Hkv, D] contiguous")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("caches and slot_mapping must be contiguous")
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    _check(_lib().pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0),
+                                       key_cache.data_ptr(), value_cache.data_ptr(), slot_mapping.data_ptr(),
+                                       T, hkv, d, bs, nb, PA_BF16, _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_attention_workspace_size(num_seqs: int, total_q_tokens: int, max_query_len: int, max_seq_len: int,
+                                num_heads: int, num_kv_heads: int, head_dim: int, block_size: int = 16) -> int:
+    n = _lib().pa_attention_workspace_size(num_seqs, total_q_tokens, max_query_len, max_seq_len, num_heads,
+                                           num_kv_heads, head_dim, block_size)
+    if n == 0 and num_seqs > 0:
+        raise ValueError("invalid sizes for pa_attention_workspace_size")
+    return int(n)
+
+
+def pa_attention_plan_info(num_seqs: int, max_seq_len: int, num_heads: int, num_kv_heads: int):
+    pt, mp = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib().pa_attention_plan_info(num_seqs, max_seq_len, num_heads, num_kv_heads,
+                                         ctypes.addressof(pt), ctypes.addressof(mp)), "pa_attention_plan_info")
+    return int(pt.value), int(mp.value)
+
+
+def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                        max_query_len: int, max_seq_len: int, scale: float, out: torch.Tensor,
+                        workspace: torch.Tensor, stream=None) -> None:
+    """q [T, H, D] bf16, caches [NB, bs, Hkv, D] bf16, block_tables [B, M] int32, seq_lens [B] int32,
+    query_start_loc [B+1] int32, out [T, H, D] bf16 contiguous, workspace uint8 (device)."""
+    _need(q, "q", torch.bfloat16)
+    _need(out, "out", torch.bfloat16)
+    _need(key_cache, "key_cache", torch.bfloat16)
+    _need(value_cache, "value_cache", torch.bfloat16)
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
+        _need(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if not out.is_contiguous() or not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("out and the caches must be contiguous")
+    T, H, D = q.shape
+    if q.stride(2) != 1 or q.stride(1) != D:
+        raise ValueError("each token row of q must be [H, D] contiguous")
+    nb, bs, hkv, _ = key_cache.shape
+    B = seq_lens.shape[0]
+    _check(_lib().pa_attention_varlen(q.data_ptr(), q.stride(0), key_cache.data_ptr(), value_cache.data_ptr(),
+                                      block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                                      query_start_loc.data_ptr(), B, T, max_query_len, max_seq_len, H, hkv, D, bs,
+                                      nb, float(scale), out.data_ptr(), workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(), PA_BF16, _stream(stream)),
+           "pa_attention_varlen")
+
+
+def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor,
+                 seq_len: int, key_out: torch.Tensor, value_out: torch.Tensor, stream=None) -> None:
+    nb, bs, hkv, d = key_cache.shape
+    _check(_lib().pa_gather_kv(key_cache.data_ptr(), value_cache.data_ptr(), block_table_row.data_ptr(), seq_len,
+                               hkv, d, bs, nb, key_out.data_ptr(), value_out.data_ptr(), PA_BF16,
+                               _stream(stream)), "pa_gather_kv")
+
+
+def pa_debug_status(stream=None) -> int:
+    """Synchronise the stream and return (then clear) the device status flags."""
+    flags = ctypes.c_uint32(0)
+    st = _lib().pa_debug_status(_stream(stream), ctypes.addressof(flags))
+    if st not in (0, -7):
+        raise PagedAttnError(st, "pa_debug_status")
+    return int(flags.value)
+
+
+def pa_launch_count() -> int:
+    return int(_lib().pa_launch_count())
+
+
+def pa_attention_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]) -> None:
+    s = start.cuda_event if start is not None else None
+    e = stop.cuda_event if stop is not None else None
+    _check(_lib().pa_attention_set_timing_events(s, e), "pa_attention_set_timing_events")
+
+
+def pa_status_string(status: int) -> str:
+    return _lib().pa_status_string(status).decode()

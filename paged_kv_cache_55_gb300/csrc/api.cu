@@ -1,0 +1,233 @@
+// C ABI of libpagedattn.so (declared in include/pagedattn.h): argument
+// validation, per-device state, and dispatch to the kernels' launchers.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_launch.h"
+
+
+// Device status word: kernels OR PA_FLAG_* bits into it when they skip work
+// because an index is out of range.
+__device__ unsigned int g_pa_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  unsigned int *status = nullptr;
+  int sm_count = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceState g_devices[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_stop = nullptr;
+
+// Per-device set-up on first use: the status word's device address and the
+// SM count (both fixed for the life of the process).
+DeviceState *device_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceState &s = g_devices[dev];
+  std::call_once(s.once, [&]() {
+    void *ptr = nullptr;
+    s.err = cudaGetSymbolAddress(&ptr, g_pa_status_word);
+    if (s.err == cudaSuccess) s.err = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    s.status = static_cast<unsigned int *>(ptr);
+  });
+  return s.err == cudaSuccess ? &s : nullptr;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool supported_dims(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (block_size != pa::kBlockSize) return false;
+  if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return false;
+  const int G = num_heads / num_kv_heads;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(int32_t status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_DIMS: return "invalid or inconsistent sizes";
+    case PA_ERR_UNSUPPORTED: return "unsupported dtype, head_dim, block_size or group size";
+    case PA_ERR_ALIGN: return "pointer or stride not aligned for 16-byte vectors";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_LAUNCH: return "kernel launch failed";
+    case PA_ERR_DEVICE_BOUNDS: return "a kernel met an out-of-range index (see status flags)";
+    case PA_ERR_CUDA: return "CUDA runtime call failed";
+    default: return "unknown status";
+  }
+}
+
+uint64_t pa_launch_count(void) { return g_launches.load(); }
+
+pa_status pa_attention_set_timing_events(void *start, void *stop) {
+  if ((start == nullptr) != (stop == nullptr)) return PA_ERR_NULL;
+  t_ev_start = static_cast<cudaEvent_t>(start);
+  t_ev_stop = static_cast<cudaEvent_t>(stop);
+  return PA_OK;
+}
+
+pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_token_stride,
+                               int64_t value_token_stride, void *key_cache, void *value_cache,
+                               const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                               void *stream) {
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+    return PA_ERR_DIMS;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row) return PA_ERR_DIMS;
+  if (key_token_stride % 8 || value_token_stride % 8) return PA_ERR_ALIGN;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  cudaError_t err = pa::launch_reshape_and_cache(
+      key, value, key_token_stride, value_token_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      static_cast<int32_t>(row), num_blocks * block_size, ds->status, ds->sm_count,
+      static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
+size_t pa_attention_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
+                                   int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size) {
+  if (max_query_len < 0 || max_seq_len < max_query_len) return 0;
+  if (!supported_dims(num_heads, num_kv_heads, head_dim, block_size)) return 0;
+  pa::WorkspaceLayout w;
+  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, w))
+    return 0;
+  return w.total;
+}
+
+pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                                 int32_t num_kv_heads, int32_t *partition_tokens, int32_t *max_partitions) {
+  pa::WorkspaceLayout w;
+  if (!pa::workspace_layout(num_seqs, 0, max_seq_len, num_heads, num_kv_heads, 128, w)) return PA_ERR_DIMS;
+  if (partition_tokens) *partition_tokens = w.part_tokens;
+  if (max_partitions) *max_partitions = w.max_parts;
+  return PA_OK;
+}
+
+pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void *key_cache,
+                              const void *value_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                              int32_t total_q_tokens, int32_t max_query_len, int32_t max_seq_len,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, float scale, void *out, void *workspace,
+                              size_t workspace_bytes, int32_t dtype, void *stream) {
+  cudaEvent_t ev_start = t_ev_start, ev_stop = t_ev_stop;
+  t_ev_start = t_ev_stop = nullptr;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || total_q_tokens < 0 || max_query_len < 0 || max_seq_len < max_query_len ||
+      max_blocks_per_seq < 0 || num_blocks < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PA_ERR_DIMS;
+  if (!supported_dims(num_heads, num_kv_heads, head_dim, block_size)) {
+    if (num_heads % num_kv_heads != 0) return PA_ERR_DIMS;
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (!std::isfinite(scale)) return PA_ERR_DIMS;
+  if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
+  if (max_query_len == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_DIMS;
+  if (static_cast<int64_t>(max_query_len) > total_q_tokens) return PA_ERR_DIMS;
+  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !query_start_loc || !out)
+    return PA_ERR_NULL;
+  if (q_token_stride < static_cast<int64_t>(num_heads) * head_dim) return PA_ERR_DIMS;
+  if (q_token_stride % 2 || !aligned(q, 4)) return PA_ERR_ALIGN;
+  if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return PA_ERR_ALIGN;
+  pa::WorkspaceLayout w;
+  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, w))
+    return PA_ERR_DIMS;
+  if (!workspace || workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+
+  pa::AttnLaunch a;
+  a.q = q;
+  a.q_stride = q_token_stride;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q_tokens;
+  a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.out = out;
+  a.workspace = workspace;
+  a.status = ds->status;
+  a.sm_count = ds->sm_count;
+  a.ev_start = ev_start;
+  a.ev_stop = ev_stop;
+  int launched = 0;
+  cudaError_t err = pa::launch_attention(a, static_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(static_cast<uint64_t>(launched));
+  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  return PA_OK;
+}
+
+pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int32_t *block_table_row,
+                       int32_t seq_len, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int64_t num_blocks, void *key_out, void *value_out, int32_t dtype, void *stream) {
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (seq_len < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_DIMS;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (seq_len == 0) return PA_OK;
+  if (!key_cache || !value_cache || !block_table_row || !key_out || !value_out) return PA_ERR_NULL;
+  if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(key_out, 16) || !aligned(value_out, 16) ||
+      !aligned(block_table_row, 4))
+    return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  cudaError_t err = pa::launch_gather_kv(key_cache, value_cache, block_table_row, seq_len,
+                                         num_kv_heads * head_dim, num_blocks, key_out, value_out, ds->status,
+                                         ds->sm_count, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
+pa_status pa_debug_status(void *stream, uint32_t *flags_out) {
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int flags = 0;
+  if (cudaMemcpy(&flags, ds->status, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  if (flags_out) *flags_out = flags;
+  return flags ? PA_ERR_DEVICE_BOUNDS : PA_OK;
+}
+
+}  // extern "C"

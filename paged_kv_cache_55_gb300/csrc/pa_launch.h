@@ -1,0 +1,54 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels'
+// translation units. Internal to libpagedattn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t key_stride,
+                                     int64_t value_stride, void *key_cache, void *value_cache,
+                                     const int64_t *slot_mapping, int32_t num_tokens, int32_t row_elems,
+                                     int64_t num_slots, unsigned int *status, int sm_count,
+                                     cudaStream_t stream);
+
+cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
+                             int32_t seq_len, int32_t row_elems, int64_t num_blocks, void *key_out,
+                             void *value_out, unsigned int *status, int sm_count, cudaStream_t stream);
+
+// Byte offsets of the pieces of the attention workspace, and the split plan.
+struct WorkspaceLayout {
+  size_t item_start, nparts, item_count, items, part_lse, part_o, total;
+  int32_t part_tokens;    // keys per partition
+  int32_t max_parts;      // partitions of the longest request
+  int32_t max_items;      // upper bound on work items (per KV head)
+  int32_t rows_per_item;  // query rows per item: 8 / group size
+};
+
+bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, int32_t num_heads,
+                      int32_t num_kv_heads, int32_t head_dim, WorkspaceLayout &w);
+
+struct AttnLaunch {
+  const void *q;
+  int64_t q_stride;
+  const void *key_cache, *value_cache;
+  const int32_t *block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t *seq_lens, *query_start_loc;
+  int32_t num_seqs, total_q, max_query_len, max_seq_len;
+  int32_t num_heads, num_kv_heads, head_dim;
+  int64_t num_blocks;
+  float scale;
+  void *out;
+  void *workspace;
+  unsigned int *status;
+  int sm_count;
+  cudaEvent_t ev_start, ev_stop;
+};
+
+// Enqueue plan + split-KV attention (+ merge) on `stream`; *launched counts kernels.
+cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *launched);
+
+}  // namespace pa

@@ -1,0 +1,254 @@
+"""CUDA path against the fp64 CPU oracle, through the C ABI (needs a GB300).
+
+Tolerance for attention outputs (bf16 inputs, fp32 accumulation, bf16
+output): |gpu - oracle| <= 2e-3 + 1e-2 * |oracle| elementwise. The cache
+scatter and block-table gather must match bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_55_gb300 import binding as B
+from paged_kv_cache_55_gb300 import workloads as W
+from paged_kv_cache_55_gb300.runner import DeviceStep, bf16_tensor, bf16_to_float64, bf16_to_numpy_bits
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def assert_attention_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
+    assert gpu.shape == ref.shape
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; "
+                             f"first {idx.tolist()} gpu={gpu[bad][:5]} ref={ref[bad][:5]}")
+
+
+def run_and_check(w: W.Workload, oracle, check_status=True):
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    if check_status:
+        assert B.pa_debug_status() == 0
+    kc, vc, ref = oracle.run_step(w)
+    assert np.array_equal(bf16_to_numpy_bits(st.key_cache), kc), "key cache differs after reshape_and_cache"
+    assert np.array_equal(bf16_to_numpy_bits(st.value_cache), vc), "value cache differs after reshape_and_cache"
+    gpu = bf16_to_float64(st.out)
+    assert np.isfinite(gpu).all(), "non-finite output (a masked or unowned slot leaked)"
+    assert_attention_close(gpu, ref, w.name)
+    return st, ref
+
+
+SMALL_CASES = {
+    # name: kwargs of make_workload
+    "ragged_decode_g4_d128": dict(context_lens=[0, 6, 15, 16, 511, 512, 513, 1100, 1535, 2047, 40, 3],
+                                  query_lens=[1] * 12, num_heads=32, num_kv_heads=8, head_dim=128),
+    "decode_g8_d128_long": dict(context_lens=[4999, 700, 32], query_lens=[1] * 3,
+                                num_heads=64, num_kv_heads=8, head_dim=128),
+    "decode_g1_d64": dict(context_lens=[100, 1, 900, 513], query_lens=[1] * 4,
+                          num_heads=4, num_kv_heads=4, head_dim=64),
+    "decode_g2_d64": dict(context_lens=[30, 1400, 7], query_lens=[1] * 3,
+                          num_heads=8, num_kv_heads=4, head_dim=64),
+    "decode_g4_d64": dict(context_lens=[77, 600], query_lens=[1, 1], num_heads=8, num_kv_heads=2, head_dim=64),
+    "decode_g8_d64": dict(context_lens=[1030, 3], query_lens=[1, 1], num_heads=16, num_kv_heads=2, head_dim=64),
+    "mixed_chunks_g4_d128": dict(context_lens=[0, 37, 600, 20, 1000, 5, 0],
+                                 query_lens=[40, 2, 1, 129, 1, 7, 1],
+                                 num_heads=32, num_kv_heads=8, head_dim=128),
+    "mixed_chunks_g1_d128": dict(context_lens=[0, 300, 64], query_lens=[17, 1, 33],
+                                 num_heads=4, num_kv_heads=4, head_dim=128),
+    "mixed_chunks_g8_d64": dict(context_lens=[10, 800, 0], query_lens=[5, 1, 24],
+                                num_heads=16, num_kv_heads=2, head_dim=64),
+    "empty_requests": dict(context_lens=[10, 0, 700, 33], query_lens=[0, 1, 0, 3],
+                           num_heads=8, num_kv_heads=2, head_dim=128),
+    "sharp_scores": dict(context_lens=[300, 1800, 4], query_lens=[1, 1, 9], num_heads=32, num_kv_heads=8,
+                         head_dim=128, q_scale=8.0),
+    "seq_len_one": dict(context_lens=[0, 0, 0], query_lens=[1, 1, 1], num_heads=8, num_kv_heads=2, head_dim=64),
+}
+
+
+def test_tiny_decode(oracle):
+    run_and_check(W.tiny_decode(seed=0), oracle)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_CASES))
+def test_small_cases(oracle, name):
+    w = W.make_workload(name, seed=5, **SMALL_CASES[name])
+    run_and_check(w, oracle)
+
+
+def test_shared_prefix_step(oracle):
+    w = W.mixed_step(seed=2, n_prefill=3, chunk=96, n_decode=20, n_shared=8, shared_blocks=6)
+    run_and_check(w, oracle)
+
+
+def test_seq_len_one_returns_v_row_exactly():
+    w = W.make_workload("one", seed=9, **SMALL_CASES["seq_len_one"])
+    st = DeviceStep(w)
+    st.run()
+    out = bf16_to_numpy_bits(st.out)
+    G = w.num_heads // w.num_kv_heads
+    for b in range(w.num_seqs):
+        for h in range(w.num_heads):
+            assert np.array_equal(out[b, h], w.value[b, h // G]), "seq_len 1 must return the new V row"
+
+
+def test_block_permutation_gives_identical_bits():
+    """Relabelling physical blocks (cache moved with the table) must not change one output bit."""
+    base = W.make_workload("perm", seed=21, **SMALL_CASES["ragged_decode_g4_d128"])
+    a = DeviceStep(base)
+    a.run()
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(base.num_blocks)  # old id -> new id
+    w2 = W.make_workload("perm", seed=21, **SMALL_CASES["ragged_decode_g4_d128"])
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    w2.key_cache = base.key_cache[inv]
+    w2.value_cache = base.value_cache[inv]
+    used = w2.block_tables >= 0
+    w2.block_tables = np.where(used & (w2.block_tables < base.num_blocks),
+                               perm[np.clip(w2.block_tables, 0, base.num_blocks - 1)], w2.block_tables).astype(np.int32)
+    bs = base.block_size
+    w2.slot_mapping = perm[base.slot_mapping // bs] * bs + base.slot_mapping % bs
+    b = DeviceStep(w2)
+    b.run()
+    assert np.array_equal(bf16_to_numpy_bits(a.out), bf16_to_numpy_bits(b.out))
+
+
+def test_gather_kv_bit_exact():
+    w = W.make_workload("gather", seed=3, **SMALL_CASES["ragged_decode_g4_d128"])
+    st = DeviceStep(w)
+    st.reshape_and_cache()
+    kc = bf16_to_numpy_bits(st.key_cache)
+    vc = bf16_to_numpy_bits(st.value_cache)
+    for b in range(w.num_seqs):
+        L = int(w.seq_lens[b])
+        ko = torch.empty((L, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+        vo = torch.empty_like(ko)
+        B.pa_gather_kv(st.key_cache, st.value_cache, st.block_tables[b], L, ko, vo)
+        j = np.arange(L)
+        rows = w.block_tables[b, j // 16]
+        assert np.array_equal(bf16_to_numpy_bits(ko), kc[rows, j % 16])
+        assert np.array_equal(bf16_to_numpy_bits(vo), vc[rows, j % 16])
+    assert B.pa_debug_status() == 0
+
+
+def test_out_of_range_slot_is_flagged_and_skipped():
+    w = W.tiny_decode(seed=1)
+    st = DeviceStep(w)
+    bad = st.slot_mapping.clone()
+    bad[1] = w.num_blocks * w.block_size + 5
+    bad[2] = -1
+    B.pa_reshape_and_cache(st.key, st.value, st.key_cache, st.value_cache, bad)
+    flags = B.pa_debug_status()
+    assert flags & B.FLAG_SLOT_RANGE
+    kc = bf16_to_numpy_bits(st.key_cache).reshape(-1, w.num_kv_heads, w.head_dim)
+    for t in (0, 3):
+        assert np.array_equal(kc[w.slot_mapping[t]], w.key[t])
+    for t in (1, 2):
+        assert np.array_equal(kc[w.slot_mapping[t]], w.key_cache.reshape(-1, w.num_kv_heads, w.head_dim)[w.slot_mapping[t]])
+    assert B.pa_debug_status() == 0  # cleared by the previous read
+
+
+def test_out_of_range_block_id_is_flagged():
+    w = W.make_workload("badblock", seed=8, **SMALL_CASES["decode_g4_d64"])
+    st = DeviceStep(w)
+    st.reshape_and_cache()
+    st.block_tables[1, 0] = w.num_blocks + 3
+    st.attention()
+    flags = B.pa_debug_status()
+    assert flags & B.FLAG_BLOCK_RANGE
+    out = bf16_to_float64(st.out)
+    assert np.isfinite(out[0]).all()
+
+
+def test_inconsistent_lengths_are_flagged():
+    w = W.make_workload("badlen", seed=8, **SMALL_CASES["decode_g4_d64"])
+    st = DeviceStep(w)
+    st.reshape_and_cache()
+    st.seq_lens[0] = w.max_seq_len + 1  # above the host bound
+    st.attention()
+    assert B.pa_debug_status() & B.FLAG_LENGTHS
+
+
+def test_host_side_errors():
+    w = W.tiny_decode(seed=0)
+    st = DeviceStep(w)
+    lib = B._lib()
+    s = torch.cuda.current_stream().cuda_stream
+    base = [st.q.data_ptr(), st.q.stride(0), st.key_cache.data_ptr(), st.value_cache.data_ptr(),
+            st.block_tables.data_ptr(), st.block_tables.shape[1], st.seq_lens.data_ptr(),
+            st.query_start_loc.data_ptr(), w.num_seqs, w.total_q, w.max_query_len, w.max_seq_len,
+            w.num_heads, w.num_kv_heads, w.head_dim, 16, w.num_blocks, w.scale, st.out.data_ptr(),
+            st.workspace.data_ptr(), st.workspace.numel(), 0, s]
+
+    def call(**chg):
+        a = list(base)
+        names = ["q", "qs", "kc", "vc", "bt", "mb", "sl", "qsl", "B", "T", "mq", "ms", "H", "Hkv", "D", "bs",
+                 "nb", "scale", "out", "ws", "wsb", "dtype", "stream"]
+        for k, v in chg.items():
+            a[names.index(k)] = v
+        return lib.pa_attention_varlen(*a)
+
+    assert call() == 0
+    assert call(q=None) == -1
+    assert call(D=96) == -3
+    assert call(bs=32) == -3
+    assert call(Hkv=3) == -2
+    assert call(dtype=1) == -3
+    assert call(wsb=16) == -5
+    assert call(out=st.out.data_ptr() + 2) == -4
+    assert call(scale=float("nan")) == -2
+    torch.cuda.synchronize()
+    assert B.pa_debug_status() == 0
+
+
+# --------------------------------------------------------------------------
+# Full-size named workloads, in the launch configuration the benchmark times,
+# checked at sampled outputs (the oracle computes them one by one).
+# --------------------------------------------------------------------------
+
+def _sample_pairs(w: W.Workload, n: int, rng):
+    """Half the samples are first/last rows of random requests, half random rows."""
+    qsl = w.query_start_loc
+    edges = set()
+    for b in range(w.num_seqs):
+        if qsl[b + 1] > qsl[b]:
+            edges.add(int(qsl[b]))
+            edges.add(int(qsl[b + 1] - 1))
+    edges = np.array(sorted(edges), dtype=np.int64)
+    pick = rng.choice(edges, size=min(n // 2, edges.size), replace=False)
+    extra = rng.integers(0, w.total_q, size=n - pick.size)
+    tokens = np.concatenate([pick, extra]).astype(np.int64)
+    heads = rng.integers(0, w.num_heads, size=tokens.size).astype(np.int32)
+    return tokens, heads
+
+
+@pytest.mark.parametrize("name", ["mha_decode", "gqa_decode", "long_decode", "mixed_step"])
+def test_named_full_size_sampled(oracle, name):
+    w = W.by_name(name, seed=0)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert B.pa_debug_status() == 0
+    out = bf16_to_float64(st.out)
+    assert np.isfinite(out).all()
+    # scatter: every written row equals its new K/V row; the rest of the cache is unchanged
+    kc = bf16_to_numpy_bits(st.key_cache).reshape(-1, w.num_kv_heads, w.head_dim)
+    assert np.array_equal(kc[w.slot_mapping], w.key)
+    vc = bf16_to_numpy_bits(st.value_cache).reshape(-1, w.num_kv_heads, w.head_dim)
+    assert np.array_equal(vc[w.slot_mapping], w.value)
+    untouched = np.ones(kc.shape[0], dtype=bool)
+    untouched[w.slot_mapping] = False
+    assert np.array_equal(kc[untouched], w.key_cache.reshape(kc.shape)[untouched])
+    # attention at sampled (token, head) pairs
+    kc_full = kc.reshape(w.key_cache.shape)
+    vc_full = vc.reshape(w.value_cache.shape)
+    tokens, heads = _sample_pairs(w, 96, np.random.default_rng(1))
+    ref = oracle.attention_sampled(w.q, kc_full, vc_full, w.block_tables, w.seq_lens, w.query_start_loc,
+                                   w.num_heads, w.scale, tokens, heads)
+    assert_attention_close(out[tokens, heads], ref, name)

@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports what include/pagedattn.h declares (no GPU)."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_cache_55_gb300 import binding as B
+from paged_kv_cache_55_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load_library()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pa_reshape_and_cache", "pa_attention_varlen", "pa_attention_workspace_size"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIBRARY], capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, f"{name} declared in include/ but not exported"
+        assert hasattr(lib, name)
+    assert set(B.SIGNATURES) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = lib.pa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.pa_status_string(5).decode() == "unknown status"
+
+
+def test_workspace_sizes_are_host_arithmetic(lib):
+    # GQA decode at batch 256 with lengths up to 8192: partials for every split
+    n = lib.pa_attention_workspace_size(256, 256, 1, 8192, 32, 8, 128, 16)
+    assert n > 256 * 8 * 16 * 8 * 128 * 4
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 16) > 0
+    # unsupported or inconsistent sizes give 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 96, 16) == 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 3, 64, 16) == 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 32) == 0
+    assert lib.pa_attention_workspace_size(4, 4, 40, 33, 4, 1, 64, 16) == 0
+    pt, mp = B.pa_attention_plan_info(8, 32768, 64, 8)
+    assert pt % 16 == 0 and mp == -(-32768 // pt)
+
+
+def test_validation_rejects_before_any_cuda_call(lib):
+    # dtype and size errors return before the library touches the device
+    args = [None, 0, None, None, None, 0, None, None, 1, 1, 1, 1, 4, 1, 64, 16, 1, 1.0, None, None, 0]
+    assert lib.pa_attention_varlen(*args, 1, None) == -3       # dtype
+    assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 7, None) == -3
+    assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, -1, 1, 64, 16, 1, 0, None) == -2
+    assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 0, 1, 64, 16, 1, 0, None) == 0
+    assert lib.pa_attention_set_timing_events(None, None) == 0
+    assert lib.pa_launch_count() == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        B.load_library(str(tmp_path / "libpagedattn.so"))
+
+
+def test_product_code_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_55_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "liboracle" not in text and "oracle.c" not in text, f
