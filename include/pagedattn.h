@@ -197,6 +197,43 @@ uint64_t pa_launch_count(void);
  */
 pa_status pa_attention_set_timing_events(void *start, void *stop);
 
+/*
+ * Attention without a caller-provided workspace, for callers that cannot
+ * allocate device memory: code running inside a CUDA graph capture that
+ * forbids allocation, plugins of a host framework that owns every allocation,
+ * or allocators that are locked down in production. The pages describe no
+ * such call; it exists only for these callers.
+ *
+ * Same arguments and result as pa_attention_varlen, minus `workspace` and
+ * `workspace_bytes`: the split-KV plan and partials live in a scratch array
+ * compiled into the library (PA_STATIC_WORKSPACE_BYTES bytes of device
+ * memory, held on every GPU that loads the library until the process exits).
+ * The call itself allocates nothing.
+ *
+ *   - A problem whose pa_attention_workspace_size() exceeds
+ *     PA_STATIC_WORKSPACE_BYTES is rejected with PA_ERR_WORKSPACE before
+ *     anything is launched; use pa_attention_varlen for it.
+ *   - The first call on a device looks up that device's copy of the scratch
+ *     array (with the device current); make that first call before any
+ *     stream capture. Later calls only read the cached address.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind. Nothing in it needs to start at zero (the planning kernel
+ *     rewrites every word that later kernels read), but calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on the array and produce garbage. Order such calls on one stream.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (32u << 20)
+
+pa_status pa_attention_varlen_static(const void *q, int64_t q_token_stride,
+                                     const void *key_cache, const void *value_cache,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *seq_lens, const int32_t *query_start_loc,
+                                     int32_t num_seqs, int32_t total_q_tokens,
+                                     int32_t max_query_len, int32_t max_seq_len,
+                                     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t block_size, int64_t num_blocks, float scale,
+                                     void *out, int32_t dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -46,7 +46,12 @@ SIGNATURES = {
     "pa_debug_status": ([_P, _P], ctypes.c_int),
     "pa_launch_count": ([], ctypes.c_uint64),
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
+    "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                    _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
 }
+
+# Size of the library's built-in scratch array used by pa_attention_varlen_static.
+PA_STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 def load_library(path: str = LIBRARY) -> ctypes.CDLL:
@@ -148,6 +153,25 @@ def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: t
                                       nb, float(scale), out.data_ptr(), workspace.data_ptr(),
                                       workspace.numel() * workspace.element_size(), PA_BF16, _stream(stream)),
            "pa_attention_varlen")
+
+
+def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                               block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                               max_query_len: int, max_seq_len: int, scale: float, out: torch.Tensor,
+                               stream=None) -> None:
+    """pa_attention_varlen without a workspace argument, for callers that cannot allocate: the
+    library's built-in scratch array (PA_STATIC_WORKSPACE_BYTES) is used instead. Calls on one device
+    share that array, so calls on different streams must not overlap."""
+    _need(q, "q", torch.bfloat16)
+    _need(out, "out", torch.bfloat16)
+    T, H, D = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    B = seq_lens.shape[0]
+    _check(_lib().pa_attention_varlen_static(q.data_ptr(), q.stride(0), key_cache.data_ptr(),
+                                             value_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                                             seq_lens.data_ptr(), query_start_loc.data_ptr(), B, T, max_query_len,
+                                             max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), PA_BF16,
+                                             _stream(stream)), "pa_attention_varlen_static")
 
 
 def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor,
