@@ -65,7 +65,8 @@ enum {
     PA_FLAG_BLOCK_RANGE = 1u << 1,  /* a block_tables entry that must be read is outside [0, num_blocks) */
     PA_FLAG_LENGTHS = 1u << 2,      /* seq_len < query_len, seq_len > max_seq_len, query_len > max_query_len,
                                        or seq_len > max_blocks_per_seq * block_size */
-    PA_FLAG_QUERY_LOC = 1u << 3     /* query_start_loc not non-decreasing from 0 to total_q_tokens */
+    PA_FLAG_QUERY_LOC = 1u << 3,    /* query_start_loc not non-decreasing from 0 to total_q_tokens */
+    PA_FLAG_TIMEOUT = 1u << 4       /* a kernel gave up waiting for its own data copy (bounded wait) */
 };
 
 /*

@@ -22,7 +22,7 @@ STATUS = {
     0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_DIMS", -3: "PA_ERR_UNSUPPORTED", -4: "PA_ERR_ALIGN",
     -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_LAUNCH", -7: "PA_ERR_DEVICE_BOUNDS", -8: "PA_ERR_CUDA",
 }
-FLAG_SLOT_RANGE, FLAG_BLOCK_RANGE, FLAG_LENGTHS, FLAG_QUERY_LOC = 1, 2, 4, 8
+FLAG_SLOT_RANGE, FLAG_BLOCK_RANGE, FLAG_LENGTHS, FLAG_QUERY_LOC, FLAG_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class PagedAttnError(RuntimeError):

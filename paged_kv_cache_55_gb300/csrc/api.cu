@@ -1,6 +1,7 @@
 // C ABI of libpagedattn.so (declared in include/pagedattn.h): argument
 // validation, per-device state, and dispatch to the kernels' launchers.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -149,6 +150,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   if (!std::isfinite(scale)) return PA_ERR_DIMS;
   if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
   if (max_query_len == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_DIMS;
+  if (num_blocks > INT32_MAX / block_size) return PA_ERR_UNSUPPORTED;  // cache rows are int32 TMA coordinates
   if (static_cast<int64_t>(max_query_len) > total_q_tokens) return PA_ERR_DIMS;
   if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !query_start_loc || !out)
     return PA_ERR_NULL;

@@ -15,29 +15,35 @@
 // results by their log-sum-exp is Flash-Decoding, which the LLM-infra reading
 // map ("lpnh.cn/news/2436702", §6) names as FlashAttention's follow-up.
 //
-// Design (one CTA of 4 warps per work item):
-//   * A work item is (request, KV head, group of up to 8/G query rows,
-//     partition of keys). The item's 8 "columns" are (query row, head of the
-//     GQA group) pairs, so one pass over a KV block serves the whole group:
-//     each K/V byte is read from HBM once per step.
+// Design:
+//   * A work unit is (request, KV head, group of up to 8/G query rows,
+//     partition of keys). Its 8 "columns" are (query row, head of the GQA
+//     group) pairs, so one pass over a KV block serves the whole group: each
+//     K/V byte is read from HBM once per step.
+//   * Every warp is an independent pipeline. It takes units from a global
+//     counter, and stages the (block, KV head) tiles of K and V with TMA
+//     (cp.async.bulk.tensor, 128-byte swizzle) into its own ring of shared
+//     memory slots, each completed through an mbarrier. The ring runs ahead
+//     across unit boundaries, so the HBM stream does not drain between units.
+//     No CTA-wide barrier is taken after start-up.
 //   * Scores are computed transposed, S^T[16 keys x 8 columns] = K Q^T, with
-//     mma.sync m16n8k16 (bf16 in, fp32 accumulate); the probabilities are
-//     moved into the B-operand layout with movmatrix and O^T += V^T P^T uses a
-//     second mma (P enters as a bf16 hi + lo pair, two mmas, so the weights keep
-//     ~16 significant bits). The tensor pipe only removes instruction pressure: the
-//     kernel is bound by HBM bandwidth.
-//   * K/V blocks are staged into shared memory with 16-byte cp.async through
-//     the block table (a 3-stage ring of 4 blocks, one block per warp), with
-//     an XOR swizzle so ldmatrix reads are free of bank conflicts. Tokens
-//     past the partition end are zero-filled, so stale or NaN cache contents
-//     never reach the arithmetic; masked scores are selected to -inf, never
-//     multiplied by zero.
+//     mma.sync m16n8k16 (bf16 in, fp32 accumulate); movmatrix moves the
+//     probabilities into the B-operand layout and O^T += V^T P^T is a second
+//     mma, with P as a bf16 hi + lo pair so the weights keep ~16 significant
+//     bits. The tensor pipe only removes instruction pressure: the kernel is
+//     bound by HBM bandwidth.
+//   * The last block of a request may hold stale or NaN rows past seq_len:
+//     the warp zeroes those V rows in its slot before use, and masked scores
+//     are selected to -inf, never multiplied by zero.
 //   * Online softmax per column in the log2 domain (scale folded with log2 e),
-//     max reductions by warp shuffles; the 4 warps' states are merged in
-//     shared memory at the end of the item.
-//   * Items of a split request write fp32 (o, lse) partials; the merge kernel
+//     max reductions by warp shuffles.
+//   * Units of a split request write fp32 (o, lse) partials; the merge kernel
 //     combines them: lse = log2 sum 2^lse_p, o = sum 2^(lse_p - lse) o_p.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <float.h>
+
+#include <mutex>
 
 #include "pa_common.cuh"
 #include "pa_launch.h"
@@ -46,10 +52,9 @@ namespace pa {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
-constexpr int kBlocksPerStage = kWarps;  // one 16-token block per warp per stage
+constexpr int kCols = 8;                         // (query row, head) columns per unit
+constexpr int kSmemBudget = 192 * 1024;          // ring bytes per CTA
+constexpr uint64_t kWaitTimeoutNs = 2000000000;  // 2 s: a TMA never takes this long
 
 struct PlanParams {
   const int32_t *seq_lens;
@@ -62,18 +67,17 @@ struct PlanParams {
   int32_t rows_per_item;  // 8 / G
   int32_t part_tokens;
   int32_t max_items;
-  int32_t *item_start;  // [num_seqs + 1]
-  int32_t *nparts;      // [num_seqs], 0 = request produces nothing
-  int4 *items;          // [2 * max_items]
-  int32_t *item_count;  // [1]
+  int32_t *class_start;   // [3][num_seqs + 1] prefix sums of the per-class item counts
+  int32_t *nparts;        // [num_seqs], 0 = request produces nothing
+  int4 *items;            // [2 * max_items]
+  int32_t *item_count;    // [1]
+  int32_t *work_counter;  // [1], zeroed here, consumed by the attention kernel
   unsigned int *status;
 };
 
 struct AttnParams {
   const bf16 *q;
   int64_t q_stride;
-  const bf16 *key_cache;
-  const bf16 *value_cache;
   const int32_t *block_tables;
   int32_t max_blocks_per_seq;
   int32_t num_heads;
@@ -83,6 +87,7 @@ struct AttnParams {
   bf16 *out;
   const int4 *items;
   const int32_t *item_count;
+  int32_t *work_counter;
   int32_t max_parts;
   float *part_o;    // [num_seqs][Hkv][max_parts][8][D]
   float *part_lse;  // [num_seqs][Hkv][max_parts][8]
@@ -109,6 +114,9 @@ __device__ __forceinline__ float ex2(float x) {
 // ---------------------------------------------------------------------------
 // Planning: per request, validate the lengths, count work items, scan, and
 // write one 32-byte record per item. One CTA; no host synchronisation needed.
+// Items are grouped by size so that the attention kernel's dynamic queue
+// hands out the long ones first: class 0 = more keys than a partition,
+// class 1 = exactly a partition, class 2 = fewer.
 // Record: {b, first query token, rows, position of first row},
 //         {key begin, key end, partition (-1 = whole range), 0}.
 // ---------------------------------------------------------------------------
@@ -134,325 +142,402 @@ __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0
   return groups * np;
 }
 
+// Keys [kb, ke) of item k of a request, and its record fields.
+struct ItemShape {
+  int r0, rows, pos0, kb, ke, part;
+};
+__device__ __forceinline__ ItemShape item_shape(const PlanParams &p, int k, int np, int ql, int L) {
+  ItemShape s;
+  const int g = k / np, part = k - g * np;
+  s.r0 = g * p.rows_per_item;
+  s.rows = min(p.rows_per_item, ql - s.r0);
+  s.pos0 = (L - ql) + s.r0;
+  s.kb = 0;
+  s.ke = s.pos0 + s.rows;  // the group's last row sees keys < pos0 + rows
+  s.part = -1;
+  if (np > 1) {
+    s.kb = part * p.part_tokens;
+    s.ke = min(L, s.kb + p.part_tokens);
+    s.part = part;
+  }
+  return s;
+}
+__device__ __forceinline__ int size_class(int len, int part_tokens) {
+  return len > part_tokens ? 0 : (len == part_tokens ? 1 : 2);
+}
+
+// Exclusive scan of one int per thread over the 1024-thread block; the block
+// total goes to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int excl = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+  *total = warp_tot[31];
+  __syncthreads();
+  return excl;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
   __shared__ int warp_tot[32];
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry = 0;
+  __shared__ int carry[3];
+  const int tid = threadIdx.x;
+  const int stride = p.num_seqs + 1;
+  if (tid < 3) carry[tid] = 0;
+  if (tid == 0) p.work_counter[0] = 0;
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int b = base + tid;
-    int cnt = 0;
+    int cnt[3] = {0, 0, 0};
     if (b < p.num_seqs) {
       int q0, ql, L, np;
-      cnt = request_shape(p, b, q0, ql, L, np);
+      const int n = request_shape(p, b, q0, ql, L, np);
       p.nparts[b] = np;
-    }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int t = warp_tot[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, t, o);
-        if (lane >= o) t += v;
+      for (int k = 0; k < n; ++k) {
+        const ItemShape s = item_shape(p, k, np, ql, L);
+        ++cnt[size_class(s.ke - s.kb, p.part_tokens)];
       }
-      warp_tot[lane] = t;  // inclusive over warps
     }
-    __syncthreads();
-    const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0);
-    if (b < p.num_seqs) p.item_start[b] = before + incl - cnt;
-    __syncthreads();
-    if (tid == 0) carry += warp_tot[31];
-    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      int tot;
+      const int excl = block_exclusive_scan(cnt[c], warp_tot, &tot);
+      if (b < p.num_seqs) p.class_start[c * stride + b] = carry[c] + excl;
+      __syncthreads();
+      if (tid == 0) carry[c] += tot;
+      __syncthreads();
+    }
   }
+  if (tid < 3) p.class_start[tid * stride + p.num_seqs] = carry[tid];
   if (tid == 0) {
-    int total = carry;
+    int total = carry[0] + carry[1] + carry[2];
     if (total > p.max_items) {
       flag_error(p.status, PA_FLAG_LENGTHS);
       total = p.max_items;
     }
-    p.item_start[p.num_seqs] = carry;
     p.item_count[0] = total;
   }
   __syncthreads();
+  const int base1 = carry[0], base2 = carry[0] + carry[1];
   for (int b = tid; b < p.num_seqs; b += 1024) {
     const int np = p.nparts[b];
     if (np == 0) continue;
     const int q0 = __ldg(p.query_start_loc + b);
     const int ql = __ldg(p.query_start_loc + b + 1) - q0;
     const int L = __ldg(p.seq_lens + b);
-    const int ctx = L - ql;
-    const int first = p.item_start[b];
-    const int cnt = p.item_start[b + 1] - first;
-    for (int k = 0; k < cnt; ++k) {
-      const int idx = first + k;
-      if (idx >= p.max_items) break;
-      const int g = k / np, part = k - g * np;
-      const int r0 = g * p.rows_per_item;
-      const int rows = min(p.rows_per_item, ql - r0);
-      const int pos0 = ctx + r0;
-      int kb = 0, ke = pos0 + rows;  // the item's last row sees keys < pos0 + rows
-      if (np > 1) {
-        kb = part * p.part_tokens;
-        ke = min(L, kb + p.part_tokens);
-      }
-      p.items[2 * idx] = make_int4(b, q0 + r0, rows, pos0);
-      p.items[2 * idx + 1] = make_int4(kb, ke, np > 1 ? part : -1, 0);
+    int next[3] = {p.class_start[b], base1 + p.class_start[stride + b], base2 + p.class_start[2 * stride + b]};
+    const int n = ((ql + p.rows_per_item - 1) / p.rows_per_item) * np;
+    for (int k = 0; k < n; ++k) {
+      const ItemShape s = item_shape(p, k, np, ql, L);
+      const int idx = next[size_class(s.ke - s.kb, p.part_tokens)]++;
+      if (idx >= p.max_items) continue;
+      p.items[2 * idx] = make_int4(b, q0 + s.r0, s.rows, s.pos0);
+      p.items[2 * idx + 1] = make_int4(s.kb, s.ke, s.part, 0);
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Split-KV attention. One CTA (4 warps) per work item, persistent over items.
+// Split-KV attention: one independent TMA pipeline per warp.
 // ---------------------------------------------------------------------------
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) splitkv_attention_kernel(const AttnParams p) {
-  constexpr int kCols = 8;
-  constexpr int CH = D / 8;                                // 16-byte chunks per row
-  constexpr int TILE = kBlockSize * D;                     // elements of one block tile
-  constexpr int STAGE = 2 * kBlocksPerStage * TILE;        // K tiles then V tiles
-  constexpr int MT = D / 16;                               // k-steps of QK^T, m-tiles of O^T
-  constexpr int RED_LD = D + 4;                            // padded row of the merge buffer
-  static_assert(kWarps * kCols * RED_LD * 4 <= kStages * STAGE * 2, "merge buffer must fit the ring");
+struct Unit {
+  int valid, b, row0, nrows, pos0, kv_begin, kv_end, part, kvh, kb0, kb1;
+};
 
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  bf16 *ring = reinterpret_cast<bf16 *>(smem_raw);
-  float *red_o = reinterpret_cast<float *>(smem_raw);  // used only while the ring is empty
-  __shared__ float red_m[kWarps][kCols];
-  __shared__ float red_l[kWarps][kCols];
+__device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units, int lane) {
+  int u = 0;
+  if (lane == 0) u = atomicAdd(p.work_counter, 1);
+  u = __shfl_sync(0xffffffffu, u, 0);
+  Unit U;
+  U.valid = u < total_units;
+  if (!U.valid) return U;
+  const int item = u / p.num_kv_heads;
+  U.kvh = u - item * p.num_kv_heads;
+  const int4 r0 = __ldg(p.items + 2 * item);
+  const int4 r1 = __ldg(p.items + 2 * item + 1);
+  U.b = r0.x;
+  U.row0 = r0.y;
+  U.nrows = r0.z;
+  U.pos0 = r0.w;
+  U.kv_begin = r1.x;
+  U.kv_end = r1.y;
+  U.part = r1.z;
+  U.kb0 = U.kv_begin / kBlockSize;
+  U.kb1 = (U.kv_end + kBlockSize - 1) / kBlockSize;
+  return U;
+}
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+template <int D>
+struct TileGeom {
+  static constexpr int HALVES = D / 64;                // 64-element (128-byte) swizzle atoms per row
+  static constexpr int HALF_BYTES = kBlockSize * 128;  // 16 rows x 128 B
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int SLOT_BYTES = 2 * TILE_BYTES;  // K tile then V tile
+  // Byte offset of 16-byte chunk c (of D/8) of row r in a TMA SW128 tile.
+  static __device__ __forceinline__ uint32_t off(int r, int c) {
+    return (c >> 3) * HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  }
+};
+
+template <int D, int G, int NWARPS>
+__global__ void __launch_bounds__(NWARPS * 32, 1)
+    splitkv_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const AttnParams p) {
+  using T = TileGeom<D>;
+  constexpr int S = kSmemBudget / (NWARPS * T::SLOT_BYTES);  // ring slots per warp
+  static_assert(S >= 2, "ring needs at least two slots");
+  constexpr int MT = D / 16;
+
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[NWARPS][S];
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < NWARPS * S) mbar_init(smem_u32(&bars[0][0] + threadIdx.x), 1);
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+  fence_mbar_init();
+  __syncthreads();
+
   const int Hkv = p.num_kv_heads;
-  const int64_t total_work = static_cast<int64_t>(__ldg(p.item_count)) * Hkv;
+  const int total_units = __ldg(p.item_count) * Hkv;
+  const uint32_t my_ring = ring + warp * S * T::SLOT_BYTES;
 
-  for (int64_t wk = blockIdx.x; wk < total_work; wk += gridDim.x) {
-    const int item = static_cast<int>(wk / Hkv);
-    const int kvh = static_cast<int>(wk - static_cast<int64_t>(item) * Hkv);
-    const int4 r0 = __ldg(p.items + 2 * item);
-    const int4 r1 = __ldg(p.items + 2 * item + 1);
-    const int b = r0.x, row0 = r0.y, nrows = r0.z, pos0 = r0.w;
-    const int kv_begin = r1.x, kv_end = r1.y, part = r1.z;
-    const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  // Producer side (lane 0 issues): stage block kb of unit U into ring slot seq % S.
+  auto issue = [&](const Unit &U, int kb, uint32_t seq) {
+    if (lane == 0) {
+      const uint32_t slot = seq % S;
+      const uint32_t bar = smem_u32(&bars[warp][slot]);
+      const uint32_t dst = my_ring + slot * T::SLOT_BYTES;
+      const int phys = __ldg(p.block_tables + static_cast<int64_t>(U.b) * p.max_blocks_per_seq + kb);
+      int z;
+      if (phys < 0 || phys >= p.num_blocks) {
+        flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+        z = -kBlockSize;  // entirely outside the tensor: TMA fills zeros
+      } else {
+        z = phys * kBlockSize;
+      }
+      mbar_arrive_expect_tx(bar, T::SLOT_BYTES);
+#pragma unroll
+      for (int h = 0; h < T::HALVES; ++h) {
+        tma_load_3d(dst + h * T::HALF_BYTES, &kmap, bar, h * 64, U.kvh, z);
+        tma_load_3d(dst + T::TILE_BYTES + h * T::HALF_BYTES, &vmap, bar, h * 64, U.kvh, z);
+      }
+    }
+  };
 
-    // B operand of S^T = K Q^T: column n = lane / 4 is (query row n / G, head n % G).
+  Unit cur = fetch_unit(p, total_units, lane);
+  Unit nxt;
+  nxt.valid = 0;
+  bool have_nxt = false;
+  int p_unit = 0;  // which unit the producer is issuing: 0 = cur, 1 = nxt
+  int p_kb = cur.kb0;
+  uint32_t issued = 0, consumed = 0;
+
+  // Issue blocks in stream order (cur's, then nxt's) while fewer than `limit` are issued.
+  auto produce = [&](uint32_t limit) {
+    while (issued < limit) {
+      if (p_unit == 0) {
+        if (!cur.valid) break;
+        if (p_kb < cur.kb1) {
+          issue(cur, p_kb++, issued++);
+          continue;
+        }
+        if (!have_nxt) {
+          nxt = fetch_unit(p, total_units, lane);
+          have_nxt = true;
+        }
+        p_unit = 1;
+        p_kb = nxt.kb0;
+        continue;
+      }
+      if (nxt.valid && p_kb < nxt.kb1) {
+        issue(nxt, p_kb++, issued++);
+        continue;
+      }
+      break;  // the producer runs at most one unit ahead
+    }
+  };
+
+  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row for K (A operand)
+  const int vrow = (lane & 7) + (lane >> 4) * 8;        // ldmatrix row for V (transposed A)
+
+  while (cur.valid) {
+    // ---- per-unit set-up: q fragments (B operand of S^T = K Q^T), causal limits ----
     uint32_t qf[MT][2];
     {
       const int n = lane >> 2, qi = n / G, g = n % G;
-      const bool ok = qi < nrows;
-      const bf16 *qp = p.q + static_cast<int64_t>(row0 + (ok ? qi : 0)) * p.q_stride +
-                       static_cast<int64_t>(kvh * G + g) * D + 2 * (lane & 3);
+      const bool ok = qi < cur.nrows;
+      const bf16 *qp = p.q + static_cast<int64_t>(cur.row0 + (ok ? qi : 0)) * p.q_stride +
+                       static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
         qf[kk][0] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
         qf[kk][1] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 8)) : 0u;
       }
     }
-    // Keys j < lim[e] are visible to this thread's accumulator column 2*(lane%4)+e.
-    int lim[2];
+    int lim[2];  // keys j < lim[e] are visible to accumulator column 2*(lane%4)+e
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int qi = (2 * (lane & 3) + e) / G;
-      lim[e] = qi < nrows ? min(pos0 + qi + 1, kv_end) : kv_begin;
+      lim[e] = qi < cur.nrows ? min(cur.pos0 + qi + 1, cur.kv_end) : cur.kv_begin;
     }
-
     float o[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
 
-    const int kb0 = kv_begin / kBlockSize;
-    const int kb1 = (kv_end + kBlockSize - 1) / kBlockSize;
-    const int nst = (kb1 - kb0 + kBlocksPerStage - 1) / kBlocksPerStage;
-
-    auto issue = [&](int s) {
-      bf16 *st = ring + (s % kStages) * STAGE;
-      constexpr int PER = 2 * kBlocksPerStage * kBlockSize * CH;
-#pragma unroll 4
-      for (int i = tid; i < PER; i += kThreads) {
-        const int c = i % CH;
-        const int row = (i / CH) % kBlockSize;
-        const int t2 = i / (CH * kBlockSize);
-        const int blk = t2 >> 1, isv = t2 & 1;
-        const int kb = kb0 + s * kBlocksPerStage + blk;
-        if (kb < kb1) {
-          int phys = __ldg(table + kb);
-          int bytes = (kb * kBlockSize + row < kv_end) ? 16 : 0;
-          if (phys < 0 || phys >= p.num_blocks) {
-            if (c == 0 && row == 0 && isv == 0) flag_error(p.status, PA_FLAG_BLOCK_RANGE);
-            phys = 0;
-            bytes = 0;
-          }
-          const bf16 *src = (isv ? p.value_cache : p.key_cache) +
-                            ((static_cast<int64_t>(phys) * kBlockSize + row) * Hkv + kvh) * D + c * 8;
-          bf16 *dst = st + isv * kBlocksPerStage * TILE + blk * TILE + swz(row, c, D);
-          cp_async_16(smem_u32(dst), src, bytes);
-        }
+    for (int kb = cur.kb0; kb < cur.kb1; ++kb) {
+      produce(consumed + S);
+      const uint32_t slot = consumed % S;
+      const bool landed = mbar_wait_bounded(smem_u32(&bars[warp][slot]), (consumed / S) & 1u, kWaitTimeoutNs);
+      if (!__all_sync(0xffffffffu, landed)) {  // leave together, never with a diverged warp
+        if (lane == 0) flag_error(p.status, PA_FLAG_TIMEOUT);
+        return;
       }
-    };
+      const uint32_t kt = my_ring + slot * T::SLOT_BYTES;
+      const uint32_t vt = kt + T::TILE_BYTES;
+      const int valid_rows = min(kBlockSize, cur.kv_end - kb * kBlockSize);
+      if (valid_rows < kBlockSize) {
+        // rows past the request's last key may hold anything (even NaN): zero them in V
+        const int n = (kBlockSize - valid_rows) * (D / 8);
+        for (int i = lane; i < n; i += 32) {
+          const int r = valid_rows + i / (D / 8), c = i % (D / 8);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + T::off(r, c)), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();  // order these generic writes before the slot's next TMA fill
+        __syncwarp();
+      }
 
+      // S^T = K Q^T over D, two independent accumulator chains
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < nst) issue(s);
-      cp_async_commit();
+      for (int kk = 0; kk < MT; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kt + T::off(arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+        if (kk & 1)
+          mma_16816(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        else
+          mma_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+      }
+      const int t0 = kb * kBlockSize + (lane >> 2), t1 = t0 + 8;
+      const float x0 = t0 < lim[0] ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
+      const float x1 = t0 < lim[1] ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
+      const float x2 = t1 < lim[0] ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
+      const float x3 = t1 < lim[1] ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
+      const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
+      const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
+      l[0] = l[0] * al0 + p0 + p2;
+      l[1] = l[1] * al1 + p1 + p3;
+      m[0] = mn0;
+      m[1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      // P^T (keys x columns) -> B operand by transposition; P as bf16 hi + lo.
+      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+      const uint32_t l01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+      const uint32_t l23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+      const uint32_t b0 = movmatrix_t(h01), b1 = movmatrix_t(h23);
+      const uint32_t c0 = movmatrix_t(l01), c1 = movmatrix_t(l23);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+        mma_16816(o[mt], a0, a1, a2, a3, b0, b1);
+        mma_16816(o[mt], a0, a1, a2, a3, c0, c1);
+      }
+      __syncwarp();  // every lane is done with this slot before it is refilled
+      ++consumed;
     }
 
-    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row for K (A operand)
-    const int vrow = (lane & 7) + (lane >> 4) * 8;        // ldmatrix row for V (transposed A)
-    for (int s = 0; s < nst; ++s) {
-      cp_async_wait<kStages - 2>();
-      __syncthreads();
-      if (s + kStages - 1 < nst) issue(s + kStages - 1);
-      cp_async_commit();
-
-      const int kb = kb0 + s * kBlocksPerStage + warp;
-      if (kb < kb1) {
-        const bf16 *kt = ring + (s % kStages) * STAGE + warp * TILE;
-        const bf16 *vt = kt + kBlocksPerStage * TILE;
-        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < MT; ++kk) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kbase + 2 * swz(arow, 2 * kk + (lane >> 4), D), a0, a1, a2, a3);
-          mma_16816(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-        }
-        const int t0 = kb * kBlockSize + (lane >> 2), t1 = t0 + 8;
-        const float x0 = t0 < lim[0] ? sc[0] * p.scale_log2 : -INFINITY;
-        const float x1 = t0 < lim[1] ? sc[1] * p.scale_log2 : -INFINITY;
-        const float x2 = t1 < lim[0] ? sc[2] * p.scale_log2 : -INFINITY;
-        const float x3 = t1 < lim[1] ? sc[3] * p.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
-        const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-        const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-        l[0] = l[0] * al0 + p0 + p2;
-        l[1] = l[1] * al1 + p1 + p3;
-        m[0] = mn0;
-        m[1] = mn1;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          o[mt][0] *= al0;
-          o[mt][1] *= al1;
-          o[mt][2] *= al0;
-          o[mt][3] *= al1;
-        }
-        // P^T rows (keys) x columns -> B operand (k = key, n = column) by transposition.
-        // P is carried as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)), so the
-        // probabilities enter the fp32 accumulation with ~16 significant bits instead of 8.
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t l01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t l23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        const uint32_t b0 = movmatrix_t(h01), b1 = movmatrix_t(h23);
-        const uint32_t c0 = movmatrix_t(l01), c1 = movmatrix_t(l23);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vbase + 2 * swz(vrow, 2 * mt + ((lane >> 3) & 1), D), a0, a1, a2, a3);
-          mma_16816(o[mt], a0, a1, a2, a3, b0, b1);
-          mma_16816(o[mt], a0, a1, a2, a3, c0, c1);
-        }
-      }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // ---- merge the 4 warps' (m, l, O) per column ----
+    // ---- unit epilogue: normalise and write the output or the partial ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
       l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
     }
-    if (lane < 4) {
-      red_m[warp][2 * lane] = m[0];
-      red_m[warp][2 * lane + 1] = m[1];
-      red_l[warp][2 * lane] = l[0];
-      red_l[warp][2 * lane + 1] = l[1];
-    }
-    __syncthreads();
-    {
-      float f[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = 2 * (lane & 3) + e;
-        float M = red_m[0][c];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red_m[w][c]);
-        const float Ms = M == -INFINITY ? 0.f : M;
-        f[e] = ex2(m[e] - Ms);
-      }
-      float *ro = red_o + warp * kCols * RED_LD;
-      const int c0 = 2 * (lane & 3);
+    const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
+    const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+    if (cur.part < 0) {
+      // transpose the bf16 result so each lane owns two consecutive d of one column
+      const int col = lane >> 2, qi = col / G, g = col % G;
+      bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (qi < cur.nrows ? qi : 0)) * p.num_heads * D +
+                  static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int d = 16 * mt + (lane >> 2);
-        ro[c0 * RED_LD + d] = o[mt][0] * f[0];
-        ro[(c0 + 1) * RED_LD + d] = o[mt][1] * f[1];
-        ro[c0 * RED_LD + d + 8] = o[mt][2] * f[0];
-        ro[(c0 + 1) * RED_LD + d + 8] = o[mt][3] * f[1];
-      }
-    }
-    __syncthreads();
-    {
-      constexpr int TPC = kThreads / kCols;  // threads per column
-      constexpr int EPT = D / TPC;           // elements per thread
-      const int col = tid / TPC, d0 = (tid % TPC) * EPT;
-      const int qi = col / G, g = col % G;
-      if (qi < nrows) {
-        float M = red_m[0][col];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red_m[w][col]);
-        const float Ms = M == -INFINITY ? 0.f : M;
-        float Lc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) Lc += red_l[w][col] * ex2(red_m[w][col] - Ms);
-        const float inv = Lc > 0.f ? 1.f / Lc : 0.f;
-        float acc[EPT];
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-          float s = 0.f;
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) s += red_o[(w * kCols + col) * RED_LD + d0 + e];
-          acc[e] = s * inv;
+        const uint32_t lo8 = movmatrix_t(pack_bf16x2(o[mt][0] * inv0, o[mt][1] * inv1));
+        const uint32_t hi8 = movmatrix_t(pack_bf16x2(o[mt][2] * inv0, o[mt][3] * inv1));
+        if (qi < cur.nrows) {
+          *reinterpret_cast<uint32_t *>(dst + 16 * mt) = lo8;
+          *reinterpret_cast<uint32_t *>(dst + 16 * mt + 8) = hi8;
         }
-        if (part < 0) {
-          bf16 *dst = p.out + static_cast<int64_t>(row0 + qi) * p.num_heads * D +
-                      static_cast<int64_t>(kvh * G + g) * D + d0;
-          uint32_t pk[EPT / 2];
+      }
+    } else {
+      const int64_t base = ((static_cast<int64_t>(cur.b) * Hkv + cur.kvh) * p.max_parts + cur.part) * kCols;
 #pragma unroll
-          for (int e = 0; e < EPT / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-          if constexpr (EPT == 8) {
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          } else {
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(pk[0], pk[1]);
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * (lane & 3) + e;
+        if (col / G < cur.nrows) {
+          const float inv = e ? inv1 : inv0;
+          float *dst = p.part_o + (base + col) * D + (lane >> 2);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            dst[16 * mt] = o[mt][e] * inv;
+            dst[16 * mt + 8] = o[mt][2 + e] * inv;
           }
-        } else {
-          const int64_t idx = ((static_cast<int64_t>(b) * Hkv + kvh) * p.max_parts + part) * kCols + col;
-          float *dst = p.part_o + idx * D + d0;
-#pragma unroll
-          for (int e = 0; e < EPT; e += 4)
-            *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-          if (tid % TPC == 0) p.part_lse[idx] = Lc > 0.f ? Ms + __log2f(Lc) : -INFINITY;
+          if (lane < 4) {
+            const float lc = e ? l[1] : l[0], mc = e ? m[1] : m[0];
+            p.part_lse[base + col] = lc > 0.f ? mc + __log2f(lc) : -INFINITY;
+          }
         }
       }
     }
-    __syncthreads();  // the merge buffers alias the ring used by the next item
+
+    // ---- advance to the next unit (the producer may already be streaming it) ----
+    if (p_unit == 0) {
+      if (!have_nxt) {
+        nxt = fetch_unit(p, total_units, lane);
+        have_nxt = true;
+      }
+      p_kb = nxt.kb0;
+    }
+    cur = nxt;
+    have_nxt = false;
+    p_unit = 0;
   }
 }
 
@@ -462,7 +547,6 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_attention_kernel(const At
 // ---------------------------------------------------------------------------
 template <int D, int G>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
-  constexpr int kCols = 8;
   constexpr int TPC = 128 / kCols;
   constexpr int EPT = D / TPC;
   const int b = blockIdx.x / p.num_kv_heads;
@@ -512,7 +596,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
 // Host side
 // ---------------------------------------------------------------------------
 
-// Keys per partition. Partitions bound the work of one item, so that a few
+// Keys per partition. Partitions bound the work of one unit, so that a few
 // long requests cannot leave most SMs idle at the end of the step.
 int partition_tokens(int32_t num_seqs, int32_t max_seq_len, int32_t num_kv_heads) {
   (void)num_seqs;
@@ -520,7 +604,6 @@ int partition_tokens(int32_t num_seqs, int32_t max_seq_len, int32_t num_kv_heads
   (void)num_kv_heads;
   return 512;
 }
-
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -536,13 +619,13 @@ bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, in
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.part_tokens - 1) / w.part_tokens : 1;
   const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts +
                         (static_cast<int64_t>(total_q) + w.rows_per_item - 1) / w.rows_per_item + num_seqs;
-  if (items > (1LL << 30)) return false;
+  if (items * num_kv_heads > (1LL << 30)) return false;
   w.max_items = static_cast<int32_t>(items);
-  const size_t nsplit = static_cast<size_t>(num_seqs) * num_kv_heads * w.max_parts * 8;
+  const size_t nsplit = static_cast<size_t>(num_seqs) * num_kv_heads * w.max_parts * kCols;
   size_t off = 0;
-  w.item_start = off; off += align256(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
+  w.item_start = off; off += align256(sizeof(int32_t) * 3 * (static_cast<size_t>(num_seqs) + 1));
   w.nparts = off;     off += align256(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
-  w.item_count = off; off += align256(sizeof(int32_t));
+  w.item_count = off; off += align256(2 * sizeof(int32_t));  // item count, work counter
   w.items = off;      off += align256(sizeof(int4) * 2 * static_cast<size_t>(w.max_items));
   w.part_lse = off;   off += align256(sizeof(float) * nsplit);
   w.part_o = off;     off += align256(sizeof(float) * nsplit * head_dim);
@@ -550,6 +633,39 @@ bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, in
   return true;
 }
 
+// cuTensorMapEncodeTiled from the driver, found once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D view of one cache, [num_blocks * 16 rows][Hkv][D], with a box of
+// 16 rows x 1 head x 64 elements (128 bytes, 128-byte swizzle).
+static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
+                             int32_t head_dim) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, 1, kBlockSize};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kAttnWarps = 8;
 
 template <int D, int G>
 static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, cudaStream_t stream,
@@ -566,11 +682,18 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.rows_per_item = w.rows_per_item;
   pp.part_tokens = w.part_tokens;
   pp.max_items = w.max_items;
-  pp.item_start = reinterpret_cast<int32_t *>(ws + w.item_start);
+  pp.class_start = reinterpret_cast<int32_t *>(ws + w.item_start);
   pp.nparts = reinterpret_cast<int32_t *>(ws + w.nparts);
   pp.items = reinterpret_cast<int4 *>(ws + w.items);
   pp.item_count = reinterpret_cast<int32_t *>(ws + w.item_count);
+  pp.work_counter = pp.item_count + 1;
   pp.status = a.status;
+
+  CUtensorMap kmap, vmap;
+  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D) ||
+      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D))
+    return cudaErrorInvalidValue;
+
   plan_kernel<<<1, 1024, 0, stream>>>(pp);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -579,8 +702,6 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   AttnParams ap;
   ap.q = static_cast<const bf16 *>(a.q);
   ap.q_stride = a.q_stride;
-  ap.key_cache = static_cast<const bf16 *>(a.key_cache);
-  ap.value_cache = static_cast<const bf16 *>(a.value_cache);
   ap.block_tables = a.block_tables;
   ap.max_blocks_per_seq = a.max_blocks_per_seq;
   ap.num_heads = a.num_heads;
@@ -590,25 +711,23 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.out = static_cast<bf16 *>(a.out);
   ap.items = pp.items;
   ap.item_count = pp.item_count;
+  ap.work_counter = pp.work_counter;
   ap.max_parts = w.max_parts;
   ap.part_o = reinterpret_cast<float *>(ws + w.part_o);
   ap.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
   ap.status = a.status;
 
-  constexpr int smem = kStages * 2 * kBlocksPerStage * kBlockSize * D * 2;
-  auto kern = splitkv_attention_kernel<D, G>;
+  constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
+  auto kern = splitkv_attention_kernel<D, G, kAttnWarps>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  int occ = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (occ < 1) occ = 1;
-  int64_t grid = static_cast<int64_t>(a.sm_count) * occ;
-  const int64_t upper = static_cast<int64_t>(w.max_items) * a.num_kv_heads;
-  if (grid > upper) grid = upper;
+  // one CTA per SM; fewer when there are fewer units than warps
+  int64_t grid = a.sm_count;
+  const int64_t units_upper = static_cast<int64_t>(w.max_items) * a.num_kv_heads;
+  if (grid * kAttnWarps > units_upper) grid = (units_upper + kAttnWarps - 1) / kAttnWarps;
   if (grid < 1) grid = 1;
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  kern<<<static_cast<int>(grid), kThreads, smem, stream>>>(ap);
+  kern<<<static_cast<int>(grid), kAttnWarps * 32, smem, stream>>>(kmap, vmap, ap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   ++*launched;
