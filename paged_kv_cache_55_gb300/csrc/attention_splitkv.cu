@@ -37,8 +37,9 @@
 //     are selected to -inf, never multiplied by zero.
 //   * Online softmax per column in the log2 domain (scale folded with log2 e),
 //     max reductions by warp shuffles.
-//   * Units of a split request write fp32 (o, lse) partials; the merge kernel
-//     combines them: lse = log2 sum 2^lse_p, o = sum 2^(lse_p - lse) o_p.
+//   * Units of a split request write fp32 (o, lse) partials; a merge kernel
+//     combines them: lse = log2 sum 2^lse_p, o = sum 2^(lse_p - lse) o_p,
+//     summing the partitions in order (deterministic bits).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <float.h>
@@ -88,22 +89,15 @@ struct AttnParams {
   const int4 *items;
   const int32_t *item_count;
   int32_t *work_counter;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_items;
   int32_t max_parts;
   float *part_o;    // [num_seqs][Hkv][max_parts][8][D]
   float *part_lse;  // [num_seqs][Hkv][max_parts][8]
   unsigned int *status;
 };
 
-struct MergeParams {
-  const int32_t *query_start_loc;
-  const int32_t *nparts;
-  int32_t num_kv_heads;
-  int32_t num_heads;
-  int32_t max_parts;
-  const float *part_o;
-  const float *part_lse;
-  bf16 *out;
-};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -118,12 +112,12 @@ __device__ __forceinline__ float ex2(float x) {
 // hands out the long ones first: class 0 = more keys than a partition,
 // class 1 = exactly a partition, class 2 = fewer.
 // Record: {b, first query token, rows, position of first row},
-//         {key begin, key end, partition (-1 = whole range), 0}.
+//         {key begin, key end, partition (-1 = whole range), partitions of the request}.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0, int &ql, int &L, int &np) {
-  q0 = __ldg(p.query_start_loc + b);
-  const int q1 = __ldg(p.query_start_loc + b + 1);
-  L = __ldg(p.seq_lens + b);
+  q0 = ld_cg(p.query_start_loc + b);
+  const int q1 = ld_cg(p.query_start_loc + b + 1);
+  L = ld_cg(p.seq_lens + b);
   ql = q1 - q0;
   np = 0;
   if (q0 < 0 || ql < 0 || q1 > p.total_q || (b == 0 && q0 != 0)) {
@@ -194,13 +188,90 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
   return excl;
 }
 
+// Exclusive block scan of a 64-bit value (three 21-bit counters packed).
+__device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned long long v,
+                                                                    unsigned long long *warp_tot,
+                                                                    unsigned long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const unsigned long long excl = (warp > 0 ? warp_tot[warp - 1] : 0ull) + incl - v;
+  *total = warp_tot[31];
+  return excl;
+}
+
+constexpr int kPackBits = 21;  // items per class below 2^21 in the one-pass planner
+constexpr unsigned long long kPackMask = (1ull << kPackBits) - 1;
+
+// One pass for batches of at most 1024 requests (one per thread): count the
+// items of each size class, scan the three counts at once, write records.
+__device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
+  __shared__ unsigned long long warp_tot[32];
+  const int b = threadIdx.x;
+  int q0 = 0, ql = 0, L = 0, np = 0, n = 0;
+  unsigned long long packed = 0;
+  if (b < p.num_seqs) {
+    n = request_shape(p, b, q0, ql, L, np);
+    p.nparts[b] = np;
+    for (int k = 0; k < n; ++k) {
+      const ItemShape s = item_shape(p, k, np, ql, L);
+      packed += 1ull << (kPackBits * size_class(s.ke - s.kb, p.part_tokens));
+    }
+  }
+  unsigned long long total;
+  const unsigned long long excl = block_exclusive_scan64(packed, warp_tot, &total);
+  const int t0 = static_cast<int>(total & kPackMask), t1 = static_cast<int>((total >> kPackBits) & kPackMask);
+  const int t2 = static_cast<int>((total >> (2 * kPackBits)) & kPackMask);
+  if (threadIdx.x == 0) {
+    int all = t0 + t1 + t2;
+    if (all > p.max_items) {
+      flag_error(p.status, PA_FLAG_LENGTHS);
+      all = p.max_items;
+    }
+    p.item_count[0] = all;
+  }
+  if (n == 0) return;
+  int next[3] = {static_cast<int>(excl & kPackMask), t0 + static_cast<int>((excl >> kPackBits) & kPackMask),
+                 t0 + t1 + static_cast<int>((excl >> (2 * kPackBits)) & kPackMask)};
+  for (int k = 0; k < n; ++k) {
+    const ItemShape s = item_shape(p, k, np, ql, L);
+    const int idx = next[size_class(s.ke - s.kb, p.part_tokens)]++;
+    if (idx < 0 || idx >= p.max_items) continue;
+    p.items[2 * idx] = make_int4(b, q0 + s.r0, s.rows, s.pos0);
+    p.items[2 * idx + 1] = make_int4(s.kb, s.ke, s.part, np);
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
   __shared__ int warp_tot[32];
   __shared__ int carry[3];
   const int tid = threadIdx.x;
   const int stride = p.num_seqs + 1;
-  if (tid < 3) carry[tid] = 0;
+  griddep_wait();  // inputs may come from the previous kernel of the stream
+  griddep_launch_dependents();
   if (tid == 0) p.work_counter[0] = 0;
+  if (p.num_seqs <= 1024 && p.max_items < static_cast<int>(kPackMask)) {
+    plan_one_pass(p);
+    return;
+  }
+  // larger batches: chunked counting and scans, then a second pass that writes
+  if (tid < 3) carry[tid] = 0;
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int b = base + tid;
@@ -238,28 +309,116 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
   for (int b = tid; b < p.num_seqs; b += 1024) {
     const int np = p.nparts[b];
     if (np == 0) continue;
-    const int q0 = __ldg(p.query_start_loc + b);
-    const int ql = __ldg(p.query_start_loc + b + 1) - q0;
-    const int L = __ldg(p.seq_lens + b);
+    const int q0 = ld_cg(p.query_start_loc + b);
+    const int ql = ld_cg(p.query_start_loc + b + 1) - q0;
+    const int L = ld_cg(p.seq_lens + b);
     int next[3] = {p.class_start[b], base1 + p.class_start[stride + b], base2 + p.class_start[2 * stride + b]};
     const int n = ((ql + p.rows_per_item - 1) / p.rows_per_item) * np;
     for (int k = 0; k < n; ++k) {
       const ItemShape s = item_shape(p, k, np, ql, L);
       const int idx = next[size_class(s.ke - s.kb, p.part_tokens)]++;
-      if (idx >= p.max_items) continue;
+      if (idx < 0 || idx >= p.max_items) continue;
       p.items[2 * idx] = make_int4(b, q0 + s.r0, s.rows, s.pos0);
-      p.items[2 * idx + 1] = make_int4(s.kb, s.ke, s.part, 0);
+      p.items[2 * idx + 1] = make_int4(s.kb, s.ke, s.part, np);
     }
+  }
+}
+
+struct Unit {
+  int valid, skip, b, row0, nrows, pos0, kv_begin, kv_end, part, nparts, kvh, kb0, kb1;
+};
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of the partitions of split requests, after the attention
+// kernel (PDL: launched early, waits for it). One CTA per (request, KV head),
+// one warp per column; each lane owns D/32 outputs and reads the partitions
+// eight at a time with independent loads, keeping a running maximum so one
+// pass suffices. Partitions are summed in order.
+// ---------------------------------------------------------------------------
+struct MergeParams {
+  const int32_t *query_start_loc;
+  const int32_t *nparts;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t num_heads;
+  int32_t max_parts;
+  const float *part_o;
+  const float *part_lse;
+  bf16 *out;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams p) {
+  constexpr int EPL = D / 32;  // outputs per lane: 4 (D=128) or 2 (D=64)
+  griddep_wait();
+  const int b = blockIdx.x / p.num_kv_heads, kvh = blockIdx.x - b * p.num_kv_heads;
+  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int np = ld_cg(p.nparts + b);
+  if (np <= 1 || np > p.max_parts) return;
+  const int q0 = ld_cg(p.query_start_loc + b);
+  const int ql = ld_cg(p.query_start_loc + b + 1) - q0;
+  const int qi = col / G, g = col % G;
+  if (qi >= ql) return;
+  const int64_t base = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.max_parts * kCols + col;
+  // one pass with a running maximum (every lane holds the same values)
+  float M = -INFINITY;
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int k0 = 0; k0 < np; k0 += 8) {
+    float lv[8], ov[8][EPL];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = min(k0 + j, np - 1);
+      lv[j] = ld_cg(p.part_lse + base + k * kCols);
+      const float *src = p.part_o + (base + k * kCols) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const float4 v = ld_cg(reinterpret_cast<const float4 *>(src));
+        ov[j][0] = v.x;
+        ov[j][1] = v.y;
+        ov[j][2] = v.z;
+        ov[j][3] = v.w;
+      } else {
+        const float2 v = ld_cg(reinterpret_cast<const float2 *>(src));
+        ov[j][0] = v.x;
+        ov[j][1] = v.y;
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (k0 + j < np) Mn = fmaxf(Mn, lv[j]);
+    const float Ms = Mn == -INFINITY ? 0.f : Mn;
+    const float r = ex2(M - Ms);  // rescale what was summed so far (0 on the first pack)
+    wsum *= r;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= r;
+    M = Mn;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (k0 + j < np) {
+        const float w = ex2(lv[j] - Ms);
+        wsum += w;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] += w * ov[j][e];
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  bf16 *dst = p.out + static_cast<int64_t>(q0 + qi) * p.num_heads * D + static_cast<int64_t>(kvh * G + g) * D +
+              lane * EPL;
+  if constexpr (EPL == 4) {
+    *reinterpret_cast<uint2 *>(dst) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Split-KV attention: one independent TMA pipeline per warp.
 // ---------------------------------------------------------------------------
-struct Unit {
-  int valid, b, row0, nrows, pos0, kv_begin, kv_end, part, kvh, kb0, kb1;
-};
-
 __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units, int lane) {
   int u = 0;
   if (lane == 0) u = atomicAdd(p.work_counter, 1);
@@ -269,8 +428,8 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   if (!U.valid) return U;
   const int item = u / p.num_kv_heads;
   U.kvh = u - item * p.num_kv_heads;
-  const int4 r0 = __ldg(p.items + 2 * item);
-  const int4 r1 = __ldg(p.items + 2 * item + 1);
+  const int4 r0 = ld_cg(p.items + 2 * item);
+  const int4 r1 = ld_cg(p.items + 2 * item + 1);
   U.b = r0.x;
   U.row0 = r0.y;
   U.nrows = r0.z;
@@ -278,6 +437,21 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   U.kv_begin = r1.x;
   U.kv_end = r1.y;
   U.part = r1.z;
+  U.nparts = r1.w;
+  // A record is trusted only inside the bounds the host passed; anything else
+  // is recorded and the unit becomes empty (no loads, no stores).
+  const bool sane = U.b >= 0 && U.b < p.num_seqs && U.nrows >= 1 && U.nrows <= kCols && U.row0 >= 0 &&
+                    U.row0 + U.nrows <= p.total_q && U.kv_begin >= 0 && U.kv_begin % kBlockSize == 0 &&
+                    U.kv_begin < U.kv_end &&
+                    U.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize &&
+                    U.part < p.max_parts && U.nparts >= 1 && U.nparts <= p.max_parts;
+  if (!sane) {
+    if (lane == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+    U.skip = 1;
+    U.kv_begin = U.kv_end = 0;
+  } else {
+    U.skip = 0;
+  }
   U.kb0 = U.kv_begin / kBlockSize;
   U.kb1 = (U.kv_end + kBlockSize - 1) / kBlockSize;
   return U;
@@ -316,9 +490,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   }
   fence_mbar_init();
   __syncthreads();
+  griddep_wait();  // the plan (and the cache scatter before it) must be complete
 
   const int Hkv = p.num_kv_heads;
-  const int total_units = __ldg(p.item_count) * Hkv;
+  const int total_units = min(max(ld_cg(p.item_count), 0), p.max_items) * Hkv;
   const uint32_t my_ring = ring + warp * S * T::SLOT_BYTES;
 
   // Producer side (lane 0 issues): stage block kb of unit U into ring slot seq % S.
@@ -485,43 +660,45 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     }
 
     // ---- unit epilogue: normalise and write the output or the partial ----
+    if (!cur.skip) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-      l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-    }
-    const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
-    const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
-    if (cur.part < 0) {
-      // transpose the bf16 result so each lane owns two consecutive d of one column
-      const int col = lane >> 2, qi = col / G, g = col % G;
-      bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (qi < cur.nrows ? qi : 0)) * p.num_heads * D +
-                  static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint32_t lo8 = movmatrix_t(pack_bf16x2(o[mt][0] * inv0, o[mt][1] * inv1));
-        const uint32_t hi8 = movmatrix_t(pack_bf16x2(o[mt][2] * inv0, o[mt][3] * inv1));
-        if (qi < cur.nrows) {
-          *reinterpret_cast<uint32_t *>(dst + 16 * mt) = lo8;
-          *reinterpret_cast<uint32_t *>(dst + 16 * mt + 8) = hi8;
-        }
+      for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
       }
-    } else {
-      const int64_t base = ((static_cast<int64_t>(cur.b) * Hkv + cur.kvh) * p.max_parts + cur.part) * kCols;
+      const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
+      const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+      if (cur.part < 0) {
+        // transpose the bf16 result so each lane owns two consecutive d of one column
+        const int col = lane >> 2, qi = col / G, g = col % G;
+        bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (qi < cur.nrows ? qi : 0)) * p.num_heads * D +
+                    static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = 2 * (lane & 3) + e;
-        if (col / G < cur.nrows) {
-          const float inv = e ? inv1 : inv0;
-          float *dst = p.part_o + (base + col) * D + (lane >> 2);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            dst[16 * mt] = o[mt][e] * inv;
-            dst[16 * mt + 8] = o[mt][2 + e] * inv;
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t lo8 = movmatrix_t(pack_bf16x2(o[mt][0] * inv0, o[mt][1] * inv1));
+          const uint32_t hi8 = movmatrix_t(pack_bf16x2(o[mt][2] * inv0, o[mt][3] * inv1));
+          if (qi < cur.nrows) {
+            *reinterpret_cast<uint32_t *>(dst + 16 * mt) = lo8;
+            *reinterpret_cast<uint32_t *>(dst + 16 * mt + 8) = hi8;
           }
-          if (lane < 4) {
-            const float lc = e ? l[1] : l[0], mc = e ? m[1] : m[0];
-            p.part_lse[base + col] = lc > 0.f ? mc + __log2f(lc) : -INFINITY;
+        }
+      } else {
+        const int64_t base = ((static_cast<int64_t>(cur.b) * Hkv + cur.kvh) * p.max_parts + cur.part) * kCols;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = 2 * (lane & 3) + e;
+          if (col / G < cur.nrows) {
+            const float inv = e ? inv1 : inv0;
+            float *dst = p.part_o + (base + col) * D + (lane >> 2);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              dst[16 * mt] = o[mt][e] * inv;
+              dst[16 * mt + 8] = o[mt][2 + e] * inv;
+            }
+            if (lane < 4) {
+              const float lc = e ? l[1] : l[0], mc = e ? m[1] : m[0];
+              p.part_lse[base + col] = lc > 0.f ? mc + __log2f(lc) : -INFINITY;
+            }
           }
         }
       }
@@ -538,57 +715,6 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     cur = nxt;
     have_nxt = false;
     p_unit = 0;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Log-sum-exp merge of the partitions of split requests (decode rows).
-// One CTA per (request, KV head); 16 threads per column.
-// ---------------------------------------------------------------------------
-template <int D, int G>
-__global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
-  constexpr int TPC = 128 / kCols;
-  constexpr int EPT = D / TPC;
-  const int b = blockIdx.x / p.num_kv_heads;
-  const int kvh = blockIdx.x - b * p.num_kv_heads;
-  const int np = __ldg(p.nparts + b);
-  if (np <= 1) return;
-  const int q0 = __ldg(p.query_start_loc + b);
-  const int ql = __ldg(p.query_start_loc + b + 1) - q0;
-  const int col = threadIdx.x / TPC, d0 = (threadIdx.x % TPC) * EPT;
-  const int qi = col / G, g = col % G;
-  if (qi >= ql) return;
-  const int64_t base = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.max_parts;
-  float M = -INFINITY;
-  for (int k = 0; k < np; ++k) M = fmaxf(M, __ldg(p.part_lse + (base + k) * kCols + col));
-  const float Ms = M == -INFINITY ? 0.f : M;
-  float acc[EPT];
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int k = 0; k < np; ++k) {
-    const int64_t idx = (base + k) * kCols + col;
-    const float w = ex2(__ldg(p.part_lse + idx) - Ms);
-    wsum += w;
-    const float *src = p.part_o + idx * D + d0;
-#pragma unroll
-    for (int e = 0; e < EPT; e += 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(src + e));
-      acc[e] += w * v.x;
-      acc[e + 1] += w * v.y;
-      acc[e + 2] += w * v.z;
-      acc[e + 3] += w * v.w;
-    }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  bf16 *dst = p.out + static_cast<int64_t>(q0 + qi) * p.num_heads * D + static_cast<int64_t>(kvh * G + g) * D + d0;
-  uint32_t pk[EPT / 2];
-#pragma unroll
-  for (int e = 0; e < EPT / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-  if constexpr (EPT == 8) {
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  } else {
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(pk[0], pk[1]);
   }
 }
 
@@ -694,8 +820,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
       !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D))
     return cudaErrorInvalidValue;
 
-  plan_kernel<<<1, 1024, 0, stream>>>(pp);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
   if (err != cudaSuccess) return err;
   ++*launched;
 
@@ -712,6 +837,9 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.items = pp.items;
   ap.item_count = pp.item_count;
   ap.work_counter = pp.work_counter;
+  ap.num_seqs = a.num_seqs;
+  ap.total_q = a.total_q;
+  ap.max_items = w.max_items;
   ap.max_parts = w.max_parts;
   ap.part_o = reinterpret_cast<float *>(ws + w.part_o);
   ap.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
@@ -727,27 +855,28 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (grid * kAttnWarps > units_upper) grid = (units_upper + kAttnWarps - 1) / kAttnWarps;
   if (grid < 1) grid = 1;
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  kern<<<static_cast<int>(grid), kAttnWarps * 32, smem, stream>>>(kmap, vmap, ap);
-  err = cudaGetLastError();
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kAttnWarps * 32), smem, stream, kmap, vmap, ap);
   if (err != cudaSuccess) return err;
   ++*launched;
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
 
-  if (w.max_parts > 1 && a.num_seqs > 0) {
+  if (w.max_parts > 1) {
     MergeParams mp;
     mp.query_start_loc = a.query_start_loc;
     mp.nparts = pp.nparts;
+    mp.num_seqs = a.num_seqs;
     mp.num_kv_heads = a.num_kv_heads;
     mp.num_heads = a.num_heads;
     mp.max_parts = w.max_parts;
     mp.part_o = ap.part_o;
     mp.part_lse = ap.part_lse;
     mp.out = ap.out;
-    lse_merge_kernel<D, G><<<a.num_seqs * a.num_kv_heads, 128, 0, stream>>>(mp);
-    err = cudaGetLastError();
+    err = launch_pdl(lse_merge_kernel<D, G>, dim3(static_cast<unsigned>(a.num_seqs * a.num_kv_heads)),
+                     dim3(kCols * 32), 0, stream, mp);
     if (err != cudaSuccess) return err;
     ++*launched;
   }
+
   return cudaSuccess;
 }
 

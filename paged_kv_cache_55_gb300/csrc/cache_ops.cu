@@ -20,19 +20,21 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     int64_t value_stride16, uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
     const int64_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t row16, int64_t num_slots,
     unsigned int *status) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t total = static_cast<int64_t>(num_tokens) * row16;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t t = static_cast<int32_t>(i / row16);
     const int32_t c = static_cast<int32_t>(i - static_cast<int64_t>(t) * row16);
-    const int64_t slot = __ldg(slot_mapping + t);
+    const int64_t slot = ld_cg(reinterpret_cast<const long long *>(slot_mapping) + t);
     if (slot < 0) continue;  // padding token
     if (slot >= num_slots) {
       if (c == 0) flag_error(status, PA_FLAG_SLOT_RANGE);
       continue;
     }
-    const uint4 k = __ldg(key + t * key_stride16 + c);
-    const uint4 v = __ldg(value + t * value_stride16 + c);
+    const uint4 k = ld_cg(key + t * key_stride16 + c);
+    const uint4 v = ld_cg(value + t * value_stride16 + c);
     key_cache[slot * row16 + c] = k;
     value_cache[slot * row16 + c] = v;
   }
@@ -76,11 +78,10 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      cudaStream_t stream) {
   const int32_t row16 = row_elems / 8;
   const int grid = grid_for(static_cast<int64_t>(num_tokens) * row16, 256, sm_count);
-  reshape_and_cache_kernel<<<grid, 256, 0, stream>>>(
-      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,
-      static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, num_tokens, row16,
-      num_slots, status);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4 *>(key),
+                    static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,
+                    static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, num_tokens,
+                    row16, num_slots, status);
 }
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,

@@ -48,7 +48,8 @@ struct AttnLaunch {
   cudaEvent_t ev_start, ev_stop;
 };
 
-// Enqueue plan + split-KV attention (+ merge) on `stream`; *launched counts kernels.
+// Enqueue planning, split-KV attention and (when a request can be split) the
+// partition merge on `stream`; *launched counts kernels.
 cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *launched);
 
 }  // namespace pa

@@ -81,6 +81,35 @@ def test_small_cases(oracle, name):
     run_and_check(w, oracle)
 
 
+def test_repeated_steps_on_reused_memory(oracle):
+    """Fresh buffers each time (the caching allocator hands back the previous
+    step's memory, stale plans included) and a torch kernel right before the
+    step: the plan must be read only after it is written."""
+    kw = SMALL_CASES["mixed_chunks_g4_d128"]
+    w = W.make_workload("repeat", seed=5, **kw)
+    kc, vc, ref = oracle.run_step(w)
+    for trial in range(6):
+        st = DeviceStep(w)
+        st.out.fill_(float("nan") if trial % 2 else 0.0)
+        st.run()
+        torch.cuda.synchronize()
+        assert B.pa_debug_status() == 0
+        gpu = bf16_to_float64(st.out)
+        assert np.isfinite(gpu).all(), f"trial {trial}: non-finite output"
+        assert_attention_close(gpu, ref, f"trial {trial}")
+        del st
+
+
+def test_batch_larger_than_one_planning_block(oracle):
+    """More than 1024 requests: the planner's chunked two-pass path."""
+    rng = np.random.default_rng(77)
+    B_ = 1500
+    ctx = rng.integers(0, 700, size=B_)
+    ql = np.where(rng.random(B_) < 0.05, rng.integers(2, 6, size=B_), 1)
+    w = W.make_workload("many", context_lens=ctx, query_lens=ql, num_heads=8, num_kv_heads=2, head_dim=64, seed=78)
+    run_and_check(w, oracle)
+
+
 def test_shared_prefix_step(oracle):
     w = W.mixed_step(seed=2, n_prefill=3, chunk=96, n_decode=20, n_shared=8, shared_blocks=6)
     run_and_check(w, oracle)
