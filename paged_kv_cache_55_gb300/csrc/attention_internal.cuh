@@ -1,0 +1,39 @@
+// Types shared by the attention translation units (internal to libpagedattn.so).
+#pragma once
+
+#include <cuda.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+using bf16 = __nv_bfloat16;
+
+// Query rows of chunked-prefill requests, packed (position, GQA head) into
+// tiles of 128 rows for the tensor-core path. Records: {b, first query
+// token, positions, absolute position of the first}, {0, key end, -1, 1}.
+struct TileParams {
+  const bf16 *q;
+  int64_t q_stride;
+  const int32_t *block_tables;
+  int32_t max_blocks_per_seq;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int64_t num_blocks;
+  float scale_log2;
+  bf16 *out;
+  const int4 *tiles;
+  const int32_t *tile_count;
+  int32_t *tile_counter;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_tiles;
+  unsigned int *status;
+};
+
+// Enqueue the tensor-core prefill-tile kernel (PDL launch) on `stream`.
+template <int D, int G>
+cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp,
+                                 int sm_count, cudaStream_t stream);
+
+}  // namespace pa

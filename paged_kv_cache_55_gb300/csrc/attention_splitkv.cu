@@ -46,12 +46,10 @@
 
 #include <mutex>
 
-#include "pa_common.cuh"
+#include "attention_internal.cuh"
 #include "pa_launch.h"
 
 namespace pa {
-
-using bf16 = __nv_bfloat16;
 
 constexpr int kCols = 8;                         // (query row, head) columns per unit
 constexpr int kSmemBudget = 192 * 1024;          // ring bytes per CTA
@@ -68,11 +66,16 @@ struct PlanParams {
   int32_t rows_per_item;  // 8 / G
   int32_t part_tokens;
   int32_t max_items;
-  int32_t *class_start;   // [3][num_seqs + 1] prefix sums of the per-class item counts
+  int32_t *class_start;   // [4][num_seqs + 1] prefix sums: 3 size classes of decode items, then tiles
   int32_t *nparts;        // [num_seqs], 0 = request produces nothing
   int4 *items;            // [2 * max_items]
   int32_t *item_count;    // [1]
   int32_t *work_counter;  // [1], zeroed here, consumed by the attention kernel
+  int4 *tiles;            // [2 * max_tiles] prefill-tile records
+  int32_t *tile_count;    // [1]
+  int32_t *tile_counter;  // [1], zeroed here, consumed by the tile kernel
+  int32_t max_tiles;
+  int32_t tile_pos;       // query positions per tile: 128 / G
   unsigned int *status;
 };
 
@@ -99,11 +102,6 @@ struct AttnParams {
 };
 
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // ---------------------------------------------------------------------------
 // Planning: per request, validate the lengths, count work items, scan, and
@@ -114,7 +112,13 @@ __device__ __forceinline__ float ex2(float x) {
 // Record: {b, first query token, rows, position of first row},
 //         {key begin, key end, partition (-1 = whole range), partitions of the request}.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0, int &ql, int &L, int &np) {
+// A request whose query rows fit one column group (query_len <= 8 / G: decode
+// tokens, speculative drafts) becomes split-KV decode items; a longer one
+// (a chunked-prefill chunk) becomes tensor-core tiles of 128 / G positions.
+// Returns the number of decode items; *ntiles receives the number of tiles.
+__device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0, int &ql, int &L, int &np,
+                                             int &ntiles) {
+  ntiles = 0;
   q0 = ld_cg(p.query_start_loc + b);
   const int q1 = ld_cg(p.query_start_loc + b + 1);
   L = ld_cg(p.seq_lens + b);
@@ -131,9 +135,21 @@ __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0
     return 0;
   }
   if (ql == 0) return 0;
-  const int groups = (ql + p.rows_per_item - 1) / p.rows_per_item;
-  np = (groups == 1) ? max(1, (L + p.part_tokens - 1) / p.part_tokens) : 1;
-  return groups * np;
+  if (ql > p.rows_per_item) {
+    np = 1;
+    ntiles = (ql + p.tile_pos - 1) / p.tile_pos;
+    return 0;
+  }
+  np = max(1, (L + p.part_tokens - 1) / p.part_tokens);
+  return np;
+}
+
+__device__ __forceinline__ void write_tile(const PlanParams &p, int idx, int b, int q0, int ql, int L, int t) {
+  const int r0 = t * p.tile_pos;
+  const int npos = min(p.tile_pos, ql - r0);
+  const int pos0 = (L - ql) + r0;
+  p.tiles[2 * idx] = make_int4(b, q0 + r0, npos, pos0);
+  p.tiles[2 * idx + 1] = make_int4(0, pos0 + npos, -1, 1);
 }
 
 // Keys [kb, ke) of item k of a request, and its record fields.
@@ -188,7 +204,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *t
   return excl;
 }
 
-// Exclusive block scan of a 64-bit value (three 21-bit counters packed).
+// Exclusive block scan of a 64-bit value (four 16-bit counters packed).
 __device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned long long v,
                                                                     unsigned long long *warp_tot,
                                                                     unsigned long long *total) {
@@ -216,7 +232,7 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned lo
   return excl;
 }
 
-constexpr int kPackBits = 21;  // items per class below 2^21 in the one-pass planner
+constexpr int kPackBits = 16;  // four counters (3 item classes, tiles) below 2^16 in the one-pass planner
 constexpr unsigned long long kPackMask = (1ull << kPackBits) - 1;
 
 // One pass for batches of at most 1024 requests (one per thread): count the
@@ -224,11 +240,12 @@ constexpr unsigned long long kPackMask = (1ull << kPackBits) - 1;
 __device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
   __shared__ unsigned long long warp_tot[32];
   const int b = threadIdx.x;
-  int q0 = 0, ql = 0, L = 0, np = 0, n = 0;
+  int q0 = 0, ql = 0, L = 0, np = 0, n = 0, nt = 0;
   unsigned long long packed = 0;
   if (b < p.num_seqs) {
-    n = request_shape(p, b, q0, ql, L, np);
+    n = request_shape(p, b, q0, ql, L, np, nt);
     p.nparts[b] = np;
+    packed += static_cast<unsigned long long>(nt) << (3 * kPackBits);
     for (int k = 0; k < n; ++k) {
       const ItemShape s = item_shape(p, k, np, ql, L);
       packed += 1ull << (kPackBits * size_class(s.ke - s.kb, p.part_tokens));
@@ -238,6 +255,7 @@ __device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
   const unsigned long long excl = block_exclusive_scan64(packed, warp_tot, &total);
   const int t0 = static_cast<int>(total & kPackMask), t1 = static_cast<int>((total >> kPackBits) & kPackMask);
   const int t2 = static_cast<int>((total >> (2 * kPackBits)) & kPackMask);
+  const int t3 = static_cast<int>((total >> (3 * kPackBits)) & kPackMask);
   if (threadIdx.x == 0) {
     int all = t0 + t1 + t2;
     if (all > p.max_items) {
@@ -245,7 +263,11 @@ __device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
       all = p.max_items;
     }
     p.item_count[0] = all;
+    p.tile_count[0] = min(t3, p.max_tiles);
   }
+  const int tile0 = static_cast<int>((excl >> (3 * kPackBits)) & kPackMask);
+  for (int t = 0; t < nt; ++t)
+    if (tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, t);
   if (n == 0) return;
   int next[3] = {static_cast<int>(excl & kPackMask), t0 + static_cast<int>((excl >> kPackBits) & kPackMask),
                  t0 + t1 + static_cast<int>((excl >> (2 * kPackBits)) & kPackMask)};
@@ -260,33 +282,37 @@ __device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
 
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
   __shared__ int warp_tot[32];
-  __shared__ int carry[3];
+  __shared__ int carry[4];
   const int tid = threadIdx.x;
   const int stride = p.num_seqs + 1;
   griddep_wait();  // inputs may come from the previous kernel of the stream
   griddep_launch_dependents();
-  if (tid == 0) p.work_counter[0] = 0;
-  if (p.num_seqs <= 1024 && p.max_items < static_cast<int>(kPackMask)) {
+  if (tid == 0) {
+    p.work_counter[0] = 0;
+    p.tile_counter[0] = 0;
+  }
+  if (p.num_seqs <= 1024 && p.max_items < static_cast<int>(kPackMask) && p.max_tiles < static_cast<int>(kPackMask)) {
     plan_one_pass(p);
     return;
   }
   // larger batches: chunked counting and scans, then a second pass that writes
-  if (tid < 3) carry[tid] = 0;
+  if (tid < 4) carry[tid] = 0;
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int b = base + tid;
-    int cnt[3] = {0, 0, 0};
+    int cnt[4] = {0, 0, 0, 0};
     if (b < p.num_seqs) {
-      int q0, ql, L, np;
-      const int n = request_shape(p, b, q0, ql, L, np);
+      int q0, ql, L, np, nt;
+      const int n = request_shape(p, b, q0, ql, L, np, nt);
       p.nparts[b] = np;
       for (int k = 0; k < n; ++k) {
         const ItemShape s = item_shape(p, k, np, ql, L);
         ++cnt[size_class(s.ke - s.kb, p.part_tokens)];
       }
+      cnt[3] = nt;
     }
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
+    for (int c = 0; c < 4; ++c) {
       int tot;
       const int excl = block_exclusive_scan(cnt[c], warp_tot, &tot);
       if (b < p.num_seqs) p.class_start[c * stride + b] = carry[c] + excl;
@@ -295,7 +321,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
       __syncthreads();
     }
   }
-  if (tid < 3) p.class_start[tid * stride + p.num_seqs] = carry[tid];
+  if (tid < 4) p.class_start[tid * stride + p.num_seqs] = carry[tid];
   if (tid == 0) {
     int total = carry[0] + carry[1] + carry[2];
     if (total > p.max_items) {
@@ -303,6 +329,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
       total = p.max_items;
     }
     p.item_count[0] = total;
+    p.tile_count[0] = min(carry[3], p.max_tiles);
   }
   __syncthreads();
   const int base1 = carry[0], base2 = carry[0] + carry[1];
@@ -312,8 +339,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
     const int q0 = ld_cg(p.query_start_loc + b);
     const int ql = ld_cg(p.query_start_loc + b + 1) - q0;
     const int L = ld_cg(p.seq_lens + b);
+    if (ql > p.rows_per_item) {
+      const int nt = (ql + p.tile_pos - 1) / p.tile_pos;
+      const int tile0 = p.class_start[3 * stride + b];
+      for (int t = 0; t < nt; ++t)
+        if (tile0 + t >= 0 && tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, t);
+      continue;
+    }
     int next[3] = {p.class_start[b], base1 + p.class_start[stride + b], base2 + p.class_start[2 * stride + b]};
-    const int n = ((ql + p.rows_per_item - 1) / p.rows_per_item) * np;
+    const int n = np;
     for (int k = 0; k < n; ++k) {
       const ItemShape s = item_shape(p, k, np, ql, L);
       const int idx = next[size_class(s.ke - s.kb, p.part_tokens)]++;
@@ -390,7 +424,7 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
     for (int j = 0; j < 8; ++j)
       if (k0 + j < np) Mn = fmaxf(Mn, lv[j]);
     const float Ms = Mn == -INFINITY ? 0.f : Mn;
-    const float r = ex2(M - Ms);  // rescale what was summed so far (0 on the first pack)
+    const float r = ex2_approx(M - Ms);  // rescale what was summed so far (0 on the first pack)
     wsum *= r;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] *= r;
@@ -398,7 +432,7 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (k0 + j < np) {
-        const float w = ex2(lv[j] - Ms);
+        const float w = ex2_approx(lv[j] - Ms);
         wsum += w;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] += w * ov[j][e];
@@ -628,9 +662,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
       const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
       const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = ex2(m[0] - ms0), al1 = ex2(m[1] - ms1);
-      const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-      const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
+      const float al0 = ex2_approx(m[0] - ms0), al1 = ex2_approx(m[1] - ms1);
+      const float p0 = ex2_approx(x0 - ms0), p1 = ex2_approx(x1 - ms1);
+      const float p2 = ex2_approx(x2 - ms0), p3 = ex2_approx(x3 - ms1);
       l[0] = l[0] * al0 + p0 + p2;
       l[1] = l[1] * al1 + p1 + p3;
       m[0] = mn0;
@@ -743,16 +777,18 @@ bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, in
   w.rows_per_item = 8 / G;
   w.part_tokens = partition_tokens(num_seqs, max_seq_len, num_kv_heads);
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.part_tokens - 1) / w.part_tokens : 1;
-  const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts +
-                        (static_cast<int64_t>(total_q) + w.rows_per_item - 1) / w.rows_per_item + num_seqs;
-  if (items * num_kv_heads > (1LL << 30)) return false;
-  w.max_items = static_cast<int32_t>(items);
+  const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts;  // decode items: one group per request
+  const int64_t tiles = (static_cast<int64_t>(total_q) * G + 127) / 128 + num_seqs;
+  if (items * num_kv_heads > (1LL << 30) || tiles * num_kv_heads > (1LL << 30)) return false;
+  w.max_items = static_cast<int32_t>(items > 0 ? items : 1);
+  w.max_tiles = static_cast<int32_t>(tiles > 0 ? tiles : 1);
   const size_t nsplit = static_cast<size_t>(num_seqs) * num_kv_heads * w.max_parts * kCols;
   size_t off = 0;
-  w.item_start = off; off += align256(sizeof(int32_t) * 3 * (static_cast<size_t>(num_seqs) + 1));
+  w.item_start = off; off += align256(sizeof(int32_t) * 4 * (static_cast<size_t>(num_seqs) + 1));
   w.nparts = off;     off += align256(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
-  w.item_count = off; off += align256(2 * sizeof(int32_t));  // item count, work counter
+  w.item_count = off; off += align256(4 * sizeof(int32_t));  // items, work counter, tiles, tile counter
   w.items = off;      off += align256(sizeof(int4) * 2 * static_cast<size_t>(w.max_items));
+  w.tiles = off;      off += align256(sizeof(int4) * 2 * static_cast<size_t>(w.max_tiles));
   w.part_lse = off;   off += align256(sizeof(float) * nsplit);
   w.part_o = off;     off += align256(sizeof(float) * nsplit * head_dim);
   w.total = off;
@@ -813,6 +849,11 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.items = reinterpret_cast<int4 *>(ws + w.items);
   pp.item_count = reinterpret_cast<int32_t *>(ws + w.item_count);
   pp.work_counter = pp.item_count + 1;
+  pp.tile_count = pp.item_count + 2;
+  pp.tile_counter = pp.item_count + 3;
+  pp.tiles = reinterpret_cast<int4 *>(ws + w.tiles);
+  pp.max_tiles = w.max_tiles;
+  pp.tile_pos = 128 / G;
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;
@@ -859,6 +900,29 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (err != cudaSuccess) return err;
   ++*launched;
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
+
+  if (a.max_query_len > w.rows_per_item) {  // some request may be a prefill chunk
+    TileParams tp;
+    tp.q = ap.q;
+    tp.q_stride = a.q_stride;
+    tp.block_tables = a.block_tables;
+    tp.max_blocks_per_seq = a.max_blocks_per_seq;
+    tp.num_heads = a.num_heads;
+    tp.num_kv_heads = a.num_kv_heads;
+    tp.num_blocks = a.num_blocks;
+    tp.scale_log2 = ap.scale_log2;
+    tp.out = ap.out;
+    tp.tiles = pp.tiles;
+    tp.tile_count = pp.tile_count;
+    tp.tile_counter = pp.tile_counter;
+    tp.num_seqs = a.num_seqs;
+    tp.total_q = a.total_q;
+    tp.max_tiles = w.max_tiles;
+    tp.status = a.status;
+    err = launch_prefill_tiles<D, G>(kmap, vmap, tp, a.sm_count, stream);
+    if (err != cudaSuccess) return err;
+    ++*launched;
+  }
 
   if (w.max_parts > 1) {
     MergeParams mp;

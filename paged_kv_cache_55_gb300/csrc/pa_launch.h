@@ -20,10 +20,11 @@ cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, con
 
 // Byte offsets of the pieces of the attention workspace, and the split plan.
 struct WorkspaceLayout {
-  size_t item_start, nparts, item_count, items, part_lse, part_o, total;
+  size_t item_start, nparts, item_count, items, tiles, part_lse, part_o, total;
   int32_t part_tokens;    // keys per partition
   int32_t max_parts;      // partitions of the longest request
-  int32_t max_items;      // upper bound on work items (per KV head)
+  int32_t max_items;      // upper bound on decode work items (per KV head)
+  int32_t max_tiles;      // upper bound on prefill tiles (per KV head)
   int32_t rows_per_item;  // query rows per item: 8 / group size
 };
 
