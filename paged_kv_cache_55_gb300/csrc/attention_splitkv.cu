@@ -266,8 +266,8 @@ __device__ __forceinline__ void plan_one_pass(const PlanParams &p) {
     p.tile_count[0] = min(t3, p.max_tiles);
   }
   const int tile0 = static_cast<int>((excl >> (3 * kPackBits)) & kPackMask);
-  for (int t = 0; t < nt; ++t)
-    if (tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, t);
+  for (int t = 0; t < nt; ++t)  // a request's last tiles see the most keys: queue them first
+    if (tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, nt - 1 - t);
   if (n == 0) return;
   int next[3] = {static_cast<int>(excl & kPackMask), t0 + static_cast<int>((excl >> kPackBits) & kPackMask),
                  t0 + t1 + static_cast<int>((excl >> (2 * kPackBits)) & kPackMask)};
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
       const int nt = (ql + p.tile_pos - 1) / p.tile_pos;
       const int tile0 = p.class_start[3 * stride + b];
       for (int t = 0; t < nt; ++t)
-        if (tile0 + t >= 0 && tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, t);
+        if (tile0 + t >= 0 && tile0 + t < p.max_tiles) write_tile(p, tile0 + t, b, q0, ql, L, nt - 1 - t);
       continue;
     }
     int next[3] = {p.class_start[b], base1 + p.class_start[stride + b], base2 + p.class_start[2 * stride + b]};
@@ -889,6 +889,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
   auto kern = splitkv_attention_kernel<D, G, kAttnWarps>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (err != cudaSuccess) return err;
   // one CTA per SM; fewer when there are fewer units than warps
   int64_t grid = a.sm_count;

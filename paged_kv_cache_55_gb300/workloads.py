@@ -307,11 +307,16 @@ def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768) -> Workload
 
 
 def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: int = 240,
-               n_shared: int = 64, shared_blocks: int = 64) -> Workload:
+               n_shared: int = 64, shared_blocks: int = 64, batch: Optional[int] = None) -> Workload:
     """Continuous-batching step: 16 prefill chunks of 512 query tokens (prior
     context U[0, 4096]) plus 240 decode requests (context U[256, 4096]); the
     first 64 physical blocks of 64 decode requests are one shared prefix.
-    Requests appear in a seeded random order."""
+    Requests appear in a seeded random order. `batch` scales the step down
+    (batch / 16 prefill chunks, the rest decode, a quarter of those sharing)."""
+    if batch is not None:
+        n_prefill = max(1, batch // 16)
+        n_decode = batch - n_prefill
+        n_shared = n_decode // 4
     rng = np.random.default_rng(seed + 3000)
     pre_ctx = rng.integers(0, 4096, size=n_prefill, endpoint=True)
     dec_ctx = rng.integers(256, 4096, size=n_decode, endpoint=True)
