@@ -191,6 +191,14 @@ pa_status pa_debug_status(void *stream, uint32_t *flags_out);
 uint64_t pa_launch_count(void);
 
 /*
+ * Name of the CUDA runtime error (a static string such as
+ * "cudaErrorInvalidValue") behind the last PA_ERR_LAUNCH or PA_ERR_CUDA that
+ * a call made by this host thread returned; "cudaSuccess" if there was none.
+ * Makes no CUDA call that touches a device.
+ */
+const char *pa_last_cuda_error(void);
+
+/*
  * Measurement hook: the next pa_attention_varlen call made by this host
  * thread records `start` (a cudaEvent_t) just before its split-KV attention
  * kernel and `stop` just after it, on the call's stream, then forgets them.

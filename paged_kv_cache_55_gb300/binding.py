@@ -45,6 +45,7 @@ SIGNATURES = {
     "pa_status_string": ([_I32], ctypes.c_char_p),
     "pa_debug_status": ([_P, _P], ctypes.c_int),
     "pa_launch_count": ([], ctypes.c_uint64),
+    "pa_last_cuda_error": ([], ctypes.c_char_p),
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
@@ -83,6 +84,8 @@ def _stream(stream) -> int:
 
 def _check(status: int, what: str) -> None:
     if status != 0:
+        if status in (-6, -8):  # PA_ERR_LAUNCH, PA_ERR_CUDA: name the CUDA error behind it
+            what = f"{what} [{pa_last_cuda_error()}]"
         raise PagedAttnError(status, what)
 
 
@@ -193,6 +196,10 @@ def pa_debug_status(stream=None) -> int:
 
 def pa_launch_count() -> int:
     return int(_lib().pa_launch_count())
+
+
+def pa_last_cuda_error() -> str:
+    return _lib().pa_last_cuda_error().decode()
 
 
 def pa_attention_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]) -> None:

@@ -27,6 +27,13 @@ DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_launches{0};
 thread_local cudaEvent_t t_ev_start = nullptr;
 thread_local cudaEvent_t t_ev_stop = nullptr;
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Record the CUDA error behind a PA_ERR_LAUNCH / PA_ERR_CUDA return.
+pa_status cuda_failure(pa_status status, cudaError_t err) {
+  t_last_cuda_error = err;
+  return status;
+}
 
 // Per-device set-up on first use: the status word's device address and the
 // SM count (both fixed for the life of the process).
@@ -40,6 +47,7 @@ DeviceState *device_state() {
     if (s.err == cudaSuccess) s.err = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
     s.status = static_cast<unsigned int *>(ptr);
   });
+  if (s.err != cudaSuccess) t_last_cuda_error = s.err;
   return s.err == cudaSuccess ? &s : nullptr;
 }
 
@@ -71,6 +79,8 @@ const char *pa_status_string(int32_t status) {
     default: return "unknown status";
   }
 }
+
+const char *pa_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
 
 uint64_t pa_launch_count(void) { return g_launches.load(); }
 
@@ -105,7 +115,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
       key, value, key_token_stride, value_token_stride, key_cache, value_cache, slot_mapping, num_tokens,
       static_cast<int32_t>(row), num_blocks * block_size, ds->status, ds->sm_count,
       static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);
   return PA_OK;
 }
@@ -194,7 +204,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   int launched = 0;
   cudaError_t err = pa::launch_attention(a, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(static_cast<uint64_t>(launched));
-  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   return PA_OK;
 }
 
@@ -215,7 +225,7 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   cudaError_t err = pa::launch_gather_kv(key_cache, value_cache, block_table_row, seq_len,
                                          num_kv_heads * head_dim, num_blocks, key_out, value_out, ds->status,
                                          ds->sm_count, static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return PA_ERR_LAUNCH;
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);
   return PA_OK;
 }
@@ -223,11 +233,14 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
 pa_status pa_debug_status(void *stream, uint32_t *flags_out) {
   DeviceState *ds = device_state();
   if (!ds) return PA_ERR_CUDA;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_CUDA, err);
   unsigned int flags = 0;
-  if (cudaMemcpy(&flags, ds->status, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  err = cudaMemcpy(&flags, ds->status, sizeof flags, cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_CUDA, err);
   const unsigned int zero = 0;
-  if (cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  err = cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_CUDA, err);
   if (flags_out) *flags_out = flags;
   return flags ? PA_ERR_DEVICE_BOUNDS : PA_OK;
 }

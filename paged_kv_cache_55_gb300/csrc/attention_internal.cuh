@@ -9,9 +9,12 @@ namespace pa {
 
 using bf16 = __nv_bfloat16;
 
-// Query rows of chunked-prefill requests, packed (position, GQA head) into
-// tiles of 128 rows for the tensor-core path. Records: {b, first query
-// token, positions, absolute position of the first}, {0, key end, -1, 1}.
+// Query rows of chunked-prefill requests are packed (position, GQA head) into
+// tiles of kPrefillTileRows rows for the tensor-core path, i.e.
+// kPrefillTileRows / G positions per tile. Records: {b, first query token,
+// positions, absolute position of the first}, {0, key end, -1, 1}.
+constexpr int kPrefillTileRows = 256;
+
 struct TileParams {
   const bf16 *q;
   int64_t q_stride;

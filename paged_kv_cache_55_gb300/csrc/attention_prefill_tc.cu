@@ -9,71 +9,91 @@
 //     position (chunked prefill, named in the LLM-infra reading map,
 //     "lpnh.cn/news/2436702", §2.3).
 //
-// One CTA handles one tile of 128 "packed rows" = (query position, head of
-// the GQA group) pairs of one request and one KV head, so each K/V byte
-// staged for the tile serves all G heads. The keys are walked in ranges of
-// 64 by three kinds of warps that hand work over through mbarriers only:
+// One CTA handles one tile of 256 "packed rows" = (query position, head of
+// the GQA group) pairs of one request and one KV head, as two halves A and B
+// of 128 rows (the UMMA M) that share every K/V range staged for the tile, so
+// each K/V byte serves 2 x 128 rows. The keys are walked in ranges of 128 (an
+// M128 x N128 product runs at close to the tensor cores' peak; N64 at half)
+// by three kinds of warps that hand work over through mbarriers only:
 //   * a producer warp issues TMA loads of the (block, KV head) tiles of K and
 //     V through the block table into 128-byte-swizzled shared memory (the
-//     decode path's boxes), two buffers each with full/empty barriers,
-//     K(r+1) ahead of V(r);
-//   * an MMA warp issues tcgen05.mma: S = Q K^T into tensor memory as soon
-//     as K(r) has landed and the softmax has released S, then O += P_hi V +
-//     P_lo V for the previous range (P read from tensor memory, V an MN-major
-//     shared-memory operand), so the softmax of range r runs while the tensor
-//     cores multiply range r-1; it zeroes V rows past the last key first;
-//   * four softmax warps own one row each per thread (its TMEM lane): they
-//     read the 64 scores, apply the causal limit, keep the running max and
-//     sum (log2 domain) and store P into tensor memory as a bf16 hi + lo pair;
-//     O accumulates in tensor memory and a row is rescaled there only when
-//     its running maximum grows by more than 2^8.
-// Two CTAs share an SM (96 KB of shared memory, 256 TMEM columns each). All
-// shared state is in the dynamic segment, whose start must be 1024-byte
-// aligned for the swizzled tiles (checked). Waits on mbarriers are bounded
-// (a thread waits out at most one timeout, then runs to the unit barrier);
-// tensor memory is released on every exit path.
+//     decode path's boxes), two buffers each with full/empty barriers, in
+//     the order the products consume them;
+//   * an MMA warp issues tcgen05.mma. Each half owns one score buffer in
+//     tensor memory: S(r) = Q K(r)^T lands there, the softmax overwrites it
+//     in place with P(r), and O += P_hi(r) V(r) + P_lo(r) V(r) reads P from
+//     there (V an MN-major shared-memory operand). The order is P V_A(r),
+//     S_A(r+1) once that product has completed, P V_B(r), S_B(r+1): while one
+//     half's softmax runs, the tensor cores work on the other half. The warp
+//     zeroes V rows past the last key before the first product reads them;
+//   * eight softmax warps, four per half, own one row each per thread (its
+//     TMEM lane). Per range they read the 128 scores once, 32 at a time,
+//     apply the causal limit, keep the running max and sum (log2 domain) and
+//     write P as bf16 hi + lo pairs over the scores they came from. O
+//     accumulates in tensor memory; O, the row sum and the probabilities
+//     already written are rescaled (by the whole warp, each row by its own
+//     factor) only when a row's running maximum grows by more than 2^8; no
+//     product is in flight then. The softmax warps of TMEM lanes 0-31 share
+//     a scheduler with the MMA warp, whose issue rate the tensor cores depend
+//     on, so their arithmetic is kept lean (paired fp32 instructions).
+// Half A holds the earlier positions, so it may stop some ranges before half
+// B (its keys end sooner); a half without valid rows does no work at all.
+// One CTA per SM (all 512 TMEM columns, 256 per half). All shared state is in
+// the dynamic segment, whose start must be 1024-byte aligned for the swizzled
+// tiles (checked). Waits on mbarriers are bounded (a thread waits out at most
+// one timeout, then runs to the unit barrier); in-flight loads and products
+// are waited for (bounded) and tensor memory is released on every exit path.
 #include "attention_internal.cuh"
 
 namespace pa {
 
-constexpr int kTileRows = 128;  // UMMA M
-constexpr int kKeyTile = 64;    // keys per range (UMMA N of S, K of P V)
-constexpr int kSoftmaxWarps = 4, kMmaWarp = 4, kTmaWarp = 5;
+constexpr int kHalfRows = 128;  // UMMA M: rows per half
+constexpr int kHalves = kPrefillTileRows / kHalfRows;
+static_assert(kHalves == 2, "the pipeline interleaves exactly two halves");
+constexpr int kKeyTile = 128;  // keys per range (UMMA N of S, K of P V)
+constexpr int kStages = 2;     // depth of the K and V rings
+constexpr int kSoftmaxWarps = 4 * kHalves, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
 constexpr int kTileThreads = 32 * (kTmaWarp + 1);
 constexpr uint64_t kTcWaitTimeoutNs = 2000000000;
+constexpr uint32_t kTmemCols = 512;
 
-// Tensor memory columns: S [0, 64), O [64, 64 + D), P_hi and P_lo 32 each.
+// Tensor memory columns of half A: the score buffer SP [0, 128) and O
+// [128, 128 + D); half B's are the same plus HALF. SP holds S (fp32, column
+// = key) and then P: the 16 keys of UMMA K step k occupy columns [16k, 16k+16)
+// of either, as 8 columns of P_hi pairs followed by 8 of P_lo pairs.
 template <int D>
 struct TcTmem {
-  static constexpr uint32_t S = 0, O = kKeyTile, PHI = kKeyTile + D, PLO = PHI + kKeyTile / 2;
-  static constexpr uint32_t USED = PLO + kKeyTile / 2;
-  static constexpr uint32_t COLS = USED <= 128 ? 128u : (USED <= 256 ? 256u : 512u);  // power of two
+  static constexpr uint32_t SP = 0, O = kKeyTile;
+  static constexpr uint32_t HALF = kTmemCols / kHalves;
+  static_assert(O + D <= HALF, "a half's columns must fit its share of TMEM");
 };
 
 template <int D>
 struct TcLayout {
-  static constexpr int HALVES = D / 64;           // 64-element swizzle atoms along D
-  static constexpr int Q_HALF = kTileRows * 128;  // 128 rows x 128 B
-  static constexpr int KV_HALF = kKeyTile * 128;  // 64 rows x 128 B
-  static constexpr int Q_BYTES = HALVES * Q_HALF;
-  static constexpr int KV_BYTES = HALVES * KV_HALF;
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;          // two K buffers
-  static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;     // two V buffers
-  static constexpr int TABLE_OFF = V_OFF + 2 * KV_BYTES;  // the tile's block-table entries
-  static constexpr int TABLE_ENTRIES = 1024;             // keys < 16384 read from here
+  static constexpr int ATOMS = D / 64;             // 64-element swizzle atoms along D
+  static constexpr int Q_ATOM = kHalfRows * 128;   // 128 rows x 128 B
+  static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
+  static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
+  static constexpr int KV_BYTES = ATOMS * KV_ATOM;
+  static constexpr int Q_OFF = 0;                               // Q of halves A and B
+  static constexpr int K_OFF = Q_OFF + kHalves * Q_BYTES;       // kStages K buffers
+  static constexpr int V_OFF = K_OFF + kStages * KV_BYTES;      // kStages V buffers
+  static constexpr int TABLE_OFF = V_OFF + kStages * KV_BYTES;  // the tile's block-table entries
+  static constexpr int TABLE_ENTRIES = 1024;                    // keys < 16384 read from here
   static constexpr int BAR_OFF = TABLE_OFF + TABLE_ENTRIES * 4;
-  // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, p_full, o_done, q_full
-  static constexpr int NBARS = 12;
+  // barriers: k_full[S], k_empty[S], v_full[S], v_empty[S], per half s_full, p_full, o_done,
+  // then q_full and drain (the MMA thread's last commit)
+  static constexpr int NBARS = 4 * kStages + 3 * kHalves + 2;
   static constexpr int BYTES = BAR_OFF + 8 * NBARS + 16;
-  // Shared memory requested per CTA: at least 77 KB so that no more than two
-  // CTAs (2 x 256 TMEM columns) can ever share an SM.
-  static constexpr int REQUEST = BYTES > 77 * 1024 ? BYTES : 77 * 1024;
-  // byte offset of 16-byte chunk c of row r in a swizzled tile with `half` bytes per atom column
-  static __device__ __forceinline__ uint32_t off(int r, int c, int half) {
-    return (c >> 3) * half + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  // Shared memory requested per CTA: more than half an SM's, so that a second
+  // CTA (which would wait for TMEM) never lands on the same SM.
+  static constexpr int REQUEST = BYTES > 116 * 1024 ? BYTES : 116 * 1024;
+  // byte offset of 16-byte chunk c of row r in a swizzled tile with `atom` bytes per atom column
+  static __device__ __forceinline__ uint32_t off(int r, int c, int atom) {
+    return (c >> 3) * atom + r * 128 + (((c & 7) ^ (r & 7)) << 4);
   }
 };
+static_assert(TcLayout<128>::BYTES <= 227 * 1024, "shared memory of one CTA");
 
 // Bounded wait that is skipped once this thread has given up: a thread waits
 // out at most one timeout, then runs to the next unit barrier.
@@ -81,8 +101,147 @@ __device__ __forceinline__ void wait_or_fail(uint32_t bar, uint32_t parity, bool
   if (!failed) failed = !mbar_wait_bounded(bar, parity, kTcWaitTimeoutNs);
 }
 
+// The two 32-bit words of a 128-byte-swizzle shared-memory descriptor (the
+// layout sw128_desc builds). The low word holds the start address >> 4 in
+// bits 0-13, so a tile's descriptors differ from its first one by adding the
+// byte offset >> 4 to the low word (shared addresses stay below 256 KB: no
+// carry out of the field). Building them once per unit keeps the issuing
+// thread at two additions per MMA: it shares its scheduler with two softmax
+// warps, and the tensor core queues only a couple of instructions.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t smem_addr, uint32_t lbo) {
+  return ((smem_addr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);  // SBO, version (bit 46), 128-byte swizzle (61-63)
+}
+// D[tmem] (+)= A[smem] * B[smem] with descriptors given as words; ACC = 0 overwrites D.
+template <int ACC>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                       uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %6, 0;\n mov.b64 a, {%1, %2};\n"
+      " mov.b64 b, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem].
+template <int ACC>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 b;\n setp.ne.b32 p, %5, 0;\n mov.b64 b, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
+// 64 consecutive 32-bit columns of this thread's TMEM lane; the wait is in
+// the same statement, so no use of the registers can be scheduled before it.
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The same for 32 columns.
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Packed pairs of fp32 operations (one instruction for two lanes of data).
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n add.rn.f32x2 d, a, b;\n"
+      " mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n sub.rn.f32x2 d, a, b;\n"
+      " mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Row maximum of 32 raw scores, key ck0 + i visible while ck0 + i < lim.
+__device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, int lim) {
+  float m = -INFINITY;
+  if (ck0 + 32 <= lim) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(s[i]), __uint_as_float(s[i + 1]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = ck0 + i < lim ? fmaxf(m, __uint_as_float(s[i])) : m;
+  }
+  return m;
+}
+
+// P for 32 keys (scores s[0..32), visible while ck0 + i < lim): p =
+// 2^(s * sl2 - ms), summed into *sum and packed as the 32 TMEM columns of two
+// UMMA K steps: [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo 16-31].
+__device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int lim, float sl2, float ms, float &sum,
+                                        uint32_t (&u)[32]) {
+  const bool full = ck0 + 32 <= lim;
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0 = __uint_as_float(s[2 * i]), x1 = __uint_as_float(s[2 * i + 1]);
+    if (!full) {
+      x0 = ck0 + 2 * i < lim ? x0 : -INFINITY;
+      x1 = ck0 + 2 * i + 1 < lim ? x1 : -INFINITY;
+    }
+    float e0, e1;
+    fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
+    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+    add2(acc0, acc1, acc0, acc1, p0, p1);
+    const uint32_t hi = pack_bf16x2(p0, p1);
+    float l0, l1;
+    sub2(l0, l1, p0, p1, bf16_lo(hi), bf16_hi(hi));
+    const int step = i >> 3, k = i & 7;
+    u[16 * step + k] = hi;
+    u[16 * step + 8 + k] = pack_bf16x2(l0, l1);
+  }
+  sum += acc0 + acc1;
+}
+
+// Multiply the probabilities already stored in a 32-column chunk of P (the
+// layout probs32 writes) by alpha, re-splitting each into hi + lo.
+__device__ __forceinline__ void rescale_p32(uint32_t taddr, float alpha) {
+  uint32_t w[32];
+  tmem_ld32_wait(taddr, w);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int hk = 16 * (i >> 3) + (i & 7);
+    const float p0 = (bf16_lo(w[hk]) + bf16_lo(w[hk + 8])) * alpha;
+    const float p1 = (bf16_hi(w[hk]) + bf16_hi(w[hk + 8])) * alpha;
+    const uint32_t hi = pack_bf16x2(p0, p1);
+    w[hk] = hi;
+    w[hk + 8] = pack_bf16x2(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
+  }
+  tmem_st32u(taddr, w);
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kTileThreads, 2)
+// Ten warps: three share two of the SM's four register-file partitions, so a
+// thread gets at most 168 registers.
+__global__ void __launch_bounds__(kTileThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const TileParams p) {
   using Lay = TcLayout<D>;
@@ -90,8 +249,9 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   constexpr int KSTEPS_S = D / 16;         // UMMA K steps of S = Q K^T
   constexpr int KSTEPS_O = kKeyTile / 16;  // UMMA K steps of O = P V
   constexpr int BLOCKS = kKeyTile / kBlockSize;
-  constexpr uint32_t IDESC_S = f16_idesc(kTileRows, kKeyTile, 0);
-  constexpr uint32_t IDESC_O = f16_idesc(kTileRows, D, 1);
+  constexpr int POS_PER_HALF = kHalfRows / G;
+  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0);
+  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1);
   // O stays in TMEM and is rescaled only when a row's running maximum grows
   // by more than 2^8 (log2 domain); in between, probabilities are taken
   // against the older maximum and stay below 256.
@@ -104,24 +264,30 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
     return;
   }
-  const uint32_t sQ = base + Lay::Q_OFF, sK0 = base + Lay::K_OFF, sV0 = base + Lay::V_OFF;
+  const uint32_t sQ0 = base + Lay::Q_OFF, sK0 = base + Lay::K_OFF, sV0 = base + Lay::V_OFF;
   const uint32_t bars = base + Lay::BAR_OFF;
-  const uint32_t bar_kfull = bars, bar_kempty = bars + 16, bar_vfull = bars + 32, bar_vempty = bars + 48;
-  const uint32_t bar_s = bars + 64, bar_p = bars + 72, bar_o = bars + 80, bar_q = bars + 88;
+  const uint32_t bar_kfull = bars, bar_kempty = bars + 8 * kStages;
+  const uint32_t bar_vfull = bars + 16 * kStages, bar_vempty = bars + 24 * kStages;
+  // per half h: barrier + 8 * h
+  const uint32_t bar_s = bars + 32 * kStages, bar_p = bar_s + 8 * kHalves, bar_o = bar_p + 8 * kHalves;
+  const uint32_t bar_q = bar_o + 8 * kHalves, bar_drain = bar_q + 8;
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS);
   int *unit_s = reinterpret_cast<int *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS + 4);
   int *stable = reinterpret_cast<int *>(smem_raw + Lay::TABLE_OFF);
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_base_s), Tm::COLS);
+    tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(bars + 8 * i, 1);  // full: producer, empty: MMA commits
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, kSoftmaxWarps);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < 4 * kStages; ++i) mbar_init(bars + 8 * i, 1);  // full: producer; empty: MMA commits
+    for (int h = 0; h < kHalves; ++h) {
+      mbar_init(bar_s + 8 * h, 1);
+      mbar_init(bar_p + 8 * h, 4);  // the half's four softmax warps
+      mbar_init(bar_o + 8 * h, 1);
+    }
     mbar_init(bar_q, kSoftmaxWarps);
+    mbar_init(bar_drain, 1);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
   }
@@ -134,12 +300,14 @@ __global__ void __launch_bounds__(kTileThreads, 2)
 
   const int Hkv = p.num_kv_heads;
   const int total_units = min(max(ld_cg(p.tile_count), 0), p.max_tiles) * Hkv;
-  // Per-role counters from which every mbarrier parity follows (they run on
-  // across units, like the barriers themselves).
-  uint32_t kload[2] = {0, 0}, vload[2] = {0, 0};  // producer: loads issued per buffer
-  uint32_t kseen[2] = {0, 0}, vseen[2] = {0, 0};  // MMA: loads consumed per buffer
-  uint32_t n_p = 0, n_q = 0;                      // MMA: softmax hand-offs consumed
-  uint32_t n_s = 0, n_o = 0;                      // softmax: S and P V products consumed
+  // Phase bookkeeping (it runs on across units, like the barriers). Each
+  // half's s_full, p_full and o_done complete once per range of that half,
+  // so range r of a unit is phase ph[h] + r. K(r) and V(r) sit in buffer
+  // r % 2 and are that buffer's load number kv[r % 2] + r / 2.
+  uint32_t ph[kHalves] = {0, 0};
+  uint32_t kv[kStages] = {0, 0};
+  uint32_t kiss[kStages] = {0, 0}, viss[kStages] = {0, 0};  // producer: loads actually issued per buffer
+  uint32_t n_q = 0;
   bool failed = false;
 
   for (;;) {
@@ -151,7 +319,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     const int4 r0 = ld_cg(p.tiles + 2 * item);
     const int4 r1 = ld_cg(p.tiles + 2 * item + 1);
     const int b = r0.x, row0 = r0.y, npos = r0.z, pos0 = r0.w, kv_end = r1.y;
-    const bool sane = b >= 0 && b < p.num_seqs && npos >= 1 && npos <= kTileRows / G && row0 >= 0 &&
+    const bool sane = b >= 0 && b < p.num_seqs && npos >= 1 && npos <= kPrefillTileRows / G && row0 >= 0 &&
                       row0 + npos <= p.total_q && pos0 >= 0 && kv_end == pos0 + npos &&
                       kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize;
     if (!sane) {
@@ -162,6 +330,13 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
     const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
     const int nkt = (kv_end + kKeyTile - 1) / kKeyTile;
+    // key ranges each half needs: up to its last valid position (0 = no valid rows)
+    int nkt_h[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      const int last = min(npos, (h + 1) * POS_PER_HALF);  // positions [h * POS_PER_HALF, last)
+      nkt_h[h] = last > h * POS_PER_HALF ? (pos0 + last + kKeyTile - 1) / kKeyTile : 0;
+    }
     for (int i = tid; i < min(nblk, Lay::TABLE_ENTRIES); i += kTileThreads) stable[i] = __ldg(table + i);
     __syncthreads();
 
@@ -169,11 +344,11 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       // ---------------- producer: K(j+1) ahead of V(j) ----------------
       if (lane == 0) {
         auto load = [&](int kt, bool is_v) {
-          const int buf = kt & 1;
-          uint32_t &n = is_v ? vload[buf] : kload[buf];
+          const int buf = kt % kStages;
+          const uint32_t n = kv[buf] + kt / kStages;  // loads into this buffer before this one
           if (n > 0) wait_or_fail((is_v ? bar_vempty : bar_kempty) + 8 * buf, (n - 1) & 1u, failed);
-          ++n;
           if (failed) return;
+          ++(is_v ? viss : kiss)[buf];
           const uint32_t bar = (is_v ? bar_vfull : bar_kfull) + 8 * buf;
           const uint32_t dst = (is_v ? sV0 : sK0) + buf * Lay::KV_BYTES;
           const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
@@ -190,211 +365,246 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                 flag_error(p.status, PA_FLAG_BLOCK_RANGE);
             }
 #pragma unroll
-            for (int h = 0; h < Lay::HALVES; ++h)
-              tma_load_3d(dst + h * Lay::KV_HALF + blk * 2048, map, bar, h * 64, kvh, z);
+            for (int a = 0; a < Lay::ATOMS; ++a)
+              tma_load_3d(dst + a * Lay::KV_ATOM + blk * 2048, map, bar, a * 64, kvh, z);
           }
         };
-        load(0, false);
+        // the order the products consume them: S(j) needs K(j) before P V(j) needs V(j)
         for (int j = 0; j < nkt; ++j) {
-          if (j + 1 < nkt) load(j + 1, false);
+          load(j, false);
           load(j, true);
         }
       }
     } else if (warp == kMmaWarp) {
-      // ---------------- MMA issue: S(kt), then P V of the previous range ----------------
+      // ---------------- MMA issue ----------------
       // The whole warp follows the loop (it zeroes the tail of the last V
-      // range); lane 0 alone issues tensor-core work and commits.
-      auto issue_pv = [&](int kt) {
-        const int buf = kt & 1;
-        wait_or_fail(bar_vfull + 8 * buf, vseen[buf] & 1u, failed);
-        ++vseen[buf];
-        const uint32_t sV = sV0 + buf * Lay::KV_BYTES;
-        const int key0 = kt * kKeyTile;
-        if (!failed && key0 + kKeyTile > kv_end) {
-          // rows of keys past kv_end may hold anything (even NaN): zero them in V
-          const int vr0 = kv_end - key0;
-          const int n = (kKeyTile - vr0) * (D / 8);
-          for (int i = lane; i < n; i += 32) {
-            const int rr = vr0 + i / (D / 8), c = i % (D / 8);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sV + Lay::off(rr, c, Lay::KV_HALF)),
-                         "r"(0u)
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
+      // range); lane 0 alone issues tensor-core work and commits. Range r is
+      // read by the halves with r < nkt_h: the first of them waits for the
+      // K/V loads, the last one's commit releases the buffers.
+      auto first_reader = [&](int kt) { return kt < nkt_h[0] ? 0 : 1; };
+      auto last_reader = [&](int kt) { return kt < nkt_h[1] ? 1 : 0; };
+      auto kv_parity = [&](int kt) { return (kv[kt % kStages] + kt / kStages) & 1u; };
+      constexpr uint32_t DHI = desc_hi(1024);
+      const uint32_t q_lo0 = desc_lo(sQ0, 16), q_lo1 = desc_lo(sQ0 + Lay::Q_BYTES, 16);
+      const uint32_t k_lo0 = desc_lo(sK0, 16), k_lo1 = desc_lo(sK0 + Lay::KV_BYTES, 16);
+      const uint32_t v_lo0 = desc_lo(sV0, Lay::KV_ATOM), v_lo1 = desc_lo(sV0 + Lay::KV_BYTES, Lay::KV_ATOM);
+      static_assert(kStages == 2 && kHalves == 2, "descriptor words are kept for two buffers and two halves");
+      auto mma_s = [&](int kt, int h) {
         if (lane == 0 && !failed) {
           tc_fence_after();
+          const uint32_t klo = (kt & 1) ? k_lo1 : k_lo0, qlo = h ? q_lo1 : q_lo0;
+          const uint32_t d = tmem + h * Tm::HALF + Tm::SP;
+          mma_ss<0>(d, qlo, DHI, klo, DHI, IDESC_S);
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS_O; ++ks) {
-            const uint64_t vd = sw128_desc(sV + ks * 2048, Lay::KV_HALF, 1024);
-            tc_mma_f16_ta(tmem + Tm::O, tmem + Tm::PHI + ks * 8, vd, IDESC_O, (kt > 0 || ks > 0) ? 1u : 0u);
-            tc_mma_f16_ta(tmem + Tm::O, tmem + Tm::PLO + ks * 8, vd, IDESC_O, 1u);
+          for (int ks = 1; ks < KSTEPS_S; ++ks) {
+            const uint32_t qo = ((ks >> 2) * Lay::Q_ATOM + (ks & 3) * 32) >> 4;
+            const uint32_t ko = ((ks >> 2) * Lay::KV_ATOM + (ks & 3) * 32) >> 4;
+            mma_ss<1>(d, qlo + qo, DHI, klo + ko, DHI, IDESC_S);
           }
-          tc_commit(bar_o);
-          tc_commit(bar_vempty + 8 * buf);
+          tc_commit(bar_s + 8 * h);
+          if (h == last_reader(kt)) tc_commit(bar_kempty + 8 * (kt % kStages));
         }
         __syncwarp();
       };
       wait_or_fail(bar_q, n_q & 1u, failed);
       ++n_q;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const int buf = kt & 1;
-        wait_or_fail(bar_kfull + 8 * buf, kseen[buf] & 1u, failed);
-        ++kseen[buf];
-        if (kt > 0) {  // softmax of the previous range is done: S is free, its P is ready
-          wait_or_fail(bar_p, n_p & 1u, failed);
-          ++n_p;
-        }
-        if (lane == 0 && !failed) {
-          tc_fence_after();
-          const uint32_t sK = sK0 + buf * Lay::KV_BYTES;
+      if (nkt > 0) {
+        wait_or_fail(bar_kfull, kv_parity(0), failed);
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS_S; ++ks) {
-            const uint64_t a = sw128_desc(sQ + (ks >> 2) * Lay::Q_HALF + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = sw128_desc(sK + (ks >> 2) * Lay::KV_HALF + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem + Tm::S, a, bd, IDESC_S, ks > 0);
-          }
-          tc_commit(bar_s);
-          tc_commit(bar_kempty + 8 * buf);
-        }
-        __syncwarp();
-        if (kt > 0) issue_pv(kt - 1);
+        for (int h = 0; h < kHalves; ++h)
+          if (nkt_h[h] > 0) mma_s(0, h);
       }
-      wait_or_fail(bar_p, n_p & 1u, failed);
-      ++n_p;
-      issue_pv(nkt - 1);
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int vbuf = kt % kStages;
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h) {
+          if (kt >= nkt_h[h]) continue;
+          wait_or_fail(bar_p + 8 * h, (ph[h] + kt) & 1u, failed);  // P(kt) is in place
+          if (h == first_reader(kt)) {
+            wait_or_fail(bar_vfull + 8 * vbuf, kv_parity(kt), failed);
+            const int key0 = kt * kKeyTile;
+            if (!failed && key0 + kKeyTile > kv_end) {
+              // rows of keys past kv_end may hold anything (even NaN): zero them in V
+              const uint32_t sV = sV0 + vbuf * Lay::KV_BYTES;
+              const int vr0 = kv_end - key0;
+              const int n = (kKeyTile - vr0) * (D / 8);
+              for (int i = lane; i < n; i += 32) {
+                const int rr = vr0 + i / (D / 8), c = i % (D / 8);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sV + Lay::off(rr, c, Lay::KV_ATOM)),
+                             "r"(0u)
+                             : "memory");
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+          if (lane == 0 && !failed) {
+            tc_fence_after();
+            const uint32_t vlo = (kt & 1) ? v_lo1 : v_lo0;
+            const uint32_t t = tmem + h * Tm::HALF;
+            if (kt == 0)
+              mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);  // the unit's first product overwrites O
+            else
+              mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);
+            mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, DHI, IDESC_O);
+#pragma unroll
+            for (int ks = 1; ks < KSTEPS_O; ++ks) {
+              const uint32_t vo = (ks * 2048) >> 4;  // 16 keys x 128 B per K step
+              mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks, vlo + vo, DHI, IDESC_O);
+              mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vo, DHI, IDESC_O);
+            }
+            tc_commit(bar_o + 8 * h);
+            if (h == last_reader(kt)) tc_commit(bar_vempty + 8 * vbuf);
+          }
+          __syncwarp();
+          if (kt + 1 < nkt_h[h]) {
+            if (h == first_reader(kt + 1)) wait_or_fail(bar_kfull + 8 * ((kt + 1) % kStages), kv_parity(kt + 1), failed);
+            wait_or_fail(bar_o + 8 * h, (ph[h] + kt) & 1u, failed);  // P V(kt) has read P(kt)
+            mma_s(kt + 1, h);
+          }
+        }
+      }
     } else {
       // ---------------- softmax: one row per thread (its TMEM lane) ----------------
-      const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-      const int r = tid, qi = r / G, g = r % G;
+      const int h = warp / 4;
+      const int r = tid % kHalfRows;  // row within the half = TMEM lane
+      const uint32_t t_lane = tmem + h * Tm::HALF + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+      const int qi = h * POS_PER_HALF + r / G, g = r % G;
       const bool row_valid = qi < npos;
-      {  // Q tile: row r = (position r / G, head r % G), K-major, swizzled
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(
-            p.q + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.q_stride + static_cast<int64_t>(kvh * G + g) * D);
+      const int nk = nkt_h[h];
+      {  // Q of the half: row r = (position, head), K-major, swizzled
+        const uint32_t sQ = sQ0 + h * Lay::Q_BYTES;
+        const bf16 *qrow =
+            p.q + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.q_stride + static_cast<int64_t>(kvh * G + g) * D;
+        // q is only required to be 4-byte aligned: 16-byte loads when rows allow them
+        const bool q16 = (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 && (p.q_stride & 7) == 0;
 #pragma unroll 4
         for (int c = 0; c < D / 8; ++c) {
-          uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
           if (row_valid) {
-            w0 = __ldg(src + 4 * c);
-            w1 = __ldg(src + 4 * c + 1);
-            w2 = __ldg(src + 4 * c + 2);
-            w3 = __ldg(src + 4 * c + 3);
+            if (q16) {
+              w = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+            } else {
+              const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow) + 4 * c;
+              w = make_uint4(__ldg(q32), __ldg(q32 + 1), __ldg(q32 + 2), __ldg(q32 + 3));
+            }
           }
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + Lay::off(r, c, Lay::Q_HALF)),
-                       "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + Lay::off(r, c, Lay::Q_ATOM)),
+                       "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
                        : "memory");
         }
         fence_proxy_async_smem();  // the MMA reads Q through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q);
       }
+      const float sl2 = p.scale_log2;  // > 0: the max of raw scores gives the max of scaled ones
       float m_used = -INFINITY, l = 0.f;
       const int lim = row_valid ? pos0 + qi + 1 : 0;  // keys j < lim are visible to this row
-      for (int kt = 0; kt < nkt; ++kt) {
+      for (int kt = 0; kt < nk; ++kt) {
         const int key0 = kt * kKeyTile;
-        wait_or_fail(bar_s, n_s & 1u, failed);
-        ++n_s;
+        const uint32_t sp = t_lane + Tm::SP;
+        wait_or_fail(bar_s + 8 * h, (ph[h] + kt) & 1u, failed);
         tc_fence_after();
-        float x[kKeyTile];
-        {
-          float s0[32], s1[32];
-          tmem_ld32(t_lane + Tm::S, s0);
-          tmem_ld32(t_lane + Tm::S + 32, s1);
-          if (key0 + kKeyTile <= lim) {  // every key of the range is visible to this row
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = s0[i] * p.scale_log2;
-              x[32 + i] = s1[i] * p.scale_log2;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = key0 + i < lim ? s0[i] * p.scale_log2 : -INFINITY;
-              x[32 + i] = key0 + 32 + i < lim ? s1[i] * p.scale_log2 : -INFINITY;
-            }
-          }
-        }
-        float t8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float a = fmaxf(fmaxf(x[j], x[j + 8]), fmaxf(x[j + 16], x[j + 24]));
-          float c = fmaxf(fmaxf(x[j + 32], x[j + 40]), fmaxf(x[j + 48], x[j + 56]));
-          t8[j] = fmaxf(a, c);
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
-                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
-        // the previous product must be complete before O is rescaled or P rewritten
-        if (kt > 0) {
-          wait_or_fail(bar_o, n_o & 1u, failed);
-          ++n_o;
-          tc_fence_after();
-        }
-        if (mx > -INFINITY && (m_used == -INFINITY || mx > m_used + kRescaleLog2)) {
-          if (kt > 0 && m_used > -INFINITY) {
-            const float alpha = ex2_approx(m_used - mx);
-            l *= alpha;
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              float t[32];
-              tmem_ld32(t_lane + Tm::O + ch * 32, t);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) t[i] *= alpha;
-              tmem_st32(t_lane + Tm::O + ch * 32, t);
+        // One pass over the range, 32 keys at a time: each chunk's maximum is
+        // checked against the running one before its probabilities are taken.
+        float sum = 0.f;     // this range's probabilities, against m_used
+        float alpha = 1.f;   // factor owed by O and l for growth within this range
+#pragma unroll 1
+        for (int c = 0; c < kKeyTile / 32; ++c) {
+          const int ck0 = key0 + 32 * c;
+          uint32_t sv[32], u[32];
+          tmem_ld32_wait(sp + 32 * c, sv);
+          const float cm = sl2 * masked_max32(sv, ck0, lim);
+          const bool grow = cm > -INFINITY && (m_used == -INFINITY || cm > m_used + kRescaleLog2);
+          if (__any_sync(0xffffffffu, grow)) {
+            // The row's maximum grew past the threshold (always in a row's
+            // first visible chunk, rarely after): what was taken against the
+            // old maximum (this range's sum and stored chunks, and O and l)
+            // is scaled by 2^(old - new). TMEM accesses are warp-wide, so the
+            // warp does it together (factor 1 in rows that did not grow).
+            const float a = grow && m_used > -INFINITY ? ex2_approx(m_used - cm) : 1.f;
+            if (grow) m_used = cm;
+            sum *= a;
+            alpha *= a;
+            if (c > 0) {
+              tmem_wait_st();  // the chunks stored so far are read back
+#pragma unroll 1
+              for (int cc = 0; cc < c; ++cc) rescale_p32(sp + 32 * cc, a);
             }
           }
-          m_used = mx;
+          probs32(sv, ck0, lim, sl2, m_used == -INFINITY ? 0.f : m_used, sum, u);
+          tmem_st32u(sp + 32 * c, u);  // P over the scores it came from
         }
-        const float ms = m_used == -INFINITY ? 0.f : m_used;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t hi[kKeyTile / 2], lo[kKeyTile / 2];
+        // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
+        // last of them finished).
+        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t t[32];
+            tmem_ld32_wait(t_lane + Tm::O + ch * 32, t);
 #pragma unroll
-        for (int i = 0; i < kKeyTile / 2; ++i) {
-          const float p0 = ex2_approx(x[2 * i] - ms);
-          const float p1 = ex2_approx(x[2 * i + 1] - ms);
-          rs4[i & 3] += p0 + p1;
-          hi[i] = pack_bf16x2(p0, p1);
-          lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+            for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st32u(t_lane + Tm::O + ch * 32, t);
+          }
         }
-        tmem_st32u(t_lane + Tm::PHI, hi);
-        tmem_st32u(t_lane + Tm::PLO, lo);
+        l = l * alpha + sum;
         tmem_wait_st();
-        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p);
+        if (lane == 0) mbar_arrive(bar_p + 8 * h);
       }
-      // epilogue: the last P V product, normalised
-      wait_or_fail(bar_o, n_o & 1u, failed);
-      ++n_o;
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      bf16 *dst = p.out + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.num_heads * D +
-                  static_cast<int64_t>(kvh * G + g) * D;
+      if (nk > 0) {
+        // epilogue: the half's last P V product, normalised
+        wait_or_fail(bar_o + 8 * h, (ph[h] + nk - 1) & 1u, failed);
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        bf16 *dst = p.out + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.num_heads * D +
+                    static_cast<int64_t>(kvh * G + g) * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        float t[32];
-        tmem_ld32(t_lane + Tm::O + ch * 32, t);
-        if (row_valid && !failed) {
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t t[64];
+          tmem_ld64_wait(t_lane + Tm::O + ch * 64, t);
+          if (row_valid && !failed) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = make_uint4(pack_bf16x2(t[8 * c] * inv, t[8 * c + 1] * inv),
-                                       pack_bf16x2(t[8 * c + 2] * inv, t[8 * c + 3] * inv),
-                                       pack_bf16x2(t[8 * c + 4] * inv, t[8 * c + 5] * inv),
-                                       pack_bf16x2(t[8 * c + 6] * inv, t[8 * c + 7] * inv));
-            *reinterpret_cast<uint4 *>(dst + ch * 32 + 8 * c) = v;
+            for (int c = 0; c < 8; ++c) {
+              const float *f = reinterpret_cast<const float *>(&t[8 * c]);
+              const uint4 v = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                                         pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+              *reinterpret_cast<uint4 *>(dst + ch * 64 + 8 * c) = v;
+            }
           }
         }
       }
       tc_fence_before();  // O is overwritten by the next unit's first product after the unit barrier
     }
+    // every role advances the phase bookkeeping alike
+#pragma unroll
+    for (int hh = 0; hh < kHalves; ++hh) ph[hh] += nkt_h[hh];
+    kv[0] += (nkt + 1) >> 1;
+    kv[1] += nkt >> 1;
   }
 
+  // Every thread left the loop at the same unit barrier. Before tensor memory
+  // and shared memory go away, wait (bounded) for work still in flight: the
+  // MMA thread's products (one last commit) and, after a timeout, the
+  // producer's loads that no product consumed (loads into a buffer complete
+  // in order, so waiting for the last one issued suffices).
+  if (warp == kMmaWarp && lane == 0) {
+    tc_commit(bar_drain);
+    if (!mbar_wait_bounded(bar_drain, 0, kTcWaitTimeoutNs)) failed = true;
+  }
+  if (warp == kTmaWarp && lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) {
+      if (kiss[i] > 0 && !mbar_wait_bounded(bar_kfull + 8 * i, (kiss[i] - 1) & 1u, kTcWaitTimeoutNs)) failed = true;
+      if (viss[i] > 0 && !mbar_wait_bounded(bar_vfull + 8 * i, (viss[i] - 1) & 1u, kTcWaitTimeoutNs)) failed = true;
+    }
+  }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, Tm::COLS);
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int D, int G>
@@ -404,9 +614,9 @@ cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vma
   auto kern = prefill_tile_kernel<D, G>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);  // two CTAs per SM
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (err != cudaSuccess) return err;
-  int64_t grid = static_cast<int64_t>(sm_count) * 2;
+  int64_t grid = sm_count;  // one CTA per SM: it holds all of the SM's tensor memory
   const int64_t units = static_cast<int64_t>(tp.max_tiles) * tp.num_kv_heads;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;

@@ -75,7 +75,7 @@ struct PlanParams {
   int32_t *tile_count;    // [1]
   int32_t *tile_counter;  // [1], zeroed here, consumed by the tile kernel
   int32_t max_tiles;
-  int32_t tile_pos;       // query positions per tile: 128 / G
+  int32_t tile_pos;       // query positions per tile: kPrefillTileRows / G
   unsigned int *status;
 };
 
@@ -114,7 +114,8 @@ struct AttnParams {
 // ---------------------------------------------------------------------------
 // A request whose query rows fit one column group (query_len <= 8 / G: decode
 // tokens, speculative drafts) becomes split-KV decode items; a longer one
-// (a chunked-prefill chunk) becomes tensor-core tiles of 128 / G positions.
+// (a chunked-prefill chunk) becomes tensor-core tiles of kPrefillTileRows / G
+// positions.
 // Returns the number of decode items; *ntiles receives the number of tiles.
 __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0, int &ql, int &L, int &np,
                                              int &ntiles) {
@@ -778,7 +779,7 @@ bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, in
   w.part_tokens = partition_tokens(num_seqs, max_seq_len, num_kv_heads);
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.part_tokens - 1) / w.part_tokens : 1;
   const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts;  // decode items: one group per request
-  const int64_t tiles = (static_cast<int64_t>(total_q) * G + 127) / 128 + num_seqs;
+  const int64_t tiles = (static_cast<int64_t>(total_q) * G + kPrefillTileRows - 1) / kPrefillTileRows + num_seqs;
   if (items * num_kv_heads > (1LL << 30) || tiles * num_kv_heads > (1LL << 30)) return false;
   w.max_items = static_cast<int32_t>(items > 0 ? items : 1);
   w.max_tiles = static_cast<int32_t>(tiles > 0 ? tiles : 1);
@@ -853,7 +854,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.tile_counter = pp.item_count + 3;
   pp.tiles = reinterpret_cast<int4 *>(ws + w.tiles);
   pp.max_tiles = w.max_tiles;
-  pp.tile_pos = 128 / G;
+  pp.tile_pos = kPrefillTileRows / G;
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;

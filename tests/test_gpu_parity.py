@@ -63,12 +63,37 @@ SMALL_CASES = {
                                  num_heads=4, num_kv_heads=4, head_dim=128),
     "mixed_chunks_g8_d64": dict(context_lens=[10, 800, 0], query_lens=[5, 1, 24],
                                 num_heads=16, num_kv_heads=2, head_dim=64),
+    # chunks that fill both 128-row halves of a tile, several tiles and a ragged tail
+    "long_chunks_g1_d64": dict(context_lens=[0, 1000, 5], query_lens=[300, 260, 129],
+                               num_heads=4, num_kv_heads=4, head_dim=64),
+    "long_chunks_g2_d128": dict(context_lens=[130, 0], query_lens=[389, 1],
+                                num_heads=8, num_kv_heads=4, head_dim=128),
+    # sharp scores over several 128-key ranges: row maxima grow within ranges
+    "sharp_long_chunks_g4_d128": dict(context_lens=[200, 0], query_lens=[300, 130], num_heads=8, num_kv_heads=2,
+                                      head_dim=128, q_scale=8.0),
     "empty_requests": dict(context_lens=[10, 0, 700, 33], query_lens=[0, 1, 0, 3],
                            num_heads=8, num_kv_heads=2, head_dim=128),
     "sharp_scores": dict(context_lens=[300, 1800, 4], query_lens=[1, 1, 9], num_heads=32, num_kv_heads=8,
                          head_dim=128, q_scale=8.0),
     "seq_len_one": dict(context_lens=[0, 0, 0], query_lens=[1, 1, 1], num_heads=8, num_kv_heads=2, head_dim=64),
 }
+
+
+def test_growing_key_norms_rescale_within_ranges(oracle):
+    # Keys whose norm grows along the chunk make each row's running maximum
+    # jump by more than 2^8 inside a 128-key range again and again, so the
+    # probabilities already written for the range, O and the row sum are
+    # rescaled mid-range (the prefill tile path; G = 4 and G = 1).
+    for heads, kv_heads, d in ((8, 2, 128), (4, 4, 64)):
+        w = W.make_workload("growing_keys", context_lens=[0, 37], query_lens=[256, 200], num_heads=heads,
+                            num_kv_heads=kv_heads, head_dim=d, seed=11, q_scale=2.0)
+        k = W.bf16_bits_to_f32(w.key)
+        q0 = np.asarray(w.query_start_loc)
+        for b in range(w.num_seqs):
+            n = int(q0[b + 1] - q0[b])
+            k[q0[b]:q0[b + 1]] *= (1.0 + np.arange(n, dtype=np.float32) / 8.0)[:, None, None]
+        w.key = W.f32_to_bf16_bits(k)
+        run_and_check(w, oracle)
 
 
 def test_tiny_decode(oracle):

@@ -74,6 +74,7 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 0, 1, 64, 16, 1, 0, None) == 0
     assert lib.pa_attention_set_timing_events(None, None) == 0
     assert lib.pa_launch_count() == 0
+    assert lib.pa_last_cuda_error() == b"cudaSuccess"
 
 
 def test_missing_library_fails_loudly(tmp_path):
