@@ -17,8 +17,9 @@
 // by three kinds of warps that hand work over through mbarriers only:
 //   * a producer warp issues TMA loads of the (block, KV head) tiles of K and
 //     V through the block table into 128-byte-swizzled shared memory (the
-//     decode path's boxes), two buffers each with full/empty barriers, in
-//     the order the products consume them;
+//     decode path's boxes), into one ring of K(0), V(0), K(1), V(1), ...
+//     (as many 128-key slots as shared memory holds: five at D = 128), each
+//     slot with full/empty barriers, so loads run two ranges ahead;
 //   * an MMA warp issues tcgen05.mma. Each half owns one score buffer in
 //     tensor memory: S(r) = Q K(r)^T lands there, the softmax overwrites it
 //     in place with P(r), and O += P_hi(r) V(r) + P_lo(r) V(r) reads P from
@@ -51,7 +52,7 @@ constexpr int kHalfRows = 128;  // UMMA M: rows per half
 constexpr int kHalves = kPrefillTileRows / kHalfRows;
 static_assert(kHalves == 2, "the pipeline interleaves exactly two halves");
 constexpr int kKeyTile = 128;  // keys per range (UMMA N of S, K of P V)
-constexpr int kStages = 2;     // depth of the K and V rings
+constexpr int kMaxSlots = 8;   // K/V ring slots (as many as shared memory holds)
 constexpr int kSoftmaxWarps = 4 * kHalves, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
 constexpr int kTileThreads = 32 * (kTmaWarp + 1);
 constexpr uint64_t kTcWaitTimeoutNs = 2000000000;
@@ -74,16 +75,19 @@ struct TcLayout {
   static constexpr int Q_ATOM = kHalfRows * 128;   // 128 rows x 128 B
   static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
-  static constexpr int KV_BYTES = ATOMS * KV_ATOM;
-  static constexpr int Q_OFF = 0;                               // Q of halves A and B
-  static constexpr int K_OFF = Q_OFF + kHalves * Q_BYTES;       // kStages K buffers
-  static constexpr int V_OFF = K_OFF + kStages * KV_BYTES;      // kStages V buffers
-  static constexpr int TABLE_OFF = V_OFF + kStages * KV_BYTES;  // the tile's block-table entries
-  static constexpr int TABLE_ENTRIES = 1024;                    // keys < 16384 read from here
-  static constexpr int BAR_OFF = TABLE_OFF + TABLE_ENTRIES * 4;
-  // barriers: k_full[S], k_empty[S], v_full[S], v_empty[S], per half s_full, p_full, o_done,
+  static constexpr int KV_BYTES = ATOMS * KV_ATOM;             // one K or V range: a ring slot
+  static constexpr int TABLE_ENTRIES = 512;                     // keys < 8192 read from here
+  // barriers: full[kMaxSlots], empty[kMaxSlots], per half s_full, p_full, o_done,
   // then q_full and drain (the MMA thread's last commit)
-  static constexpr int NBARS = 4 * kStages + 3 * kHalves + 2;
+  static constexpr int NBARS = 2 * kMaxSlots + 3 * kHalves + 2;
+  static constexpr int FIXED = kHalves * Q_BYTES + TABLE_ENTRIES * 4 + 8 * NBARS + 16;
+  static constexpr int FIT = (227 * 1024 - FIXED) / KV_BYTES;
+  static constexpr int SLOTS = FIT < kMaxSlots ? FIT : kMaxSlots;
+  static_assert(SLOTS >= 4, "the ring holds at least K and V of two ranges");
+  static constexpr int Q_OFF = 0;                                // Q of halves A and B
+  static constexpr int RING_OFF = Q_OFF + kHalves * Q_BYTES;     // K(0), V(0), K(1), V(1), ... in SLOTS slots
+  static constexpr int TABLE_OFF = RING_OFF + SLOTS * KV_BYTES;  // the tile's block-table entries
+  static constexpr int BAR_OFF = TABLE_OFF + TABLE_ENTRIES * 4;
   static constexpr int BYTES = BAR_OFF + 8 * NBARS + 16;
   // Shared memory requested per CTA: more than half an SM's, so that a second
   // CTA (which would wait for TMEM) never lands on the same SM.
@@ -264,12 +268,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
     return;
   }
-  const uint32_t sQ0 = base + Lay::Q_OFF, sK0 = base + Lay::K_OFF, sV0 = base + Lay::V_OFF;
+  constexpr int SLOTS = Lay::SLOTS;
+  const uint32_t sQ0 = base + Lay::Q_OFF, sRing = base + Lay::RING_OFF;
   const uint32_t bars = base + Lay::BAR_OFF;
-  const uint32_t bar_kfull = bars, bar_kempty = bars + 8 * kStages;
-  const uint32_t bar_vfull = bars + 16 * kStages, bar_vempty = bars + 24 * kStages;
+  const uint32_t bar_full = bars, bar_empty = bars + 8 * kMaxSlots;  // per ring slot: barrier + 8 * slot
   // per half h: barrier + 8 * h
-  const uint32_t bar_s = bars + 32 * kStages, bar_p = bar_s + 8 * kHalves, bar_o = bar_p + 8 * kHalves;
+  const uint32_t bar_s = bars + 16 * kMaxSlots, bar_p = bar_s + 8 * kHalves, bar_o = bar_p + 8 * kHalves;
   const uint32_t bar_q = bar_o + 8 * kHalves, bar_drain = bar_q + 8;
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS);
   int *unit_s = reinterpret_cast<int *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS + 4);
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 4 * kStages; ++i) mbar_init(bars + 8 * i, 1);  // full: producer; empty: MMA commits
+    for (int i = 0; i < 2 * kMaxSlots; ++i) mbar_init(bars + 8 * i, 1);  // full: producer; empty: MMA commits
     for (int h = 0; h < kHalves; ++h) {
       mbar_init(bar_s + 8 * h, 1);
       mbar_init(bar_p + 8 * h, 4);  // the half's four softmax warps
@@ -302,11 +306,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const int total_units = min(max(ld_cg(p.tile_count), 0), p.max_tiles) * Hkv;
   // Phase bookkeeping (it runs on across units, like the barriers). Each
   // half's s_full, p_full and o_done complete once per range of that half,
-  // so range r of a unit is phase ph[h] + r. K(r) and V(r) sit in buffer
-  // r % 2 and are that buffer's load number kv[r % 2] + r / 2.
+  // so range r of a unit is phase ph[h] + r. The ring carries K(0), V(0),
+  // K(1), V(1), ... of every unit in turn: load number g = ring0 + 2 r (+1
+  // for V) sits in slot g % SLOTS as that slot's use g / SLOTS.
   uint32_t ph[kHalves] = {0, 0};
-  uint32_t kv[kStages] = {0, 0};
-  uint32_t kiss[kStages] = {0, 0}, viss[kStages] = {0, 0};  // producer: loads actually issued per buffer
+  uint32_t ring0 = 0;
+  uint32_t issued = 0;  // producer: loads actually issued
   uint32_t n_q = 0;
   bool failed = false;
 
@@ -344,13 +349,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       // ---------------- producer: K(j+1) ahead of V(j) ----------------
       if (lane == 0) {
         auto load = [&](int kt, bool is_v) {
-          const int buf = kt % kStages;
-          const uint32_t n = kv[buf] + kt / kStages;  // loads into this buffer before this one
-          if (n > 0) wait_or_fail((is_v ? bar_vempty : bar_kempty) + 8 * buf, (n - 1) & 1u, failed);
+          const uint32_t g = ring0 + 2 * kt + (is_v ? 1 : 0);
+          const uint32_t slot = g % SLOTS, use = g / SLOTS;
+          if (use > 0) wait_or_fail(bar_empty + 8 * slot, (use - 1) & 1u, failed);
           if (failed) return;
-          ++(is_v ? viss : kiss)[buf];
-          const uint32_t bar = (is_v ? bar_vfull : bar_kfull) + 8 * buf;
-          const uint32_t dst = (is_v ? sV0 : sK0) + buf * Lay::KV_BYTES;
+          issued = g + 1;
+          const uint32_t bar = bar_full + 8 * slot;
+          const uint32_t dst = sRing + slot * Lay::KV_BYTES;
           const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
           mbar_arrive_expect_tx(bar, Lay::KV_BYTES);
 #pragma unroll
@@ -383,16 +388,18 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       // K/V loads, the last one's commit releases the buffers.
       auto first_reader = [&](int kt) { return kt < nkt_h[0] ? 0 : 1; };
       auto last_reader = [&](int kt) { return kt < nkt_h[1] ? 1 : 0; };
-      auto kv_parity = [&](int kt) { return (kv[kt % kStages] + kt / kStages) & 1u; };
+      // ring slot of K(kt) (v = 0) or V(kt) (v = 1), and the parity of its full barrier
+      auto slot_of = [&](int kt, int v) { return (ring0 + 2 * kt + v) % SLOTS; };
+      auto full_parity = [&](int kt, int v) { return ((ring0 + 2 * kt + v) / SLOTS) & 1u; };
       constexpr uint32_t DHI = desc_hi(1024);
       const uint32_t q_lo0 = desc_lo(sQ0, 16), q_lo1 = desc_lo(sQ0 + Lay::Q_BYTES, 16);
-      const uint32_t k_lo0 = desc_lo(sK0, 16), k_lo1 = desc_lo(sK0 + Lay::KV_BYTES, 16);
-      const uint32_t v_lo0 = desc_lo(sV0, Lay::KV_ATOM), v_lo1 = desc_lo(sV0 + Lay::KV_BYTES, Lay::KV_ATOM);
-      static_assert(kStages == 2 && kHalves == 2, "descriptor words are kept for two buffers and two halves");
+      const uint32_t k_lo = desc_lo(sRing, 16), v_lo = desc_lo(sRing, Lay::KV_ATOM);  // slot 0
+      constexpr uint32_t SLOT_STEP = Lay::KV_BYTES >> 4;                            // per slot
+      static_assert(kHalves == 2, "descriptor words are kept for two halves");
       auto mma_s = [&](int kt, int h) {
         if (lane == 0 && !failed) {
           tc_fence_after();
-          const uint32_t klo = (kt & 1) ? k_lo1 : k_lo0, qlo = h ? q_lo1 : q_lo0;
+          const uint32_t klo = k_lo + slot_of(kt, 0) * SLOT_STEP, qlo = h ? q_lo1 : q_lo0;
           const uint32_t d = tmem + h * Tm::HALF + Tm::SP;
           mma_ss<0>(d, qlo, DHI, klo, DHI, IDESC_S);
 #pragma unroll
@@ -402,30 +409,30 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             mma_ss<1>(d, qlo + qo, DHI, klo + ko, DHI, IDESC_S);
           }
           tc_commit(bar_s + 8 * h);
-          if (h == last_reader(kt)) tc_commit(bar_kempty + 8 * (kt % kStages));
+          if (h == last_reader(kt)) tc_commit(bar_empty + 8 * slot_of(kt, 0));
         }
         __syncwarp();
       };
       wait_or_fail(bar_q, n_q & 1u, failed);
       ++n_q;
       if (nkt > 0) {
-        wait_or_fail(bar_kfull, kv_parity(0), failed);
+        wait_or_fail(bar_full + 8 * slot_of(0, 0), full_parity(0, 0), failed);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h)
           if (nkt_h[h] > 0) mma_s(0, h);
       }
       for (int kt = 0; kt < nkt; ++kt) {
-        const int vbuf = kt % kStages;
+        const uint32_t vslot = slot_of(kt, 1);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
           if (kt >= nkt_h[h]) continue;
           wait_or_fail(bar_p + 8 * h, (ph[h] + kt) & 1u, failed);  // P(kt) is in place
           if (h == first_reader(kt)) {
-            wait_or_fail(bar_vfull + 8 * vbuf, kv_parity(kt), failed);
+            wait_or_fail(bar_full + 8 * vslot, full_parity(kt, 1), failed);
             const int key0 = kt * kKeyTile;
             if (!failed && key0 + kKeyTile > kv_end) {
               // rows of keys past kv_end may hold anything (even NaN): zero them in V
-              const uint32_t sV = sV0 + vbuf * Lay::KV_BYTES;
+              const uint32_t sV = sRing + vslot * Lay::KV_BYTES;
               const int vr0 = kv_end - key0;
               const int n = (kKeyTile - vr0) * (D / 8);
               for (int i = lane; i < n; i += 32) {
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           }
           if (lane == 0 && !failed) {
             tc_fence_after();
-            const uint32_t vlo = (kt & 1) ? v_lo1 : v_lo0;
+            const uint32_t vlo = v_lo + vslot * SLOT_STEP;
             const uint32_t t = tmem + h * Tm::HALF;
             if (kt == 0)
               mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);  // the unit's first product overwrites O
@@ -454,11 +461,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
               mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vo, DHI, IDESC_O);
             }
             tc_commit(bar_o + 8 * h);
-            if (h == last_reader(kt)) tc_commit(bar_vempty + 8 * vbuf);
+            if (h == last_reader(kt)) tc_commit(bar_empty + 8 * vslot);
           }
           __syncwarp();
           if (kt + 1 < nkt_h[h]) {
-            if (h == first_reader(kt + 1)) wait_or_fail(bar_kfull + 8 * ((kt + 1) % kStages), kv_parity(kt + 1), failed);
+            if (h == first_reader(kt + 1))
+              wait_or_fail(bar_full + 8 * slot_of(kt + 1, 0), full_parity(kt + 1, 0), failed);
             wait_or_fail(bar_o + 8 * h, (ph[h] + kt) & 1u, failed);  // P V(kt) has read P(kt)
             mma_s(kt + 1, h);
           }
@@ -505,6 +513,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t sp = t_lane + Tm::SP;
         wait_or_fail(bar_s + 8 * h, (ph[h] + kt) & 1u, failed);
         tc_fence_after();
+        // One pass over the range, 32 keys at a time: each chunk's maximum is
+        // checked against the running one before its probabilities are taken.
         // One pass over the range, 32 keys at a time: each chunk's maximum is
         // checked against the running one before its probabilities are taken.
         float sum = 0.f;     // this range's probabilities, against m_used
@@ -580,8 +590,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // every role advances the phase bookkeeping alike
 #pragma unroll
     for (int hh = 0; hh < kHalves; ++hh) ph[hh] += nkt_h[hh];
-    kv[0] += (nkt + 1) >> 1;
-    kv[1] += nkt >> 1;
+    ring0 += 2 * nkt;
   }
 
   // Every thread left the loop at the same unit barrier. Before tensor memory
@@ -594,11 +603,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (!mbar_wait_bounded(bar_drain, 0, kTcWaitTimeoutNs)) failed = true;
   }
   if (warp == kTmaWarp && lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kStages; ++i) {
-      if (kiss[i] > 0 && !mbar_wait_bounded(bar_kfull + 8 * i, (kiss[i] - 1) & 1u, kTcWaitTimeoutNs)) failed = true;
-      if (viss[i] > 0 && !mbar_wait_bounded(bar_vfull + 8 * i, (viss[i] - 1) & 1u, kTcWaitTimeoutNs)) failed = true;
-    }
+    for (uint32_t g = issued > SLOTS ? issued - SLOTS : 0; g < issued; ++g)
+      if (!mbar_wait_bounded(bar_full + 8 * (g % SLOTS), (g / SLOTS) & 1u, kTcWaitTimeoutNs)) failed = true;
   }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
   tc_fence_before();
