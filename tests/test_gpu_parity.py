@@ -50,6 +50,8 @@ SMALL_CASES = {
                                   query_lens=[1] * 12, num_heads=32, num_kv_heads=8, head_dim=128),
     "decode_g8_d128_long": dict(context_lens=[4999, 700, 32], query_lens=[1] * 3,
                                 num_heads=64, num_kv_heads=8, head_dim=128),
+    # one very long request: few (request, KV head) pairs, so partitions of 1024 keys
+    "single_long_request_g8": dict(context_lens=[99999], query_lens=[1], num_heads=64, num_kv_heads=8, head_dim=128),
     "decode_g1_d64": dict(context_lens=[100, 1, 900, 513], query_lens=[1] * 4,
                           num_heads=4, num_kv_heads=4, head_dim=64),
     "decode_g2_d64": dict(context_lens=[30, 1400, 7], query_lens=[1] * 3,

@@ -66,14 +66,14 @@ def test_static_workspace_refuses_problems_that_do_not_fit():
     st = DeviceStep(w)
     launches = B.pa_launch_count()
     lib = B._lib()
-    big_seq = 1 << 22  # a 4M-token bound needs far more partials than the array holds
+    big_seq = 1 << 25  # a 32M-token bound needs more partials than the array holds, at any partition size
+    assert B.pa_attention_workspace_size(w.num_seqs, w.total_q, st.max_query_len, big_seq, w.num_heads,
+                                         w.num_kv_heads, w.head_dim) > B.PA_STATIC_WORKSPACE_BYTES
     rc = lib.pa_attention_varlen_static(
         st.q.data_ptr(), st.q.stride(0), st.key_cache.data_ptr(), st.value_cache.data_ptr(),
         st.block_tables.data_ptr(), st.block_tables.shape[1], st.seq_lens.data_ptr(), st.query_start_loc.data_ptr(),
         w.num_seqs, w.total_q, st.max_query_len, big_seq, w.num_heads, w.num_kv_heads, w.head_dim,
         w.block_size, w.num_blocks, ctypes.c_float(w.scale), st.out.data_ptr(), B.PA_BF16,
         torch.cuda.current_stream().cuda_stream)
-    assert B.pa_attention_workspace_size(w.num_seqs, w.total_q, st.max_query_len, big_seq, w.num_heads,
-                                         w.num_kv_heads, w.head_dim) > B.PA_STATIC_WORKSPACE_BYTES
     assert rc == -5  # PA_ERR_WORKSPACE
     assert B.pa_launch_count() == launches
