@@ -198,7 +198,7 @@ def oracle_rate(w, kc, vc, target_s: float, rng, threads: int):
         s = sub_workload(w, take)
         t0 = time.perf_counter()
         orc.attention(s["q"], kc, vc, s["block_tables"], s["seq_lens"], s["query_start_loc"], w.num_heads,
-                      w.scale, num_threads=threads)
+                      w.scale, num_threads=threads, dtype=w.dtype)
         t_total += time.perf_counter() - t0
         done_bytes += int(s["seq_lens"].astype(np.int64).sum()) * kv_tok
         done_tok += int(s["query_start_loc"][-1])
@@ -258,6 +258,7 @@ def run_reference(args, world, rank) -> None:
     from paged_kv_cache_55_gb300 import workloads as W
     import oracle as oracle_mod
     kw = {"batch": args.batch} if args.batch else {}
+    kw["dtype"] = args.dtype
     w = W.by_name(args.workload, seed=args.seed, **kw)
     kc, vc = w.key_cache.copy(), w.value_cache.copy()
     orc = oracle_mod.default()
@@ -291,6 +292,8 @@ def run_reference(args, world, rank) -> None:
 
 def workload_text(args) -> str:
     text = WORKLOAD_TEXT[args.workload]
+    if args.dtype != "bf16":
+        text += f" [{args.dtype} elements]"
     return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
 
 
@@ -307,6 +310,7 @@ def run_ours(args, world, rank, local_rank) -> None:
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     kw = {"batch": args.batch} if args.batch else {}
+    kw["dtype"] = args.dtype
     w = W.by_name(args.workload, seed=rank_seed(args.seed, rank), **kw)
     acct = step_accounting(w)
     st = DeviceStep(w, device=str(device))
@@ -385,11 +389,11 @@ def run_ours(args, world, rank, local_rank) -> None:
 
     peaks = load_peaks()
     kern_achieved = acct["attention_bytes"] / (kern_ms * 1e-3) / 1e9
-    traffic = committed_traffic(args.workload)
+    traffic = committed_traffic(args.workload) if args.dtype == "bf16" else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "hbm_frac": value / peaks["hbm_gbs"],
         "decode_tokens_per_s": total_tok / (max_ms * 1e-3),
         "config": {"workload": workload_text(args), "seed": args.seed,
@@ -429,6 +433,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="gqa_decode")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
+                    help="element type of q, K/V and out (the metric's workload is bf16)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's number of requests (small profiling cases only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

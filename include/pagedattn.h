@@ -23,7 +23,10 @@
  *     allocates no device memory and frees nothing.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Calls enqueue work on it and return without synchronising.
- *   - Element data is bf16 (dtype PA_BF16). Indices are int32, except
+ *   - Element data (q, key, value, the caches and out of one call) is one
+ *     16-bit float type: bf16 (dtype PA_BF16) or IEEE fp16 (PA_FP16). The
+ *     arithmetic is the same for both (fp32 accumulation, outputs rounded to
+ *     nearest even in the element type). Indices are int32, except
  *     slot_mapping, which is int64.
  *   - Errors the host can see (null pointers, bad sizes, unsupported shapes,
  *     misalignment, small workspace) are returned before anything is
@@ -57,7 +60,7 @@ typedef enum pa_status {
     PA_ERR_CUDA = -8           /* another CUDA runtime call failed */
 } pa_status;
 
-enum { PA_BF16 = 0 };
+enum { PA_BF16 = 0, PA_FP16 = 1 };
 
 /* Bits of the device status word (pa_debug_status). */
 enum {

@@ -32,6 +32,10 @@ ERRORS = {
 }
 
 
+# element types of q, the caches and out (the oracle's ORACLE_BF16 / ORACLE_FP16)
+DTYPES = {"bf16": 0, "fp16": 1}
+
+
 class OracleError(RuntimeError):
     pass
 
@@ -68,13 +72,15 @@ class Oracle:
         L = self.lib
         L.oracle_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64]
         L.oracle_reshape_and_cache.restype = ctypes.c_int
-        common = [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, ctypes.c_float]
+        common = [_P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, ctypes.c_float, _I32]
         L.oracle_attention_varlen.argtypes = common + [_P, _I32]
         L.oracle_attention_varlen.restype = ctypes.c_int
         L.oracle_attention_sampled.argtypes = common + [_I64, _P, _P, _P]
         L.oracle_attention_sampled.restype = ctypes.c_int
         L.oracle_attention_weights.argtypes = common + [_I64, _I32, _P]
         L.oracle_attention_weights.restype = ctypes.c_int
+        L.oracle_decode_elements.argtypes = [_P, _I64, _I32, _P]
+        L.oracle_decode_elements.restype = ctypes.c_int
 
     @staticmethod
     def _check(rc: int, what: str) -> None:
@@ -95,8 +101,16 @@ class Oracle:
                                                hkv, d, bs, nb)
         self._check(rc, "reshape_and_cache")
 
+    def decode_elements(self, bits, dtype: str = "bf16") -> np.ndarray:
+        """The oracle's widening of 16-bit element bit patterns to float64."""
+        bits = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.zeros(bits.shape, dtype=np.float64)
+        rc = self.lib.oracle_decode_elements(_ptr(bits), int(bits.size), DTYPES[dtype], _ptr(out))
+        self._check(rc, "decode_elements")
+        return out
+
     def _common(self, q, key_cache, value_cache, block_tables, seq_lens, query_start_loc,
-                num_heads, scale):
+                num_heads, scale, dtype):
         q = np.ascontiguousarray(q, dtype=np.uint16)
         kc = np.ascontiguousarray(key_cache, dtype=np.uint16)
         vc = np.ascontiguousarray(value_cache, dtype=np.uint16)
@@ -106,14 +120,14 @@ class Oracle:
         nb, bs, hkv, d = kc.shape
         keep = (q, kc, vc, bt, sl, qsl)
         args = [_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(sl), _ptr(qsl),
-                int(sl.shape[0]), int(num_heads), hkv, d, bs, nb, float(scale)]
+                int(sl.shape[0]), int(num_heads), hkv, d, bs, nb, float(scale), DTYPES[dtype]]
         return keep, args, d
 
     def attention(self, q, key_cache, value_cache, block_tables, seq_lens, query_start_loc,
-                  num_heads, scale, num_threads: int = 0) -> np.ndarray:
-        """fp64 output [total_q, num_heads, head_dim]."""
+                  num_heads, scale, num_threads: int = 0, dtype: str = "bf16") -> np.ndarray:
+        """fp64 output [total_q, num_heads, head_dim]; elements decode as ``dtype``."""
         keep, args, d = self._common(q, key_cache, value_cache, block_tables, seq_lens,
-                                     query_start_loc, num_heads, scale)
+                                     query_start_loc, num_heads, scale, dtype)
         total_q = int(keep[5][-1])
         out = np.zeros((total_q, num_heads, d), dtype=np.float64)
         if num_threads <= 0:
@@ -123,10 +137,10 @@ class Oracle:
         return out
 
     def attention_sampled(self, q, key_cache, value_cache, block_tables, seq_lens, query_start_loc,
-                          num_heads, scale, tokens, heads) -> np.ndarray:
+                          num_heads, scale, tokens, heads, dtype: str = "bf16") -> np.ndarray:
         """fp64 output [n_samples, head_dim] for the given (token, head) pairs."""
         keep, args, d = self._common(q, key_cache, value_cache, block_tables, seq_lens,
-                                     query_start_loc, num_heads, scale)
+                                     query_start_loc, num_heads, scale, dtype)
         tokens = np.ascontiguousarray(tokens, dtype=np.int64)
         heads = np.ascontiguousarray(heads, dtype=np.int32)
         out = np.zeros((tokens.shape[0], d), dtype=np.float64)
@@ -136,10 +150,10 @@ class Oracle:
         return out
 
     def attention_weights(self, q, key_cache, value_cache, block_tables, seq_lens, query_start_loc,
-                          num_heads, scale, token, head) -> np.ndarray:
+                          num_heads, scale, token, head, dtype: str = "bf16") -> np.ndarray:
         """Softmax weights of one (token, head) pair over its visible keys."""
         keep, args, d = self._common(q, key_cache, value_cache, block_tables, seq_lens,
-                                     query_start_loc, num_heads, scale)
+                                     query_start_loc, num_heads, scale, dtype)
         w = np.zeros(int(keep[4].max()) + 1, dtype=np.float64)
         n = self.lib.oracle_attention_weights(*args, int(token), int(head), _ptr(w))
         self._check(n, "attention_weights")
@@ -152,7 +166,7 @@ class Oracle:
         vc = w.value_cache.copy()
         self.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
         out = self.attention(w.q, kc, vc, w.block_tables, w.seq_lens, w.query_start_loc,
-                             w.num_heads, w.scale, num_threads=num_threads)
+                             w.num_heads, w.scale, num_threads=num_threads, dtype=w.dtype)
         return kc, vc, out
 
 

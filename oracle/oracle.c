@@ -51,6 +51,9 @@
 #define ORACLE_ERR_LENGTHS (-5)
 #define ORACLE_ERR_NOMEM (-6)
 
+#define ORACLE_BF16 0
+#define ORACLE_FP16 1
+
 /* bf16 is the upper half of an IEEE binary32; widening is exact. */
 static double bf16_to_double(uint16_t h)
 {
@@ -58,6 +61,42 @@ static double bf16_to_double(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * IEEE 754 binary16: sign bit, 5-bit exponent with bias 15, 10-bit fraction.
+ * Exponent 0 holds zero and the subnormals fraction * 2^-24; exponent 31
+ * holds the infinities (fraction 0) and NaNs; otherwise the value is
+ * (1024 + fraction) * 2^(exponent - 25). Every value is exact in a double.
+ */
+static double fp16_to_double(uint16_t h)
+{
+    const int sign = h >> 15;
+    const int e = (h >> 10) & 0x1f;
+    const int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+static double elem_to_double(int32_t dtype, uint16_t h)
+{
+    return dtype == ORACLE_FP16 ? fp16_to_double(h) : bf16_to_double(h);
+}
+
+/* The element decoders over an array, for the tests that pin them. */
+int oracle_decode_elements(const uint16_t *bits, int64_t n, int32_t dtype, double *out)
+{
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = elem_to_double(dtype, bits[i]);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -132,6 +171,7 @@ typedef struct {
     int32_t block_size;
     int64_t num_blocks;
     double scale;
+    int32_t dtype;  /* ORACLE_BF16 or ORACLE_FP16: how the 16-bit elements decode */
 } problem_t;
 
 static int check_problem(const problem_t *p)
@@ -140,6 +180,8 @@ static int check_problem(const problem_t *p)
         p->block_size <= 0 || p->max_blocks_per_seq < 0 || p->num_blocks < 0)
         return ORACLE_ERR_ARG;
     if (p->num_heads % p->num_kv_heads != 0)
+        return ORACLE_ERR_ARG;
+    if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16)
         return ORACLE_ERR_ARG;
     if (p->query_start_loc[0] != 0)
         return ORACLE_ERR_LENGTHS;
@@ -176,8 +218,8 @@ static void gather_request(const problem_t *p, int32_t b, int32_t kvh, double *K
         int64_t slot = phys * p->block_size + offset;
         int64_t base = (slot * p->num_kv_heads + kvh) * D;
         for (int32_t d = 0; d < D; ++d) {
-            K[(int64_t)j * D + d] = bf16_to_double(p->key_cache[base + d]);
-            V[(int64_t)j * D + d] = bf16_to_double(p->value_cache[base + d]);
+            K[(int64_t)j * D + d] = elem_to_double(p->dtype, p->key_cache[base + d]);
+            V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->value_cache[base + d]);
         }
     }
 }
@@ -206,7 +248,7 @@ static int32_t weights_for_query(const problem_t *p, int32_t b, int32_t i, int32
         qv = heap;
     }
     for (int32_t d = 0; d < D; ++d)
-        qv[d] = bf16_to_double(qrow[d]);
+        qv[d] = elem_to_double(p->dtype, qrow[d]);
 
     for (int32_t j = 0; j < n; ++j) {
         double dot = 0.0;
@@ -307,12 +349,12 @@ int oracle_attention_varlen(const uint16_t *q, const uint16_t *key_cache,
                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
                             const int32_t *query_start_loc, int32_t num_seqs,
                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                            int32_t block_size, int64_t num_blocks, float scale,
+                            int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
                             double *out, int32_t num_threads)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale};
+                   block_size, num_blocks, (double)scale, dtype};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;
@@ -350,13 +392,13 @@ int oracle_attention_sampled(const uint16_t *q, const uint16_t *key_cache,
                              int32_t max_blocks_per_seq, const int32_t *seq_lens,
                              const int32_t *query_start_loc, int32_t num_seqs,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t block_size, int64_t num_blocks, float scale,
+                             int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
                              int64_t n_samples, const int64_t *sample_token,
                              const int32_t *sample_head, double *out)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale};
+                   block_size, num_blocks, (double)scale, dtype};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;
@@ -397,12 +439,12 @@ int oracle_attention_weights(const uint16_t *q, const uint16_t *key_cache,
                              int32_t max_blocks_per_seq, const int32_t *seq_lens,
                              const int32_t *query_start_loc, int32_t num_seqs,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t block_size, int64_t num_blocks, float scale,
+                             int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
                              int64_t token, int32_t head, double *weights)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale};
+                   block_size, num_blocks, (double)scale, dtype};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;

@@ -17,7 +17,8 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(HERE, "libpagedattn.so")
 
-PA_BF16 = 0
+PA_BF16, PA_FP16 = 0, 1
+_ELEM_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
 STATUS = {
     0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_DIMS", -3: "PA_ERR_UNSUPPORTED", -4: "PA_ERR_ALIGN",
     -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_LAUNCH", -7: "PA_ERR_DEVICE_BOUNDS", -8: "PA_ERR_CUDA",
@@ -96,11 +97,21 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _elem_code(*named) -> int:
+    """The C dtype of element tensors that must share one 16-bit float type (bf16 or fp16)."""
+    first = named[0][0]
+    if not isinstance(first, torch.Tensor) or first.dtype not in _ELEM_CODES:
+        raise TypeError(f"{named[0][1]} must be a bfloat16 or float16 CUDA tensor")
+    for t, n in named:
+        _need(t, n, first.dtype)
+    return _ELEM_CODES[first.dtype]
+
+
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
                          value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
-    """key/value [T, Hkv, D] bf16 (token stride free), caches [NB, bs, Hkv, D] bf16, slots int64 [T]."""
-    for t, n in ((key, "key"), (value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache")):
-        _need(t, n, torch.bfloat16)
+    """key/value [T, Hkv, D] (token stride free), caches [NB, bs, Hkv, D], all bf16 or all fp16;
+    slots int64 [T]."""
+    dt = _elem_code((key, "key"), (value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache"))
     _need(slot_mapping, "slot_mapping", torch.int64)
     T, hkv, d = key.shape
     if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
@@ -110,7 +121,7 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torc
     nb, bs = key_cache.shape[0], key_cache.shape[1]
     _check(_lib().pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0),
                                        key_cache.data_ptr(), value_cache.data_ptr(), slot_mapping.data_ptr(),
-                                       T, hkv, d, bs, nb, PA_BF16, _stream(stream)), "pa_reshape_and_cache")
+                                       T, hkv, d, bs, nb, dt, _stream(stream)), "pa_reshape_and_cache")
 
 
 def pa_attention_workspace_size(num_seqs: int, total_q_tokens: int, max_query_len: int, max_seq_len: int,
@@ -133,12 +144,9 @@ def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: t
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
                         max_query_len: int, max_seq_len: int, scale: float, out: torch.Tensor,
                         workspace: torch.Tensor, stream=None) -> None:
-    """q [T, H, D] bf16, caches [NB, bs, Hkv, D] bf16, block_tables [B, M] int32, seq_lens [B] int32,
-    query_start_loc [B+1] int32, out [T, H, D] bf16 contiguous, workspace uint8 (device)."""
-    _need(q, "q", torch.bfloat16)
-    _need(out, "out", torch.bfloat16)
-    _need(key_cache, "key_cache", torch.bfloat16)
-    _need(value_cache, "value_cache", torch.bfloat16)
+    """q [T, H, D], caches [NB, bs, Hkv, D], out [T, H, D] contiguous (all bf16 or all fp16),
+    block_tables [B, M] int32, seq_lens [B] int32, query_start_loc [B+1] int32, workspace uint8 (device)."""
+    dt = _elem_code((q, "q"), (out, "out"), (key_cache, "key_cache"), (value_cache, "value_cache"))
     for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
         _need(t, n, torch.int32)
         if not t.is_contiguous():
@@ -154,7 +162,7 @@ def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: t
                                       block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
                                       query_start_loc.data_ptr(), B, T, max_query_len, max_seq_len, H, hkv, D, bs,
                                       nb, float(scale), out.data_ptr(), workspace.data_ptr(),
-                                      workspace.numel() * workspace.element_size(), PA_BF16, _stream(stream)),
+                                      workspace.numel() * workspace.element_size(), dt, _stream(stream)),
            "pa_attention_varlen")
 
 
@@ -165,23 +173,24 @@ def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_c
     """pa_attention_varlen without a workspace argument, for callers that cannot allocate: the
     library's built-in scratch array (PA_STATIC_WORKSPACE_BYTES) is used instead. Calls on one device
     share that array, so calls on different streams must not overlap."""
-    _need(q, "q", torch.bfloat16)
-    _need(out, "out", torch.bfloat16)
+    dt = _elem_code((q, "q"), (out, "out"), (key_cache, "key_cache"), (value_cache, "value_cache"))
     T, H, D = q.shape
     nb, bs, hkv, _ = key_cache.shape
     B = seq_lens.shape[0]
     _check(_lib().pa_attention_varlen_static(q.data_ptr(), q.stride(0), key_cache.data_ptr(),
                                              value_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
                                              seq_lens.data_ptr(), query_start_loc.data_ptr(), B, T, max_query_len,
-                                             max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), PA_BF16,
+                                             max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), dt,
                                              _stream(stream)), "pa_attention_varlen_static")
 
 
 def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor,
                  seq_len: int, key_out: torch.Tensor, value_out: torch.Tensor, stream=None) -> None:
+    dt = _elem_code((key_cache, "key_cache"), (value_cache, "value_cache"), (key_out, "key_out"),
+                    (value_out, "value_out"))
     nb, bs, hkv, d = key_cache.shape
     _check(_lib().pa_gather_kv(key_cache.data_ptr(), value_cache.data_ptr(), block_table_row.data_ptr(), seq_len,
-                               hkv, d, bs, nb, key_out.data_ptr(), value_out.data_ptr(), PA_BF16,
+                               hkv, d, bs, nb, key_out.data_ptr(), value_out.data_ptr(), dt,
                                _stream(stream)), "pa_gather_kv")
 
 

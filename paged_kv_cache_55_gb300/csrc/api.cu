@@ -96,7 +96,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
                                const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                                int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
                                void *stream) {
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
     return PA_ERR_DIMS;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
@@ -149,7 +149,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
                               size_t workspace_bytes, int32_t dtype, void *stream) {
   cudaEvent_t ev_start = t_ev_start, ev_stop = t_ev_stop;
   t_ev_start = t_ev_stop = nullptr;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || total_q_tokens < 0 || max_query_len < 0 || max_seq_len < max_query_len ||
       max_blocks_per_seq < 0 || num_blocks < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
     return PA_ERR_DIMS;
@@ -195,6 +195,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   a.head_dim = head_dim;
   a.num_blocks = num_blocks;
   a.scale = scale;
+  a.dtype = dtype;
   a.out = out;
   a.workspace = workspace;
   a.status = ds->status;
@@ -211,7 +212,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
 pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int32_t *block_table_row,
                        int32_t seq_len, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int64_t num_blocks, void *key_out, void *value_out, int32_t dtype, void *stream) {
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (seq_len < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_DIMS;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;

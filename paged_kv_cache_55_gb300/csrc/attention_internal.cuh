@@ -34,8 +34,9 @@ struct TileParams {
   unsigned int *status;
 };
 
-// Enqueue the tensor-core prefill-tile kernel (PDL launch) on `stream`.
-template <int D, int G>
+// Enqueue the tensor-core prefill-tile kernel (PDL launch) on `stream`; E is
+// the element type (ElemBf16 or ElemFp16).
+template <int D, int G, typename E>
 cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp,
                                  int sm_count, cudaStream_t stream);
 

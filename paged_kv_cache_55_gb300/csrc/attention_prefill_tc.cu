@@ -200,6 +200,7 @@ __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, 
 // P for 32 keys (scores s[0..32), visible while ck0 + i < lim): p =
 // 2^(s * sl2 - ms), summed into *sum and packed as the 32 TMEM columns of two
 // UMMA K steps: [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo 16-31].
+template <typename E>
 __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int lim, float sl2, float ms, float &sum,
                                         uint32_t (&u)[32]) {
   const bool full = ck0 + 32 <= lim;
@@ -215,34 +216,35 @@ __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int li
     fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
     const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
     add2(acc0, acc1, acc0, acc1, p0, p1);
-    const uint32_t hi = pack_bf16x2(p0, p1);
+    const uint32_t hi = E::pack(p0, p1);
     float l0, l1;
-    sub2(l0, l1, p0, p1, bf16_lo(hi), bf16_hi(hi));
+    sub2(l0, l1, p0, p1, E::lo(hi), E::hi(hi));
     const int step = i >> 3, k = i & 7;
     u[16 * step + k] = hi;
-    u[16 * step + 8 + k] = pack_bf16x2(l0, l1);
+    u[16 * step + 8 + k] = E::pack(l0, l1);
   }
   sum += acc0 + acc1;
 }
 
 // Multiply the probabilities already stored in a 32-column chunk of P (the
 // layout probs32 writes) by alpha, re-splitting each into hi + lo.
+template <typename E>
 __device__ __forceinline__ void rescale_p32(uint32_t taddr, float alpha) {
   uint32_t w[32];
   tmem_ld32_wait(taddr, w);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int hk = 16 * (i >> 3) + (i & 7);
-    const float p0 = (bf16_lo(w[hk]) + bf16_lo(w[hk + 8])) * alpha;
-    const float p1 = (bf16_hi(w[hk]) + bf16_hi(w[hk + 8])) * alpha;
-    const uint32_t hi = pack_bf16x2(p0, p1);
+    const float p0 = (E::lo(w[hk]) + E::lo(w[hk + 8])) * alpha;
+    const float p1 = (E::hi(w[hk]) + E::hi(w[hk + 8])) * alpha;
+    const uint32_t hi = E::pack(p0, p1);
     w[hk] = hi;
-    w[hk + 8] = pack_bf16x2(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
+    w[hk + 8] = E::pack(p0 - E::lo(hi), p1 - E::hi(hi));
   }
   tmem_st32u(taddr, w);
 }
 
-template <int D, int G>
+template <int D, int G, typename E>
 // Ten warps: three share two of the SM's four register-file partitions, so a
 // thread gets at most 168 registers.
 __global__ void __launch_bounds__(kTileThreads, 1)
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   constexpr int KSTEPS_O = kKeyTile / 16;  // UMMA K steps of O = P V
   constexpr int BLOCKS = kKeyTile / kBlockSize;
   constexpr int POS_PER_HALF = kHalfRows / G;
-  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0);
-  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1);
+  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, E::kUmmaFormat);
+  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, E::kUmmaFormat);
   // O stays in TMEM and is rescaled only when a row's running maximum grows
   // by more than 2^8 (log2 domain); in between, probabilities are taken
   // against the older maximum and stay below 256.
@@ -539,10 +541,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             if (c > 0) {
               tmem_wait_st();  // the chunks stored so far are read back
 #pragma unroll 1
-              for (int cc = 0; cc < c; ++cc) rescale_p32(sp + 32 * cc, a);
+              for (int cc = 0; cc < c; ++cc) rescale_p32<E>(sp + 32 * cc, a);
             }
           }
-          probs32(sv, ck0, lim, sl2, m_used == -INFINITY ? 0.f : m_used, sum, u);
+          probs32<E>(sv, ck0, lim, sl2, m_used == -INFINITY ? 0.f : m_used, sum, u);
           tmem_st32u(sp + 32 * c, u);  // P over the scores it came from
         }
         // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
@@ -578,8 +580,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const float *f = reinterpret_cast<const float *>(&t[8 * c]);
-              const uint4 v = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                                         pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+              const uint4 v = make_uint4(E::pack(f[0] * inv, f[1] * inv), E::pack(f[2] * inv, f[3] * inv),
+                                         E::pack(f[4] * inv, f[5] * inv), E::pack(f[6] * inv, f[7] * inv));
               *reinterpret_cast<uint4 *>(dst + ch * 64 + 8 * c) = v;
             }
           }
@@ -613,11 +615,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, int G>
+template <int D, int G, typename E>
 cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp, int sm_count,
                                  cudaStream_t stream) {
   constexpr int smem = TcLayout<D>::REQUEST;
-  auto kern = prefill_tile_kernel<D, G>;
+  auto kern = prefill_tile_kernel<D, G, E>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -629,9 +631,11 @@ cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vma
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTileThreads), smem, stream, kmap, vmap, tp);
 }
 
-#define PA_TILE_INST(DD, GG)                                                                                    \
-  template cudaError_t launch_prefill_tiles<DD, GG>(const CUtensorMap &, const CUtensorMap &, const TileParams &, \
-                                                    int, cudaStream_t);
+#define PA_TILE_INST(DD, GG)                                                                               \
+  template cudaError_t launch_prefill_tiles<DD, GG, ElemBf16>(const CUtensorMap &, const CUtensorMap &,     \
+                                                              const TileParams &, int, cudaStream_t);      \
+  template cudaError_t launch_prefill_tiles<DD, GG, ElemFp16>(const CUtensorMap &, const CUtensorMap &,     \
+                                                              const TileParams &, int, cudaStream_t);
 PA_TILE_INST(128, 1)
 PA_TILE_INST(128, 2)
 PA_TILE_INST(128, 4)

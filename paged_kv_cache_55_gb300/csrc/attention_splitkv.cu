@@ -382,7 +382,7 @@ struct MergeParams {
   bf16 *out;
 };
 
-template <int D, int G>
+template <int D, int G, typename E>
 __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams p) {
   constexpr int EPL = D / 32;  // outputs per lane: 4 (D=128) or 2 (D=64)
   griddep_wait();
@@ -445,9 +445,9 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
               lane * EPL;
   if constexpr (EPL == 4) {
     *reinterpret_cast<uint2 *>(dst) =
-        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        make_uint2(E::pack(acc[0] * inv, acc[1] * inv), E::pack(acc[2] * inv, acc[3] * inv));
   } else {
-    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    *reinterpret_cast<uint32_t *>(dst) = E::pack(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -504,7 +504,7 @@ struct TileGeom {
   }
 };
 
-template <int D, int G, int NWARPS>
+template <int D, int G, int NWARPS, typename E>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     splitkv_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                              const AttnParams p) {
@@ -645,9 +645,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         uint32_t a0, a1, a2, a3;
         ldsm_x4(kt + T::off(arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
         if (kk & 1)
-          mma_16816(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+          E::mma(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         else
-          mma_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+          E::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
       }
       const int t0 = kb * kBlockSize + (lane >> 2), t1 = t0 + 8;
       const float x0 = t0 < lim[0] ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
@@ -678,17 +678,17 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         o[mt][3] *= al1;
       }
       // P^T (keys x columns) -> B operand by transposition; P as bf16 hi + lo.
-      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-      const uint32_t l01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-      const uint32_t l23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+      const uint32_t h01 = E::pack(p0, p1), h23 = E::pack(p2, p3);
+      const uint32_t l01 = E::pack(p0 - E::lo(h01), p1 - E::hi(h01));
+      const uint32_t l23 = E::pack(p2 - E::lo(h23), p3 - E::hi(h23));
       const uint32_t b0 = movmatrix_t(h01), b1 = movmatrix_t(h23);
       const uint32_t c0 = movmatrix_t(l01), c1 = movmatrix_t(l23);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
-        mma_16816(o[mt], a0, a1, a2, a3, b0, b1);
-        mma_16816(o[mt], a0, a1, a2, a3, c0, c1);
+        E::mma(o[mt], a0, a1, a2, a3, b0, b1);
+        E::mma(o[mt], a0, a1, a2, a3, c0, c1);
       }
       __syncwarp();  // every lane is done with this slot before it is refilled
       ++consumed;
@@ -710,8 +710,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                     static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t lo8 = movmatrix_t(pack_bf16x2(o[mt][0] * inv0, o[mt][1] * inv1));
-          const uint32_t hi8 = movmatrix_t(pack_bf16x2(o[mt][2] * inv0, o[mt][3] * inv1));
+          const uint32_t lo8 = movmatrix_t(E::pack(o[mt][0] * inv0, o[mt][1] * inv1));
+          const uint32_t hi8 = movmatrix_t(E::pack(o[mt][2] * inv0, o[mt][3] * inv1));
           if (qi < cur.nrows) {
             *reinterpret_cast<uint32_t *>(dst + 16 * mt) = lo8;
             *reinterpret_cast<uint32_t *>(dst + 16 * mt + 8) = hi8;
@@ -824,7 +824,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D view of one cache, [num_blocks * 16 rows][Hkv][D], with a box of
 // 16 rows x 1 head x 64 elements (128 bytes, 128-byte swizzle).
 static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
-                             int32_t head_dim) {
+                             int32_t head_dim, int32_t dtype) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
@@ -833,14 +833,15 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_bl
                                  static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
   const cuuint32_t box[3] = {64, 1, kBlockSize};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims, strides, box, estr,
+  const CUtensorMapDataType type = dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode(map, type, 3, const_cast<void *>(cache), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 constexpr int kAttnWarps = 8;
 
-template <int D, int G>
+template <int D, int G, typename E>
 static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, cudaStream_t stream,
                                 int *launched) {
   char *ws = static_cast<char *>(a.workspace);
@@ -868,8 +869,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D) ||
-      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D))
+  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.dtype) ||
+      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.dtype))
     return cudaErrorInvalidValue;
 
   cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
@@ -898,7 +899,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
-  auto kern = splitkv_attention_kernel<D, G, kAttnWarps>;
+  auto kern = splitkv_attention_kernel<D, G, kAttnWarps, E>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -932,7 +933,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.total_q = a.total_q;
     tp.max_tiles = w.max_tiles;
     tp.status = a.status;
-    err = launch_prefill_tiles<D, G>(kmap, vmap, tp, a.sm_count, stream);
+    err = launch_prefill_tiles<D, G, E>(kmap, vmap, tp, a.sm_count, stream);
     if (err != cudaSuccess) return err;
     ++*launched;
   }
@@ -948,7 +949,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     mp.part_o = ap.part_o;
     mp.part_lse = ap.part_lse;
     mp.out = ap.out;
-    err = launch_pdl(lse_merge_kernel<D, G>, dim3(static_cast<unsigned>(a.num_seqs * a.num_kv_heads)),
+    err = launch_pdl(lse_merge_kernel<D, G, E>, dim3(static_cast<unsigned>(a.num_seqs * a.num_kv_heads)),
                      dim3(kCols * 32), 0, stream, mp);
     if (err != cudaSuccess) return err;
     ++*launched;
@@ -962,8 +963,10 @@ cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *laun
   if (!workspace_layout(a.num_seqs, a.total_q, a.max_seq_len, a.num_heads, a.num_kv_heads, a.head_dim, w))
     return cudaErrorInvalidValue;
   const int G = a.num_heads / a.num_kv_heads;
-#define PA_DISPATCH(DD, GG) \
-  if (a.head_dim == DD && G == GG) return launch_typed<DD, GG>(a, w, stream, launched);
+#define PA_DISPATCH(DD, GG)                                                                     \
+  if (a.head_dim == DD && G == GG)                                                              \
+    return a.dtype == PA_FP16 ? launch_typed<DD, GG, ElemFp16>(a, w, stream, launched)          \
+                              : launch_typed<DD, GG, ElemBf16>(a, w, stream, launched);
   PA_DISPATCH(128, 1) PA_DISPATCH(128, 2) PA_DISPATCH(128, 4) PA_DISPATCH(128, 8)
   PA_DISPATCH(64, 1) PA_DISPATCH(64, 2) PA_DISPATCH(64, 4) PA_DISPATCH(64, 8)
 #undef PA_DISPATCH

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -289,8 +290,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo,
 }
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
-__host__ __device__ constexpr uint32_t f16_idesc(int M, int N, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+// `fmt` is the A/B operand format: 1 = bf16 (default), 0 = fp16.
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N, int b_mn, uint32_t fmt = 1) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -302,6 +304,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // The two bf16 halves of a packed pair, widened to float (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// ---- element types ---------------------------------------------------------
+// The cache, q and out of one call hold 16-bit floats of one type, bf16 or
+// fp16. The kernels move them as raw 16-bit patterns and are instantiated per
+// type; a type supplies the tensor-core operand type, the packing of two
+// floats into a pair (round to nearest even) and the exact widening of a
+// pair's halves.
+struct ElemBf16 {
+  static constexpr uint32_t kUmmaFormat = 1;  // tcgen05 kind::f16 A/B format
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  static __device__ __forceinline__ float lo(uint32_t v) { return bf16_lo(v); }
+  static __device__ __forceinline__ float hi(uint32_t v) { return bf16_hi(v); }
+  static __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    mma_16816(c, a0, a1, a2, a3, b0, b1);
+  }
+};
+struct ElemFp16 {
+  static constexpr uint32_t kUmmaFormat = 0;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+  static __device__ __forceinline__ float lo(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xffffu)));
+  }
+  static __device__ __forceinline__ float hi(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+  }
+  static __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+};
 
 // Swizzled offset (in elements) of 16-byte chunk `chunk` of row `row` in a
 // tile whose rows are `row_elems` bf16 long: chunk c of row r is stored at

@@ -42,6 +42,7 @@ struct AttnLaunch {
   int32_t num_heads, num_kv_heads, head_dim;
   int64_t num_blocks;
   float scale;
+  int32_t dtype;  // PA_BF16 or PA_FP16 (q, caches and out alike)
   void *out;
   void *workspace;
   unsigned int *status;

@@ -15,9 +15,12 @@ from . import binding as B
 from .workloads import Workload
 
 
-def bf16_tensor(a: np.ndarray, device) -> torch.Tensor:
-    """uint16 bf16 bit patterns -> a bf16 tensor on `device` (bits preserved)."""
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def bf16_tensor(a: np.ndarray, device, dtype: str = "bf16") -> torch.Tensor:
+    """uint16 bit patterns of the element type -> a bf16 / fp16 tensor on `device` (bits preserved)."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(TORCH_DTYPES[dtype])
 
 
 def bf16_to_numpy_bits(t: torch.Tensor) -> np.ndarray:
@@ -33,18 +36,18 @@ class DeviceStep:
         self.w = w
         self.device = torch.device(device)
         dev = self.device
-        self.q = bf16_tensor(w.q, dev)
-        self.key = bf16_tensor(w.key, dev)
-        self.value = bf16_tensor(w.value, dev)
+        self.q = bf16_tensor(w.q, dev, w.dtype)
+        self.key = bf16_tensor(w.key, dev, w.dtype)
+        self.value = bf16_tensor(w.value, dev, w.dtype)
         self.slot_mapping = torch.from_numpy(w.slot_mapping).to(dev)
-        self.key_cache0 = bf16_tensor(w.key_cache, dev)
-        self.value_cache0 = bf16_tensor(w.value_cache, dev)
+        self.key_cache0 = bf16_tensor(w.key_cache, dev, w.dtype)
+        self.value_cache0 = bf16_tensor(w.value_cache, dev, w.dtype)
         self.key_cache = self.key_cache0.clone()
         self.value_cache = self.value_cache0.clone()
         self.block_tables = torch.from_numpy(w.block_tables).to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
         self.query_start_loc = torch.from_numpy(w.query_start_loc).to(dev)
-        self.out = torch.empty((w.total_q, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((w.total_q, w.num_heads, w.head_dim), dtype=TORCH_DTYPES[w.dtype], device=dev)
         self.max_query_len = w.max_query_len
         self.max_seq_len = w.max_seq_len
         nbytes = B.pa_attention_workspace_size(w.num_seqs, w.total_q, self.max_query_len, self.max_seq_len,

@@ -36,6 +36,9 @@ from typing import Optional, Sequence
 import numpy as np
 
 BF16_NAN = np.uint16(0x7FC0)
+FP16_NAN = np.uint16(0x7E00)
+DTYPES = ("bf16", "fp16")
+NAN_BITS = {"bf16": BF16_NAN, "fp16": FP16_NAN}
 TABLE_JUNK = np.int32(-2147483648)
 
 
@@ -63,7 +66,27 @@ def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
+def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE fp16 (round to nearest even), as uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def fp16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """Widen fp16 bit patterns to float32 (exact)."""
+    return np.asarray(h, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_fp16_bits(x) if dtype == "fp16" else f32_to_bf16_bits(x)
+
+
+def bits_to_f32(h: np.ndarray, dtype: str) -> np.ndarray:
+    return fp16_bits_to_f32(h) if dtype == "fp16" else bf16_bits_to_f32(h)
+
+
+def _normal_elems(rng: np.random.Generator, shape, scale: float = 1.0, dtype: str = "bf16") -> np.ndarray:
+    """Seeded N(0, scale^2) values rounded to the element type, as uint16 bits
+    (the same draws for either type)."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
     step = 1 << 24
@@ -72,7 +95,7 @@ def _normal_bf16(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndar
         x = rng.standard_normal(e - s, dtype=np.float32)
         if scale != 1.0:
             x *= np.float32(scale)
-        out[s:e] = f32_to_bf16_bits(x)
+        out[s:e] = f32_to_bits(x, dtype)
     return out.reshape(shape)
 
 
@@ -98,6 +121,7 @@ class Workload:
     seq_lens: np.ndarray        # int32  [B]
     query_start_loc: np.ndarray  # int32 [B + 1]
     shared_blocks: Optional[np.ndarray] = None  # physical ids shared by several requests
+    dtype: str = "bf16"          # element type of q, key, value and the caches: "bf16" or "fp16"
     meta: dict = dataclasses.field(default_factory=dict)
 
     @property
@@ -160,6 +184,7 @@ def make_workload(
     shared_prefix_blocks: int = 0,
     extra_table_cols: int = 2,
     scale: Optional[float] = None,
+    dtype: str = "bf16",
 ) -> Workload:
     """Build one step: request ``b`` has ``context_lens[b]`` cached tokens and
     ``query_lens[b]`` new tokens, so ``seq_len = context + query``.
@@ -169,7 +194,11 @@ def make_workload(
     ``shared_prefix_requests`` map their first ``shared_prefix_blocks`` logical
     blocks to the same physical blocks (a copy-on-write shared prefix); their
     contexts must fill those blocks so that new tokens land in private blocks.
+    Elements are bf16 or fp16 (``dtype``); unowned cache slots hold that
+    type's NaN.
     """
+    if dtype not in DTYPES:
+        raise ValueError(f"dtype must be one of {DTYPES}")
     rng = np.random.default_rng(seed)
     ctx = np.asarray(context_lens, dtype=np.int64)
     ql = np.asarray(query_lens, dtype=np.int64)
@@ -215,8 +244,8 @@ def make_workload(
         tables[b, first:n] = pool[cursor:cursor + take]
         cursor += take
 
-    kc = np.full((num_blocks, bs, Hkv, D), BF16_NAN, dtype=np.uint16)
-    vc = np.full((num_blocks, bs, Hkv, D), BF16_NAN, dtype=np.uint16)
+    kc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
+    vc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
     kflat = kc.reshape(num_blocks * bs, Hkv, D)
     vflat = vc.reshape(num_blocks * bs, Hkv, D)
 
@@ -229,23 +258,23 @@ def make_workload(
             if not prefix_written:
                 pos = np.arange(S * bs)
                 slots = tables[b, pos // bs].astype(np.int64) * bs + pos % bs
-                kflat[slots] = _normal_bf16(rng, (pos.size, Hkv, D))
-                vflat[slots] = _normal_bf16(rng, (pos.size, Hkv, D))
+                kflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
+                vflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
                 prefix_written = True
             start = S * bs
         if c > start:
             pos = np.arange(start, c)
             slots = tables[b, pos // bs].astype(np.int64) * bs + pos % bs
-            kflat[slots] = _normal_bf16(rng, (pos.size, Hkv, D))
-            vflat[slots] = _normal_bf16(rng, (pos.size, Hkv, D))
+            kflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
+            vflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
 
     # This step's tokens: query rows and the new K/V rows with their slots.
     T = int(ql.sum())
     qsl = np.zeros(B + 1, dtype=np.int32)
     qsl[1:] = np.cumsum(ql)
-    q = _normal_bf16(rng, (T, H, D), scale=q_scale)
-    key = _normal_bf16(rng, (T, Hkv, D))
-    value = _normal_bf16(rng, (T, Hkv, D))
+    q = _normal_elems(rng, (T, H, D), scale=q_scale, dtype=dtype)
+    key = _normal_elems(rng, (T, Hkv, D), dtype=dtype)
+    value = _normal_elems(rng, (T, Hkv, D), dtype=dtype)
     slot_mapping = np.empty(T, dtype=np.int64)
     for b in range(B):
         pos = np.arange(int(ctx[b]), int(L[b]))
@@ -258,7 +287,7 @@ def make_workload(
         q=q, key=key, value=value, slot_mapping=slot_mapping,
         key_cache=kc, value_cache=vc, block_tables=tables,
         seq_lens=L.astype(np.int32), query_start_loc=qsl,
-        shared_blocks=shared_ids if S else None,
+        shared_blocks=shared_ids if S else None, dtype=dtype,
         meta={"context_lens": ctx.astype(np.int32)},
     )
 
@@ -268,20 +297,20 @@ def make_workload(
 # 7B/8B-class head counts, 16-token blocks, variable lengths).
 # --------------------------------------------------------------------------
 
-def tiny_decode(seed: int = 0) -> Workload:
+def tiny_decode(seed: int = 0, dtype: str = "bf16") -> Workload:
     """4 requests with seq_lens {1, 7, 16, 33}, one new token each; H=4, Hkv=1,
     D=64, 32 physical blocks in a seeded random order."""
     L = np.array([1, 7, 16, 33])
     return make_workload("tiny_decode", context_lens=L - 1, query_lens=[1] * 4,
-                         num_heads=4, num_kv_heads=1, head_dim=64, num_blocks=32, seed=seed)
+                         num_heads=4, num_kv_heads=1, head_dim=64, num_blocks=32, seed=seed, dtype=dtype)
 
 
-def mha_decode(seed: int = 0, batch: int = 64) -> Workload:
+def mha_decode(seed: int = 0, batch: int = 64, dtype: str = "bf16") -> Workload:
     """MHA 7B-like decode layer: H=Hkv=32, D=128, seq_lens ~ U[128, 2048]."""
     rng = np.random.default_rng(seed + 1000)
     L = rng.integers(128, 2048, size=batch, endpoint=True)
     return make_workload("mha_decode", context_lens=L - 1, query_lens=[1] * batch,
-                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed)
+                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed, dtype=dtype)
 
 
 def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
@@ -291,23 +320,24 @@ def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
     return np.clip(np.rint(x), 16, 8192).astype(np.int64)
 
 
-def gqa_decode(seed: int = 0, batch: int = 256) -> Workload:
+def gqa_decode(seed: int = 0, batch: int = 256, dtype: str = "bf16") -> Workload:
     """GQA 8B-like decode layer: batch 256, H=32, Hkv=8, D=128, lognormal lengths."""
     L = gqa_seq_lens(seed, batch)
     w = make_workload("gqa_decode", context_lens=L - 1, query_lens=[1] * batch,
-                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed)
+                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype)
     w.meta["lognormal_sigma"] = 1.0
     return w
 
 
-def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768) -> Workload:
+def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768, dtype: str = "bf16") -> Workload:
     """Long-context decode: 8 requests of 32768 tokens, H=64, Hkv=8, D=128."""
     return make_workload("long_decode", context_lens=[seq_len - 1] * batch, query_lens=[1] * batch,
-                         num_heads=64, num_kv_heads=8, head_dim=128, seed=seed)
+                         num_heads=64, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype)
 
 
 def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: int = 240,
-               n_shared: int = 64, shared_blocks: int = 64, batch: Optional[int] = None) -> Workload:
+               n_shared: int = 64, shared_blocks: int = 64, batch: Optional[int] = None,
+               dtype: str = "bf16") -> Workload:
     """Continuous-batching step: 16 prefill chunks of 512 query tokens (prior
     context U[0, 4096]) plus 240 decode requests (context U[256, 4096]); the
     first 64 physical blocks of 64 decode requests are one shared prefix.
@@ -331,7 +361,7 @@ def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: i
     w = make_workload("mixed_step", context_lens=ctx, query_lens=ql,
                       num_heads=32, num_kv_heads=8, head_dim=128, seed=seed,
                       shared_prefix_requests=np.nonzero(is_shared)[0].tolist(),
-                      shared_prefix_blocks=shared_blocks)
+                      shared_prefix_blocks=shared_blocks, dtype=dtype)
     return w
 
 

@@ -13,7 +13,11 @@ What pins what:
     the mean of the visible V rows, two keys give logistic weights;
   * invariants: physical block permutation, causal future perturbation, GQA
     equals MHA with replicated KV heads, weights sum to one;
-  * the slot address formula, from the golden fixture.
+  * the slot address formula, from the golden fixture;
+  * the element decoders: fp16 against numpy's IEEE binary16 on all 65536 bit
+    patterns, bf16 at values the format fixes (1, -2, pi rounded, the largest
+    finite, the smallest subnormal, signed zero, infinities, NaN); the dense
+    brute force and the seq_len-1 closed form are repeated on fp16 data.
 """
 
 from __future__ import annotations
@@ -24,7 +28,7 @@ import os
 import numpy as np
 import torch
 
-from paged_kv_cache_55_gb300.workloads import bf16_bits_to_f32, f32_to_bf16_bits
+from paged_kv_cache_55_gb300.workloads import NAN_BITS, bf16_bits_to_f32, bits_to_f32, f32_to_bf16_bits, f32_to_bits
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -47,18 +51,19 @@ class DenseProblem:
     """Contiguous K/V per request plus the same rows scattered into a shuffled pool."""
 
     def __init__(self, rng, ctx_lens, q_lens, H, Hkv, D, bs=16, extra_blocks=3, q_scale=1.0,
-                 perm=None):
+                 perm=None, dtype="bf16"):
         self.H, self.Hkv, self.D, self.bs = H, Hkv, D, bs
+        self.dtype = dtype
         self.ctx = list(ctx_lens)
         self.ql = list(q_lens)
         self.L = [c + q for c, q in zip(self.ctx, self.ql)]
         B = len(self.L)
         nblk = [(x + bs - 1) // bs for x in self.L]
         self.num_blocks = sum(nblk) + extra_blocks
-        self.kd = [f32_to_bf16_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32)) for x in self.L]
-        self.vd = [f32_to_bf16_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32)) for x in self.L]
+        self.kd = [f32_to_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32), dtype) for x in self.L]
+        self.vd = [f32_to_bits(rng.standard_normal((x, Hkv, D)).astype(np.float32), dtype) for x in self.L]
         T = sum(self.ql)
-        self.q = f32_to_bf16_bits((q_scale * rng.standard_normal((T, H, D))).astype(np.float32))
+        self.q = f32_to_bits((q_scale * rng.standard_normal((T, H, D))).astype(np.float32), dtype)
         self.qsl = np.zeros(B + 1, dtype=np.int32)
         self.qsl[1:] = np.cumsum(self.ql)
         self.seq_lens = np.array(self.L, dtype=np.int32)
@@ -71,8 +76,8 @@ class DenseProblem:
         """Write the dense rows into a pool whose unowned slots hold NaN."""
         bs = self.bs
         self.bt = np.full((len(self.L), self.max_blocks), -7, dtype=np.int32)
-        self.kc = np.full((self.num_blocks, bs, self.Hkv, self.D), 0x7FC0, dtype=np.uint16)
-        self.vc = np.full_like(self.kc, 0x7FC0)
+        self.kc = np.full((self.num_blocks, bs, self.Hkv, self.D), NAN_BITS[self.dtype], dtype=np.uint16)
+        self.vc = np.full_like(self.kc, NAN_BITS[self.dtype])
         cursor = 0
         for b, L in enumerate(self.L):
             for i in range((L + bs - 1) // bs):
@@ -85,7 +90,7 @@ class DenseProblem:
 
     def run(self, oracle, num_threads=2):
         return oracle.attention(self.q, self.kc, self.vc, self.bt, self.seq_lens, self.qsl,
-                                self.H, self.scale, num_threads=num_threads)
+                                self.H, self.scale, num_threads=num_threads, dtype=self.dtype)
 
     def sdpa(self):
         """PyTorch SDPA per request in float64 with a bottom-right causal mask."""
@@ -94,9 +99,9 @@ class DenseProblem:
             q0, ql = int(self.qsl[b]), self.ql[b]
             if ql == 0:
                 continue
-            qb = torch.from_numpy(bf16_bits_to_f32(self.q[q0:q0 + ql]).astype(np.float64)).transpose(0, 1)
-            kb = torch.from_numpy(bf16_bits_to_f32(self.kd[b]).astype(np.float64)).transpose(0, 1)
-            vb = torch.from_numpy(bf16_bits_to_f32(self.vd[b]).astype(np.float64)).transpose(0, 1)
+            qb = torch.from_numpy(bits_to_f32(self.q[q0:q0 + ql], self.dtype).astype(np.float64)).transpose(0, 1)
+            kb = torch.from_numpy(bits_to_f32(self.kd[b], self.dtype).astype(np.float64)).transpose(0, 1)
+            vb = torch.from_numpy(bits_to_f32(self.vd[b], self.dtype).astype(np.float64)).transpose(0, 1)
             i = torch.arange(ql).unsqueeze(1)
             j = torch.arange(L).unsqueeze(0)
             mask = j <= (L - ql) + i
@@ -121,14 +126,18 @@ DENSE_CASES = [
 ]
 
 
-def pin_dense_vs_sdpa(oracle):
+def pin_dense_vs_sdpa(oracle, dtype="bf16"):
     rng = np.random.default_rng(11)
     for ctx, ql, H, Hkv, D, bs in DENSE_CASES:
-        p = DenseProblem(rng, ctx, ql, H, Hkv, D, bs)
+        p = DenseProblem(rng, ctx, ql, H, Hkv, D, bs, dtype=dtype)
         got = p.run(oracle)
         ref = p.sdpa()
         err = float(np.max(np.abs(got - ref))) if got.size else 0.0
-        assert err <= 1e-12, f"oracle vs SDPA max |diff| {err} for case {(ctx, ql, H, Hkv, D, bs)}"
+        assert err <= 1e-12, f"oracle vs SDPA max |diff| {err} for case {(ctx, ql, H, Hkv, D, bs)} ({dtype})"
+
+
+def pin_dense_vs_sdpa_fp16(oracle):
+    pin_dense_vs_sdpa(oracle, dtype="fp16")
 
 
 def pin_block_permutation_invariance(oracle):
@@ -141,14 +150,39 @@ def pin_block_permutation_invariance(oracle):
     assert np.array_equal(a, b), "output changed under a permutation of physical block ids"
 
 
-def pin_seq_len_one_is_v_row(oracle):
+def pin_seq_len_one_is_v_row(oracle, dtype="bf16"):
     rng = np.random.default_rng(13)
-    p = DenseProblem(rng, [0, 0], [1, 1], 4, 2, 64)
+    p = DenseProblem(rng, [0, 0], [1, 1], 4, 2, 64, dtype=dtype)
     out = p.run(oracle)
     for b in range(2):
         for h in range(4):
-            v = bf16_bits_to_f32(p.vd[b][0, h // 2]).astype(np.float64)
-            assert np.array_equal(out[b, h], v), "seq_len 1 must return the V row exactly"
+            v = bits_to_f32(p.vd[b][0, h // 2], dtype).astype(np.float64)
+            assert np.array_equal(out[b, h], v), f"seq_len 1 must return the V row exactly ({dtype})"
+
+
+def pin_seq_len_one_is_v_row_fp16(oracle):
+    pin_seq_len_one_is_v_row(oracle, dtype="fp16")
+
+
+def pin_fp16_decoding_matches_ieee(oracle):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode_elements(bits, "fp16")
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan), "fp16 NaN patterns must decode to NaN"
+    assert np.array_equal(got[~nan], ref[~nan]), "fp16 decoding must match IEEE binary16"
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), "fp16 signs (incl. -0)"
+
+
+def pin_bf16_decoding_special_values(oracle):
+    cases = [(0x3F80, 1.0), (0xC000, -2.0), (0x4049, 3.140625), (0x0001, 2.0 ** -133),
+             (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127), (0x0080, 2.0 ** -126), (0x0000, 0.0), (0x8000, -0.0),
+             (0x7F80, math.inf), (0xFF80, -math.inf)]
+    bits = np.array([c[0] for c in cases] + [0x7FC0], dtype=np.uint16)
+    got = oracle.decode_elements(bits, "bf16")
+    for (h, v), g in zip(cases, got[:-1]):
+        assert g == v and math.copysign(1.0, g) == math.copysign(1.0, v), f"bf16 {h:#06x} must be {v}, got {g}"
+    assert math.isnan(got[-1]), "bf16 0x7FC0 is a NaN"
 
 
 def pin_constant_v(oracle):
@@ -273,6 +307,10 @@ def pin_reshape_matches_numpy_scatter(oracle):
 
 PINS = [
     pin_dense_vs_sdpa,
+    pin_dense_vs_sdpa_fp16,
+    pin_seq_len_one_is_v_row_fp16,
+    pin_fp16_decoding_matches_ieee,
+    pin_bf16_decoding_special_values,
     pin_block_permutation_invariance,
     pin_seq_len_one_is_v_row,
     pin_constant_v,

@@ -108,6 +108,19 @@ def test_small_cases(oracle, name):
     run_and_check(w, oracle)
 
 
+FP16_CASES = ["ragged_decode_g4_d128", "decode_g8_d64", "decode_g1_d64", "mixed_chunks_g4_d128",
+              "mixed_chunks_g1_d128", "mixed_chunks_g8_d64", "long_chunks_g2_d128", "sharp_long_chunks_g4_d128",
+              "empty_requests", "seq_len_one"]
+
+
+@pytest.mark.parametrize("name", FP16_CASES)
+def test_small_cases_fp16(oracle, name):
+    """The same cases with fp16 q, K/V and out (the oracle decodes IEEE binary16)."""
+    w = W.make_workload(name, seed=6, dtype="fp16", **SMALL_CASES[name])
+    assert w.dtype == "fp16"
+    run_and_check(w, oracle)
+
+
 def test_repeated_steps_on_reused_memory(oracle):
     """Fresh buffers each time (the caching allocator hands back the previous
     step's memory, stale plans included) and a torch kernel right before the
@@ -255,7 +268,7 @@ def test_host_side_errors():
     assert call(D=96) == -3
     assert call(bs=32) == -3
     assert call(Hkv=3) == -2
-    assert call(dtype=1) == -3
+    assert call(dtype=2) == -3  # 0 = bf16, 1 = fp16
     assert call(wsb=16) == -5
     assert call(out=st.out.data_ptr() + 2) == -4
     assert call(scale=float("nan")) == -2
@@ -284,9 +297,10 @@ def _sample_pairs(w: W.Workload, n: int, rng):
     return tokens, heads
 
 
-@pytest.mark.parametrize("name", ["mha_decode", "gqa_decode", "long_decode", "mixed_step"])
-def test_named_full_size_sampled(oracle, name):
-    w = W.by_name(name, seed=0)
+@pytest.mark.parametrize("name,dtype", [("mha_decode", "bf16"), ("gqa_decode", "bf16"), ("long_decode", "bf16"),
+                                        ("mixed_step", "bf16"), ("gqa_decode", "fp16"), ("mixed_step", "fp16")])
+def test_named_full_size_sampled(oracle, name, dtype):
+    w = W.by_name(name, seed=0, dtype=dtype)
     st = DeviceStep(w)
     st.run()
     torch.cuda.synchronize()
@@ -306,5 +320,5 @@ def test_named_full_size_sampled(oracle, name):
     vc_full = vc.reshape(w.value_cache.shape)
     tokens, heads = _sample_pairs(w, 96, np.random.default_rng(1))
     ref = oracle.attention_sampled(w.q, kc_full, vc_full, w.block_tables, w.seq_lens, w.query_start_loc,
-                                   w.num_heads, w.scale, tokens, heads)
-    assert_attention_close(out[tokens, heads], ref, name)
+                                   w.num_heads, w.scale, tokens, heads, dtype=w.dtype)
+    assert_attention_close(out[tokens, heads], ref, f"{name} {dtype}")

@@ -68,7 +68,9 @@ def test_workspace_sizes_are_host_arithmetic(lib):
 def test_validation_rejects_before_any_cuda_call(lib):
     # dtype and size errors return before the library touches the device
     args = [None, 0, None, None, None, 0, None, None, 1, 1, 1, 1, 4, 1, 64, 16, 1, 1.0, None, None, 0]
-    assert lib.pa_attention_varlen(*args, 1, None) == -3       # dtype
+    assert lib.pa_attention_varlen(*args, 2, None) == -3       # dtype (0 = bf16, 1 = fp16)
+    assert lib.pa_attention_varlen(*args, 1, None) != -3       # fp16 passes the dtype check
+    assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 0, 1, 64, 16, 1, 1, None) == 0
     assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 7, None) == -3
     assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, -1, 1, 64, 16, 1, 0, None) == -2
     assert lib.pa_reshape_and_cache(None, None, 0, 0, None, None, None, 0, 1, 64, 16, 1, 0, None) == 0

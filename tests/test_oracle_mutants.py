@@ -25,8 +25,12 @@ MUTANTS = {
     "dot_drops_last_dim": ("for (int32_t d = 0; d < D; ++d)\n            dot += qv[d]",
                            "for (int32_t d = 0; d < D - 1; ++d)\n            dot += qv[d]"),
     "unnormalised_weights": ("w[j] /= z;", "w[j] /= 1.0;"),
-    "v_read_from_k_cache": ("V[(int64_t)j * D + d] = bf16_to_double(p->value_cache[base + d]);",
-                            "V[(int64_t)j * D + d] = bf16_to_double(p->key_cache[base + d]);"),
+    "v_read_from_k_cache": ("V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->value_cache[base + d]);",
+                            "V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->key_cache[base + d]);"),
+    "fp16_exponent_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "fp16_decoded_as_bf16": ("return dtype == ORACLE_FP16 ? fp16_to_double(h) : bf16_to_double(h);",
+                             "return bf16_to_double(h);"),
     "first_query_row_only": ("const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;",
                              "const uint16_t *qrow = p->q + ((int64_t)(q0) * p->num_heads + h) * D;"),
     "drops_last_token": ("        if (s < 0)\n            continue;\n        int64_t block",

@@ -101,3 +101,25 @@ def test_unowned_slots_hold_nan_sentinel():
     flat = w.key_cache.reshape(-1, w.num_kv_heads * w.head_dim)
     assert (flat[~owned] == 0x7FC0).all()
     assert not (flat[owned] == 0x7FC0).any()
+
+
+def test_fp16_workload_rounds_the_same_draws():
+    """dtype="fp16" rounds the very draws the bf16 workload rounds (numpy's IEEE
+    binary16 conversion), keeps the structure, and fills unowned slots with the
+    fp16 NaN."""
+    kw = dict(context_lens=[5, 40, 0], query_lens=[1, 3, 9], num_heads=8, num_kv_heads=2, head_dim=64, seed=4)
+    wb = W.make_workload("b", **kw)
+    wh = W.make_workload("h", dtype="fp16", **kw)
+    assert wh.dtype == "fp16" and wb.dtype == "bf16"
+    for f in ("slot_mapping", "block_tables", "seq_lens", "query_start_loc"):
+        assert np.array_equal(getattr(wb, f), getattr(wh, f))
+    qb = W.bf16_bits_to_f32(wb.q).astype(np.float64)
+    qh = wh.q.view(np.float16).astype(np.float64)
+    assert np.all(np.abs(qb - qh) <= 2.0 ** -8 * np.abs(qh) + 1e-7)  # both round one float32 draw
+    own = np.zeros(wh.key_cache.shape[0] * wh.block_size, dtype=bool)
+    for b in range(wh.num_seqs):
+        L = int(wh.seq_lens[b])
+        j = np.arange(L)
+        own[wh.block_tables[b, j // wh.block_size].astype(np.int64) * wh.block_size + j % wh.block_size] = True
+    flat = wh.key_cache.reshape(-1, wh.num_kv_heads, wh.head_dim)
+    assert (flat[~own] == 0x7E00).all() and np.isnan(flat[~own].view(np.float16)).all()
