@@ -49,7 +49,11 @@ WORKLOAD_TEXT = {
     "long_decode": "long-context decode: batch 8, seq_len 32768, H=64, Hkv=8, D=128, bs=16",
     "mixed_step": "mixed continuous-batching step: 16 prefill chunks x 512 (ctx U[0,4096]) + 240 decode "
                   "(ctx U[256,4096], 64 share a 64-block prefix), H=32, Hkv=8, D=128, bs=16",
+    "copy_blocks": "copy-on-write block copy: 4096 (source, destination) pairs per step over a pool of 16384 "
+                   "blocks of the GQA cache shape (bs=16, Hkv=8, D=128; 32 KB per block and cache)",
 }
+COPY_POOL_BLOCKS, COPY_PAIRS = 16384, 4096
+COPY_METRIC = "CoW block copy GB/s (read + write) & fraction of GB300 HBM peak"
 
 
 # --------------------------------------------------------------------------
@@ -425,6 +429,160 @@ def run_ours(args, world, rank, local_rank) -> None:
         print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# Copy-on-write block copy (a separate workload: pa_copy_blocks alone)
+# --------------------------------------------------------------------------
+
+def copy_mapping(seed: int) -> np.ndarray:
+    """COPY_PAIRS distinct sources and distinct destinations, no destination a source."""
+    ids = np.random.default_rng(seed + 4000).permutation(COPY_POOL_BLOCKS)
+    return np.stack([ids[:COPY_PAIRS], ids[COPY_PAIRS:2 * COPY_PAIRS]], axis=1).astype(np.int64)
+
+
+def copy_oracle_rate(target_s: float, seed: int):
+    """The oracle's block copy on a host pool (512 blocks, 128 pairs per call) until
+    about target_s; returns (GB/s read + write, seconds, pairs)."""
+    import oracle as oracle_mod
+    orc = oracle_mod.default()
+    rng = np.random.default_rng(seed)
+    shape = (512, 16, 8, 128)
+    kc = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    per_pair = 2 * 2 * int(np.prod(shape[1:])) * 2  # K and V, read and write
+    t_total, pairs = 0.0, 0
+    while t_total < target_s:
+        ids = rng.permutation(shape[0])
+        m = np.stack([ids[:128], ids[128:256]], axis=1)
+        t0 = time.perf_counter()
+        orc.copy_blocks(kc, vc, m)
+        t_total += time.perf_counter() - t0
+        pairs += 128
+    return pairs * per_pair / t_total / 1e9, t_total, pairs
+
+
+def run_copy_reference(args, world, rank) -> None:
+    if rank != 0:
+        return
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        copy_oracle_rate(per_step / 4, args.seed)
+    rates, secs, pairs = [], 0.0, 0
+    for k in range(args.steps):
+        r, t, n = copy_oracle_rate(per_step, args.seed + k)
+        rates.append(r)
+        secs += t
+        pairs += n
+    value = statistics.median(rates)
+    line = {
+        "metric": COPY_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "raw 16-bit", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "copy-on-write block copy on the host: bounded sample (128 pairs per call over a "
+                               "512-block pool of the GQA block shape)", "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{pairs} block pairs, {secs:.1f} s of memcpy-based oracle copy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_copy_blocks(args, world, rank, local_rank) -> None:
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_55_gb300 import binding as B
+    from paged_kv_cache_55_gb300 import build as build_mod
+
+    build_mod.build()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    tdt = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(rank_seed(args.seed, rank))
+    shape = (COPY_POOL_BLOCKS, 16, 8, 128)
+    # seeded random 16-bit patterns (the copy moves raw bits; NaN patterns included)
+    kc = torch.randint(-32768, 32767, shape, dtype=torch.int16, device=device, generator=gen).view(tdt)
+    vc = torch.randint(-32768, 32767, shape, dtype=torch.int16, device=device, generator=gen).view(tdt)
+    m_host = torch.from_numpy(copy_mapping(rank_seed(args.seed, rank))).pin_memory()
+    m = m_host.to(device)
+    block_bytes = 16 * 8 * 128 * 2
+    step_bytes = COPY_PAIRS * 2 * 2 * block_bytes  # K and V blocks, read once and written once
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 1)):
+        B.pa_copy_blocks(kc, vc, m)
+    torch.cuda.synchronize()
+    if B.pa_debug_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+    gpu_id = str(torch.cuda.get_device_properties(device).uuid)
+    gpu_id = gpu_id if gpu_id.startswith("GPU-") else f"GPU-{gpu_id}"
+    sampler = ClockSampler(gpu_id)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = B.pa_launch_count()
+    t0.record(stream)
+    for _ in range(args.steps):
+        B.pa_copy_blocks(kc, vc, m)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = B.pa_launch_count() - launches0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    step_ms = t0.elapsed_time(t1) / args.steps
+    max_ms = reduce_max(step_ms, device)
+    total_bytes = reduce_sum(float(step_bytes), device)
+    value = aggregate_rate(total_bytes, max_ms * 1e-3) / 1e9
+
+    # end to end: the mapping from pinned host memory, the copy, one destination block's first row back
+    host_out = torch.empty((8, 128), dtype=tdt).pin_memory()
+    probe_block = int(m_host[-1, 1])
+
+    def e2e_step():
+        m.copy_(m_host, non_blocking=True)
+        B.pa_copy_blocks(kc, vc, m)
+        host_out.copy_(vc[probe_block, 0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, device)
+    assert B.pa_debug_status() == 0
+    peaks = load_peaks()
+    line = {
+        "metric": COPY_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic (seeded random 16-bit patterns)",
+        "hbm_frac": value / peaks["hbm_gbs"],
+        "config": {"workload": workload_text(args), "seed": args.seed,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "no flush: 512 MB moved per step, larger than L2", "step_bytes": step_bytes},
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": value, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": value / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "kernel_ms": step_ms, "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+        "e2e": {"value": aggregate_rate(total_bytes, e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": int(m_host.numel() * 8),
+                "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size())},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, secs, pairs = copy_oracle_rate(min(args.cpu_seconds, 5.0), args.seed)
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{pairs} block pairs over a 512-block host pool, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,7 +603,10 @@ def main() -> None:
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        if args.workload == "copy_blocks":
+            run_copy_reference(args, world, rank)
+        else:
+            run_reference(args, world, rank)
         return
     if world > 1:
         import torch
@@ -453,7 +614,10 @@ def main() -> None:
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, world, rank, local_rank)
+        if args.workload == "copy_blocks":
+            run_copy_blocks(args, world, rank, local_rank)
+        else:
+            run_ours(args, world, rank, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -167,6 +167,24 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
                               int32_t dtype, void *stream);
 
 /*
+ * Copy-on-write block copy (LLM-infra reading map, §2.2: a physical block
+ * shared by several requests is copied before one of them writes into it).
+ * For each pair i < num_pairs, copy physical block block_mapping[2*i] to
+ * physical block block_mapping[2*i + 1] in both caches: all block_size
+ * tokens, all KV heads, raw bits (any 16-bit dtype).
+ *   key_cache, value_cache (device): [num_blocks, block_size, num_kv_heads,
+ *       head_dim], 16-byte aligned, head_dim a multiple of 8.
+ *   block_mapping (device): int64 [num_pairs, 2] = (source, destination).
+ * Destinations must be distinct and no destination may also be a source in
+ * the same call (the result is unspecified otherwise). A pair with an id
+ * outside [0, num_blocks) is skipped and sets PA_FLAG_BLOCK_RANGE.
+ * Returns PA_OK without launching when num_pairs == 0.
+ */
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, int32_t dtype, void *stream);
+
+/*
  * Block-table addressing on its own: copy the seq_len logical K/V rows of one
  * request, read through its block-table row, into contiguous
  * [seq_len, num_kv_heads, head_dim] buffers (device, 16-byte aligned).

@@ -25,7 +25,7 @@ ERRORS = {
     0: "ok",
     -1: "bad argument",
     -2: "slot out of range",
-    -3: "duplicate slot",
+    -3: "duplicate slot or destination block",
     -4: "block id out of range",
     -5: "inconsistent lengths",
     -6: "out of memory",
@@ -79,6 +79,8 @@ class Oracle:
         L.oracle_attention_sampled.restype = ctypes.c_int
         L.oracle_attention_weights.argtypes = common + [_I64, _I32, _P]
         L.oracle_attention_weights.restype = ctypes.c_int
+        L.oracle_copy_blocks.argtypes = [_P, _P, _P, _I64, _I64, _I64]
+        L.oracle_copy_blocks.restype = ctypes.c_int
         L.oracle_decode_elements.argtypes = [_P, _I64, _I32, _P]
         L.oracle_decode_elements.restype = ctypes.c_int
 
@@ -100,6 +102,18 @@ class Oracle:
                                                _ptr(slot_mapping), int(slot_mapping.shape[0]),
                                                hkv, d, bs, nb)
         self._check(rc, "reshape_and_cache")
+
+    def copy_blocks(self, key_cache, value_cache, block_mapping) -> None:
+        """Copy-on-write block copy in place on ``key_cache`` / ``value_cache`` (uint16
+        [num_blocks, bs, Hkv, D]); ``block_mapping`` int64 [n, 2] = (source, destination)."""
+        assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+        assert key_cache.dtype == np.uint16 and value_cache.dtype == np.uint16
+        m = np.ascontiguousarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+        nb = key_cache.shape[0]
+        block_elems = int(np.prod(key_cache.shape[1:]))
+        rc = self.lib.oracle_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(m), int(m.shape[0]),
+                                         block_elems, nb)
+        self._check(rc, "copy_blocks")
 
     def decode_elements(self, bits, dtype: str = "bf16") -> np.ndarray:
         """The oracle's widening of 16-bit element bit patterns to float64."""

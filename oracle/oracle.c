@@ -152,6 +152,37 @@ int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
     return ORACLE_OK;
 }
 
+/*
+ * Copy-on-write block copy (§2.2 of the LLM-infra reading map: a shared block
+ * is copied before a request writes into it): for each pair, the raw bits of
+ * physical block mapping[2i] become those of block mapping[2i+1], in both
+ * caches. block_elems = block_size * num_kv_heads * head_dim. Rejects ids out
+ * of range, repeated destinations and destinations that are also sources.
+ */
+int oracle_copy_blocks(uint16_t *key_cache, uint16_t *value_cache, const int64_t *mapping,
+                       int64_t num_pairs, int64_t block_elems, int64_t num_blocks)
+{
+    if (num_pairs < 0 || block_elems <= 0 || num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return ORACLE_ERR_BLOCK_RANGE;
+        for (int64_t k = 0; k < num_pairs; ++k) {
+            if (k != i && mapping[2 * k + 1] == dst)
+                return ORACLE_ERR_SLOT_DUPLICATE;
+            if (mapping[2 * k] == dst)
+                return ORACLE_ERR_ARG;
+        }
+    }
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+        memcpy(key_cache + dst * block_elems, key_cache + src * block_elems, sizeof(uint16_t) * block_elems);
+        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems, sizeof(uint16_t) * block_elems);
+    }
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step 2: attention over the paged cache                                    */
 /* ------------------------------------------------------------------------ */

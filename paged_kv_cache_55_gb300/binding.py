@@ -47,6 +47,7 @@ SIGNATURES = {
     "pa_debug_status": ([_P, _P], ctypes.c_int),
     "pa_launch_count": ([], ctypes.c_uint64),
     "pa_last_cuda_error": ([], ctypes.c_char_p),
+    "pa_copy_blocks": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I64, _I32, _P], ctypes.c_int32),
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
@@ -182,6 +183,20 @@ def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_c
                                              seq_lens.data_ptr(), query_start_loc.data_ptr(), B, T, max_query_len,
                                              max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), dt,
                                              _stream(stream)), "pa_attention_varlen_static")
+
+
+def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,
+                   stream=None) -> None:
+    """Copy-on-write block copy: block_mapping int64 [n, 2] (source, destination) on the device."""
+    dt = _elem_code((key_cache, "key_cache"), (value_cache, "value_cache"))
+    _need(block_mapping, "block_mapping", torch.int64)
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous() and block_mapping.is_contiguous()):
+        raise ValueError("caches and block_mapping must be contiguous")
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be [n, 2]")
+    nb, bs, hkv, d = key_cache.shape
+    _check(_lib().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), block_mapping.data_ptr(),
+                                 block_mapping.shape[0], hkv, d, bs, nb, dt, _stream(stream)), "pa_copy_blocks")
 
 
 def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor,

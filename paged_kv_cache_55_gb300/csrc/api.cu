@@ -209,6 +209,25 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   return PA_OK;
 }
 
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping, int32_t num_pairs,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         int32_t dtype, void *stream) {
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0) return PA_ERR_DIMS;
+  if (head_dim % 8) return PA_ERR_ALIGN;  // a block is a whole number of 16-byte vectors
+  if (num_pairs == 0) return PA_OK;
+  if (!key_cache || !value_cache || !block_mapping) return PA_ERR_NULL;
+  if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(block_mapping, 8)) return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  const int64_t block_elems = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
+  cudaError_t err = pa::launch_copy_blocks(key_cache, value_cache, block_mapping, num_pairs, block_elems, num_blocks,
+                                           ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
 pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int32_t *block_table_row,
                        int32_t seq_len, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int64_t num_blocks, void *key_out, void *value_out, int32_t dtype, void *stream) {

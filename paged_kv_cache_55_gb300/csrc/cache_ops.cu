@@ -1,5 +1,6 @@
-// reshape_and_cache (scatter of a step's new K/V rows into the paged cache)
-// and the block-table gather used to check addressing.
+// reshape_and_cache (scatter of a step's new K/V rows into the paged cache),
+// the copy-on-write block copy, and the block-table gather used to check
+// addressing.
 //
 // vLLM inference notes ("AI Infra入门干货总结：大模型是如何高效推理的"),
 // §Paged Attention: slot_mapping names where each new token's K/V goes;
@@ -63,6 +64,50 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(
   }
 }
 
+// Copy-on-write block copy (LLM-infra reading map, §2.2: a shared block is
+// copied before a request that shares it writes to it): pair i copies
+// physical block mapping[2i] to block mapping[2i + 1] in both caches. A block
+// of one cache is one contiguous run of block16 16-byte vectors; a CTA copies
+// whole blocks, its threads striding over the vectors with four loads of each
+// cache in flight. Sources are read after the dependency wait with
+// ld.global.cg: a preceding kernel (the cache scatter) may have written them.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *key_cache, uint4 *value_cache,
+                                                          const int64_t *__restrict__ mapping, int32_t num_pairs,
+                                                          int64_t block16, int64_t num_blocks, unsigned int *status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int kUnroll = 4;
+  for (int32_t pair = blockIdx.x; pair < num_pairs; pair += gridDim.x) {
+    const int64_t src = ld_cg(reinterpret_cast<const long long *>(mapping) + 2 * static_cast<int64_t>(pair));
+    const int64_t dst = ld_cg(reinterpret_cast<const long long *>(mapping) + 2 * static_cast<int64_t>(pair) + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      if (threadIdx.x == 0) flag_error(status, PA_FLAG_BLOCK_RANGE);
+      continue;
+    }
+    const uint4 *ks = key_cache + src * block16, *vs = value_cache + src * block16;
+    uint4 *kd = key_cache + dst * block16, *vd = value_cache + dst * block16;
+    for (int64_t i0 = threadIdx.x; i0 < block16; i0 += kUnroll * blockDim.x) {
+      uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * blockDim.x;
+        if (i < block16) {
+          a[u] = ld_cg(ks + i);
+          b[u] = ld_cg(vs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * blockDim.x;
+        if (i < block16) {
+          kd[i] = a[u];
+          vd[i] = b[u];
+        }
+      }
+    }
+  }
+}
+
 static int grid_for(int64_t work, int threads, int sm_count) {
   int64_t g = (work + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;
@@ -82,6 +127,17 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                     static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,
                     static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, num_tokens,
                     row16, num_slots, status);
+}
+
+cudaError_t launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *mapping, int32_t num_pairs,
+                               int64_t block_elems, int64_t num_blocks, unsigned int *status, int sm_count,
+                               cudaStream_t stream) {
+  int64_t grid = static_cast<int64_t>(sm_count) * 4;  // 4 CTAs of 256 threads per SM
+  if (grid > num_pairs) grid = num_pairs;
+  if (grid < 1) grid = 1;
+  return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                    static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), mapping, num_pairs,
+                    block_elems / 8, num_blocks, status);
 }
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,

@@ -14,6 +14,10 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      int64_t num_slots, unsigned int *status, int sm_count,
                                      cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *mapping, int32_t num_pairs,
+                               int64_t block_elems, int64_t num_blocks, unsigned int *status, int sm_count,
+                               cudaStream_t stream);
+
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
                              int32_t seq_len, int32_t row_elems, int64_t num_blocks, void *key_out,
                              void *value_out, unsigned int *status, int sm_count, cudaStream_t stream);

@@ -305,6 +305,20 @@ def pin_reshape_matches_numpy_scatter(oracle):
     assert np.array_equal(kc, ek) and np.array_equal(vc, ev), "scatter must match numpy fancy assignment"
 
 
+def pin_copy_blocks_matches_numpy(oracle):
+    rng = np.random.default_rng(20)
+    nb, bs, hkv, d = 40, 16, 2, 8
+    kc = rng.integers(0, 65535, size=(nb, bs, hkv, d), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(nb, bs, hkv, d), dtype=np.uint16)
+    ids = rng.permutation(nb)
+    src, dst = ids[:9], ids[9:18]  # disjoint: no destination is also a source
+    ek, ev = kc.copy(), vc.copy()
+    ek[dst] = kc[src]
+    ev[dst] = vc[src]
+    oracle.copy_blocks(kc, vc, np.stack([src, dst], axis=1))
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev), "block copy must match numpy assignment"
+
+
 PINS = [
     pin_dense_vs_sdpa,
     pin_dense_vs_sdpa_fp16,
@@ -321,4 +335,5 @@ PINS = [
     pin_gqa_equals_replicated_mha,
     pin_slot_formula_golden,
     pin_reshape_matches_numpy_scatter,
+    pin_copy_blocks_matches_numpy,
 ]

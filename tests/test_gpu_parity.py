@@ -188,6 +188,42 @@ def test_block_permutation_gives_identical_bits():
     assert np.array_equal(bf16_to_numpy_bits(a.out), bf16_to_numpy_bits(b.out))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_copy_blocks_bit_exact(oracle, dtype):
+    """Copy-on-write block copy against the oracle, bit for bit; 3000 pairs over a
+    GQA-shaped pool (and a small D = 64 pool), raw bits of either element type."""
+    rng = np.random.default_rng(31)
+    for nb, hkv, d, npairs in ((7000, 8, 128, 3000), (50, 2, 64, 17)):
+        w = W.make_workload("copy", context_lens=[nb * 16 // 2], query_lens=[1], num_heads=hkv * 4,
+                            num_kv_heads=hkv, head_dim=d, num_blocks=nb, seed=8, dtype=dtype)
+        ids = rng.permutation(nb)
+        m = np.stack([ids[:npairs], ids[npairs:2 * npairs]], axis=1).astype(np.int64)
+        kc, vc = w.key_cache.copy(), w.value_cache.copy()
+        oracle.copy_blocks(kc, vc, m)
+        kt = bf16_tensor(w.key_cache, "cuda", dtype)
+        vt = bf16_tensor(w.value_cache, "cuda", dtype)
+        B.pa_copy_blocks(kt, vt, torch.from_numpy(m).cuda())
+        torch.cuda.synchronize()
+        assert B.pa_debug_status() == 0
+        assert np.array_equal(bf16_to_numpy_bits(kt), kc) and np.array_equal(bf16_to_numpy_bits(vt), vc)
+
+
+def test_copy_blocks_flags_and_skips_bad_ids():
+    w = W.make_workload("copy", context_lens=[100], query_lens=[1], num_heads=8, num_kv_heads=2, head_dim=64,
+                        num_blocks=12, seed=9)
+    kt = bf16_tensor(w.key_cache, "cuda")
+    vt = bf16_tensor(w.value_cache, "cuda")
+    m = torch.tensor([[1, 2], [3, 12], [-1, 4], [5, 6]], dtype=torch.int64, device="cuda")
+    B.pa_copy_blocks(kt, vt, m)
+    flags = B.pa_debug_status()
+    assert flags == B.FLAG_BLOCK_RANGE
+    k = bf16_to_numpy_bits(kt)
+    assert np.array_equal(k[2], w.key_cache[1]) and np.array_equal(k[6], w.key_cache[5])
+    assert np.array_equal(k[4], w.key_cache[4]) and np.array_equal(k[11], w.key_cache[11])  # skipped pairs
+    B.pa_copy_blocks(kt, vt, torch.zeros((0, 2), dtype=torch.int64, device="cuda"))  # nothing to do
+    assert B.pa_debug_status() == 0
+
+
 def test_gather_kv_bit_exact():
     w = W.make_workload("gather", seed=3, **SMALL_CASES["ragged_decode_g4_d128"])
     st = DeviceStep(w)

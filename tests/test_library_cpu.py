@@ -77,6 +77,11 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.pa_attention_set_timing_events(None, None) == 0
     assert lib.pa_launch_count() == 0
     assert lib.pa_last_cuda_error() == b"cudaSuccess"
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 10, 2, None) == -3   # dtype
+    assert lib.pa_copy_blocks(None, None, None, -1, 8, 128, 16, 10, 0, None) == -2  # negative count
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 100, 16, 10, 0, None) == -4   # rows not 16-byte vectors
+    assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, 1, None) == 0    # nothing to do
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 10, 0, None) == -1   # null pointers
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -29,6 +29,9 @@ MUTANTS = {
                             "V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->key_cache[base + d]);"),
     "fp16_exponent_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
     "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "copy_blocks_k_only": ("        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems, "
+                           "sizeof(uint16_t) * block_elems);",
+                           "        (void)value_cache;"),
     "fp16_decoded_as_bf16": ("return dtype == ORACLE_FP16 ? fp16_to_double(h) : bf16_to_double(h);",
                              "return bf16_to_double(h);"),
     "first_query_row_only": ("const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;",
