@@ -60,7 +60,7 @@ COPY_METRIC = "CoW block copy GB/s (read + write) & fraction of GB300 HBM peak"
 # Byte and FLOP accounting (algorithmic: what the step must move at minimum)
 # --------------------------------------------------------------------------
 
-def step_accounting(w) -> dict:
+def step_accounting(w, rope: bool = False) -> dict:
     H, Hkv, D, bs = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     kv_tok = 2 * Hkv * D * 2
     uniq = w.kv_tokens_unique()
@@ -70,6 +70,8 @@ def step_accounting(w) -> dict:
     meta = (2 * w.num_seqs + 1) * 4
     q_out = 2 * T * H * D * 2
     reshape = T * (2 * Hkv * D * 2) * 2 + T * 8
+    if rope:  # q rotated in place (read + write), positions, one table row per token
+        reshape += 2 * T * H * D * 2 + T * 8 + T * D * 4
     kv_bytes = uniq * kv_tok
     flops = 0
     ql = w.query_lens
@@ -298,6 +300,8 @@ def workload_text(args) -> str:
     text = WORKLOAD_TEXT[args.workload]
     if args.dtype != "bf16":
         text += f" [{args.dtype} elements]"
+    if getattr(args, "rope", False):
+        text += " [rotary embedding fused into the cache scatter]"
     return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
 
 
@@ -316,8 +320,13 @@ def run_ours(args, world, rank, local_rank) -> None:
     kw = {"batch": args.batch} if args.batch else {}
     kw["dtype"] = args.dtype
     w = W.by_name(args.workload, seed=rank_seed(args.seed, rank), **kw)
-    acct = step_accounting(w)
-    st = DeviceStep(w, device=str(device))
+    acct = step_accounting(w, rope=args.rope)
+    rope = None
+    if args.rope:
+        pos = np.concatenate([int(w.seq_lens[b]) - int(w.query_lens[b]) + np.arange(int(w.query_lens[b]))
+                              for b in range(w.num_seqs)]).astype(np.int64)
+        rope = (W.rope_cos_sin_cache(int(w.max_seq_len) + 1, w.head_dim), pos, True)
+    st = DeviceStep(w, device=str(device), rope=rope)
     stream = torch.cuda.current_stream()
 
     # warm-up (the first call also creates the timing events)
@@ -367,15 +376,18 @@ def run_ours(args, world, rank, local_rank) -> None:
 
     # end to end through the C ABI with host buffers: H2D inputs, the step, D2H output
     pin = lambda t: t.cpu().pin_memory()
-    host_in = {k: pin(getattr(st, k)) for k in ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens",
-                                                "query_start_loc")}
+    dev_in = [getattr(st, k) for k in ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens",
+                                       "query_start_loc")]
+    if st.rope is not None:
+        dev_in.append(st.rope[1])  # this step's positions (the rotary table stays resident, like weights)
+    host_in = [(d, pin(d)) for d in dev_in]
     host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for k, t in host_in.items():
-            getattr(st, k).copy_(t, non_blocking=True)
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
         st.run()
         host_out.copy_(st.out, non_blocking=True)
 
@@ -403,7 +415,8 @@ def run_ours(args, world, rank, local_rank) -> None:
         "config": {"workload": workload_text(args), "seed": args.seed,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "no flush: KV working set per step is larger than L2",
-                   "step": "pa_reshape_and_cache + pa_attention_varlen (plan, split-KV, merge)",
+                   "step": ("pa_rope_reshape_and_cache" if args.rope else "pa_reshape_and_cache")
+                           + " + pa_attention_varlen (plan, split-KV, merge)",
                    "step_bytes": acct["step_bytes"], "kv_bytes": acct["kv_bytes"],
                    "kv_bytes_logical": acct["kv_bytes_logical"], "flops": acct["flops"]},
         "roofline": {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
@@ -593,6 +606,9 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="element type of q, K/V and out (the metric's workload is bf16)")
+    ap.add_argument("--rope", action="store_true",
+                    help="the step rotates q and K (pa_rope_reshape_and_cache, neox pairing, rotary_dim = D) "
+                         "instead of pa_reshape_and_cache")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's number of requests (small profiling cases only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

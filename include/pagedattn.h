@@ -69,7 +69,8 @@ enum {
     PA_FLAG_LENGTHS = 1u << 2,      /* seq_len < query_len, seq_len > max_seq_len, query_len > max_query_len,
                                        or seq_len > max_blocks_per_seq * block_size */
     PA_FLAG_QUERY_LOC = 1u << 3,    /* query_start_loc not non-decreasing from 0 to total_q_tokens */
-    PA_FLAG_TIMEOUT = 1u << 4       /* a kernel gave up waiting for its own data copy (bounded wait) */
+    PA_FLAG_TIMEOUT = 1u << 4,      /* a kernel gave up waiting for its own data copy (bounded wait) */
+    PA_FLAG_POSITION_RANGE = 1u << 5 /* rope_reshape_and_cache: position outside [0, max_position) */
 };
 
 /*
@@ -165,6 +166,41 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
                               int32_t block_size, int64_t num_blocks, float scale,
                               void *out, void *workspace, size_t workspace_bytes,
                               int32_t dtype, void *stream);
+
+/*
+ * Rotary position embedding fused with reshape_and_cache (vLLM notes, §LLM
+ * 推理全流程 2: a token's position is a rotation angle, with a precomputed
+ * cos_sin_cache of shape [max_position, rotary_dim]). For every token t with
+ * positions[t] in [0, max_position):
+ *   - every head of q[t] is rotated in place;
+ *   - if slot_mapping[t] >= 0, key[t] rotated and value[t] unchanged are
+ *     written to the slot, exactly as pa_reshape_and_cache writes them (key
+ *     and value themselves are not modified).
+ * Row p of cos_sin_cache (device, fp32, 16-byte aligned) holds
+ * cos(p * theta_i) for i < rotary_dim / 2 followed by sin(p * theta_i) for the
+ * same i. A rotated pair (x1, x2) becomes (x1 cos - x2 sin, x2 cos + x1 sin),
+ * computed in fp32 and rounded once to the element type. Pairs are element
+ * i with i + rotary_dim / 2 (is_neox != 0) or elements 2i and 2i + 1
+ * (is_neox == 0), for i < rotary_dim / 2; elements at rotary_dim and above
+ * pass through. rotary_dim must be a multiple of 16, at most head_dim and at
+ * most 512; head_dim a multiple of 8.
+ *   q (device): [num_tokens, num_heads, head_dim], token stride q_token_stride
+ *       elements (a multiple of 8, >= num_heads * head_dim), 16-byte aligned.
+ *   key, value, caches, slot_mapping: as for pa_reshape_and_cache (any
+ *       block_size).
+ *   positions (device): int64 [num_tokens].
+ * A token whose position is out of range is skipped entirely (q unrotated,
+ * nothing cached) and sets PA_FLAG_POSITION_RANGE; a slot out of range sets
+ * PA_FLAG_SLOT_RANGE.
+ */
+pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void *key, const void *value,
+                                    int64_t key_token_stride, int64_t value_token_stride,
+                                    void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                                    const int64_t *positions, const float *cos_sin_cache,
+                                    int32_t max_position, int32_t rotary_dim, int32_t is_neox,
+                                    int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                    int32_t dtype, void *stream);
 
 /*
  * Copy-on-write block copy (LLM-infra reading map, §2.2: a physical block

@@ -81,6 +81,11 @@ class Oracle:
         L.oracle_attention_weights.restype = ctypes.c_int
         L.oracle_copy_blocks.argtypes = [_P, _P, _P, _I64, _I64, _I64]
         L.oracle_copy_blocks.restype = ctypes.c_int
+        L.oracle_round_elements.argtypes = [_P, _I64, _I32, _P]
+        L.oracle_round_elements.restype = ctypes.c_int
+        L.oracle_rope_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I64, _I32,
+                                                    _I32, _I32, _I32, _I64, _I32]
+        L.oracle_rope_reshape_and_cache.restype = ctypes.c_int
         L.oracle_decode_elements.argtypes = [_P, _I64, _I32, _P]
         L.oracle_decode_elements.restype = ctypes.c_int
 
@@ -114,6 +119,33 @@ class Oracle:
         rc = self.lib.oracle_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(m), int(m.shape[0]),
                                          block_elems, nb)
         self._check(rc, "copy_blocks")
+
+    def round_elements(self, x, dtype: str = "bf16") -> np.ndarray:
+        """The oracle's round-to-nearest-even of float64 values to 16-bit element bits."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.zeros(x.shape, dtype=np.uint16)
+        rc = self.lib.oracle_round_elements(_ptr(x), int(x.size), DTYPES[dtype], _ptr(out))
+        self._check(rc, "round_elements")
+        return out
+
+    def rope_reshape_and_cache(self, q, key, value, key_cache, value_cache, slot_mapping, positions,
+                               cos_sin_cache, is_neox: bool, block_size: int, dtype: str = "bf16"):
+        """Rotate ``q`` in place (uint16 [T, H, D]); write the rotated key and the value rows
+        into the caches in place. cos_sin_cache: float32 [max_position, rotary_dim]."""
+        assert q.flags.c_contiguous and q.dtype == np.uint16
+        assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+        key = np.ascontiguousarray(key, dtype=np.uint16)
+        value = np.ascontiguousarray(value, dtype=np.uint16)
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        pos = np.ascontiguousarray(positions, dtype=np.int64)
+        cs = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+        T, H, D = q.shape
+        nb, bs, hkv, d = key_cache.shape
+        assert bs == block_size and d == D
+        rc = self.lib.oracle_rope_reshape_and_cache(
+            _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slots), _ptr(pos), _ptr(cs),
+            int(cs.shape[0]), int(cs.shape[1]), int(bool(is_neox)), T, H, hkv, D, bs, nb, DTYPES[dtype])
+        self._check(rc, "rope_reshape_and_cache")
 
     def decode_elements(self, bits, dtype: str = "bf16") -> np.ndarray:
         """The oracle's widening of 16-bit element bit patterns to float64."""

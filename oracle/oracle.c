@@ -89,6 +89,65 @@ static double elem_to_double(int32_t dtype, uint16_t h)
     return dtype == ORACLE_FP16 ? fp16_to_double(h) : bf16_to_double(h);
 }
 
+/*
+ * Round a double to the nearest element of a binary floating-point format
+ * with `mant` stored fraction bits, exponent bias `bias` and largest exponent
+ * `emax` (bf16: 7, 127, 127; fp16: 10, 15, 15), ties to even, directly from
+ * the double (no intermediate float). Overflow goes to infinity, NaN to the
+ * format's quiet NaN. Returns the 16-bit pattern.
+ */
+static uint16_t round_to_format(double x, int mant, int bias, int emax)
+{
+    const int ebits = (mant == 7) ? 8 : 5;
+    const uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
+    const uint16_t inf = (uint16_t)(((1u << ebits) - 1) << mant);
+    if (isnan(x))
+        return (uint16_t)(inf | (1u << (mant - 1)));
+    double a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | inf);
+    if (a == 0.0)
+        return sign;
+    const int emin = 1 - bias;
+    int k;
+    (void)frexp(a, &k); /* a = f * 2^k, f in [0.5, 1): exponent e = k - 1 */
+    int e = k - 1;
+    if (e < emin)
+        e = emin; /* subnormal range: fixed quantum */
+    const double q = ldexp(1.0, e - mant);
+    const double n = a / q; /* exact: q is a power of two */
+    double r = floor(n);
+    const double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    const double v = r * q;
+    if (v == 0.0)
+        return sign;
+    (void)frexp(v, &k);
+    int ev = k - 1;
+    if (ev > emax)
+        return (uint16_t)(sign | inf);
+    if (ev < emin) /* subnormal: exponent field 0 */
+        return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, emin - mant)));
+    const uint32_t frac_bits = (uint32_t)(v / ldexp(1.0, ev - mant)) - (1u << mant);
+    return (uint16_t)(sign | (uint16_t)((uint32_t)(ev + bias) << mant) | frac_bits);
+}
+
+static uint16_t double_to_elem(int32_t dtype, double x)
+{
+    return dtype == ORACLE_FP16 ? round_to_format(x, 10, 15, 15) : round_to_format(x, 7, 127, 127);
+}
+
+/* The rounding over an array, for the tests that pin it. */
+int oracle_round_elements(const double *x, int64_t n, int32_t dtype, uint16_t *out)
+{
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = double_to_elem(dtype, x[i]);
+    return 0;
+}
+
 /* The element decoders over an array, for the tests that pin them. */
 int oracle_decode_elements(const uint16_t *bits, int64_t n, int32_t dtype, double *out)
 {
@@ -180,6 +239,83 @@ int oracle_copy_blocks(uint16_t *key_cache, uint16_t *value_cache, const int64_t
         memcpy(key_cache + dst * block_elems, key_cache + src * block_elems, sizeof(uint16_t) * block_elems);
         memcpy(value_cache + dst * block_elems, value_cache + src * block_elems, sizeof(uint16_t) * block_elems);
     }
+    return ORACLE_OK;
+}
+
+/*
+ * Rotary position embedding applied on the way into the cache (§LLM 推理全流程
+ * 2 of the vLLM notes: a token's position is a rotation angle, with a
+ * precomputed cos_sin_cache of shape [max_position, rotary_dim]).
+ * Row p of the cache holds cos(p * theta_i) in columns i < rotary_dim / 2 and
+ * sin(p * theta_i) in the next rotary_dim / 2. Each rotated pair (x1, x2)
+ * becomes (x1 cos - x2 sin, x2 cos + x1 sin); pairs are element i with
+ * i + rotary_dim / 2 (is_neox) or elements 2i and 2i + 1, for
+ * i < rotary_dim / 2; elements at rotary_dim and above are unchanged. The
+ * rotation is computed in double from the decoded elements and the float
+ * cache entries and rounded once to the element type.
+ * For each token t with positions[t] in [0, max_position): q[t] (every head)
+ * is rotated in place; if slot_mapping[t] >= 0, the rotated key[t] and the
+ * unchanged value[t] are written to the slot as reshape_and_cache does.
+ * A token whose position is out of range is an error (ORACLE_ERR_ARG).
+ */
+static void rotate_row(uint16_t *dst, const uint16_t *src, int32_t D, const float *cs, int32_t rot,
+                       int32_t is_neox, int32_t dtype)
+{
+    const int32_t half = rot / 2;
+    for (int32_t d = 0; d < D; ++d)
+        dst[d] = src[d];
+    for (int32_t i = 0; i < half; ++i) {
+        const int32_t a = is_neox ? i : 2 * i;
+        const int32_t b = is_neox ? i + half : 2 * i + 1;
+        const double x1 = elem_to_double(dtype, src[a]), x2 = elem_to_double(dtype, src[b]);
+        const double c = (double)cs[i], s = (double)cs[half + i];
+        dst[a] = double_to_elem(dtype, x1 * c - x2 * s);
+        dst[b] = double_to_elem(dtype, x2 * c + x1 * s);
+    }
+}
+
+int oracle_rope_reshape_and_cache(uint16_t *q, const uint16_t *key, const uint16_t *value,
+                                  uint16_t *key_cache, uint16_t *value_cache, const int64_t *slot_mapping,
+                                  const int64_t *positions, const float *cos_sin_cache, int32_t max_position,
+                                  int32_t rotary_dim, int32_t is_neox, int64_t num_tokens, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                  int32_t dtype)
+{
+    if (num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        rotary_dim <= 0 || rotary_dim % 2 || rotary_dim > head_dim || max_position <= 0 ||
+        (dtype != ORACLE_BF16 && dtype != ORACLE_FP16))
+        return ORACLE_ERR_ARG;
+    const int64_t D = head_dim;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)D);
+    if (!tmp)
+        return ORACLE_ERR_NOMEM;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t pos = positions[t];
+        if (pos < 0 || pos >= max_position) {
+            free(tmp);
+            return ORACLE_ERR_ARG;
+        }
+        const float *cs = cos_sin_cache + pos * rotary_dim;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            uint16_t *row = q + (t * num_heads + h) * D;
+            rotate_row(tmp, row, head_dim, cs, rotary_dim, is_neox, dtype);
+            memcpy(row, tmp, sizeof(uint16_t) * (size_t)D);
+        }
+        const int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= num_blocks * block_size) {
+            free(tmp);
+            return ORACLE_ERR_SLOT_RANGE;
+        }
+        const int64_t row = (int64_t)num_kv_heads * D; /* cache row of slot s starts at s * row */
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            rotate_row(key_cache + s * row + h * D, key + (t * num_kv_heads + h) * D, head_dim, cs, rotary_dim,
+                       is_neox, dtype);
+            memcpy(value_cache + s * row + h * D, value + (t * num_kv_heads + h) * D, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    free(tmp);
     return ORACLE_OK;
 }
 

@@ -24,6 +24,7 @@ STATUS = {
     -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_LAUNCH", -7: "PA_ERR_DEVICE_BOUNDS", -8: "PA_ERR_CUDA",
 }
 FLAG_SLOT_RANGE, FLAG_BLOCK_RANGE, FLAG_LENGTHS, FLAG_QUERY_LOC, FLAG_TIMEOUT = 1, 2, 4, 8, 16
+FLAG_POSITION_RANGE = 32
 
 
 class PagedAttnError(RuntimeError):
@@ -48,6 +49,8 @@ SIGNATURES = {
     "pa_launch_count": ([], ctypes.c_uint64),
     "pa_last_cuda_error": ([], ctypes.c_char_p),
     "pa_copy_blocks": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I64, _I32, _P], ctypes.c_int32),
+    "pa_rope_reshape_and_cache": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                                   _I32, _I32, _I32, _I64, _I32, _P], ctypes.c_int32),
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
@@ -183,6 +186,33 @@ def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_c
                                              seq_lens.data_ptr(), query_start_loc.data_ptr(), B, T, max_query_len,
                                              max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), dt,
                                              _stream(stream)), "pa_attention_varlen_static")
+
+
+def pa_rope_reshape_and_cache(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                              value_cache: torch.Tensor, slot_mapping: torch.Tensor, positions: torch.Tensor,
+                              cos_sin_cache: torch.Tensor, is_neox: bool = True, stream=None) -> None:
+    """Rotate q in place and write the rotated key and the value rows into the caches.
+    q [T, H, D], key/value [T, Hkv, D] (token strides free), caches [NB, bs, Hkv, D] (one 16-bit type);
+    slot_mapping and positions int64 [T]; cos_sin_cache float32 [max_position, rotary_dim]."""
+    dt = _elem_code((q, "q"), (key, "key"), (value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache"))
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(positions, "positions", torch.int64)
+    _need(cos_sin_cache, "cos_sin_cache", torch.float32)
+    T, H, D = q.shape
+    _, hkv, d = key.shape
+    for t, n, h in ((q, "q", H), (key, "key", hkv), (value, "value", hkv)):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"each token row of {n} must be [heads, D] contiguous")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous() and cos_sin_cache.is_contiguous()
+            and slot_mapping.is_contiguous() and positions.is_contiguous()):
+        raise ValueError("caches, cos_sin_cache, slot_mapping and positions must be contiguous")
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    max_pos, rot = cos_sin_cache.shape
+    _check(_lib().pa_rope_reshape_and_cache(q.data_ptr(), q.stride(0), key.data_ptr(), value.data_ptr(),
+                                            key.stride(0), value.stride(0), key_cache.data_ptr(),
+                                            value_cache.data_ptr(), slot_mapping.data_ptr(), positions.data_ptr(),
+                                            cos_sin_cache.data_ptr(), max_pos, rot, int(bool(is_neox)), T, H, hkv, D,
+                                            bs, nb, dt, _stream(stream)), "pa_rope_reshape_and_cache")
 
 
 def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,

@@ -209,6 +209,41 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   return PA_OK;
 }
 
+pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void *key, const void *value,
+                                    int64_t key_token_stride, int64_t value_token_stride, void *key_cache,
+                                    void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
+                                    const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
+                                    int32_t is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                                    void *stream) {
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks < 0 || max_position <= 0 || rotary_dim <= 0 || rotary_dim > head_dim)
+    return PA_ERR_DIMS;
+  if (head_dim % 8 || rotary_dim % 16) return PA_ERR_ALIGN;
+  if (rotary_dim > 512) return PA_ERR_UNSUPPORTED;  // the table row is staged in shared memory
+  if (num_tokens == 0) return PA_OK;
+  if (!q || !key || !value || !key_cache || !value_cache || !slot_mapping || !positions || !cos_sin_cache)
+    return PA_ERR_NULL;
+  const int64_t kv_row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (q_token_stride < static_cast<int64_t>(num_heads) * head_dim || key_token_stride < kv_row ||
+      value_token_stride < kv_row)
+    return PA_ERR_DIMS;
+  if (q_token_stride % 8 || key_token_stride % 8 || value_token_stride % 8) return PA_ERR_ALIGN;
+  if (!aligned(q, 16) || !aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(cos_sin_cache, 16) || !aligned(slot_mapping, 8) || !aligned(positions, 8))
+    return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  cudaError_t err = pa::launch_rope_reshape_and_cache(
+      q, q_token_stride, key, value, key_token_stride, value_token_stride, key_cache, value_cache, slot_mapping,
+      positions, cos_sin_cache, max_position, rotary_dim, is_neox != 0, num_tokens, num_heads, num_kv_heads,
+      head_dim, num_blocks * block_size, dtype, ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
 pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping, int32_t num_pairs,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
                          int32_t dtype, void *stream) {

@@ -108,6 +108,137 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *key_cache, uint
   }
 }
 
+// Rotary position embedding fused with the cache scatter (vLLM notes, §LLM
+// 推理全流程 2: a token's position is a rotation angle; cos_sin_cache is
+// [max_position, rotary_dim], precomputed). Row p holds cos(p theta_i) in
+// columns i < rotary_dim / 2 and sin(p theta_i) in the next rotary_dim / 2;
+// a pair (x1, x2) becomes (x1 cos - x2 sin, x2 cos + x1 sin). Pairs are
+// (i, i + rotary_dim / 2) (NEOX) or (2i, 2i + 1). One thread per 16-byte chunk
+// c of one row of one token: rows [0, H) are q heads (rotated in place),
+// [H, H + Hkv) K heads (rotated into the cache slot), the next Hkv V heads
+// (copied to the slot). With NEOX pairing the thread of chunk c < rot / 16
+// also does its partner chunk c + rot / 16. fp32 arithmetic, one rounding to
+// the element type; a token whose position is outside [0, max_position) is
+// skipped and flagged.
+template <typename E>
+__device__ __forceinline__ void rope_pair8(uint4 &a, uint4 &b, const float *c, const float *s) {
+  // a holds x1 of 8 pairs, b their x2 (NEOX layout)
+  uint32_t *pa = reinterpret_cast<uint32_t *>(&a), *pb = reinterpret_cast<uint32_t *>(&b);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float x10 = E::lo(pa[k]), x11 = E::hi(pa[k]), x20 = E::lo(pb[k]), x21 = E::hi(pb[k]);
+    const float c0 = c[2 * k], c1 = c[2 * k + 1], s0 = s[2 * k], s1 = s[2 * k + 1];
+    pa[k] = E::pack(fmaf(x10, c0, -x20 * s0), fmaf(x11, c1, -x21 * s1));
+    pb[k] = E::pack(fmaf(x20, c0, x10 * s0), fmaf(x21, c1, x11 * s1));
+  }
+}
+template <typename E>
+__device__ __forceinline__ void rope_adjacent8(uint4 &a, const float *c, const float *s) {
+  // a holds 4 pairs (x1, x2) side by side (GPT-J layout)
+  uint32_t *pa = reinterpret_cast<uint32_t *>(&a);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float x1 = E::lo(pa[k]), x2 = E::hi(pa[k]);
+    pa[k] = E::pack(fmaf(x1, c[k], -x2 * s[k]), fmaf(x2, c[k], x1 * s[k]));
+  }
+}
+
+constexpr int kRopeMaxRot = 512;  // largest rotary_dim (the table row is staged in shared memory)
+
+template <typename E, bool NEOX>
+__global__ void __launch_bounds__(256) rope_reshape_and_cache_kernel(
+    uint4 *q, int64_t q_stride16, const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+    int64_t key_stride16, int64_t value_stride16, uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+    const int64_t *__restrict__ slot_mapping, const int64_t *__restrict__ positions,
+    const float *__restrict__ cos_sin, int32_t max_position, int32_t rot, int32_t num_tokens, int32_t num_heads,
+    int32_t num_kv_heads, int32_t d16, int64_t num_slots, unsigned int *status) {
+  // One CTA per token at a time: the position, slot and table row are read
+  // once and shared, so the chunks of the token's rows need no dependent
+  // global loads.
+  __shared__ __align__(16) float tab[kRopeMaxRot];
+  __shared__ int64_t s_pos, s_slot;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int32_t rows = num_heads + 2 * num_kv_heads;
+  const int32_t items = rows * d16;
+  const int32_t half16 = rot / 16;  // chunks in one half of the rotated part (NEOX)
+  const int64_t row16 = static_cast<int64_t>(num_kv_heads) * d16;
+  for (int32_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
+    if (threadIdx.x == 0) {
+      s_pos = ld_cg(reinterpret_cast<const long long *>(positions) + t);
+      s_slot = ld_cg(reinterpret_cast<const long long *>(slot_mapping) + t);
+    }
+    __syncthreads();
+    const int64_t pos = s_pos, slot = s_slot;
+    const bool pos_ok = pos >= 0 && pos < max_position;
+    if (pos_ok) {
+      const float4 *row4 = reinterpret_cast<const float4 *>(cos_sin + pos * rot);
+      for (int32_t i = threadIdx.x; i < rot / 4; i += blockDim.x) reinterpret_cast<float4 *>(tab)[i] = __ldg(row4 + i);
+    } else if (threadIdx.x == 0) {
+      flag_error(status, PA_FLAG_POSITION_RANGE);
+    }
+    if (pos_ok && slot >= num_slots && threadIdx.x == 0) flag_error(status, PA_FLAG_SLOT_RANGE);
+    __syncthreads();
+    if (pos_ok) {
+      const bool cache_ok = slot >= 0 && slot < num_slots;  // slot < 0: padding token, nothing cached
+#pragma unroll 2
+      for (int32_t w = threadIdx.x; w < items; w += blockDim.x) {
+        const int32_t r = w / d16, c = w - r * d16;
+        // which chunks this thread rotates: NEOX chunk c < half16 with c + half16;
+        // GPT-J chunk c < rot / 8 on its own; chunks in [half16, 2 half16) (NEOX)
+        // belong to their partner's thread
+        const bool partner = NEOX && c >= half16 && c < 2 * half16;
+        const bool rotates = NEOX ? c < half16 : c < rot / 8;
+        float cf[8], sf[8];
+        if (rotates) {
+          const int base = NEOX ? 8 * c : 4 * c;  // first frequency index of this chunk
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            cf[k] = (NEOX || k < 4) ? tab[base + k] : 0.f;
+            sf[k] = (NEOX || k < 4) ? tab[rot / 2 + base + k] : 0.f;
+          }
+        }
+        if (r < num_heads) {  // q head: in place
+          if (!rotates) continue;
+          uint4 *qrow = q + static_cast<int64_t>(t) * q_stride16 + static_cast<int64_t>(r) * d16;
+          uint4 x = ld_cg(qrow + c);
+          if (NEOX) {
+            uint4 y = ld_cg(qrow + c + half16);
+            rope_pair8<E>(x, y, cf, sf);
+            qrow[c + half16] = y;
+          } else {
+            rope_adjacent8<E>(x, cf, sf);
+          }
+          qrow[c] = x;
+        } else if (!cache_ok) {
+          continue;
+        } else if (r < num_heads + num_kv_heads) {  // K head: rotated into the cache
+          if (partner) continue;
+          const int32_t h = r - num_heads;
+          const uint4 *src = key + static_cast<int64_t>(t) * key_stride16 + static_cast<int64_t>(h) * d16;
+          uint4 *dst = key_cache + slot * row16 + static_cast<int64_t>(h) * d16;
+          uint4 x = ld_cg(src + c);
+          if (rotates) {
+            if (NEOX) {
+              uint4 y = ld_cg(src + c + half16);
+              rope_pair8<E>(x, y, cf, sf);
+              dst[c + half16] = y;
+            } else {
+              rope_adjacent8<E>(x, cf, sf);
+            }
+          }
+          dst[c] = x;
+        } else {  // V head: copied
+          const int32_t h = r - num_heads - num_kv_heads;
+          value_cache[slot * row16 + static_cast<int64_t>(h) * d16 + c] =
+              ld_cg(value + static_cast<int64_t>(t) * value_stride16 + static_cast<int64_t>(h) * d16 + c);
+        }
+      }
+    }
+    __syncthreads();  // the next token rewrites s_pos, s_slot and tab
+  }
+}
+
 static int grid_for(int64_t work, int threads, int sm_count) {
   int64_t g = (work + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;
@@ -138,6 +269,32 @@ cudaError_t launch_copy_blocks(void *key_cache, void *value_cache, const int64_t
   return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
                     static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), mapping, num_pairs,
                     block_elems / 8, num_blocks, status);
+}
+
+cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void *key, const void *value,
+                                          int64_t key_stride, int64_t value_stride, void *key_cache,
+                                          void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
+                                          const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
+                                          bool is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int64_t num_slots, int32_t dtype, unsigned int *status,
+                                          int sm_count, cudaStream_t stream) {
+  const int32_t d16 = head_dim / 8;
+  int64_t g = static_cast<int64_t>(sm_count) * 8;  // CTAs (tokens in flight): 8 per SM
+  if (g > num_tokens) g = num_tokens;
+  const int grid = static_cast<int>(g < 1 ? 1 : g);
+#define PA_ROPE_LAUNCH(EE, NN)                                                                                    \
+  return launch_pdl(rope_reshape_and_cache_kernel<EE, NN>, dim3(grid), dim3(256), 0, stream,                      \
+                    static_cast<uint4 *>(q), q_stride / 8, static_cast<const uint4 *>(key),                        \
+                    static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,                            \
+                    static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, positions,     \
+                    cos_sin_cache, max_position, rotary_dim, num_tokens, num_heads, num_kv_heads, d16, num_slots,  \
+                    status);
+  if (dtype == PA_FP16) {
+    if (is_neox) PA_ROPE_LAUNCH(ElemFp16, true) else PA_ROPE_LAUNCH(ElemFp16, false)
+  } else {
+    if (is_neox) PA_ROPE_LAUNCH(ElemBf16, true) else PA_ROPE_LAUNCH(ElemBf16, false)
+  }
+#undef PA_ROPE_LAUNCH
 }
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,

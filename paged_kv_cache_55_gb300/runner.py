@@ -32,7 +32,9 @@ def bf16_to_float64(t: torch.Tensor) -> np.ndarray:
 
 
 class DeviceStep:
-    def __init__(self, w: Workload, device: str = "cuda"):
+    def __init__(self, w: Workload, device: str = "cuda", rope=None):
+        """``rope``: optional (cos_sin_cache float32 [P, rotary_dim], positions int64 [T], is_neox):
+        the step then rotates q and K with pa_rope_reshape_and_cache instead of pa_reshape_and_cache."""
         self.w = w
         self.device = torch.device(device)
         dev = self.device
@@ -53,6 +55,11 @@ class DeviceStep:
         nbytes = B.pa_attention_workspace_size(w.num_seqs, w.total_q, self.max_query_len, self.max_seq_len,
                                                w.num_heads, w.num_kv_heads, w.head_dim, w.block_size)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.rope = None
+        if rope is not None:
+            table, positions, is_neox = rope
+            self.rope = (torch.from_numpy(np.ascontiguousarray(table, dtype=np.float32)).to(dev),
+                         torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int64)).to(dev), bool(is_neox))
 
     def reset_cache(self) -> None:
         """Restore the cache to its state before the step."""
@@ -60,6 +67,11 @@ class DeviceStep:
         self.value_cache.copy_(self.value_cache0)
 
     def reshape_and_cache(self, stream=None) -> None:
+        if self.rope is not None:
+            table, positions, is_neox = self.rope
+            B.pa_rope_reshape_and_cache(self.q, self.key, self.value, self.key_cache, self.value_cache,
+                                        self.slot_mapping, positions, table, is_neox=is_neox, stream=stream)
+            return
         B.pa_reshape_and_cache(self.key, self.value, self.key_cache, self.value_cache, self.slot_mapping,
                                stream=stream)
 

@@ -84,6 +84,16 @@ def bits_to_f32(h: np.ndarray, dtype: str) -> np.ndarray:
     return fp16_bits_to_f32(h) if dtype == "fp16" else bf16_bits_to_f32(h)
 
 
+def rope_cos_sin_cache(max_position: int, rotary_dim: int, base: float = 10000.0) -> np.ndarray:
+    """The precomputed rotary table (float32 [max_position, rotary_dim]): row p holds
+    cos(p * theta_i) for i < rotary_dim / 2, then sin(p * theta_i), with RoFormer's
+    frequencies theta_i = base^(-2 i / rotary_dim). Input data for the rotary step."""
+    i = np.arange(rotary_dim // 2, dtype=np.float64)
+    theta = base ** (-2.0 * i / rotary_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * theta[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
 def _normal_elems(rng: np.random.Generator, shape, scale: float = 1.0, dtype: str = "bf16") -> np.ndarray:
     """Seeded N(0, scale^2) values rounded to the element type, as uint16 bits
     (the same draws for either type)."""

@@ -28,7 +28,8 @@ import os
 import numpy as np
 import torch
 
-from paged_kv_cache_55_gb300.workloads import NAN_BITS, bf16_bits_to_f32, bits_to_f32, f32_to_bf16_bits, f32_to_bits
+from paged_kv_cache_55_gb300.workloads import (NAN_BITS, bf16_bits_to_f32, bits_to_f32, f32_to_bf16_bits, f32_to_bits,
+                                               rope_cos_sin_cache)
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -319,6 +320,129 @@ def pin_copy_blocks_matches_numpy(oracle):
     assert np.array_equal(kc, ek) and np.array_equal(vc, ev), "block copy must match numpy assignment"
 
 
+def pin_round_fp16_matches_numpy(oracle):
+    rng = np.random.default_rng(21)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, size=20000),
+        # exact halfway points between neighbouring fp16 values, and one ulp of a double either side
+        (np.arange(1, 2048) + 0.5) * 2.0 ** -24, (np.arange(1024, 2048) + 0.5) * 2.0 ** -9,
+        np.nextafter((np.arange(1024, 2048) + 0.5) * 2.0 ** -9, np.inf),
+        np.nextafter((np.arange(1024, 2048) + 0.5) * 2.0 ** -9, -np.inf),
+        [65504.0, 65519.99, 65520.0, 1e6, -1e6, 0.0, -0.0, np.inf, -np.inf]])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = oracle.round_elements(x, "fp16")
+    assert np.array_equal(got, ref), "fp16 rounding must match numpy's float64 -> float16"
+
+
+def pin_round_bf16_definition_cases(oracle):
+    # round to nearest, ties to even, straight from the double (8 significant bits)
+    cases = [(1 + 2.0 ** -8, 0x3F80), (1 + 2.0 ** -8 + 2.0 ** -40, 0x3F81), (1 + 3 * 2.0 ** -8, 0x3F82),
+             (-(1 + 2.0 ** -9), 0xBF80), (3.4e38, 0x7F80), (2.0 ** -133, 0x0001), (2.0 ** -134, 0x0000),
+             (3 * 2.0 ** -135, 0x0001), (-2.0, 0xC000), (np.inf, 0x7F80), (-0.0, 0x8000), (0.1, 0x3DCD)]
+    got = oracle.round_elements(np.array([c[0] for c in cases]), "bf16")
+    for (x, want), g in zip(cases, got):
+        assert int(g) == want, f"bf16 rounding of {x!r}: want {want:#06x}, got {int(g):#06x}"
+    # values exact in float32 agree with the float32 -> bf16 rounding of the generator
+    f = np.random.default_rng(22).standard_normal(5000).astype(np.float32)
+    assert np.array_equal(oracle.round_elements(f.astype(np.float64), "bf16"), f32_to_bf16_bits(f))
+
+
+class RopeProblem:
+    """q, key, value rows of T tokens, a cache to scatter into, positions and a table."""
+
+    def __init__(self, rng, T=6, H=4, Hkv=2, D=32, rot=32, dtype="bf16", table=None, positions=None):
+        self.dtype, self.D = dtype, D
+        self.q = f32_to_bits(rng.standard_normal((T, H, D)).astype(np.float32), dtype)
+        self.k = f32_to_bits(rng.standard_normal((T, Hkv, D)).astype(np.float32), dtype)
+        self.v = f32_to_bits(rng.standard_normal((T, Hkv, D)).astype(np.float32), dtype)
+        self.nb, self.bs = 4, 4
+        self.slots = rng.permutation(self.nb * self.bs)[:T].astype(np.int64)
+        self.table = rope_cos_sin_cache(64, rot) if table is None else table
+        self.pos = rng.integers(0, self.table.shape[0], size=T) if positions is None else np.asarray(positions)
+
+    def run(self, oracle, is_neox=True):
+        q = self.q.copy()
+        kc = np.zeros((self.nb, self.bs, self.k.shape[1], self.D), dtype=np.uint16)
+        vc = np.zeros_like(kc)
+        oracle.rope_reshape_and_cache(q, self.k, self.v, kc, vc, self.slots, self.pos, self.table, is_neox,
+                                      self.bs, self.dtype)
+        flat_k = kc.reshape(-1, self.k.shape[1], self.D)[self.slots]
+        flat_v = vc.reshape(-1, self.k.shape[1], self.D)[self.slots]
+        return q, flat_k, flat_v
+
+
+def pin_rope_position_zero_is_identity(oracle):
+    rng = np.random.default_rng(23)
+    for dtype in ("bf16", "fp16"):
+        p = RopeProblem(rng, dtype=dtype, positions=[0] * 6)
+        for neox in (True, False):
+            q, k, v = p.run(oracle, neox)
+            assert np.array_equal(q, p.q) and np.array_equal(k, p.k) and np.array_equal(v, p.v), \
+                "position 0 (cos 1, sin 0) leaves q and k as they are and caches them"
+
+
+def pin_rope_quarter_turn(oracle):
+    # a table row with cos 0 and sin 1 turns every pair (x1, x2) into (-x2, x1)
+    rng = np.random.default_rng(24)
+    D, rot, half = 32, 16, 8
+    table = np.zeros((2, rot), dtype=np.float32)
+    table[0, :half] = 1.0
+    table[1, half:] = 1.0
+    p = RopeProblem(rng, D=D, rot=rot, table=table, positions=[1] * 6)
+    x = bits_to_f32(p.q, "bf16")
+    kx = bits_to_f32(p.k, "bf16")
+    for neox in (True, False):
+        q, k, v = p.run(oracle, neox)
+        a = np.arange(half) if neox else 2 * np.arange(half)
+        b = a + half if neox else a + 1
+        for got, src in ((bits_to_f32(q, "bf16"), x), (bits_to_f32(k, "bf16"), kx)):
+            assert np.array_equal(got[..., a], -src[..., b]) and np.array_equal(got[..., b], src[..., a]), \
+                "a quarter turn maps (x1, x2) to (-x2, x1) for q and k"
+            assert np.array_equal(got[..., rot:], src[..., rot:]), "elements past rotary_dim pass through"
+        assert np.array_equal(v, p.v), "value rows are cached unchanged"
+
+
+def pin_rope_interleaved_is_permuted_neox(oracle):
+    # pairing (2i, 2i + 1) on x equals pairing (i, i + rot/2) on x with those dims moved together
+    rng = np.random.default_rng(25)
+    D, rot = 64, 48
+    p = RopeProblem(rng, D=D, rot=rot, dtype="fp16")
+    perm = np.concatenate([np.arange(0, rot, 2), np.arange(1, rot, 2), np.arange(rot, D)])
+    qi, ki, _ = p.run(oracle, is_neox=False)
+    pp = RopeProblem(rng, D=D, rot=rot, dtype="fp16", table=p.table, positions=p.pos)
+    pp.q, pp.k, pp.v, pp.slots = p.q[..., perm].copy(), p.k[..., perm].copy(), p.v.copy(), p.slots
+    qn, kn, _ = pp.run(oracle, is_neox=True)
+    inv = np.argsort(perm)
+    assert np.array_equal(qi, qn[..., inv]) and np.array_equal(ki, kn[..., inv]), \
+        "interleaved pairing must be the neox pairing under the index permutation"
+
+
+def pin_rope_relative_positions(oracle):
+    # RoPE's defining property: after rotation, q(p) . k(p') depends only on p - p'
+    rng = np.random.default_rng(26)
+    D = rot = 64
+    q0 = rng.standard_normal((1, 1, D)).astype(np.float32)
+    k0 = rng.standard_normal((1, 1, D)).astype(np.float32)
+    table = rope_cos_sin_cache(200, rot)
+    dots = []
+    for shift in (0, 17, 90):
+        pq = RopeProblem(rng, T=1, H=1, Hkv=1, D=D, rot=rot, table=table, positions=[30 + shift], dtype="fp16")
+        pq.q = f32_to_bits(q0, "fp16")
+        pq.k = f32_to_bits(k0, "fp16")
+        pq.slots = np.array([0], dtype=np.int64)
+        q_rot, _, _ = pq.run(oracle)
+        pk = RopeProblem(rng, T=1, H=1, Hkv=1, D=D, rot=rot, table=table, positions=[12 + shift], dtype="fp16")
+        pk.q = f32_to_bits(q0, "fp16")
+        pk.k = f32_to_bits(k0, "fp16")
+        pk.slots = np.array([0], dtype=np.int64)
+        _, k_rot, _ = pk.run(oracle)
+        dots.append(float(np.dot(bits_to_f32(q_rot, "fp16").ravel().astype(np.float64),
+                                 bits_to_f32(k_rot, "fp16").ravel().astype(np.float64))))
+    scale = float(np.linalg.norm(q0) * np.linalg.norm(k0))
+    assert max(dots) - min(dots) <= 4e-3 * scale, f"q.k must depend on the position gap only: {dots}"
+
+
 PINS = [
     pin_dense_vs_sdpa,
     pin_dense_vs_sdpa_fp16,
@@ -336,4 +460,10 @@ PINS = [
     pin_slot_formula_golden,
     pin_reshape_matches_numpy_scatter,
     pin_copy_blocks_matches_numpy,
+    pin_round_fp16_matches_numpy,
+    pin_round_bf16_definition_cases,
+    pin_rope_position_zero_is_identity,
+    pin_rope_quarter_turn,
+    pin_rope_interleaved_is_permuted_neox,
+    pin_rope_relative_positions,
 ]

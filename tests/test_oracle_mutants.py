@@ -32,6 +32,17 @@ MUTANTS = {
     "copy_blocks_k_only": ("        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems, "
                            "sizeof(uint16_t) * block_elems);",
                            "        (void)value_cache;"),
+    "rope_sign_flipped": ("dst[a] = double_to_elem(dtype, x1 * c - x2 * s);",
+                          "dst[a] = double_to_elem(dtype, x1 * c + x2 * s);"),
+    "rope_cos_sin_swapped": ("const double c = (double)cs[i], s = (double)cs[half + i];",
+                             "const double s = (double)cs[i], c = (double)cs[half + i];"),
+    "rope_neox_pairs_adjacent": ("const int32_t b = is_neox ? i + half : 2 * i + 1;",
+                                 "const int32_t b = is_neox ? i + 1 : 2 * i + 1;"),
+    "rope_key_not_rotated": ("            rotate_row(key_cache + s * row + h * D, key + (t * num_kv_heads + h) * D, "
+                             "head_dim, cs, rotary_dim,\n                       is_neox, dtype);",
+                             "            memcpy(key_cache + s * row + h * D, key + (t * num_kv_heads + h) * D, "
+                             "sizeof(uint16_t) * (size_t)D);"),
+    "round_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))", "if (frac >= 0.5)"),
     "fp16_decoded_as_bf16": ("return dtype == ORACLE_FP16 ? fp16_to_double(h) : bf16_to_double(h);",
                              "return bf16_to_double(h);"),
     "first_query_row_only": ("const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;",
