@@ -265,6 +265,8 @@ def run_reference(args, world, rank) -> None:
     import oracle as oracle_mod
     kw = {"batch": args.batch} if args.batch else {}
     kw["dtype"] = args.dtype
+    if args.block_size != 16:
+        kw["block_size"] = args.block_size
     w = W.by_name(args.workload, seed=args.seed, **kw)
     kc, vc = w.key_cache.copy(), w.value_cache.copy()
     orc = oracle_mod.default()
@@ -300,6 +302,8 @@ def workload_text(args) -> str:
     text = WORKLOAD_TEXT[args.workload]
     if args.dtype != "bf16":
         text += f" [{args.dtype} elements]"
+    if getattr(args, "block_size", 16) != 16:
+        text += f" [block_size {args.block_size}]"
     if getattr(args, "rope", False):
         text += " [rotary embedding fused into the cache scatter]"
     return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
@@ -319,6 +323,8 @@ def run_ours(args, world, rank, local_rank) -> None:
     device = torch.device("cuda", local_rank)
     kw = {"batch": args.batch} if args.batch else {}
     kw["dtype"] = args.dtype
+    if args.block_size != 16:
+        kw["block_size"] = args.block_size
     w = W.by_name(args.workload, seed=rank_seed(args.seed, rank), **kw)
     acct = step_accounting(w, rope=args.rope)
     rope = None
@@ -606,6 +612,8 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="element type of q, K/V and out (the metric's workload is bf16)")
+    ap.add_argument("--block-size", type=int, choices=[8, 16, 32], default=16,
+                    help="tokens per cache block (the configurations are quoted at 16)")
     ap.add_argument("--rope", action="store_true",
                     help="the step rotates q and K (pa_rope_reshape_and_cache, neox pairing, rotary_dim = D) "
                          "instead of pa_reshape_and_cache")

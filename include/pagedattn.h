@@ -35,8 +35,10 @@
  *     the offending work and set bits in a device status word, which
  *     pa_debug_status() reads; outputs of the offending request are then
  *     undefined.
- *   - Supported now: head_dim 64 or 128; block_size 16; num_heads a multiple
- *     of num_kv_heads with group size 1, 2, 4 or 8.
+ *   - Supported now: head_dim 64 or 128; block_size 8, 16 or 32 (the
+ *     reading map, §2.3, sweeps page sizes; the kernels stage K/V 16 keys at a
+ *     time); num_heads a multiple of num_kv_heads with group size 1, 2, 4 or 8.
+ *     pa_rope_reshape_and_cache and pa_copy_blocks take any block_size.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H

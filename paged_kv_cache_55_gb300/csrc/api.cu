@@ -55,7 +55,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool supported_dims(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
   if (head_dim != 64 && head_dim != 128) return false;
-  if (block_size != pa::kBlockSize) return false;
+  if (block_size != 8 && block_size != 16 && block_size != 32) return false;
   if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return false;
   const int G = num_heads / num_kv_heads;
   return G == 1 || G == 2 || G == 4 || G == 8;
@@ -100,7 +100,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
     return PA_ERR_DIMS;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
@@ -193,6 +193,7 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   a.num_heads = num_heads;
   a.num_kv_heads = num_kv_heads;
   a.head_dim = head_dim;
+  a.block_size = block_size;
   a.num_blocks = num_blocks;
   a.scale = scale;
   a.dtype = dtype;
@@ -269,7 +270,7 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (seq_len < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_DIMS;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != pa::kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (seq_len == 0) return PA_OK;
   if (!key_cache || !value_cache || !block_table_row || !key_out || !value_out) return PA_ERR_NULL;
   if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(key_out, 16) || !aligned(value_out, 16) ||
@@ -278,7 +279,8 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   DeviceState *ds = device_state();
   if (!ds) return PA_ERR_CUDA;
   cudaError_t err = pa::launch_gather_kv(key_cache, value_cache, block_table_row, seq_len,
-                                         num_kv_heads * head_dim, num_blocks, key_out, value_out, ds->status,
+                                         num_kv_heads * head_dim, block_size, num_blocks, key_out, value_out,
+                                         ds->status,
                                          ds->sm_count, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);

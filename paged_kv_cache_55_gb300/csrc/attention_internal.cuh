@@ -20,6 +20,8 @@ struct TileParams {
   int64_t q_stride;
   const int32_t *block_tables;
   int32_t max_blocks_per_seq;
+  int32_t block_size;   // tokens per cache block: 8, 16 or 32
+  int32_t block_shift;  // log2(block_size)
   int32_t num_heads;
   int32_t num_kv_heads;
   int64_t num_blocks;

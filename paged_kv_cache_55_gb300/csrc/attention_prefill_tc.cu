@@ -76,7 +76,7 @@ struct TcLayout {
   static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;             // one K or V range: a ring slot
-  static constexpr int TABLE_ENTRIES = 512;                     // keys < 8192 read from here
+  static constexpr int TABLE_ENTRIES = 512;  // staged TMA row coordinates: boxes of keys < 8192 (4096 at bs 8)
   // barriers: full[kMaxSlots], empty[kMaxSlots], per half s_full, p_full, o_done,
   // then q_full and drain (the MMA thread's last commit)
   static constexpr int NBARS = 2 * kMaxSlots + 3 * kHalves + 2;
@@ -86,7 +86,7 @@ struct TcLayout {
   static_assert(SLOTS >= 4, "the ring holds at least K and V of two ranges");
   static constexpr int Q_OFF = 0;                                // Q of halves A and B
   static constexpr int RING_OFF = Q_OFF + kHalves * Q_BYTES;     // K(0), V(0), K(1), V(1), ... in SLOTS slots
-  static constexpr int TABLE_OFF = RING_OFF + SLOTS * KV_BYTES;  // the tile's block-table entries
+  static constexpr int TABLE_OFF = RING_OFF + SLOTS * KV_BYTES;  // the unit's box coordinates
   static constexpr int BAR_OFF = TABLE_OFF + TABLE_ENTRIES * 4;
   static constexpr int BYTES = BAR_OFF + 8 * NBARS + 16;
   // Shared memory requested per CTA: more than half an SM's, so that a second
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   using Tm = TcTmem<D>;
   constexpr int KSTEPS_S = D / 16;         // UMMA K steps of S = Q K^T
   constexpr int KSTEPS_O = kKeyTile / 16;  // UMMA K steps of O = P V
-  constexpr int BLOCKS = kKeyTile / kBlockSize;
+  constexpr int TILES = kKeyTile / kTileKeys;  // 16-key tiles per range
   constexpr int POS_PER_HALF = kHalfRows / G;
   constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, E::kUmmaFormat);
   constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, E::kUmmaFormat);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const uint32_t bar_q = bar_o + 8 * kHalves, bar_drain = bar_q + 8;
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS);
   int *unit_s = reinterpret_cast<int *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS + 4);
-  int *stable = reinterpret_cast<int *>(smem_raw + Lay::TABLE_OFF);
+  int *zbox = reinterpret_cast<int *>(smem_raw + Lay::TABLE_OFF);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
@@ -328,14 +328,32 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const int b = r0.x, row0 = r0.y, npos = r0.z, pos0 = r0.w, kv_end = r1.y;
     const bool sane = b >= 0 && b < p.num_seqs && npos >= 1 && npos <= kPrefillTileRows / G && row0 >= 0 &&
                       row0 + npos <= p.total_q && pos0 >= 0 && kv_end == pos0 + npos &&
-                      kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize;
+                      kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
     if (!sane) {
       if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
       __syncthreads();  // unit_s is rewritten next iteration
       continue;
     }
     const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+    const int bs = p.block_size;
+    // A TMA box is box_rows consecutive keys of one block (16, or 8 with
+    // 8-token blocks). The cache row of box i's first key, k = i * box_rows,
+    // is table[k / bs] * bs + k % bs (powers of two: shift and mask); boxes
+    // past the keys, or of a block id out of range, are read at -box_rows
+    // (zero fill). All threads compute the unit's coordinates once here, so
+    // the producer only reads one from shared memory per box.
+    const int box_rows = bs < kTileKeys ? bs : kTileKeys;
+    const int nboxes = (kv_end + box_rows - 1) / box_rows;
+    auto box_z = [&](int i) {
+      const int key = i * box_rows;
+      if (key >= kv_end) return -box_rows;
+      const int phys = __ldg(table + (key >> p.block_shift));
+      if (phys < 0 || phys >= p.num_blocks) {
+        flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+        return -box_rows;
+      }
+      return (phys << p.block_shift) + (key & (bs - 1));
+    };
     const int nkt = (kv_end + kKeyTile - 1) / kKeyTile;
     // key ranges each half needs: up to its last valid position (0 = no valid rows)
     int nkt_h[kHalves];
@@ -344,7 +362,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       const int last = min(npos, (h + 1) * POS_PER_HALF);  // positions [h * POS_PER_HALF, last)
       nkt_h[h] = last > h * POS_PER_HALF ? (pos0 + last + kKeyTile - 1) / kKeyTile : 0;
     }
-    for (int i = tid; i < min(nblk, Lay::TABLE_ENTRIES); i += kTileThreads) stable[i] = __ldg(table + i);
+    for (int i = tid; i < min(nboxes, Lay::TABLE_ENTRIES); i += kTileThreads) zbox[i] = box_z(i);
     __syncthreads();
 
     if (warp == kTmaWarp) {
@@ -360,21 +378,26 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           const uint32_t dst = sRing + slot * Lay::KV_BYTES;
           const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
           mbar_arrive_expect_tx(bar, Lay::KV_BYTES);
+          // a 16-key tile is one 16-row box (16- or 32-token blocks) or two
+          // 8-row boxes of consecutive 8-token blocks
+          auto boxes = [&](auto nbox_c) {
+            constexpr int NBOX = decltype(nbox_c)::value, ROWS = kTileKeys / NBOX;
 #pragma unroll
-          for (int blk = 0; blk < BLOCKS; ++blk) {
-            const int kb = kt * BLOCKS + blk;
-            int z = -kBlockSize;  // past the keys this tile needs: TMA fills zeros
-            if (kb < nblk) {
-              const int phys = kb < Lay::TABLE_ENTRIES ? stable[kb] : __ldg(table + kb);
-              if (phys >= 0 && phys < p.num_blocks)
-                z = phys * kBlockSize;
-              else if (!is_v)
-                flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+            for (int tile = 0; tile < TILES; ++tile) {
+#pragma unroll
+              for (int j = 0; j < NBOX; ++j) {
+                const int i = (kt * TILES + tile) * NBOX + j;
+                const int z = i < nboxes ? (i < Lay::TABLE_ENTRIES ? zbox[i] : box_z(i)) : -ROWS;
+#pragma unroll
+                for (int a = 0; a < Lay::ATOMS; ++a)
+                  tma_load_3d(dst + a * Lay::KV_ATOM + tile * 2048 + j * ROWS * 128, map, bar, a * 64, kvh, z);
+              }
             }
-#pragma unroll
-            for (int a = 0; a < Lay::ATOMS; ++a)
-              tma_load_3d(dst + a * Lay::KV_ATOM + blk * 2048, map, bar, a * 64, kvh, z);
-          }
+          };
+          if (bs < kTileKeys)
+            boxes(std::integral_constant<int, 2>());
+          else
+            boxes(std::integral_constant<int, 1>());
         };
         // the order the products consume them: S(j) needs K(j) before P V(j) needs V(j)
         for (int j = 0; j < nkt; ++j) {

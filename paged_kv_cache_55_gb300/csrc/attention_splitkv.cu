@@ -63,6 +63,7 @@ struct PlanParams {
   int32_t max_query_len;
   int32_t max_seq_len;
   int32_t max_blocks_per_seq;
+  int32_t block_size;     // tokens per cache block: 8, 16 or 32
   int32_t rows_per_item;  // 8 / G
   int32_t part_tokens;
   int32_t max_items;
@@ -84,6 +85,8 @@ struct AttnParams {
   int64_t q_stride;
   const int32_t *block_tables;
   int32_t max_blocks_per_seq;
+  int32_t block_size;   // tokens per cache block: 8, 16 or 32
+  int32_t block_shift;  // log2(block_size)
   int32_t num_heads;
   int32_t num_kv_heads;
   int64_t num_blocks;
@@ -131,7 +134,7 @@ __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0
   }
   if (b == p.num_seqs - 1 && q1 != p.total_q) flag_error(p.status, PA_FLAG_QUERY_LOC);
   if (L < ql || L > p.max_seq_len || ql > p.max_query_len ||
-      static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
+      static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
     flag_error(p.status, PA_FLAG_LENGTHS);
     return 0;
   }
@@ -476,9 +479,9 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   // A record is trusted only inside the bounds the host passed; anything else
   // is recorded and the unit becomes empty (no loads, no stores).
   const bool sane = U.b >= 0 && U.b < p.num_seqs && U.nrows >= 1 && U.nrows <= kCols && U.row0 >= 0 &&
-                    U.row0 + U.nrows <= p.total_q && U.kv_begin >= 0 && U.kv_begin % kBlockSize == 0 &&
+                    U.row0 + U.nrows <= p.total_q && U.kv_begin >= 0 && U.kv_begin % kTileKeys == 0 &&
                     U.kv_begin < U.kv_end &&
-                    U.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize &&
+                    U.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size &&
                     U.part < p.max_parts && U.nparts >= 1 && U.nparts <= p.max_parts;
   if (!sane) {
     if (lane == 0) flag_error(p.status, PA_FLAG_LENGTHS);
@@ -487,15 +490,15 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   } else {
     U.skip = 0;
   }
-  U.kb0 = U.kv_begin / kBlockSize;
-  U.kb1 = (U.kv_end + kBlockSize - 1) / kBlockSize;
+  U.kb0 = U.kv_begin / kTileKeys;
+  U.kb1 = (U.kv_end + kTileKeys - 1) / kTileKeys;
   return U;
 }
 
 template <int D>
 struct TileGeom {
   static constexpr int HALVES = D / 64;                // 64-element (128-byte) swizzle atoms per row
-  static constexpr int HALF_BYTES = kBlockSize * 128;  // 16 rows x 128 B
+  static constexpr int HALF_BYTES = kTileKeys * 128;  // 16 rows x 128 B
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;  // K tile then V tile
   // Byte offset of 16-byte chunk c (of D/8) of row r in a TMA SW128 tile.
@@ -531,25 +534,37 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   const int total_units = min(max(ld_cg(p.item_count), 0), p.max_items) * Hkv;
   const uint32_t my_ring = ring + warp * S * T::SLOT_BYTES;
 
-  // Producer side (lane 0 issues): stage block kb of unit U into ring slot seq % S.
+  // Producer side (lane 0 issues): stage 16-key tile kb of unit U into ring
+  // slot seq % S. Keys k live in cache row table[k / bs] * bs + k % bs: with
+  // 16- or 32-token blocks a tile is 16 consecutive rows of one block (one
+  // 16-row box), with 8-token blocks two 8-row boxes of consecutive blocks
+  // (each fills one 1 KB swizzle atom). A block-table entry is read only for a
+  // block that holds a key below the unit's end.
   auto issue = [&](const Unit &U, int kb, uint32_t seq) {
     if (lane == 0) {
       const uint32_t slot = seq % S;
       const uint32_t bar = smem_u32(&bars[warp][slot]);
       const uint32_t dst = my_ring + slot * T::SLOT_BYTES;
-      const int phys = __ldg(p.block_tables + static_cast<int64_t>(U.b) * p.max_blocks_per_seq + kb);
-      int z;
-      if (phys < 0 || phys >= p.num_blocks) {
-        flag_error(p.status, PA_FLAG_BLOCK_RANGE);
-        z = -kBlockSize;  // entirely outside the tensor: TMA fills zeros
-      } else {
-        z = phys * kBlockSize;
-      }
+      const int32_t *trow = p.block_tables + static_cast<int64_t>(U.b) * p.max_blocks_per_seq;
+      const int bs = p.block_size;
+      const int nbox = bs < kTileKeys ? 2 : 1;
+      const int box_rows = kTileKeys / nbox;
       mbar_arrive_expect_tx(bar, T::SLOT_BYTES);
+      for (int j = 0; j < nbox; ++j) {
+        const int key = kb * kTileKeys + j * box_rows;  // first key of this box
+        int z = -box_rows;                              // entirely outside the tensor: TMA fills zeros
+        if (key < U.kv_end) {  // block sizes are powers of two: shift and mask
+          const int phys = __ldg(trow + (key >> p.block_shift));
+          if (phys < 0 || phys >= p.num_blocks)
+            flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+          else
+            z = (phys << p.block_shift) + (key & (bs - 1));
+        }
 #pragma unroll
-      for (int h = 0; h < T::HALVES; ++h) {
-        tma_load_3d(dst + h * T::HALF_BYTES, &kmap, bar, h * 64, U.kvh, z);
-        tma_load_3d(dst + T::TILE_BYTES + h * T::HALF_BYTES, &vmap, bar, h * 64, U.kvh, z);
+        for (int h = 0; h < T::HALVES; ++h) {
+          tma_load_3d(dst + h * T::HALF_BYTES + j * box_rows * 128, &kmap, bar, h * 64, U.kvh, z);
+          tma_load_3d(dst + T::TILE_BYTES + h * T::HALF_BYTES + j * box_rows * 128, &vmap, bar, h * 64, U.kvh, z);
+        }
       }
     }
   };
@@ -626,10 +641,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       }
       const uint32_t kt = my_ring + slot * T::SLOT_BYTES;
       const uint32_t vt = kt + T::TILE_BYTES;
-      const int valid_rows = min(kBlockSize, cur.kv_end - kb * kBlockSize);
-      if (valid_rows < kBlockSize) {
+      const int valid_rows = min(kTileKeys, cur.kv_end - kb * kTileKeys);
+      if (valid_rows < kTileKeys) {
         // rows past the request's last key may hold anything (even NaN): zero them in V
-        const int n = (kBlockSize - valid_rows) * (D / 8);
+        const int n = (kTileKeys - valid_rows) * (D / 8);
         for (int i = lane; i < n; i += 32) {
           const int r = valid_rows + i / (D / 8), c = i % (D / 8);
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + T::off(r, c)), "r"(0u) : "memory");
@@ -649,7 +664,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         else
           E::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
       }
-      const int t0 = kb * kBlockSize + (lane >> 2), t1 = t0 + 8;
+      const int t0 = kb * kTileKeys + (lane >> 2), t1 = t0 + 8;
       const float x0 = t0 < lim[0] ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
       const float x1 = t0 < lim[1] ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
       const float x2 = t1 < lim[0] ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
@@ -824,14 +839,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D view of one cache, [num_blocks * 16 rows][Hkv][D], with a box of
 // 16 rows x 1 head x 64 elements (128 bytes, 128-byte swizzle).
 static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t dtype) {
+                             int32_t head_dim, int32_t block_size, int32_t dtype) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
-                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+                              static_cast<cuuint64_t>(num_blocks) * block_size};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
                                  static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-  const cuuint32_t box[3] = {64, 1, kBlockSize};
+  // one box per 16-key tile of a 16- or 32-token block, two per tile of 8-token blocks
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size < kTileKeys ? block_size : kTileKeys)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType type = dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return encode(map, type, 3, const_cast<void *>(cache), dims, strides, box, estr,
@@ -853,6 +869,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.max_query_len = a.max_query_len;
   pp.max_seq_len = a.max_seq_len;
   pp.max_blocks_per_seq = a.max_blocks_per_seq;
+  pp.block_size = a.block_size;
   pp.rows_per_item = w.rows_per_item;
   pp.part_tokens = w.part_tokens;
   pp.max_items = w.max_items;
@@ -869,8 +886,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.dtype) ||
-      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.dtype))
+  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype) ||
+      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype))
     return cudaErrorInvalidValue;
 
   cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
@@ -882,6 +899,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.q_stride = a.q_stride;
   ap.block_tables = a.block_tables;
   ap.max_blocks_per_seq = a.max_blocks_per_seq;
+  ap.block_size = a.block_size;
+  ap.block_shift = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   ap.num_heads = a.num_heads;
   ap.num_kv_heads = a.num_kv_heads;
   ap.num_blocks = a.num_blocks;
@@ -921,6 +940,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.q_stride = a.q_stride;
     tp.block_tables = a.block_tables;
     tp.max_blocks_per_seq = a.max_blocks_per_seq;
+    tp.block_size = a.block_size;
+    tp.block_shift = ap.block_shift;
     tp.num_heads = a.num_heads;
     tp.num_kv_heads = a.num_kv_heads;
     tp.num_blocks = a.num_blocks;

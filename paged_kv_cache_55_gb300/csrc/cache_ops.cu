@@ -44,21 +44,21 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
 // Logical row j of one request -> contiguous output row j.
 __global__ void __launch_bounds__(256) gather_kv_kernel(
     const uint4 *__restrict__ key_cache, const uint4 *__restrict__ value_cache,
-    const int32_t *__restrict__ table_row, int32_t seq_len, int32_t row16, int64_t num_blocks,
+    const int32_t *__restrict__ table_row, int32_t seq_len, int32_t row16, int32_t block_size, int64_t num_blocks,
     uint4 *__restrict__ key_out, uint4 *__restrict__ value_out, unsigned int *status) {
   const int64_t total = static_cast<int64_t>(seq_len) * row16;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t j = static_cast<int32_t>(i / row16);
     const int32_t c = static_cast<int32_t>(i - static_cast<int64_t>(j) * row16);
-    const int32_t phys = __ldg(table_row + j / kBlockSize);
+    const int32_t phys = __ldg(table_row + j / block_size);
     if (phys < 0 || phys >= num_blocks) {
       if (c == 0) flag_error(status, PA_FLAG_BLOCK_RANGE);
       key_out[i] = make_uint4(0, 0, 0, 0);
       value_out[i] = make_uint4(0, 0, 0, 0);
       continue;
     }
-    const int64_t src = (static_cast<int64_t>(phys) * kBlockSize + (j % kBlockSize)) * row16 + c;
+    const int64_t src = (static_cast<int64_t>(phys) * block_size + (j % block_size)) * row16 + c;
     key_out[i] = __ldg(key_cache + src);
     value_out[i] = __ldg(value_cache + src);
   }
@@ -298,13 +298,13 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
 }
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
-                             int32_t seq_len, int32_t row_elems, int64_t num_blocks, void *key_out,
+                             int32_t seq_len, int32_t row_elems, int32_t block_size, int64_t num_blocks, void *key_out,
                              void *value_out, unsigned int *status, int sm_count, cudaStream_t stream) {
   const int32_t row16 = row_elems / 8;
   const int grid = grid_for(static_cast<int64_t>(seq_len) * row16, 256, sm_count);
   gather_kv_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(key_cache),
                                              static_cast<const uint4 *>(value_cache), table_row, seq_len,
-                                             row16, num_blocks, static_cast<uint4 *>(key_out),
+                                             row16, block_size, num_blocks, static_cast<uint4 *>(key_out),
                                              static_cast<uint4 *>(value_out), status);
   return cudaGetLastError();
 }

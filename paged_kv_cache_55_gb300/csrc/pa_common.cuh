@@ -12,7 +12,10 @@
 
 namespace pa {
 
-constexpr int kBlockSize = 16;  // tokens per cache block (the only size built)
+// Keys per staged tile: the kernels move and multiply K/V 16 keys at a time
+// (one m16n8k16 step). Cache blocks are 8, 16 or 32 tokens (runtime
+// block_size); a tile is then two 8-row blocks, one block, or half a block.
+constexpr int kTileKeys = 16;
 
 // ---- status word --------------------------------------------------------
 __device__ __forceinline__ void flag_error(unsigned int *status, unsigned int bits) {

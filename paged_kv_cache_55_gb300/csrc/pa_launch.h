@@ -27,7 +27,7 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
                                           int sm_count, cudaStream_t stream);
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
-                             int32_t seq_len, int32_t row_elems, int64_t num_blocks, void *key_out,
+                             int32_t seq_len, int32_t row_elems, int32_t block_size, int64_t num_blocks, void *key_out,
                              void *value_out, unsigned int *status, int sm_count, cudaStream_t stream);
 
 // Byte offsets of the pieces of the attention workspace, and the split plan.
@@ -51,7 +51,7 @@ struct AttnLaunch {
   int32_t max_blocks_per_seq;
   const int32_t *seq_lens, *query_start_loc;
   int32_t num_seqs, total_q, max_query_len, max_seq_len;
-  int32_t num_heads, num_kv_heads, head_dim;
+  int32_t num_heads, num_kv_heads, head_dim, block_size;
   int64_t num_blocks;
   float scale;
   int32_t dtype;  // PA_BF16 or PA_FP16 (q, caches and out alike)

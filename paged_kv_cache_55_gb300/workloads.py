@@ -315,12 +315,12 @@ def tiny_decode(seed: int = 0, dtype: str = "bf16") -> Workload:
                          num_heads=4, num_kv_heads=1, head_dim=64, num_blocks=32, seed=seed, dtype=dtype)
 
 
-def mha_decode(seed: int = 0, batch: int = 64, dtype: str = "bf16") -> Workload:
+def mha_decode(seed: int = 0, batch: int = 64, dtype: str = "bf16", block_size: int = 16) -> Workload:
     """MHA 7B-like decode layer: H=Hkv=32, D=128, seq_lens ~ U[128, 2048]."""
     rng = np.random.default_rng(seed + 1000)
     L = rng.integers(128, 2048, size=batch, endpoint=True)
     return make_workload("mha_decode", context_lens=L - 1, query_lens=[1] * batch,
-                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed, dtype=dtype)
+                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed, dtype=dtype, block_size=block_size)
 
 
 def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
@@ -330,24 +330,26 @@ def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
     return np.clip(np.rint(x), 16, 8192).astype(np.int64)
 
 
-def gqa_decode(seed: int = 0, batch: int = 256, dtype: str = "bf16") -> Workload:
+def gqa_decode(seed: int = 0, batch: int = 256, dtype: str = "bf16", block_size: int = 16) -> Workload:
     """GQA 8B-like decode layer: batch 256, H=32, Hkv=8, D=128, lognormal lengths."""
     L = gqa_seq_lens(seed, batch)
     w = make_workload("gqa_decode", context_lens=L - 1, query_lens=[1] * batch,
-                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype)
+                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype, block_size=block_size)
     w.meta["lognormal_sigma"] = 1.0
     return w
 
 
-def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768, dtype: str = "bf16") -> Workload:
+def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768, dtype: str = "bf16",
+                block_size: int = 16) -> Workload:
     """Long-context decode: 8 requests of 32768 tokens, H=64, Hkv=8, D=128."""
     return make_workload("long_decode", context_lens=[seq_len - 1] * batch, query_lens=[1] * batch,
-                         num_heads=64, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype)
+                         num_heads=64, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype,
+                         block_size=block_size)
 
 
 def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: int = 240,
                n_shared: int = 64, shared_blocks: int = 64, batch: Optional[int] = None,
-               dtype: str = "bf16") -> Workload:
+               dtype: str = "bf16", block_size: int = 16) -> Workload:
     """Continuous-batching step: 16 prefill chunks of 512 query tokens (prior
     context U[0, 4096]) plus 240 decode requests (context U[256, 4096]); the
     first 64 physical blocks of 64 decode requests are one shared prefix.
@@ -360,7 +362,7 @@ def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: i
     rng = np.random.default_rng(seed + 3000)
     pre_ctx = rng.integers(0, 4096, size=n_prefill, endpoint=True)
     dec_ctx = rng.integers(256, 4096, size=n_decode, endpoint=True)
-    lo = shared_blocks * 16 + 1
+    lo = shared_blocks * block_size + 1
     dec_ctx[:n_shared] = rng.integers(lo, 4096, size=n_shared, endpoint=True)
     ctx = np.concatenate([pre_ctx, dec_ctx])
     ql = np.concatenate([np.full(n_prefill, chunk), np.ones(n_decode, dtype=np.int64)])
@@ -371,7 +373,7 @@ def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: i
     w = make_workload("mixed_step", context_lens=ctx, query_lens=ql,
                       num_heads=32, num_kv_heads=8, head_dim=128, seed=seed,
                       shared_prefix_requests=np.nonzero(is_shared)[0].tolist(),
-                      shared_prefix_blocks=shared_blocks, dtype=dtype)
+                      shared_prefix_blocks=shared_blocks, dtype=dtype, block_size=block_size)
     return w
 
 

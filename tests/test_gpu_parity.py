@@ -73,6 +73,17 @@ SMALL_CASES = {
     # sharp scores over several 128-key ranges: row maxima grow within ranges
     "sharp_long_chunks_g4_d128": dict(context_lens=[200, 0], query_lens=[300, 130], num_heads=8, num_kv_heads=2,
                                       head_dim=128, q_scale=8.0),
+    # 8- and 32-token cache blocks (16-key tiles are two blocks or half a block)
+    "block8_decode_g4_d128": dict(context_lens=[0, 6, 15, 16, 511, 1100, 40, 3], query_lens=[1] * 8, num_heads=32,
+                                  num_kv_heads=8, head_dim=128, block_size=8),
+    "block32_decode_g8_d64": dict(context_lens=[1030, 3, 31, 32, 33, 700], query_lens=[1] * 6, num_heads=16,
+                                  num_kv_heads=2, head_dim=64, block_size=32),
+    "block8_mixed_chunks_g4_d128": dict(context_lens=[0, 37, 600, 20, 5], query_lens=[40, 2, 1, 129, 7],
+                                        num_heads=32, num_kv_heads=8, head_dim=128, block_size=8),
+    "block32_mixed_chunks_g2_d128": dict(context_lens=[130, 0, 999], query_lens=[389, 1, 70], num_heads=8,
+                                         num_kv_heads=4, head_dim=128, block_size=32),
+    "block8_long_request_g8": dict(context_lens=[20000], query_lens=[1], num_heads=64, num_kv_heads=8,
+                                   head_dim=128, block_size=8),
     "empty_requests": dict(context_lens=[10, 0, 700, 33], query_lens=[0, 1, 0, 3],
                            num_heads=8, num_kv_heads=2, head_dim=128),
     "sharp_scores": dict(context_lens=[300, 1800, 4], query_lens=[1, 1, 9], num_heads=32, num_kv_heads=8,
@@ -108,7 +119,7 @@ def test_small_cases(oracle, name):
     run_and_check(w, oracle)
 
 
-FP16_CASES = ["ragged_decode_g4_d128", "decode_g8_d64", "decode_g1_d64", "mixed_chunks_g4_d128",
+FP16_CASES = ["block8_mixed_chunks_g4_d128", "block32_decode_g8_d64", "ragged_decode_g4_d128", "decode_g8_d64", "decode_g1_d64", "mixed_chunks_g4_d128",
               "mixed_chunks_g1_d128", "mixed_chunks_g8_d64", "long_chunks_g2_d128", "sharp_long_chunks_g4_d128",
               "empty_requests", "seq_len_one"]
 
@@ -224,8 +235,10 @@ def test_copy_blocks_flags_and_skips_bad_ids():
     assert B.pa_debug_status() == 0
 
 
-def test_gather_kv_bit_exact():
-    w = W.make_workload("gather", seed=3, **SMALL_CASES["ragged_decode_g4_d128"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_gather_kv_bit_exact(bs):
+    kw = dict(SMALL_CASES["ragged_decode_g4_d128"], block_size=bs)
+    w = W.make_workload("gather", seed=3, **kw)
     st = DeviceStep(w)
     st.reshape_and_cache()
     kc = bf16_to_numpy_bits(st.key_cache)
@@ -236,9 +249,9 @@ def test_gather_kv_bit_exact():
         vo = torch.empty_like(ko)
         B.pa_gather_kv(st.key_cache, st.value_cache, st.block_tables[b], L, ko, vo)
         j = np.arange(L)
-        rows = w.block_tables[b, j // 16]
-        assert np.array_equal(bf16_to_numpy_bits(ko), kc[rows, j % 16])
-        assert np.array_equal(bf16_to_numpy_bits(vo), vc[rows, j % 16])
+        rows = w.block_tables[b, j // bs]
+        assert np.array_equal(bf16_to_numpy_bits(ko), kc[rows, j % bs])
+        assert np.array_equal(bf16_to_numpy_bits(vo), vc[rows, j % bs])
     assert B.pa_debug_status() == 0
 
 
@@ -302,7 +315,7 @@ def test_host_side_errors():
     assert call() == 0
     assert call(q=None) == -1
     assert call(D=96) == -3
-    assert call(bs=32) == -3
+    assert call(bs=64) == -3
     assert call(Hkv=3) == -2
     assert call(dtype=2) == -3  # 0 = bf16, 1 = fp16
     assert call(wsb=16) == -5

@@ -59,7 +59,8 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     # unsupported or inconsistent sizes give 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 96, 16) == 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 3, 64, 16) == 0
-    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 32) == 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 64) == 0  # block sizes 8, 16, 32 only
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 32) > 0
     assert lib.pa_attention_workspace_size(4, 4, 40, 33, 4, 1, 64, 16) == 0
     pt, mp = B.pa_attention_plan_info(8, 32768, 64, 8)
     assert pt % 16 == 0 and mp == -(-32768 // pt)
