@@ -53,6 +53,7 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_FP16 1
+#define ORACLE_FP8_E4M3 2 /* 8-bit cache codes (see the FP8 section below) */
 
 /* bf16 is the upper half of an IEEE binary32; widening is exact. */
 static double bf16_to_double(uint16_t h)
@@ -159,6 +160,106 @@ int oracle_decode_elements(const uint16_t *bits, int64_t n, int32_t dtype, doubl
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) cache codes                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * KV-cache quantisation (LLM-infra reading map, §4.2): the cache is stored in
+ * 8 bits instead of 16, quantised online as K/V are written and dequantised
+ * as attention reads them. The page fixes neither the 8-bit format nor the
+ * scale, so the readings are: the E4M3 format (sign, 4-bit exponent with bias
+ * 7, 3-bit fraction; no infinities; S.1111.111 is NaN, so the largest finite
+ * value is 1.75 * 2^8 = 448) with one float scale per cache:
+ *   code  = E4M3(x / scale), the quotient taken in binary32 (correctly
+ *           rounded), then rounded to the nearest E4M3 value, ties to even,
+ *           with magnitudes beyond 448 saturating to 448;
+ *   value = decode(code) * scale, exact in a double.
+ */
+
+/* Exponent 0: the subnormals fraction * 2^-9; otherwise (8 + fraction) * 2^(exponent - 10). */
+static double e4m3_to_double(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, f = c & 7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+/*
+ * Nearest E4M3 code to x, ties to the even fraction, saturating at 448; a NaN
+ * gives the NaN code 0x7F. The spacing of representable values is 2^-9 below
+ * 2^-6 (the subnormals) and 2^(E - 3) within the binade [2^E, 2^(E+1)).
+ */
+static uint8_t e4m3_from_double(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int E;
+    frexp(a, &E); /* a = m * 2^E with m in [0.5, 1): a lies in [2^(E-1), 2^E) */
+    int e_unb = E - 1;
+    if (e_unb < -6)
+        e_unb = -6; /* the subnormal range shares the spacing of [2^-6, 2^-5) */
+    double quantum = ldexp(1.0, e_unb - 3);
+    double n = a / quantum; /* exact: a power-of-two division */
+    double fl = floor(n);
+    double rem = n - fl;
+    double r = fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    double v = r * quantum; /* a representable value: exact */
+    if (v >= 448.0)
+        return sign | 0x7E;
+    if (v == 0.0)
+        return sign;
+    if (v < ldexp(1.0, -6))
+        return sign | (uint8_t)(v / ldexp(1.0, -9)); /* exponent 0, fraction = v / 2^-9 */
+    frexp(v, &E);
+    int e = E - 1;                                  /* v in [2^e, 2^(e+1)) */
+    int f = (int)(v / ldexp(1.0, e) * 8.0) - 8;     /* 3-bit fraction */
+    return sign | (uint8_t)(((e + 7) << 3) | f);
+}
+
+/* The binary32 quotient x / scale of one 16-bit element, then its code. */
+static uint8_t quantize_elem(int32_t dtype, uint16_t h, float scale)
+{
+    float xf = (float)elem_to_double(dtype, h); /* exact: 16-bit floats widen exactly */
+    float qf = xf / scale;                      /* binary32 division, correctly rounded */
+    return e4m3_from_double((double)qf);
+}
+
+int oracle_fp8_decode(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_to_double(codes[i]);
+    return ORACLE_OK;
+}
+
+int oracle_fp8_round(const double *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_from_double(x[i]);
+    return ORACLE_OK;
+}
+
+int oracle_fp8_quantize(const uint16_t *bits, int64_t n, int32_t dtype, float scale, uint8_t *out)
+{
+    if ((dtype != ORACLE_BF16 && dtype != ORACLE_FP16) || !(scale > 0.0f) || isinf(scale))
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = quantize_elem(dtype, bits[i], scale);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step 1: reshape_and_cache                                                 */
 /* ------------------------------------------------------------------------ */
 
@@ -206,6 +307,53 @@ int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
         for (int64_t e = 0; e < row; ++e) {
             key_cache[dst + e] = key[t * row + e];
             value_cache[dst + e] = value[t * row + e];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * reshape_and_cache into 8-bit caches: the same slots as above, each element
+ * quantised on the way in (code = E4M3(x / k_scale) for K, v_scale for V;
+ * LLM-infra reading map, §4.2: quantise online as the cache is written).
+ */
+int oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
+                                 uint8_t *key_cache, uint8_t *value_cache,
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t num_blocks, int32_t dtype,
+                                 float k_scale, float v_scale)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    if ((dtype != ORACLE_BF16 && dtype != ORACLE_FP16) || !(k_scale > 0.0f) || !(v_scale > 0.0f) ||
+        isinf(k_scale) || isinf(v_scale))
+        return ORACLE_ERR_ARG;
+    if (num_tokens == 0)
+        return ORACLE_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return ORACLE_ERR_ARG;
+
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    const int64_t num_slots = num_blocks * block_size;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s >= num_slots)
+            return ORACLE_ERR_SLOT_RANGE;
+        if (s < 0)
+            continue;
+        for (int64_t u = 0; u < t; ++u)
+            if (slot_mapping[u] == s)
+                return ORACLE_ERR_SLOT_DUPLICATE;
+    }
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        int64_t dst = ((s / block_size) * block_size + s % block_size) * row;
+        for (int64_t e = 0; e < row; ++e) {
+            key_cache[dst + e] = quantize_elem(dtype, key[t * row + e], k_scale);
+            value_cache[dst + e] = quantize_elem(dtype, value[t * row + e], v_scale);
         }
     }
     return ORACLE_OK;
@@ -325,8 +473,8 @@ int oracle_rope_reshape_and_cache(uint16_t *q, const uint16_t *key, const uint16
 
 typedef struct {
     const uint16_t *q;
-    const uint16_t *key_cache;
-    const uint16_t *value_cache;
+    const void *key_cache;   /* 16-bit elements, or 8-bit codes when kv_dtype is ORACLE_FP8_E4M3 */
+    const void *value_cache;
     const int32_t *block_tables;
     int32_t max_blocks_per_seq;
     const int32_t *seq_lens;
@@ -338,7 +486,10 @@ typedef struct {
     int32_t block_size;
     int64_t num_blocks;
     double scale;
-    int32_t dtype;  /* ORACLE_BF16 or ORACLE_FP16: how the 16-bit elements decode */
+    int32_t dtype;    /* ORACLE_BF16 or ORACLE_FP16: how q's 16-bit elements decode */
+    int32_t kv_dtype; /* dtype (16-bit caches) or ORACLE_FP8_E4M3 */
+    double k_scale;   /* 8-bit caches: K value = decode(code) * k_scale */
+    double v_scale;
 } problem_t;
 
 static int check_problem(const problem_t *p)
@@ -349,6 +500,11 @@ static int check_problem(const problem_t *p)
     if (p->num_heads % p->num_kv_heads != 0)
         return ORACLE_ERR_ARG;
     if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16)
+        return ORACLE_ERR_ARG;
+    if (p->kv_dtype != p->dtype && p->kv_dtype != ORACLE_FP8_E4M3)
+        return ORACLE_ERR_ARG;
+    if (p->kv_dtype == ORACLE_FP8_E4M3 &&
+        (!(p->k_scale > 0.0) || !(p->v_scale > 0.0) || isinf(p->k_scale) || isinf(p->v_scale)))
         return ORACLE_ERR_ARG;
     if (p->query_start_loc[0] != 0)
         return ORACLE_ERR_LENGTHS;
@@ -369,6 +525,14 @@ static int check_problem(const problem_t *p)
     return ORACLE_OK;
 }
 
+/* Element idx of a cache as a double: a 16-bit element, or an 8-bit code times its scale. */
+static double cache_value(const problem_t *p, const void *cache, int64_t idx, double scale)
+{
+    if (p->kv_dtype == ORACLE_FP8_E4M3)
+        return e4m3_to_double(((const uint8_t *)cache)[idx]) * scale;
+    return elem_to_double(p->dtype, ((const uint16_t *)cache)[idx]);
+}
+
 /*
  * Gather the logical K and V rows 0..L-1 of request b, KV head kvh, into
  * contiguous [L, head_dim] arrays of doubles. Logical token j lives in
@@ -385,8 +549,8 @@ static void gather_request(const problem_t *p, int32_t b, int32_t kvh, double *K
         int64_t slot = phys * p->block_size + offset;
         int64_t base = (slot * p->num_kv_heads + kvh) * D;
         for (int32_t d = 0; d < D; ++d) {
-            K[(int64_t)j * D + d] = elem_to_double(p->dtype, p->key_cache[base + d]);
-            V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->value_cache[base + d]);
+            K[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->k_scale);
+            V[(int64_t)j * D + d] = cache_value(p, p->value_cache, base + d, p->v_scale);
         }
     }
 }
@@ -511,17 +675,18 @@ static void *pool_worker(void *arg)
  * out: [total_q, num_heads, head_dim] doubles. Rows of requests with
  * query_len 0 are absent (total_q counts only scheduled tokens).
  */
-int oracle_attention_varlen(const uint16_t *q, const uint16_t *key_cache,
-                            const uint16_t *value_cache, const int32_t *block_tables,
+int oracle_attention_varlen(const uint16_t *q, const void *key_cache,
+                            const void *value_cache, const int32_t *block_tables,
                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
                             const int32_t *query_start_loc, int32_t num_seqs,
                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                             int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
+                            int32_t kv_dtype, float k_scale, float v_scale,
                             double *out, int32_t num_threads)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale, dtype};
+                   block_size, num_blocks, (double)scale, dtype, kv_dtype, (double)k_scale, (double)v_scale};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;
@@ -554,18 +719,19 @@ int oracle_attention_varlen(const uint16_t *q, const uint16_t *key_cache,
  * The same definition for a chosen list of (query token, head) pairs, so that
  * full-size problems can be checked at sampled outputs. out: [n_samples, head_dim].
  */
-int oracle_attention_sampled(const uint16_t *q, const uint16_t *key_cache,
-                             const uint16_t *value_cache, const int32_t *block_tables,
+int oracle_attention_sampled(const uint16_t *q, const void *key_cache,
+                             const void *value_cache, const int32_t *block_tables,
                              int32_t max_blocks_per_seq, const int32_t *seq_lens,
                              const int32_t *query_start_loc, int32_t num_seqs,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
+                            int32_t kv_dtype, float k_scale, float v_scale,
                              int64_t n_samples, const int64_t *sample_token,
                              const int32_t *sample_head, double *out)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale, dtype};
+                   block_size, num_blocks, (double)scale, dtype, kv_dtype, (double)k_scale, (double)v_scale};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;
@@ -601,17 +767,18 @@ int oracle_attention_sampled(const uint16_t *q, const uint16_t *key_cache,
  * the tests' checks of the weights themselves. weights: at least seq_len
  * doubles. Returns the number of visible keys, or a negative error code.
  */
-int oracle_attention_weights(const uint16_t *q, const uint16_t *key_cache,
-                             const uint16_t *value_cache, const int32_t *block_tables,
+int oracle_attention_weights(const uint16_t *q, const void *key_cache,
+                             const void *value_cache, const int32_t *block_tables,
                              int32_t max_blocks_per_seq, const int32_t *seq_lens,
                              const int32_t *query_start_loc, int32_t num_seqs,
                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                              int32_t block_size, int64_t num_blocks, float scale, int32_t dtype,
+                            int32_t kv_dtype, float k_scale, float v_scale,
                              int64_t token, int32_t head, double *weights)
 {
     problem_t p = {q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_heads, num_kv_heads, head_dim,
-                   block_size, num_blocks, (double)scale, dtype};
+                   block_size, num_blocks, (double)scale, dtype, kv_dtype, (double)k_scale, (double)v_scale};
     int rc = check_problem(&p);
     if (rc != ORACLE_OK)
         return rc;

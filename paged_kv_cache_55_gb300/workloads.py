@@ -94,6 +94,27 @@ def rope_cos_sin_cache(max_position: int, rotary_dim: int, base: float = 10000.0
     return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
 
 
+FP8_E4M3 = "fp8_e4m3"
+FP8_NAN = np.uint8(0x7F)  # E4M3 S.1111.111
+
+
+def fp8_codes(rng: np.random.Generator, shape, magnitude: float = 16.0) -> np.ndarray:
+    """Seeded E4M3 codes (uint8) for cache history: random sign and 3-bit
+    fraction, and the exponent field of ``magnitude * |z|`` for z ~ N(0, 1)
+    (clipped to the format's exponents 0..15; the NaN pattern becomes the
+    largest finite code). Decoded, the values follow ``magnitude * N(0, 1)``
+    to within a factor of two, like N(0, 1) data stored with a cache scale of
+    1 / magnitude."""
+    n = int(np.prod(shape))
+    sign = rng.integers(0, 2, size=n, dtype=np.uint8)
+    z = np.abs(rng.standard_normal(n)) * magnitude
+    e = np.clip(np.floor(np.log2(np.maximum(z, 1e-30))) + 7, 0, 15).astype(np.uint8)
+    f = rng.integers(0, 8, size=n, dtype=np.uint8)
+    codes = (sign << 7) | (e << 3) | f
+    codes[(codes & 0x7F) == 0x7F] -= 1
+    return codes.reshape(shape)
+
+
 def _normal_elems(rng: np.random.Generator, shape, scale: float = 1.0, dtype: str = "bf16") -> np.ndarray:
     """Seeded N(0, scale^2) values rounded to the element type, as uint16 bits
     (the same draws for either type)."""
@@ -131,8 +152,15 @@ class Workload:
     seq_lens: np.ndarray        # int32  [B]
     query_start_loc: np.ndarray  # int32 [B + 1]
     shared_blocks: Optional[np.ndarray] = None  # physical ids shared by several requests
-    dtype: str = "bf16"          # element type of q, key, value and the caches: "bf16" or "fp16"
+    dtype: str = "bf16"          # element type of q, key, value (and 16-bit caches): "bf16" or "fp16"
     meta: dict = dataclasses.field(default_factory=dict)
+    kv_dtype: str = ""           # cache type: "" (= dtype) or "fp8_e4m3" (uint8 codes)
+    k_scale: float = 1.0         # 8-bit caches: K value = code * k_scale
+    v_scale: float = 1.0
+
+    @property
+    def kv_fp8(self) -> bool:
+        return self.kv_dtype == FP8_E4M3
 
     @property
     def num_seqs(self) -> int:
@@ -195,6 +223,9 @@ def make_workload(
     extra_table_cols: int = 2,
     scale: Optional[float] = None,
     dtype: str = "bf16",
+    kv_dtype: str = "",
+    k_scale: float = 0.0625 * 1.1,
+    v_scale: float = 0.0625 * 0.7,
 ) -> Workload:
     """Build one step: request ``b`` has ``context_lens[b]`` cached tokens and
     ``query_lens[b]`` new tokens, so ``seq_len = context + query``.
@@ -205,10 +236,15 @@ def make_workload(
     blocks to the same physical blocks (a copy-on-write shared prefix); their
     contexts must fill those blocks so that new tokens land in private blocks.
     Elements are bf16 or fp16 (``dtype``); unowned cache slots hold that
-    type's NaN.
+    type's NaN. With ``kv_dtype="fp8_e4m3"`` the caches hold 8-bit codes
+    (history drawn by ``fp8_codes``, unowned slots the E4M3 NaN) read with the
+    float scales ``k_scale`` and ``v_scale``; the new K/V rows stay 16-bit.
     """
     if dtype not in DTYPES:
         raise ValueError(f"dtype must be one of {DTYPES}")
+    if kv_dtype not in ("", dtype, FP8_E4M3):
+        raise ValueError("kv_dtype must be empty, equal to dtype, or fp8_e4m3")
+    fp8 = kv_dtype == FP8_E4M3
     rng = np.random.default_rng(seed)
     ctx = np.asarray(context_lens, dtype=np.int64)
     ql = np.asarray(query_lens, dtype=np.int64)
@@ -254,10 +290,17 @@ def make_workload(
         tables[b, first:n] = pool[cursor:cursor + take]
         cursor += take
 
-    kc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
-    vc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
+    if fp8:
+        kc = np.full((num_blocks, bs, Hkv, D), FP8_NAN, dtype=np.uint8)
+        vc = np.full((num_blocks, bs, Hkv, D), FP8_NAN, dtype=np.uint8)
+    else:
+        kc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
+        vc = np.full((num_blocks, bs, Hkv, D), NAN_BITS[dtype], dtype=np.uint16)
     kflat = kc.reshape(num_blocks * bs, Hkv, D)
     vflat = vc.reshape(num_blocks * bs, Hkv, D)
+
+    def history(n):
+        return fp8_codes(rng, (n, Hkv, D)) if fp8 else _normal_elems(rng, (n, Hkv, D), dtype=dtype)
 
     # History rows (positions < context). Shared-prefix rows are written once.
     prefix_written = False
@@ -268,15 +311,15 @@ def make_workload(
             if not prefix_written:
                 pos = np.arange(S * bs)
                 slots = tables[b, pos // bs].astype(np.int64) * bs + pos % bs
-                kflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
-                vflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
+                kflat[slots] = history(pos.size)
+                vflat[slots] = history(pos.size)
                 prefix_written = True
             start = S * bs
         if c > start:
             pos = np.arange(start, c)
             slots = tables[b, pos // bs].astype(np.int64) * bs + pos % bs
-            kflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
-            vflat[slots] = _normal_elems(rng, (pos.size, Hkv, D), dtype=dtype)
+            kflat[slots] = history(pos.size)
+            vflat[slots] = history(pos.size)
 
     # This step's tokens: query rows and the new K/V rows with their slots.
     T = int(ql.sum())
@@ -299,6 +342,9 @@ def make_workload(
         seq_lens=L.astype(np.int32), query_start_loc=qsl,
         shared_blocks=shared_ids if S else None, dtype=dtype,
         meta={"context_lens": ctx.astype(np.int32)},
+        kv_dtype=FP8_E4M3 if fp8 else "",
+        k_scale=float(np.float32(k_scale)) if fp8 else 1.0,
+        v_scale=float(np.float32(v_scale)) if fp8 else 1.0,
     )
 
 
@@ -307,20 +353,23 @@ def make_workload(
 # 7B/8B-class head counts, 16-token blocks, variable lengths).
 # --------------------------------------------------------------------------
 
-def tiny_decode(seed: int = 0, dtype: str = "bf16") -> Workload:
+def tiny_decode(seed: int = 0, dtype: str = "bf16", kv_dtype: str = "") -> Workload:
     """4 requests with seq_lens {1, 7, 16, 33}, one new token each; H=4, Hkv=1,
     D=64, 32 physical blocks in a seeded random order."""
     L = np.array([1, 7, 16, 33])
     return make_workload("tiny_decode", context_lens=L - 1, query_lens=[1] * 4,
-                         num_heads=4, num_kv_heads=1, head_dim=64, num_blocks=32, seed=seed, dtype=dtype)
+                         num_heads=4, num_kv_heads=1, head_dim=64, num_blocks=32, seed=seed, dtype=dtype,
+                         kv_dtype=kv_dtype)
 
 
-def mha_decode(seed: int = 0, batch: int = 64, dtype: str = "bf16", block_size: int = 16) -> Workload:
+def mha_decode(seed: int = 0, batch: int = 64, dtype: str = "bf16", block_size: int = 16,
+               kv_dtype: str = "") -> Workload:
     """MHA 7B-like decode layer: H=Hkv=32, D=128, seq_lens ~ U[128, 2048]."""
     rng = np.random.default_rng(seed + 1000)
     L = rng.integers(128, 2048, size=batch, endpoint=True)
     return make_workload("mha_decode", context_lens=L - 1, query_lens=[1] * batch,
-                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed, dtype=dtype, block_size=block_size)
+                         num_heads=32, num_kv_heads=32, head_dim=128, seed=seed, dtype=dtype, block_size=block_size,
+                         kv_dtype=kv_dtype)
 
 
 def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
@@ -330,26 +379,28 @@ def gqa_seq_lens(seed: int, batch: int) -> np.ndarray:
     return np.clip(np.rint(x), 16, 8192).astype(np.int64)
 
 
-def gqa_decode(seed: int = 0, batch: int = 256, dtype: str = "bf16", block_size: int = 16) -> Workload:
+def gqa_decode(seed: int = 0, batch: int = 256, dtype: str = "bf16", block_size: int = 16,
+               kv_dtype: str = "") -> Workload:
     """GQA 8B-like decode layer: batch 256, H=32, Hkv=8, D=128, lognormal lengths."""
     L = gqa_seq_lens(seed, batch)
     w = make_workload("gqa_decode", context_lens=L - 1, query_lens=[1] * batch,
-                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype, block_size=block_size)
+                      num_heads=32, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype, block_size=block_size,
+                      kv_dtype=kv_dtype)
     w.meta["lognormal_sigma"] = 1.0
     return w
 
 
 def long_decode(seed: int = 0, batch: int = 8, seq_len: int = 32768, dtype: str = "bf16",
-                block_size: int = 16) -> Workload:
+                block_size: int = 16, kv_dtype: str = "") -> Workload:
     """Long-context decode: 8 requests of 32768 tokens, H=64, Hkv=8, D=128."""
     return make_workload("long_decode", context_lens=[seq_len - 1] * batch, query_lens=[1] * batch,
                          num_heads=64, num_kv_heads=8, head_dim=128, seed=seed, dtype=dtype,
-                         block_size=block_size)
+                         block_size=block_size, kv_dtype=kv_dtype)
 
 
 def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: int = 240,
                n_shared: int = 64, shared_blocks: int = 64, batch: Optional[int] = None,
-               dtype: str = "bf16", block_size: int = 16) -> Workload:
+               dtype: str = "bf16", block_size: int = 16, kv_dtype: str = "") -> Workload:
     """Continuous-batching step: 16 prefill chunks of 512 query tokens (prior
     context U[0, 4096]) plus 240 decode requests (context U[256, 4096]); the
     first 64 physical blocks of 64 decode requests are one shared prefix.
@@ -373,7 +424,8 @@ def mixed_step(seed: int = 0, n_prefill: int = 16, chunk: int = 512, n_decode: i
     w = make_workload("mixed_step", context_lens=ctx, query_lens=ql,
                       num_heads=32, num_kv_heads=8, head_dim=128, seed=seed,
                       shared_prefix_requests=np.nonzero(is_shared)[0].tolist(),
-                      shared_prefix_blocks=shared_blocks, dtype=dtype, block_size=block_size)
+                      shared_prefix_blocks=shared_blocks, dtype=dtype, block_size=block_size,
+                      kv_dtype=kv_dtype)
     return w
 
 

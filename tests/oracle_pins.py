@@ -17,7 +17,14 @@ What pins what:
   * the element decoders: fp16 against numpy's IEEE binary16 on all 65536 bit
     patterns, bf16 at values the format fixes (1, -2, pi rounded, the largest
     finite, the smallest subnormal, signed zero, infinities, NaN); the dense
-    brute force and the seq_len-1 closed form are repeated on fp16 data.
+    brute force and the seq_len-1 closed form are repeated on fp16 data;
+  * 8-bit (E4M3) cache codes: decoding against PyTorch's float8_e4m3fn on all
+    256 codes; rounding against PyTorch's cast inside the finite range (random
+    values, every tie, values next to every tie) and against the format's
+    closed forms at saturation, zero, signed zero, subnormal ties and NaN; the
+    quantiser against a numpy binary32 division followed by that cast; the
+    quantising scatter against a numpy scatter; attention over 8-bit caches
+    against float64 SDPA over the decoded values times the scales.
 """
 
 from __future__ import annotations
@@ -466,4 +473,148 @@ PINS = [
     pin_rope_quarter_turn,
     pin_rope_interleaved_is_permuted_neox,
     pin_rope_relative_positions,
+]
+
+
+# --------------------------------------------------------------------------
+# 8-bit (E4M3) cache codes
+# --------------------------------------------------------------------------
+
+def _torch_e4m3_codes(x32: np.ndarray) -> np.ndarray:
+    """PyTorch's float32 -> float8_e4m3fn cast (round to nearest even inside the finite range)."""
+    return torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def pin_fp8_decode_matches_torch(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.fp8_decode(codes)
+    ref = _torch_e4m3_values(codes)
+    nan = np.isnan(ref)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF], "E4M3 has exactly two NaN codes"
+    assert np.array_equal(np.isnan(got), nan), "E4M3 NaN codes"
+    assert np.array_equal(got[~nan], ref[~nan]), "E4M3 decoding must match PyTorch's float8_e4m3fn"
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), "E4M3 signs (incl. -0)"
+    # values the format fixes: 1.0, the largest finite, the smallest subnormal and normal
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def pin_fp8_round_matches_torch(oracle):
+    rng = np.random.default_rng(41)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = _torch_e4m3_values(finite)
+    pos = np.unique(vals[vals >= 0])
+    mids = (pos[:-1] + pos[1:]) / 2.0  # exact ties, ties to the even code
+    mag = np.exp2(rng.uniform(-12.0, np.log2(448.0), size=20000))
+    x = np.concatenate([vals, mids, -mids, mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20),
+                        mag * rng.choice([-1.0, 1.0], size=mag.size)]).astype(np.float32)
+    got = oracle.fp8_round(x.astype(np.float64))
+    ref = _torch_e4m3_codes(x)
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, f"E4M3 rounding differs from PyTorch at {x[bad[:5]]}: {got[bad[:5]]} vs {ref[bad[:5]]}"
+    assert np.array_equal(oracle.fp8_round(vals), finite), "every finite code must round-trip"
+
+
+def pin_fp8_round_saturates_and_specials(oracle):
+    cases = [(448.0, 0x7E), (449.0, 0x7E), (464.0, 0x7E), (480.0, 0x7E), (1e6, 0x7E), (math.inf, 0x7E),
+             (-448.0, 0xFE), (-1e30, 0xFE), (-math.inf, 0xFE), (0.0, 0x00), (-0.0, 0x80),
+             (2.0 ** -10, 0x00),        # half the smallest subnormal: tie to the even code 0
+             (3 * 2.0 ** -10, 0x02),    # 1.5 quanta: tie to 2 quanta
+             (5 * 2.0 ** -10, 0x02),    # 2.5 quanta: tie to 2 quanta
+             (1.0625, 0x38),            # between 1 and 1.125: tie to 1.0 (even fraction 0)
+             (1.1875, 0x3A),            # between 1.125 and 1.25: tie to 1.25 (fraction 2)
+             (440.0, 0x7E),             # between 416 and 448: tie to 448 (fraction 6)
+             (math.nan, 0x7F)]
+    x = np.array([c[0] for c in cases], dtype=np.float64)
+    got = oracle.fp8_round(x)
+    want = np.array([c[1] for c in cases], dtype=np.uint8)
+    assert np.array_equal(got, want), f"E4M3 special cases: {list(zip(x, got, want))}"
+
+
+def pin_fp8_quantize_is_float32_quotient(oracle):
+    rng = np.random.default_rng(42)
+    for dtype in ("bf16", "fp16"):
+        bits = f32_to_bits((4.0 * rng.standard_normal(50000)).astype(np.float32), dtype)
+        for scale in (0.0371, 0.0625, 1.7):
+            s32 = np.float32(scale)
+            q = bits_to_f32(bits, dtype) / s32  # numpy binary32 division
+            keep = np.abs(q) < 448.0
+            got = oracle.fp8_quantize(bits, float(s32), dtype)
+            ref = _torch_e4m3_codes(q)
+            assert np.array_equal(got[keep], ref[keep]), f"quantiser vs float32 quotient + cast ({dtype}, {scale})"
+            big = ~keep
+            assert np.all((got[big] & 0x7F) == 0x7E), "quotients beyond 448 saturate"
+
+
+def pin_fp8_reshape_matches_numpy_scatter(oracle):
+    rng = np.random.default_rng(43)
+    nb, bs, hkv, d, T = 6, 8, 2, 16, 20
+    slots = rng.permutation(nb * bs)[:T].astype(np.int64)
+    slots[3] = -1
+    key = f32_to_bits(rng.standard_normal((T, hkv, d)).astype(np.float32), "bf16")
+    value = f32_to_bits(rng.standard_normal((T, hkv, d)).astype(np.float32), "bf16")
+    ks, vs = np.float32(0.05), np.float32(0.03)
+    kc = np.full((nb, bs, hkv, d), 0x7F, dtype=np.uint8)
+    vc = kc.copy()
+    oracle.reshape_and_cache_fp8(key, value, kc, vc, slots, bs, float(ks), float(vs), "bf16")
+    kref = np.full_like(kc, 0x7F).reshape(nb * bs, hkv, d)
+    vref = kref.copy()
+    ok = slots >= 0
+    kref[slots[ok]] = _torch_e4m3_codes(bf16_bits_to_f32(key[ok]) / ks)
+    vref[slots[ok]] = _torch_e4m3_codes(bf16_bits_to_f32(value[ok]) / vs)
+    assert np.array_equal(kc.reshape(nb * bs, hkv, d), kref), "8-bit K scatter"
+    assert np.array_equal(vc.reshape(nb * bs, hkv, d), vref), "8-bit V scatter"
+
+
+def pin_fp8_attention_vs_sdpa(oracle):
+    """Attention over 8-bit caches: dense float64 SDPA over the decoded values times the scales."""
+    from paged_kv_cache_55_gb300.workloads import fp8_codes
+    rng = np.random.default_rng(44)
+    ks, vs = float(np.float32(0.0625 * 1.1)), float(np.float32(0.0437))
+    for ctx, ql, H, Hkv, D, bs in DENSE_CASES:
+        p = DenseProblem(rng, ctx, ql, H, Hkv, D, bs)
+        p.kd = [fp8_codes(rng, (x, Hkv, D)) for x in p.L]
+        p.vd = [fp8_codes(rng, (x, Hkv, D)) for x in p.L]
+        bt = np.full((len(p.L), p.max_blocks), -7, dtype=np.int32)
+        kc = np.full((p.num_blocks, bs, Hkv, D), 0x7F, dtype=np.uint8)
+        vc = kc.copy()
+        cursor = 0
+        for b, L in enumerate(p.L):
+            for i in range((L + bs - 1) // bs):
+                bt[b, i] = p.perm[cursor]
+                cursor += 1
+            for j in range(L):
+                kc[bt[b, j // bs], j % bs] = p.kd[b][j]
+                vc[bt[b, j // bs], j % bs] = p.vd[b][j]
+        got = oracle.attention(p.q, kc, vc, bt, p.seq_lens, p.qsl, H, p.scale, num_threads=2,
+                               k_scale=ks, v_scale=vs)
+        ref = np.zeros_like(got)
+        for b, L in enumerate(p.L):
+            q0, n = int(p.qsl[b]), p.ql[b]
+            if n == 0:
+                continue
+            qb = torch.from_numpy(bf16_bits_to_f32(p.q[q0:q0 + n]).astype(np.float64)).transpose(0, 1)
+            kb = torch.from_numpy(_torch_e4m3_values(p.kd[b]) * ks).transpose(0, 1)
+            vb = torch.from_numpy(_torch_e4m3_values(p.vd[b]) * vs).transpose(0, 1)
+            mask = torch.arange(L).unsqueeze(0) <= (L - n) + torch.arange(n).unsqueeze(1)
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qb.unsqueeze(0), kb.unsqueeze(0), vb.unsqueeze(0), attn_mask=mask, scale=p.scale,
+                enable_gqa=(H != Hkv))
+            ref[q0:q0 + n] = o[0].transpose(0, 1).numpy()
+        err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+        assert err <= 1e-12, f"8-bit cache attention vs SDPA max |diff| {err} for {(ctx, ql, H, Hkv, D, bs)}"
+
+
+PINS += [
+    pin_fp8_decode_matches_torch,
+    pin_fp8_round_matches_torch,
+    pin_fp8_round_saturates_and_specials,
+    pin_fp8_quantize_is_float32_quotient,
+    pin_fp8_reshape_matches_numpy_scatter,
+    pin_fp8_attention_vs_sdpa,
 ]

@@ -25,8 +25,19 @@ MUTANTS = {
     "dot_drops_last_dim": ("for (int32_t d = 0; d < D; ++d)\n            dot += qv[d]",
                            "for (int32_t d = 0; d < D - 1; ++d)\n            dot += qv[d]"),
     "unnormalised_weights": ("w[j] /= z;", "w[j] /= 1.0;"),
-    "v_read_from_k_cache": ("V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->value_cache[base + d]);",
-                            "V[(int64_t)j * D + d] = elem_to_double(p->dtype, p->key_cache[base + d]);"),
+    "v_read_from_k_cache": ("V[(int64_t)j * D + d] = cache_value(p, p->value_cache, base + d, p->v_scale);",
+                            "V[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->v_scale);"),
+    "fp8_exponent_bias": ("v = ldexp((double)(8 + f), e - 10);", "v = ldexp((double)(8 + f), e - 9);"),
+    "fp8_subnormals_flushed": ("v = ldexp((double)f, -9);", "v = 0.0;"),
+    "fp8_rounds_toward_zero": ("    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0))\n        r = fl + 1.0;",
+                               "    (void)rem;"),
+    "fp8_no_saturation": ("    if (a >= 448.0)\n        return sign | 0x7E;", "    if (a >= 480.0)\n        return 0x7F;"),
+    "fp8_scale_divides": ("return e4m3_to_double(((const uint8_t *)cache)[idx]) * scale;",
+                          "return e4m3_to_double(((const uint8_t *)cache)[idx]) / scale;"),
+    "fp8_v_scale_for_k": ("K[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->k_scale);",
+                          "K[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->v_scale);"),
+    "fp8_quotient_in_double": ("float qf = xf / scale;                      /* binary32 division, correctly rounded */",
+                               "double qf = (double)xf / (double)scale;"),
     "fp16_exponent_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
     "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "copy_blocks_k_only": ("        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems, "
