@@ -62,14 +62,15 @@ COPY_METRIC = "CoW block copy GB/s (read + write) & fraction of GB300 HBM peak"
 
 def step_accounting(w, rope: bool = False) -> dict:
     H, Hkv, D, bs = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
-    kv_tok = 2 * Hkv * D * 2
+    cache_elem = 1 if w.kv_fp8 else 2  # 8-bit caches: one byte per element
+    kv_tok = 2 * Hkv * D * cache_elem
     uniq = w.kv_tokens_unique()
     logical = w.kv_tokens_logical()
     T = w.total_q
     tables = int(sum(-(-int(L) // bs) for L in w.seq_lens)) * 4
     meta = (2 * w.num_seqs + 1) * 4
     q_out = 2 * T * H * D * 2
-    reshape = T * (2 * Hkv * D * 2) * 2 + T * 8
+    reshape = T * (2 * Hkv * D) * (2 + cache_elem) + T * 8  # read 16-bit rows, write cache rows
     if rope:  # q rotated in place (read + write), positions, one table row per token
         reshape += 2 * T * H * D * 2 + T * 8 + T * D * 4
     kv_bytes = uniq * kv_tok
@@ -191,7 +192,7 @@ def oracle_rate(w, kc, vc, target_s: float, rng, threads: int):
     (KV GB/s, query tokens/s, seconds, requests, threads)."""
     import oracle as oracle_mod
     orc = oracle_mod.default()
-    kv_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    kv_tok = 2 * w.num_kv_heads * w.head_dim * (1 if w.kv_fp8 else 2)
     order = rng.permutation(w.num_seqs)
     done_bytes = done_tok = 0
     used = 0
@@ -204,12 +205,25 @@ def oracle_rate(w, kc, vc, target_s: float, rng, threads: int):
         s = sub_workload(w, take)
         t0 = time.perf_counter()
         orc.attention(s["q"], kc, vc, s["block_tables"], s["seq_lens"], s["query_start_loc"], w.num_heads,
-                      w.scale, num_threads=threads, dtype=w.dtype)
+                      w.scale, num_threads=threads, dtype=w.dtype, k_scale=w.k_scale, v_scale=w.v_scale)
         t_total += time.perf_counter() - t0
         done_bytes += int(s["seq_lens"].astype(np.int64).sum()) * kv_tok
         done_tok += int(s["query_start_loc"][-1])
         n = min(2 * n, 64)
     return done_bytes / t_total / 1e9, done_tok / t_total, t_total, used, threads
+
+
+def scattered_caches(w):
+    """Host copies of the caches after the oracle's scatter of the step's new rows."""
+    import oracle as oracle_mod
+    orc = oracle_mod.default()
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    if w.kv_fp8:
+        orc.reshape_and_cache_fp8(w.key, w.value, kc, vc, w.slot_mapping, w.block_size, w.k_scale, w.v_scale,
+                                  dtype=w.dtype)
+    else:
+        orc.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
+    return kc, vc
 
 
 def host_threads() -> int:
@@ -267,10 +281,10 @@ def run_reference(args, world, rank) -> None:
     kw["dtype"] = args.dtype
     if args.block_size != 16:
         kw["block_size"] = args.block_size
+    if args.kv_dtype:
+        kw["kv_dtype"] = args.kv_dtype
     w = W.by_name(args.workload, seed=args.seed, **kw)
-    kc, vc = w.key_cache.copy(), w.value_cache.copy()
-    orc = oracle_mod.default()
-    orc.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
+    kc, vc = scattered_caches(w)
     threads = host_threads()
     rng = np.random.default_rng(args.seed)
     per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -306,6 +320,8 @@ def workload_text(args) -> str:
         text += f" [block_size {args.block_size}]"
     if getattr(args, "rope", False):
         text += " [rotary embedding fused into the cache scatter]"
+    if getattr(args, "kv_dtype", ""):
+        text += " [8-bit E4M3 KV cache, one scale per cache]"
     return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
 
 
@@ -325,6 +341,8 @@ def run_ours(args, world, rank, local_rank) -> None:
     kw["dtype"] = args.dtype
     if args.block_size != 16:
         kw["block_size"] = args.block_size
+    if args.kv_dtype:
+        kw["kv_dtype"] = args.kv_dtype
     w = W.by_name(args.workload, seed=rank_seed(args.seed, rank), **kw)
     acct = step_accounting(w, rope=args.rope)
     rope = None
@@ -411,7 +429,7 @@ def run_ours(args, world, rank, local_rank) -> None:
 
     peaks = load_peaks()
     kern_achieved = acct["attention_bytes"] / (kern_ms * 1e-3) / 1e9
-    traffic = committed_traffic(args.workload) if args.dtype == "bf16" else None
+    traffic = committed_traffic(args.workload) if args.dtype == "bf16" and not args.kv_dtype else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
@@ -422,7 +440,9 @@ def run_ours(args, world, rank, local_rank) -> None:
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "no flush: KV working set per step is larger than L2",
                    "step": ("pa_rope_reshape_and_cache" if args.rope else "pa_reshape_and_cache")
-                           + " + pa_attention_varlen (plan, split-KV, merge)",
+                           + ("_fp8 + pa_attention_varlen_fp8" if args.kv_dtype else " + pa_attention_varlen")
+                           + " (plan, split-KV, merge)",
+                   "kv_cache": args.kv_dtype or args.dtype,
                    "step_bytes": acct["step_bytes"], "kv_bytes": acct["kv_bytes"],
                    "kv_bytes_logical": acct["kv_bytes_logical"], "flops": acct["flops"]},
         "roofline": {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
@@ -435,10 +455,7 @@ def run_ours(args, world, rank, local_rank) -> None:
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        kc = w.key_cache.copy()
-        vc = w.value_cache.copy()
-        import oracle as oracle_mod
-        oracle_mod.default().reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping, w.block_size)
+        kc, vc = scattered_caches(w)
         r, _, secs, n, threads = oracle_rate(w, kc, vc, args.cpu_seconds, np.random.default_rng(1), host_threads())
         line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": f"{n} request evaluations drawn in random order from the workload's "
@@ -612,6 +629,8 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="element type of q, K/V and out (the metric's workload is bf16)")
+    ap.add_argument("--kv-dtype", choices=["", "fp8_e4m3"], default="",
+                    help="cache element type: empty = the element type of q (16-bit), fp8_e4m3 = 8-bit codes")
     ap.add_argument("--block-size", type=int, choices=[8, 16, 32], default=16,
                     help="tokens per cache block (the configurations are quoted at 16)")
     ap.add_argument("--rope", action="store_true",

@@ -35,6 +35,15 @@
  *     the offending work and set bits in a device status word, which
  *     pa_debug_status() reads; outputs of the offending request are then
  *     undefined.
+ *   - 8-bit caches (LLM-infra reading map, §4.2: the KV cache is stored in
+ *     8 bits, quantised online as it is written and dequantised as attention
+ *     reads it): the *_fp8 calls keep K and V caches of E4M3 codes (sign,
+ *     4-bit exponent with bias 7, 3-bit fraction, no infinities, largest
+ *     finite 448; 0x7F and 0xFF are NaN), one byte per element, with one
+ *     float scale per cache. Writing stores code = E4M3(x / scale): the
+ *     quotient in binary32 (correctly rounded), then rounded to the nearest
+ *     code, ties to even, magnitudes beyond 448 saturating to 448. Reading
+ *     uses code * scale. q, key, value and out stay bf16 or fp16.
  *   - Supported now: head_dim 64 or 128; block_size 8, 16 or 32 (the
  *     reading map, §2.3, sweeps page sizes; the kernels stage K/V 16 keys at a
  *     time); num_heads a multiple of num_kv_heads with group size 1, 2, 4 or 8.
@@ -62,7 +71,9 @@ typedef enum pa_status {
     PA_ERR_CUDA = -8           /* another CUDA runtime call failed */
 } pa_status;
 
-enum { PA_BF16 = 0, PA_FP16 = 1 };
+/* Element types. PA_FP8_E4M3 names 8-bit cache codes (the *_fp8 calls, and
+ * pa_copy_blocks / pa_gather_kv on such caches). */
+enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 };
 
 /* Bits of the device status word (pa_debug_status). */
 enum {
@@ -103,6 +114,23 @@ pa_status pa_reshape_and_cache(const void *key, const void *value,
                                int32_t num_kv_heads, int32_t head_dim,
                                int32_t block_size, int64_t num_blocks,
                                int32_t dtype, void *stream);
+
+/*
+ * reshape_and_cache into 8-bit caches: the same slots and arguments as
+ * pa_reshape_and_cache (key and value are `dtype`, bf16 or fp16), but every
+ * element is stored as the E4M3 code of x / k_scale (keys) or x / v_scale
+ * (values). key_cache, value_cache: (device) uint8 [num_blocks, block_size,
+ * num_kv_heads, head_dim], 16-byte aligned. k_scale and v_scale must be
+ * finite and positive (PA_ERR_DIMS otherwise); a NaN element gives a NaN
+ * code.
+ */
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                   int64_t key_token_stride, int64_t value_token_stride,
+                                   void *key_cache, void *value_cache,
+                                   const int64_t *slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_blocks,
+                                   float k_scale, float v_scale, int32_t dtype, void *stream);
 
 /*
  * Bytes of device workspace pa_attention_varlen needs for these host-side
@@ -170,6 +198,32 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
                               int32_t dtype, void *stream);
 
 /*
+ * Attention over 8-bit caches: the same operation and arguments as
+ * pa_attention_varlen (same workspace size), with key_cache and value_cache
+ * holding E4M3 codes (uint8 [num_blocks, block_size, num_kv_heads, head_dim],
+ * 16-byte aligned) whose values are code * k_scale and code * v_scale:
+ *   out[t][h][:] = round( sum_j softmax_j(scale * q[t][h] . (k_scale * Kc[j]))
+ *                         * (v_scale * Vc[j]) )
+ * q and out are `dtype` (bf16 or fp16). k_scale and v_scale must be finite and
+ * positive (PA_ERR_DIMS otherwise). Each code is widened exactly and the
+ * products accumulate in fp32, as for 16-bit caches.
+ * Supported now for query_len <= 8 / (num_heads / num_kv_heads) per request
+ * (decode tokens and short drafts); a larger max_query_len returns
+ * PA_ERR_UNSUPPORTED.
+ */
+pa_status pa_attention_varlen_fp8(const void *q, int64_t q_token_stride,
+                                  const void *key_cache, const void *value_cache,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, const int32_t *query_start_loc,
+                                  int32_t num_seqs, int32_t total_q_tokens,
+                                  int32_t max_query_len, int32_t max_seq_len,
+                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int64_t num_blocks, float scale,
+                                  float k_scale, float v_scale,
+                                  void *out, void *workspace, size_t workspace_bytes,
+                                  int32_t dtype, void *stream);
+
+/*
  * Rotary position embedding fused with reshape_and_cache (vLLM notes, §LLM
  * 推理全流程 2: a token's position is a rotation angle, with a precomputed
  * cos_sin_cache of shape [max_position, rotary_dim]). For every token t with
@@ -209,7 +263,8 @@ pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void 
  * shared by several requests is copied before one of them writes into it).
  * For each pair i < num_pairs, copy physical block block_mapping[2*i] to
  * physical block block_mapping[2*i + 1] in both caches: all block_size
- * tokens, all KV heads, raw bits (any 16-bit dtype).
+ * tokens, all KV heads, raw bits: dtype PA_BF16 or PA_FP16 for 16-bit caches,
+ * PA_FP8_E4M3 for 8-bit ones (head_dim a multiple of 16 then).
  *   key_cache, value_cache (device): [num_blocks, block_size, num_kv_heads,
  *       head_dim], 16-byte aligned, head_dim a multiple of 8.
  *   block_mapping (device): int64 [num_pairs, 2] = (source, destination).
@@ -225,7 +280,8 @@ pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *bloc
 /*
  * Block-table addressing on its own: copy the seq_len logical K/V rows of one
  * request, read through its block-table row, into contiguous
- * [seq_len, num_kv_heads, head_dim] buffers (device, 16-byte aligned).
+ * [seq_len, num_kv_heads, head_dim] buffers (device, 16-byte aligned), raw
+ * bits of `dtype` (PA_BF16, PA_FP16, or PA_FP8_E4M3 for 8-bit caches).
  * block_table_row is a device pointer to that request's row. Used to check
  * the addressing bit for bit.
  */

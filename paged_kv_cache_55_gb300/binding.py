@@ -17,8 +17,10 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(HERE, "libpagedattn.so")
 
-PA_BF16, PA_FP16 = 0, 1
+PA_BF16, PA_FP16, PA_FP8_E4M3 = 0, 1, 2
 _ELEM_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
+# 8-bit caches are uint8 tensors of E4M3 codes
+_CACHE_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.uint8: PA_FP8_E4M3}
 STATUS = {
     0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_DIMS", -3: "PA_ERR_UNSUPPORTED", -4: "PA_ERR_ALIGN",
     -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_LAUNCH", -7: "PA_ERR_DEVICE_BOUNDS", -8: "PA_ERR_CUDA",
@@ -54,6 +56,11 @@ SIGNATURES = {
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
+    "pa_reshape_and_cache_fp8": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, ctypes.c_float,
+                                  ctypes.c_float, _I32, _P], ctypes.c_int),
+    "pa_attention_varlen_fp8": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                 _I32, _I64, ctypes.c_float, ctypes.c_float, ctypes.c_float, _P, _P, _SZ, _I32, _P],
+                                ctypes.c_int),
 }
 
 # Size of the library's built-in scratch array used by pa_attention_varlen_static.
@@ -111,6 +118,16 @@ def _elem_code(*named) -> int:
     return _ELEM_CODES[first.dtype]
 
 
+def _cache_code(*named) -> int:
+    """The C dtype of cache tensors that share one type: bf16, fp16, or uint8 (E4M3 codes)."""
+    first = named[0][0]
+    if not isinstance(first, torch.Tensor) or first.dtype not in _CACHE_CODES:
+        raise TypeError(f"{named[0][1]} must be a bfloat16, float16 or uint8 CUDA tensor")
+    for t, n in named:
+        _need(t, n, first.dtype)
+    return _CACHE_CODES[first.dtype]
+
+
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
                          value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
     """key/value [T, Hkv, D] (token stride free), caches [NB, bs, Hkv, D], all bf16 or all fp16;
@@ -126,6 +143,27 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torc
     _check(_lib().pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0),
                                        key_cache.data_ptr(), value_cache.data_ptr(), slot_mapping.data_ptr(),
                                        T, hkv, d, bs, nb, dt, _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                             value_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                             stream=None) -> None:
+    """Quantising scatter: key/value [T, Hkv, D] bf16 or fp16 (token stride free), caches uint8
+    [NB, bs, Hkv, D] of E4M3 codes (code = E4M3(x / scale)); slots int64 [T]."""
+    dt = _elem_code((key, "key"), (value, "value"))
+    _need(key_cache, "key_cache", torch.uint8)
+    _need(value_cache, "value_cache", torch.uint8)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T, hkv, d = key.shape
+    if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
+        raise ValueError("each token row of key/value must be [Hkv, D] contiguous")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("caches and slot_mapping must be contiguous")
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    _check(_lib().pa_reshape_and_cache_fp8(key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0),
+                                           key_cache.data_ptr(), value_cache.data_ptr(), slot_mapping.data_ptr(),
+                                           T, hkv, d, bs, nb, float(k_scale), float(v_scale), dt,
+                                           _stream(stream)), "pa_reshape_and_cache_fp8")
 
 
 def pa_attention_workspace_size(num_seqs: int, total_q_tokens: int, max_query_len: int, max_seq_len: int,
@@ -168,6 +206,34 @@ def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: t
                                       nb, float(scale), out.data_ptr(), workspace.data_ptr(),
                                       workspace.numel() * workspace.element_size(), dt, _stream(stream)),
            "pa_attention_varlen")
+
+
+def pa_attention_varlen_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                            max_query_len: int, max_seq_len: int, scale: float, k_scale: float, v_scale: float,
+                            out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """pa_attention_varlen over 8-bit caches: caches uint8 [NB, bs, Hkv, D] of E4M3 codes whose values
+    are code * k_scale and code * v_scale; q and out bf16 or fp16."""
+    dt = _elem_code((q, "q"), (out, "out"))
+    _need(key_cache, "key_cache", torch.uint8)
+    _need(value_cache, "value_cache", torch.uint8)
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
+        _need(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if not out.is_contiguous() or not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("out and the caches must be contiguous")
+    T, H, D = q.shape
+    if q.stride(2) != 1 or q.stride(1) != D:
+        raise ValueError("each token row of q must be [H, D] contiguous")
+    nb, bs, hkv, _ = key_cache.shape
+    B = seq_lens.shape[0]
+    _check(_lib().pa_attention_varlen_fp8(q.data_ptr(), q.stride(0), key_cache.data_ptr(), value_cache.data_ptr(),
+                                          block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                                          query_start_loc.data_ptr(), B, T, max_query_len, max_seq_len, H, hkv, D,
+                                          bs, nb, float(scale), float(k_scale), float(v_scale), out.data_ptr(),
+                                          workspace.data_ptr(), workspace.numel() * workspace.element_size(), dt,
+                                          _stream(stream)), "pa_attention_varlen_fp8")
 
 
 def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
@@ -217,8 +283,9 @@ def pa_rope_reshape_and_cache(q: torch.Tensor, key: torch.Tensor, value: torch.T
 
 def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,
                    stream=None) -> None:
-    """Copy-on-write block copy: block_mapping int64 [n, 2] (source, destination) on the device."""
-    dt = _elem_code((key_cache, "key_cache"), (value_cache, "value_cache"))
+    """Copy-on-write block copy: block_mapping int64 [n, 2] (source, destination) on the device;
+    caches bf16, fp16 or uint8 (8-bit codes)."""
+    dt = _cache_code((key_cache, "key_cache"), (value_cache, "value_cache"))
     _need(block_mapping, "block_mapping", torch.int64)
     if not (key_cache.is_contiguous() and value_cache.is_contiguous() and block_mapping.is_contiguous()):
         raise ValueError("caches and block_mapping must be contiguous")
@@ -231,8 +298,8 @@ def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_map
 
 def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor,
                  seq_len: int, key_out: torch.Tensor, value_out: torch.Tensor, stream=None) -> None:
-    dt = _elem_code((key_cache, "key_cache"), (value_cache, "value_cache"), (key_out, "key_out"),
-                    (value_out, "value_out"))
+    dt = _cache_code((key_cache, "key_cache"), (value_cache, "value_cache"), (key_out, "key_out"),
+                     (value_out, "value_out"))
     nb, bs, hkv, d = key_cache.shape
     _check(_lib().pa_gather_kv(key_cache.data_ptr(), value_cache.data_ptr(), block_table_row.data_ptr(), seq_len,
                                hkv, d, bs, nb, key_out.data_ptr(), value_out.data_ptr(), dt,

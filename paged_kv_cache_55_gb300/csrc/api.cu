@@ -53,6 +53,13 @@ DeviceState *device_state() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+bool valid_cache_scale(float s) { return std::isfinite(s) && s > 0.0f; }
+
+// Bytes of one cache element: 2 for the 16-bit types, 1 for E4M3 codes; 0 if unknown.
+int cache_elem_bytes(int32_t dtype) {
+  return (dtype == PA_BF16 || dtype == PA_FP16) ? 2 : (dtype == PA_FP8_E4M3 ? 1 : 0);
+}
+
 bool supported_dims(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
   if (head_dim != 64 && head_dim != 128) return false;
   if (block_size != 8 && block_size != 16 && block_size != 32) return false;
@@ -120,6 +127,36 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
   return PA_OK;
 }
 
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t key_token_stride,
+                                   int64_t value_token_stride, void *key_cache, void *value_cache,
+                                   const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int64_t num_blocks, float k_scale,
+                                   float v_scale, int32_t dtype, void *stream) {
+  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+    return PA_ERR_DIMS;
+  if (!valid_cache_scale(k_scale) || !valid_cache_scale(v_scale)) return PA_ERR_DIMS;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row) return PA_ERR_DIMS;
+  if (key_token_stride % 8 || value_token_stride % 8) return PA_ERR_ALIGN;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_ALIGN;
+  DeviceState *ds = device_state();
+  if (!ds) return PA_ERR_CUDA;
+  cudaError_t err = pa::launch_reshape_and_cache_fp8(
+      key, value, key_token_stride, value_token_stride, key_cache, value_cache, slot_mapping, num_tokens,
+      static_cast<int32_t>(row), num_blocks * block_size, k_scale, v_scale, dtype, ds->status, ds->sm_count,
+      static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
 size_t pa_attention_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
                                    int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t block_size) {
@@ -140,16 +177,22 @@ pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len, int32_t 
   return PA_OK;
 }
 
-pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void *key_cache,
-                              const void *value_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
-                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
-                              int32_t total_q_tokens, int32_t max_query_len, int32_t max_seq_len,
-                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                              int64_t num_blocks, float scale, void *out, void *workspace,
-                              size_t workspace_bytes, int32_t dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// pa_attention_varlen and pa_attention_varlen_fp8: validation, then the launch.
+pa_status attention_call(const void *q, int64_t q_token_stride, const void *key_cache, const void *value_cache,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                         const int32_t *query_start_loc, int32_t num_seqs, int32_t total_q_tokens,
+                         int32_t max_query_len, int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale, bool kv_fp8,
+                         float k_scale, float v_scale, void *out, void *workspace, size_t workspace_bytes,
+                         int32_t dtype, void *stream) {
   cudaEvent_t ev_start = t_ev_start, ev_stop = t_ev_stop;
   t_ev_start = t_ev_stop = nullptr;
   if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (kv_fp8 && (!valid_cache_scale(k_scale) || !valid_cache_scale(v_scale))) return PA_ERR_DIMS;
   if (num_seqs < 0 || total_q_tokens < 0 || max_query_len < 0 || max_seq_len < max_query_len ||
       max_blocks_per_seq < 0 || num_blocks < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
     return PA_ERR_DIMS;
@@ -158,6 +201,8 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
     return PA_ERR_UNSUPPORTED;
   }
   if (!std::isfinite(scale)) return PA_ERR_DIMS;
+  // 8-bit caches: decode tokens and short drafts (query_len <= 8 / group size) only, for now
+  if (kv_fp8 && max_query_len > 8 / (num_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
   if (max_query_len == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_DIMS;
   if (num_blocks > INT32_MAX / block_size) return PA_ERR_UNSUPPORTED;  // cache rows are int32 TMA coordinates
@@ -197,6 +242,9 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   a.num_blocks = num_blocks;
   a.scale = scale;
   a.dtype = dtype;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = kv_fp8 ? k_scale : 1.0f;
+  a.v_scale = kv_fp8 ? v_scale : 1.0f;
   a.out = out;
   a.workspace = workspace;
   a.status = ds->status;
@@ -208,6 +256,36 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void 
   g_launches.fetch_add(static_cast<uint64_t>(launched));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_attention_varlen(const void *q, int64_t q_token_stride, const void *key_cache,
+                              const void *value_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                              int32_t total_q_tokens, int32_t max_query_len, int32_t max_seq_len,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, float scale, void *out, void *workspace,
+                              size_t workspace_bytes, int32_t dtype, void *stream) {
+  return attention_call(q, q_token_stride, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, total_q_tokens, max_query_len, max_seq_len, num_heads,
+                        num_kv_heads, head_dim, block_size, num_blocks, scale, false, 1.0f, 1.0f, out, workspace,
+                        workspace_bytes, dtype, stream);
+}
+
+pa_status pa_attention_varlen_fp8(const void *q, int64_t q_token_stride, const void *key_cache,
+                                  const void *value_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                                  int32_t total_q_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, float scale, float k_scale, float v_scale, void *out,
+                                  void *workspace, size_t workspace_bytes, int32_t dtype, void *stream) {
+  return attention_call(q, q_token_stride, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, total_q_tokens, max_query_len, max_seq_len, num_heads,
+                        num_kv_heads, head_dim, block_size, num_blocks, scale, true, k_scale, v_scale, out,
+                        workspace, workspace_bytes, dtype, stream);
 }
 
 pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void *key, const void *value,
@@ -248,16 +326,17 @@ pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void 
 pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping, int32_t num_pairs,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
                          int32_t dtype, void *stream) {
-  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  const int esize = cache_elem_bytes(dtype);
+  if (!esize) return PA_ERR_UNSUPPORTED;
   if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0) return PA_ERR_DIMS;
-  if (head_dim % 8) return PA_ERR_ALIGN;  // a block is a whole number of 16-byte vectors
+  if ((head_dim * esize) % 16) return PA_ERR_ALIGN;  // a block is a whole number of 16-byte vectors
   if (num_pairs == 0) return PA_OK;
   if (!key_cache || !value_cache || !block_mapping) return PA_ERR_NULL;
   if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(block_mapping, 8)) return PA_ERR_ALIGN;
   DeviceState *ds = device_state();
   if (!ds) return PA_ERR_CUDA;
-  const int64_t block_elems = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
-  cudaError_t err = pa::launch_copy_blocks(key_cache, value_cache, block_mapping, num_pairs, block_elems, num_blocks,
+  const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * esize;
+  cudaError_t err = pa::launch_copy_blocks(key_cache, value_cache, block_mapping, num_pairs, block_bytes, num_blocks,
                                            ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);
@@ -267,7 +346,8 @@ pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *bloc
 pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int32_t *block_table_row,
                        int32_t seq_len, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int64_t num_blocks, void *key_out, void *value_out, int32_t dtype, void *stream) {
-  if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  const int esize = cache_elem_bytes(dtype);
+  if (!esize) return PA_ERR_UNSUPPORTED;
   if (seq_len < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_DIMS;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
@@ -279,9 +359,8 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   DeviceState *ds = device_state();
   if (!ds) return PA_ERR_CUDA;
   cudaError_t err = pa::launch_gather_kv(key_cache, value_cache, block_table_row, seq_len,
-                                         num_kv_heads * head_dim, block_size, num_blocks, key_out, value_out,
-                                         ds->status,
-                                         ds->sm_count, static_cast<cudaStream_t>(stream));
+                                         num_kv_heads * head_dim * esize, block_size, num_blocks, key_out,
+                                         value_out, ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);
   return PA_OK;

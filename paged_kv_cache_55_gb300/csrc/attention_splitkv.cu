@@ -90,7 +90,8 @@ struct AttnParams {
   int32_t num_heads;
   int32_t num_kv_heads;
   int64_t num_blocks;
-  float scale_log2;
+  float scale_log2;  // softmax scale (times the K cache scale for 8-bit caches) * log2(e)
+  float out_scale;   // 1, or the V cache scale for 8-bit caches
   bf16 *out;
   const int4 *items;
   const int32_t *item_count;
@@ -495,8 +496,11 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   return U;
 }
 
+template <int D, bool KV8>
+struct TileGeom;
+// 16-bit caches: a 16-key tile is D / 64 boxes of 16 rows x 128 bytes (128-byte swizzle).
 template <int D>
-struct TileGeom {
+struct TileGeom<D, false> {
   static constexpr int HALVES = D / 64;                // 64-element (128-byte) swizzle atoms per row
   static constexpr int HALF_BYTES = kTileKeys * 128;  // 16 rows x 128 B
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
@@ -506,12 +510,25 @@ struct TileGeom {
     return (c >> 3) * HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
   }
 };
+// 8-bit caches: a 16-key tile is one box of 16 rows x D codes, with 128-byte
+// swizzle at D = 128 (16-byte chunk c of row r at c ^ (r % 8)) and 64-byte
+// swizzle at D = 64 (chunk c of row r at c ^ (r / 2 % 4)); either way eight
+// consecutive rows read at one chunk hit eight different bank groups.
+template <int D>
+struct TileGeom<D, true> {
+  static_assert(D == 64 || D == 128, "8-bit tiles are one swizzle span wide");
+  static constexpr int TILE_BYTES = kTileKeys * D;
+  static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
+  static __device__ __forceinline__ uint32_t off(int r, int c) {
+    return D == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
+  }
+};
 
-template <int D, int G, int NWARPS, typename E>
+template <int D, int G, int NWARPS, typename E, bool KV8>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     splitkv_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                              const AttnParams p) {
-  using T = TileGeom<D>;
+  using T = TileGeom<D, KV8>;
   constexpr int S = kSmemBudget / (NWARPS * T::SLOT_BYTES);  // ring slots per warp
   static_assert(S >= 2, "ring needs at least two slots");
   constexpr int MT = D / 16;
@@ -560,10 +577,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           else
             z = (phys << p.block_shift) + (key & (bs - 1));
         }
+        if constexpr (KV8) {
+          tma_load_3d(dst + j * box_rows * D, &kmap, bar, 0, U.kvh, z);
+          tma_load_3d(dst + T::TILE_BYTES + j * box_rows * D, &vmap, bar, 0, U.kvh, z);
+        } else {
 #pragma unroll
-        for (int h = 0; h < T::HALVES; ++h) {
-          tma_load_3d(dst + h * T::HALF_BYTES + j * box_rows * 128, &kmap, bar, h * 64, U.kvh, z);
-          tma_load_3d(dst + T::TILE_BYTES + h * T::HALF_BYTES + j * box_rows * 128, &vmap, bar, h * 64, U.kvh, z);
+          for (int h = 0; h < T::HALVES; ++h) {
+            tma_load_3d(dst + h * T::HALF_BYTES + j * box_rows * 128, &kmap, bar, h * 64, U.kvh, z);
+            tma_load_3d(dst + T::TILE_BYTES + h * T::HALF_BYTES + j * box_rows * 128, &vmap, bar, h * 64, U.kvh,
+                        z);
+          }
         }
       }
     }
@@ -612,11 +635,25 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const int n = lane >> 2, qi = n / G, g = n % G;
       const bool ok = qi < cur.nrows;
       const bf16 *qp = p.q + static_cast<int64_t>(cur.row0 + (ok ? qi : 0)) * p.q_stride +
-                       static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
+                       static_cast<int64_t>(cur.kvh * G + g) * D;
+      if constexpr (KV8) {
+        // k step kk pairs d = 16kk + 4(lane % 4) + (0, 2) and (1, 3): the order
+        // in which the 8-bit K fragments below hold d
+        qp += 4 * (lane & 3);
 #pragma unroll
-      for (int kk = 0; kk < MT; ++kk) {
-        qf[kk][0] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
-        qf[kk][1] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 8)) : 0u;
+        for (int kk = 0; kk < MT; ++kk) {
+          const uint32_t x = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
+          const uint32_t y = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 2)) : 0u;
+          qf[kk][0] = __byte_perm(x, y, 0x5410);
+          qf[kk][1] = __byte_perm(x, y, 0x7632);
+        }
+      } else {
+        qp += 2 * (lane & 3);
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk) {
+          qf[kk][0] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
+          qf[kk][1] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 8)) : 0u;
+        }
       }
     }
     int lim[2];  // keys j < lim[e] are visible to accumulator column 2*(lane%4)+e
@@ -644,9 +681,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const int valid_rows = min(kTileKeys, cur.kv_end - kb * kTileKeys);
       if (valid_rows < kTileKeys) {
         // rows past the request's last key may hold anything (even NaN): zero them in V
-        const int n = (kTileKeys - valid_rows) * (D / 8);
+        constexpr int CPR = KV8 ? D / 16 : D / 8;  // 16-byte chunks per row
+        const int n = (kTileKeys - valid_rows) * CPR;
         for (int i = lane; i < n; i += 32) {
-          const int r = valid_rows + i / (D / 8), c = i % (D / 8);
+          const int r = valid_rows + i / CPR, c = i % CPR;
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + T::off(r, c)), "r"(0u) : "memory");
         }
         fence_proxy_async_smem();  // order these generic writes before the slot's next TMA fill
@@ -655,14 +693,31 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 
       // S^T = K Q^T over D, two independent accumulator chains
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (KV8) {
+        // one x4 load = 16 keys x 32 codes: per lane 4 consecutive d of keys
+        // lane/4 and lane/4 + 8 in each of two 16-d chunks, widened exactly
+        // into the A fragments of two k steps (d paired as q is above)
 #pragma unroll
-      for (int kk = 0; kk < MT; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(kt + T::off(arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
-        if (kk & 1)
-          E::mma(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-        else
-          E::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
+          ldsm_x4(kt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
+          E::from_e4m3x4(r0, l0, h0);
+          E::from_e4m3x4(r1, l1, h1);
+          E::mma(sa, l0, l1, h0, h1, qf[2 * j][0], qf[2 * j][1]);
+          E::from_e4m3x4(r2, l0, h0);
+          E::from_e4m3x4(r3, l1, h1);
+          E::mma(sb, l0, l1, h0, h1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kt + T::off(arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+          if (kk & 1)
+            E::mma(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+          else
+            E::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        }
       }
       const int t0 = kb * kTileKeys + (lane >> 2), t1 = t0 + 8;
       const float x0 = t0 < lim[0] ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
@@ -698,12 +753,32 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const uint32_t l23 = E::pack(p2 - E::lo(h23), p3 - E::hi(h23));
       const uint32_t b0 = movmatrix_t(h01), b1 = movmatrix_t(h23);
       const uint32_t c0 = movmatrix_t(l01), c1 = movmatrix_t(l23);
+      if constexpr (KV8) {
+        // transposed x4 load of 16 keys x 32 codes: per lane keys (2(lane%4),
+        // +1) (+8) at d = 2(lane/4) and 2(lane/4) + 1 of each 16-d chunk. Row
+        // lane/4 of m tile mt holds d = 16mt + 2(lane/4), row lane/4 + 8 holds
+        // d = 16mt + 2(lane/4) + 1; the epilogue puts d back in order.
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
-        E::mma(o[mt], a0, a1, a2, a3, b0, b1);
-        E::mma(o[mt], a0, a1, a2, a3, c0, c1);
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
+          ldsm_x4_t(vt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
+          E::from_e4m3x4(r0, l0, h0);
+          E::from_e4m3x4(r1, l1, h1);
+          E::mma(o[2 * j], l0, h0, l1, h1, b0, b1);
+          E::mma(o[2 * j], l0, h0, l1, h1, c0, c1);
+          E::from_e4m3x4(r2, l0, h0);
+          E::from_e4m3x4(r3, l1, h1);
+          E::mma(o[2 * j + 1], l0, h0, l1, h1, b0, b1);
+          E::mma(o[2 * j + 1], l0, h0, l1, h1, c0, c1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+          E::mma(o[mt], a0, a1, a2, a3, b0, b1);
+          E::mma(o[mt], a0, a1, a2, a3, c0, c1);
+        }
       }
       __syncwarp();  // every lane is done with this slot before it is refilled
       ++consumed;
@@ -716,20 +791,26 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
         l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
       }
-      const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
-      const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+      const float inv0 = l[0] > 0.f ? p.out_scale / l[0] : 0.f;
+      const float inv1 = l[1] > 0.f ? p.out_scale / l[1] : 0.f;
       if (cur.part < 0) {
         // transpose the bf16 result so each lane owns two consecutive d of one column
         const int col = lane >> 2, qi = col / G, g = col % G;
         bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (qi < cur.nrows ? qi : 0)) * p.num_heads * D +
-                    static_cast<int64_t>(cur.kvh * G + g) * D + 2 * (lane & 3);
+                    static_cast<int64_t>(cur.kvh * G + g) * D;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const uint32_t lo8 = movmatrix_t(E::pack(o[mt][0] * inv0, o[mt][1] * inv1));
           const uint32_t hi8 = movmatrix_t(E::pack(o[mt][2] * inv0, o[mt][3] * inv1));
           if (qi < cur.nrows) {
-            *reinterpret_cast<uint32_t *>(dst + 16 * mt) = lo8;
-            *reinterpret_cast<uint32_t *>(dst + 16 * mt + 8) = hi8;
+            if constexpr (KV8) {
+              // lo8 holds d = 16mt + 4(lane%4) + (0, 2), hi8 d + (1, 3)
+              *reinterpret_cast<uint2 *>(dst + 16 * mt + 4 * (lane & 3)) =
+                  make_uint2(__byte_perm(lo8, hi8, 0x5410), __byte_perm(lo8, hi8, 0x7632));
+            } else {
+              *reinterpret_cast<uint32_t *>(dst + 16 * mt + 2 * (lane & 3)) = lo8;
+              *reinterpret_cast<uint32_t *>(dst + 16 * mt + 2 * (lane & 3) + 8) = hi8;
+            }
           }
         }
       } else {
@@ -739,11 +820,18 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           const int col = 2 * (lane & 3) + e;
           if (col / G < cur.nrows) {
             const float inv = e ? inv1 : inv0;
-            float *dst = p.part_o + (base + col) * D + (lane >> 2);
+            if constexpr (KV8) {
+              float *dst = p.part_o + (base + col) * D + 2 * (lane >> 2);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              dst[16 * mt] = o[mt][e] * inv;
-              dst[16 * mt + 8] = o[mt][2 + e] * inv;
+              for (int mt = 0; mt < MT; ++mt)
+                *reinterpret_cast<float2 *>(dst + 16 * mt) = make_float2(o[mt][e] * inv, o[mt][2 + e] * inv);
+            } else {
+              float *dst = p.part_o + (base + col) * D + (lane >> 2);
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                dst[16 * mt] = o[mt][e] * inv;
+                dst[16 * mt + 8] = o[mt][2 + e] * inv;
+              }
             }
             if (lane < 4) {
               const float lc = e ? l[1] : l[0], mc = e ? m[1] : m[0];
@@ -838,26 +926,34 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 3-D view of one cache, [num_blocks * 16 rows][Hkv][D], with a box of
 // 16 rows x 1 head x 64 elements (128 bytes, 128-byte swizzle).
+// 8-bit caches: elements of one byte and a box of 16 rows x 1 head x D codes
+// (128-byte swizzle at D = 128, 64-byte at D = 64).
 static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t block_size, int32_t dtype) {
+                             int32_t head_dim, int32_t block_size, int32_t dtype, bool kv8) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
+  const cuuint64_t esize = kv8 ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
                               static_cast<cuuint64_t>(num_blocks) * block_size};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * esize,
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * esize};
   // one box per 16-key tile of a 16- or 32-token block, two per tile of 8-token blocks
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size < kTileKeys ? block_size : kTileKeys)};
+  const cuuint32_t rows = static_cast<cuuint32_t>(block_size < kTileKeys ? block_size : kTileKeys);
+  const cuuint32_t box[3] = {kv8 ? static_cast<cuuint32_t>(head_dim) : 64u, 1, rows};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType type = dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType type = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : (dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  const CUtensorMapSwizzle swz =
+      kv8 && head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return encode(map, type, 3, const_cast<void *>(cache), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 constexpr int kAttnWarps = 8;
 
-template <int D, int G, typename E>
+template <int D, int G, typename E, bool KV8>
 static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, cudaStream_t stream,
                                 int *launched) {
   char *ws = static_cast<char *>(a.workspace);
@@ -886,8 +982,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype) ||
-      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype))
+  if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype, KV8) ||
+      !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype, KV8))
     return cudaErrorInvalidValue;
 
   cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
@@ -904,7 +1000,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.num_heads = a.num_heads;
   ap.num_kv_heads = a.num_kv_heads;
   ap.num_blocks = a.num_blocks;
-  ap.scale_log2 = a.scale * 1.4426950408889634f;
+  ap.scale_log2 = (KV8 ? a.scale * a.k_scale : a.scale) * 1.4426950408889634f;
+  ap.out_scale = KV8 ? a.v_scale : 1.0f;
   ap.out = static_cast<bf16 *>(a.out);
   ap.items = pp.items;
   ap.item_count = pp.item_count;
@@ -918,7 +1015,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
-  auto kern = splitkv_attention_kernel<D, G, kAttnWarps, E>;
+  auto kern = splitkv_attention_kernel<D, G, kAttnWarps, E, KV8>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -935,6 +1032,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
 
   if (a.max_query_len > w.rows_per_item) {  // some request may be a prefill chunk
+    if (KV8) return cudaErrorNotSupported;    // rejected by the caller
     TileParams tp;
     tp.q = ap.q;
     tp.q_stride = a.q_stride;
@@ -985,9 +1083,13 @@ cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *laun
     return cudaErrorInvalidValue;
   const int G = a.num_heads / a.num_kv_heads;
 #define PA_DISPATCH(DD, GG)                                                                     \
-  if (a.head_dim == DD && G == GG)                                                              \
-    return a.dtype == PA_FP16 ? launch_typed<DD, GG, ElemFp16>(a, w, stream, launched)          \
-                              : launch_typed<DD, GG, ElemBf16>(a, w, stream, launched);
+  if (a.head_dim == DD && G == GG) {                                                            \
+    if (a.kv_fp8)                                                                               \
+      return a.dtype == PA_FP16 ? launch_typed<DD, GG, ElemFp16, true>(a, w, stream, launched)  \
+                                : launch_typed<DD, GG, ElemBf16, true>(a, w, stream, launched); \
+    return a.dtype == PA_FP16 ? launch_typed<DD, GG, ElemFp16, false>(a, w, stream, launched)   \
+                              : launch_typed<DD, GG, ElemBf16, false>(a, w, stream, launched);  \
+  }
   PA_DISPATCH(128, 1) PA_DISPATCH(128, 2) PA_DISPATCH(128, 4) PA_DISPATCH(128, 8)
   PA_DISPATCH(64, 1) PA_DISPATCH(64, 2) PA_DISPATCH(64, 4) PA_DISPATCH(64, 8)
 #undef PA_DISPATCH

@@ -41,6 +41,51 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
   }
 }
 
+// 8-bit caches (LLM-infra reading map, §4.2: the cache is quantised online
+// as it is written): the same slots, each element stored as the E4M3 code of
+// its binary32 quotient by the cache's scale. One thread turns 16 elements
+// (two 16-byte loads) into one 16-byte vector of codes.
+template <typename E>
+__device__ __forceinline__ uint4 quantize16(uint4 a, uint4 b, float scale) {
+  const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t p0 = e4m3x2_from_f32(__fdiv_rn(E::lo(x[2 * k]), scale), __fdiv_rn(E::hi(x[2 * k]), scale));
+    const uint32_t p1 =
+        e4m3x2_from_f32(__fdiv_rn(E::lo(x[2 * k + 1]), scale), __fdiv_rn(E::hi(x[2 * k + 1]), scale));
+    c[k] = p0 | (p1 << 16);
+  }
+  return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
+    const uint4 *__restrict__ key, const uint4 *__restrict__ value, int64_t key_stride16,
+    int64_t value_stride16, uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+    const int64_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t row16, int64_t num_slots, float k_scale,
+    float v_scale, unsigned int *status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  // row16: 16-element groups per token row (one 16-byte vector of codes, two of elements)
+  const int64_t total = static_cast<int64_t>(num_tokens) * row16;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t t = static_cast<int32_t>(i / row16);
+    const int32_t c = static_cast<int32_t>(i - static_cast<int64_t>(t) * row16);
+    const int64_t slot = ld_cg(reinterpret_cast<const long long *>(slot_mapping) + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (c == 0) flag_error(status, PA_FLAG_SLOT_RANGE);
+      continue;
+    }
+    const uint4 *kp = key + t * key_stride16 + 2 * c;
+    const uint4 *vp = value + t * value_stride16 + 2 * c;
+    key_cache[slot * row16 + c] = quantize16<E>(ld_cg(kp), ld_cg(kp + 1), k_scale);
+    value_cache[slot * row16 + c] = quantize16<E>(ld_cg(vp), ld_cg(vp + 1), v_scale);
+  }
+}
+
 // Logical row j of one request -> contiguous output row j.
 __global__ void __launch_bounds__(256) gather_kv_kernel(
     const uint4 *__restrict__ key_cache, const uint4 *__restrict__ value_cache,
@@ -260,15 +305,29 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                     row16, num_slots, status);
 }
 
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, int64_t key_stride,
+                                         int64_t value_stride, void *key_cache, void *value_cache,
+                                         const int64_t *slot_mapping, int32_t num_tokens, int32_t row_elems,
+                                         int64_t num_slots, float k_scale, float v_scale, int32_t dtype,
+                                         unsigned int *status, int sm_count, cudaStream_t stream) {
+  const int32_t row16 = row_elems / 16;
+  const int grid = grid_for(static_cast<int64_t>(num_tokens) * row16, 256, sm_count);
+  auto kern = dtype == PA_FP16 ? reshape_and_cache_fp8_kernel<ElemFp16> : reshape_and_cache_fp8_kernel<ElemBf16>;
+  return launch_pdl(kern, dim3(grid), dim3(256), 0, stream, static_cast<const uint4 *>(key),
+                    static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,
+                    static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, num_tokens,
+                    row16, num_slots, k_scale, v_scale, status);
+}
+
 cudaError_t launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *mapping, int32_t num_pairs,
-                               int64_t block_elems, int64_t num_blocks, unsigned int *status, int sm_count,
+                               int64_t block_bytes, int64_t num_blocks, unsigned int *status, int sm_count,
                                cudaStream_t stream) {
   int64_t grid = static_cast<int64_t>(sm_count) * 4;  // 4 CTAs of 256 threads per SM
   if (grid > num_pairs) grid = num_pairs;
   if (grid < 1) grid = 1;
   return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
                     static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), mapping, num_pairs,
-                    block_elems / 8, num_blocks, status);
+                    block_bytes / 16, num_blocks, status);
 }
 
 cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void *key, const void *value,
@@ -298,9 +357,9 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
 }
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
-                             int32_t seq_len, int32_t row_elems, int32_t block_size, int64_t num_blocks, void *key_out,
+                             int32_t seq_len, int32_t row_bytes, int32_t block_size, int64_t num_blocks, void *key_out,
                              void *value_out, unsigned int *status, int sm_count, cudaStream_t stream) {
-  const int32_t row16 = row_elems / 8;
+  const int32_t row16 = row_bytes / 16;
   const int grid = grid_for(static_cast<int64_t>(seq_len) * row16, 256, sm_count);
   gather_kv_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(key_cache),
                                              static_cast<const uint4 *>(value_cache), table_row, seq_len,

@@ -314,8 +314,35 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // type; a type supplies the tensor-core operand type, the packing of two
 // floats into a pair (round to nearest even) and the exact widening of a
 // pair's halves.
+// ---------------------------------------------------------------------------
+// 8-bit E4M3 cache codes (sign, 4-bit exponent with bias 7, 3-bit fraction;
+// exponent 0 holds the subnormals fraction * 2^-9; no infinities; largest
+// finite 448). A cache stores code = E4M3(x / scale), the quotient taken in
+// binary32 and rounded to nearest even with saturation; a reader uses
+// code * scale. A 32-bit word holds four codes c0..c3 (c0 in the low byte).
+// ---------------------------------------------------------------------------
+
+// Two binary32 values -> two codes in one 16-bit value (lo in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 struct ElemBf16 {
   static constexpr uint32_t kUmmaFormat = 1;  // tcgen05 kind::f16 A/B format
+  // Codes c0..c3 of w -> two bf16 pairs, lo = (c0, c2) and hi = (c1, c3),
+  // exactly. Shifting a code's exponent and fraction bits into bf16's low
+  // exponent bits gives the code's value times 2^(7 - 127) for every code,
+  // subnormals included (bf16 subnormals then); one paired multiply by 2^120,
+  // exact as every product is representable, restores the value.
+  static __device__ __forceinline__ void from_e4m3x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t a = ((w << 8) & 0x80008000u) | ((w << 4) & 0x07F007F0u);
+    const uint32_t b = (w & 0x80008000u) | ((w >> 4) & 0x07F007F0u);
+    const uint32_t k = 0x7B807B80u;  // (2^120, 2^120)
+    asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(a), "r"(k));
+    asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(k));
+  }
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
   static __device__ __forceinline__ float lo(uint32_t v) { return bf16_lo(v); }
   static __device__ __forceinline__ float hi(uint32_t v) { return bf16_hi(v); }
@@ -326,6 +353,15 @@ struct ElemBf16 {
 };
 struct ElemFp16 {
   static constexpr uint32_t kUmmaFormat = 0;
+  // Codes c0..c3 of w -> fp16 pairs lo = (c0, c2), hi = (c1, c3): the bytes
+  // are regrouped, then each pair is widened by the hardware conversion
+  // (exact: every E4M3 value is an fp16 value).
+  static __device__ __forceinline__ void from_e4m3x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t p = __byte_perm(w, 0u, 0x3120);  // bytes (c0, c2, c1, c3) from low to high
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(p));
+  }
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

@@ -14,8 +14,15 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      int64_t num_slots, unsigned int *status, int sm_count,
                                      cudaStream_t stream);
 
+// 8-bit caches: elements of `dtype` in, E4M3 codes of x / scale out.
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, int64_t key_stride,
+                                         int64_t value_stride, void *key_cache, void *value_cache,
+                                         const int64_t *slot_mapping, int32_t num_tokens, int32_t row_elems,
+                                         int64_t num_slots, float k_scale, float v_scale, int32_t dtype,
+                                         unsigned int *status, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *mapping, int32_t num_pairs,
-                               int64_t block_elems, int64_t num_blocks, unsigned int *status, int sm_count,
+                               int64_t block_bytes, int64_t num_blocks, unsigned int *status, int sm_count,
                                cudaStream_t stream);
 
 cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void *key, const void *value,
@@ -27,7 +34,7 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
                                           int sm_count, cudaStream_t stream);
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
-                             int32_t seq_len, int32_t row_elems, int32_t block_size, int64_t num_blocks, void *key_out,
+                             int32_t seq_len, int32_t row_bytes, int32_t block_size, int64_t num_blocks, void *key_out,
                              void *value_out, unsigned int *status, int sm_count, cudaStream_t stream);
 
 // Byte offsets of the pieces of the attention workspace, and the split plan.
@@ -54,7 +61,9 @@ struct AttnLaunch {
   int32_t num_heads, num_kv_heads, head_dim, block_size;
   int64_t num_blocks;
   float scale;
-  int32_t dtype;  // PA_BF16 or PA_FP16 (q, caches and out alike)
+  int32_t dtype;  // PA_BF16 or PA_FP16 (q and out; the caches too unless kv_fp8)
+  bool kv_fp8;    // caches hold E4M3 codes: K = code * k_scale, V = code * v_scale
+  float k_scale, v_scale;
   void *out;
   void *workspace;
   unsigned int *status;

@@ -42,8 +42,13 @@ class DeviceStep:
         self.key = bf16_tensor(w.key, dev, w.dtype)
         self.value = bf16_tensor(w.value, dev, w.dtype)
         self.slot_mapping = torch.from_numpy(w.slot_mapping).to(dev)
-        self.key_cache0 = bf16_tensor(w.key_cache, dev, w.dtype)
-        self.value_cache0 = bf16_tensor(w.value_cache, dev, w.dtype)
+        self.kv_fp8 = w.kv_fp8
+        if self.kv_fp8:  # 8-bit caches: uint8 E4M3 codes
+            self.key_cache0 = torch.from_numpy(np.ascontiguousarray(w.key_cache)).to(dev)
+            self.value_cache0 = torch.from_numpy(np.ascontiguousarray(w.value_cache)).to(dev)
+        else:
+            self.key_cache0 = bf16_tensor(w.key_cache, dev, w.dtype)
+            self.value_cache0 = bf16_tensor(w.value_cache, dev, w.dtype)
         self.key_cache = self.key_cache0.clone()
         self.value_cache = self.value_cache0.clone()
         self.block_tables = torch.from_numpy(w.block_tables).to(dev)
@@ -57,6 +62,8 @@ class DeviceStep:
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.rope = None
         if rope is not None:
+            if self.kv_fp8:
+                raise ValueError("the fused rotary scatter writes 16-bit caches only")
             table, positions, is_neox = rope
             self.rope = (torch.from_numpy(np.ascontiguousarray(table, dtype=np.float32)).to(dev),
                          torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int64)).to(dev), bool(is_neox))
@@ -72,10 +79,19 @@ class DeviceStep:
             B.pa_rope_reshape_and_cache(self.q, self.key, self.value, self.key_cache, self.value_cache,
                                         self.slot_mapping, positions, table, is_neox=is_neox, stream=stream)
             return
+        if self.kv_fp8:
+            B.pa_reshape_and_cache_fp8(self.key, self.value, self.key_cache, self.value_cache, self.slot_mapping,
+                                       self.w.k_scale, self.w.v_scale, stream=stream)
+            return
         B.pa_reshape_and_cache(self.key, self.value, self.key_cache, self.value_cache, self.slot_mapping,
                                stream=stream)
 
     def attention(self, stream=None) -> None:
+        if self.kv_fp8:
+            B.pa_attention_varlen_fp8(self.q, self.key_cache, self.value_cache, self.block_tables, self.seq_lens,
+                                      self.query_start_loc, self.max_query_len, self.max_seq_len, self.w.scale,
+                                      self.w.k_scale, self.w.v_scale, self.out, self.workspace, stream=stream)
+            return
         B.pa_attention_varlen(self.q, self.key_cache, self.value_cache, self.block_tables, self.seq_lens,
                               self.query_start_loc, self.max_query_len, self.max_seq_len, self.w.scale,
                               self.out, self.workspace, stream=stream)

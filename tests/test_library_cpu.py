@@ -78,7 +78,9 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.pa_attention_set_timing_events(None, None) == 0
     assert lib.pa_launch_count() == 0
     assert lib.pa_last_cuda_error() == b"cudaSuccess"
-    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 10, 2, None) == -3   # dtype
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 10, 3, None) == -3   # dtype
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 10, 2, None) == -1   # 8-bit caches pass the checks
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 8, 16, 10, 2, None) == -4     # 8 codes: half a vector
     assert lib.pa_copy_blocks(None, None, None, -1, 8, 128, 16, 10, 0, None) == -2  # negative count
     assert lib.pa_copy_blocks(None, None, None, 3, 8, 100, 16, 10, 0, None) == -4   # rows not 16-byte vectors
     assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 10, 1, None) == 0    # nothing to do
@@ -98,3 +100,25 @@ def test_product_code_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_fp8_validation_rejects_before_any_cuda_call(lib):
+    # pa_reshape_and_cache_fp8: element type, scales, shapes
+    r = lib.pa_reshape_and_cache_fp8
+    assert r(None, None, 0, 0, None, None, None, 0, 1, 64, 16, 1, 1.0, 1.0, 0, None) == 0
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, 1.0, 2, None) == -3   # 8-bit inputs
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 0.0, 1.0, 0, None) == -2   # zero scale
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, float("inf"), 0, None) == -2
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 96, 16, 1, 1.0, 1.0, 0, None) == -3   # head_dim
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, 1.0, 1, None) == -1   # fp16: null pointers
+    # pa_attention_varlen_fp8: scales, and query_len limited to 8 / G for now
+    a = lib.pa_attention_varlen_fp8
+    base = [None, 0, None, None, None, 1, None, None, 1, 1, 1, 1, 8, 2, 64, 16, 1, 1.0]
+    assert a(*base, 1.0, 1.0, None, None, 0, 0, None) == -1                 # passes to the null check
+    assert a(*base, -1.0, 1.0, None, None, 0, 0, None) == -2
+    assert a(*base, 1.0, float("nan"), None, None, 0, 0, None) == -2
+    assert a(*base, 1.0, 1.0, None, None, 0, 2, None) == -3                 # q must be bf16 or fp16
+    long_q = [None, 0, None, None, None, 0, None, None, 1, 8, 8, 8, 8, 2, 64, 16, 1, 1.0]
+    assert a(*long_q, 1.0, 1.0, None, None, 0, 0, None) == -3               # query_len 8 > 8 / 4
+    assert lib.pa_gather_kv(None, None, None, 4, 2, 64, 16, 10, None, None, 2, None) == -1
+    assert lib.pa_launch_count() == 0
