@@ -45,6 +45,7 @@
 #include <float.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "attention_internal.cuh"
 #include "pa_launch.h"
@@ -458,6 +459,8 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
 // ---------------------------------------------------------------------------
 // Split-KV attention: one independent TMA pipeline per warp.
 // ---------------------------------------------------------------------------
+// KT: keys per ring tile (units start at multiples of it).
+template <int KT>
 __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units, int lane) {
   int u = 0;
   if (lane == 0) u = atomicAdd(p.work_counter, 1);
@@ -480,7 +483,7 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   // A record is trusted only inside the bounds the host passed; anything else
   // is recorded and the unit becomes empty (no loads, no stores).
   const bool sane = U.b >= 0 && U.b < p.num_seqs && U.nrows >= 1 && U.nrows <= kCols && U.row0 >= 0 &&
-                    U.row0 + U.nrows <= p.total_q && U.kv_begin >= 0 && U.kv_begin % kTileKeys == 0 &&
+                    U.row0 + U.nrows <= p.total_q && U.kv_begin >= 0 && U.kv_begin % KT == 0 &&
                     U.kv_begin < U.kv_end &&
                     U.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size &&
                     U.part < p.max_parts && U.nparts >= 1 && U.nparts <= p.max_parts;
@@ -491,8 +494,8 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
   } else {
     U.skip = 0;
   }
-  U.kb0 = U.kv_begin / kTileKeys;
-  U.kb1 = (U.kv_end + kTileKeys - 1) / kTileKeys;
+  U.kb0 = U.kv_begin / KT;
+  U.kb1 = (U.kv_end + KT - 1) / KT;
   return U;
 }
 
@@ -510,14 +513,17 @@ struct TileGeom<D, false> {
     return (c >> 3) * HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
   }
 };
-// 8-bit caches: a 16-key tile is one box of 16 rows x D codes, with 128-byte
+// 8-bit caches: a ring tile is 32 keys (half the bytes of a 16-bit key, so
+// the per-tile bookkeeping is paid per 32 keys), rows of D codes with 128-byte
 // swizzle at D = 128 (16-byte chunk c of row r at c ^ (r % 8)) and 64-byte
 // swizzle at D = 64 (chunk c of row r at c ^ (r / 2 % 4)); either way eight
-// consecutive rows read at one chunk hit eight different bank groups.
+// consecutive rows read at one chunk hit eight different bank groups, and
+// rows 16..31 have the layout of rows 0..15 shifted by 16 * D bytes.
+constexpr int kTileKeys8 = 32;
 template <int D>
 struct TileGeom<D, true> {
   static_assert(D == 64 || D == 128, "8-bit tiles are one swizzle span wide");
-  static constexpr int TILE_BYTES = kTileKeys * D;
+  static constexpr int TILE_BYTES = kTileKeys8 * D;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static __device__ __forceinline__ uint32_t off(int r, int c) {
     return D == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
@@ -529,6 +535,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     splitkv_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                              const AttnParams p) {
   using T = TileGeom<D, KV8>;
+  // Tensor-core operand type: E, except over 8-bit caches, where K, V and P
+  // are fp16 whatever q is (E4M3 widens to fp16 in one hardware conversion)
+  // and a bf16 q is converted to fp16 exactly (see the unit set-up).
+  using M = typename std::conditional<KV8, ElemFp16, E>::type;
+  constexpr int KT = KV8 ? kTileKeys8 : kTileKeys;            // keys per ring tile
   constexpr int S = kSmemBudget / (NWARPS * T::SLOT_BYTES);  // ring slots per warp
   static_assert(S >= 2, "ring needs at least two slots");
   constexpr int MT = D / 16;
@@ -551,12 +562,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   const int total_units = min(max(ld_cg(p.item_count), 0), p.max_items) * Hkv;
   const uint32_t my_ring = ring + warp * S * T::SLOT_BYTES;
 
-  // Producer side (lane 0 issues): stage 16-key tile kb of unit U into ring
-  // slot seq % S. Keys k live in cache row table[k / bs] * bs + k % bs: with
-  // 16- or 32-token blocks a tile is 16 consecutive rows of one block (one
-  // 16-row box), with 8-token blocks two 8-row boxes of consecutive blocks
-  // (each fills one 1 KB swizzle atom). A block-table entry is read only for a
-  // block that holds a key below the unit's end.
+  // Producer side (lane 0 issues): stage KT-key tile kb of unit U into ring
+  // slot seq % S. Keys k live in cache row table[k / bs] * bs + k % bs: a
+  // tile is KT / box_rows boxes of box_rows = min(bs, KT) consecutive rows of
+  // one block each (16-bit caches: 16-key tiles; 8-bit: 32-key tiles). A
+  // block-table entry is read only for a block that holds a key below the
+  // unit's end; boxes past it are read at a negative row (zero fill).
   auto issue = [&](const Unit &U, int kb, uint32_t seq) {
     if (lane == 0) {
       const uint32_t slot = seq % S;
@@ -564,11 +575,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const uint32_t dst = my_ring + slot * T::SLOT_BYTES;
       const int32_t *trow = p.block_tables + static_cast<int64_t>(U.b) * p.max_blocks_per_seq;
       const int bs = p.block_size;
-      const int nbox = bs < kTileKeys ? 2 : 1;
-      const int box_rows = kTileKeys / nbox;
+      const int box_rows = bs < KT ? bs : KT;
+      const int nbox = KT / box_rows;
       mbar_arrive_expect_tx(bar, T::SLOT_BYTES);
       for (int j = 0; j < nbox; ++j) {
-        const int key = kb * kTileKeys + j * box_rows;  // first key of this box
+        const int key = kb * KT + j * box_rows;  // first key of this box
         int z = -box_rows;                              // entirely outside the tensor: TMA fills zeros
         if (key < U.kv_end) {  // block sizes are powers of two: shift and mask
           const int phys = __ldg(trow + (key >> p.block_shift));
@@ -592,7 +603,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     }
   };
 
-  Unit cur = fetch_unit(p, total_units, lane);
+  Unit cur = fetch_unit<KT>(p, total_units, lane);
   Unit nxt;
   nxt.valid = 0;
   bool have_nxt = false;
@@ -610,7 +621,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           continue;
         }
         if (!have_nxt) {
-          nxt = fetch_unit(p, total_units, lane);
+          nxt = fetch_unit<KT>(p, total_units, lane);
           have_nxt = true;
         }
         p_unit = 1;
@@ -631,6 +642,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   while (cur.valid) {
     // ---- per-unit set-up: q fragments (B operand of S^T = K Q^T), causal limits ----
     uint32_t qf[MT][2];
+    float col_scale[2] = {p.scale_log2, p.scale_log2};  // log2-domain score factor of accumulator columns
     {
       const int n = lane >> 2, qi = n / G, g = n % G;
       const bool ok = qi < cur.nrows;
@@ -646,6 +658,35 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           const uint32_t y = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 2)) : 0u;
           qf[kk][0] = __byte_perm(x, y, 0x5410);
           qf[kk][1] = __byte_perm(x, y, 0x7632);
+        }
+        if constexpr (std::is_same<E, ElemBf16>::value) {
+          // bf16 -> fp16, exactly: a column (lanes 4n..4n+3 hold column n)
+          // whose largest |q| reaches 2^15 is first scaled by 2^-e so that it
+          // lies in [2^14, 2^15); its scores are scaled back by 2^e below.
+          // Every bf16 value of at least 2^-17 times the column's scale then
+          // converts exactly (fp16 keeps 11 significant bits, bf16 has 8).
+          float amax = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < MT; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(qf[kk][h])), fabsf(ElemBf16::hi(qf[kk][h]))));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // floor(log2(amax))
+          const int e = ex >= 15 ? min(ex - 14, 120) : 0;
+          const float f = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+#pragma unroll
+          for (int kk = 0; kk < MT; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              qf[kk][h] = ElemFp16::pack(ElemBf16::lo(qf[kk][h]) * f, ElemBf16::hi(qf[kk][h]) * f);
+          // accumulator column c = 2(lane % 4) + j is B-fragment column c, held by lane 4c
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int ec = __shfl_sync(0xffffffffu, e, 4 * (2 * (lane & 3) + j));
+            col_scale[j] = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + ec) << 23);
+          }
         }
       } else {
         qp += 2 * (lane & 3);
@@ -668,30 +709,19 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
 
-    for (int kb = cur.kb0; kb < cur.kb1; ++kb) {
-      produce(consumed + S);
-      const uint32_t slot = consumed % S;
-      const bool landed = mbar_wait_bounded(smem_u32(&bars[warp][slot]), (consumed / S) & 1u, kWaitTimeoutNs);
-      if (!__all_sync(0xffffffffu, landed)) {  // leave together, never with a diverged warp
-        if (lane == 0) flag_error(p.status, PA_FLAG_TIMEOUT);
-        return;
+    // Rows past the request's last key may hold anything (even NaN): zero them in V.
+    auto zero_tail = [&](uint32_t vt, int valid_rows) {
+      constexpr int CPR = KV8 ? D / 16 : D / 8;  // 16-byte chunks per row
+      const int n = (KT - valid_rows) * CPR;
+      for (int i = lane; i < n; i += 32) {
+        const int r = valid_rows + i / CPR, c = i % CPR;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + T::off(r, c)), "r"(0u) : "memory");
       }
-      const uint32_t kt = my_ring + slot * T::SLOT_BYTES;
-      const uint32_t vt = kt + T::TILE_BYTES;
-      const int valid_rows = min(kTileKeys, cur.kv_end - kb * kTileKeys);
-      if (valid_rows < kTileKeys) {
-        // rows past the request's last key may hold anything (even NaN): zero them in V
-        constexpr int CPR = KV8 ? D / 16 : D / 8;  // 16-byte chunks per row
-        const int n = (kTileKeys - valid_rows) * CPR;
-        for (int i = lane; i < n; i += 32) {
-          const int r = valid_rows + i / CPR, c = i % CPR;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + T::off(r, c)), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();  // order these generic writes before the slot's next TMA fill
-        __syncwarp();
-      }
-
-      // S^T = K Q^T over D, two independent accumulator chains
+      fence_proxy_async_smem();  // order these generic writes before the slot's next TMA fill
+      __syncwarp();
+    };
+    // S^T = K Q^T of one 16-key tile over D (two independent accumulator chains), summed into s.
+    auto scores = [&](uint32_t kt, float (&s)[4]) {
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV8) {
         // one x4 load = 16 keys x 32 codes: per lane 4 consecutive d of keys
@@ -701,12 +731,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         for (int j = 0; j < D / 32; ++j) {
           uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
           ldsm_x4(kt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
-          E::from_e4m3x4(r0, l0, h0);
-          E::from_e4m3x4(r1, l1, h1);
-          E::mma(sa, l0, l1, h0, h1, qf[2 * j][0], qf[2 * j][1]);
-          E::from_e4m3x4(r2, l0, h0);
-          E::from_e4m3x4(r3, l1, h1);
-          E::mma(sb, l0, l1, h0, h1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+          M::from_e4m3x4(r0, l0, h0);
+          M::from_e4m3x4(r1, l1, h1);
+          M::mma(sa, l0, l1, h0, h1, qf[2 * j][0], qf[2 * j][1]);
+          M::from_e4m3x4(r2, l0, h0);
+          M::from_e4m3x4(r3, l1, h1);
+          M::mma(sb, l0, l1, h0, h1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
         }
       } else {
 #pragma unroll
@@ -714,17 +744,95 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           uint32_t a0, a1, a2, a3;
           ldsm_x4(kt + T::off(arow, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
           if (kk & 1)
-            E::mma(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            M::mma(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
           else
-            E::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            M::mma(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         }
       }
-      const int t0 = kb * kTileKeys + (lane >> 2), t1 = t0 + 8;
-      const float x0 = t0 < lim[0] ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
-      const float x1 = t0 < lim[1] ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
-      const float x2 = t1 < lim[0] ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
-      const float x3 = t1 < lim[1] ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[i] = sa[i] + sb[i];
+    };
+    // O^T += V^T P^T of one tile; P^T (keys x columns) comes as hi (b0, b1) + lo (c0, c1).
+    auto pv = [&](uint32_t vt, uint32_t b0, uint32_t b1, uint32_t c0, uint32_t c1) {
+      if constexpr (KV8) {
+        // transposed x4 load of 16 keys x 32 codes: per lane keys (2(lane%4),
+        // +1) (+8) at d = 2(lane/4) and 2(lane/4) + 1 of each 16-d chunk. Row
+        // lane/4 of m tile mt holds d = 16mt + 2(lane/4), row lane/4 + 8 holds
+        // d = 16mt + 2(lane/4) + 1; the epilogue puts d back in order.
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
+          ldsm_x4_t(vt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
+          M::from_e4m3x4(r0, l0, h0);
+          M::from_e4m3x4(r1, l1, h1);
+          M::mma(o[2 * j], l0, h0, l1, h1, b0, b1);
+          M::mma(o[2 * j], l0, h0, l1, h1, c0, c1);
+          M::from_e4m3x4(r2, l0, h0);
+          M::from_e4m3x4(r3, l1, h1);
+          M::mma(o[2 * j + 1], l0, h0, l1, h1, b0, b1);
+          M::mma(o[2 * j + 1], l0, h0, l1, h1, c0, c1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+          M::mma(o[mt], a0, a1, a2, a3, b0, b1);
+          M::mma(o[mt], a0, a1, a2, a3, c0, c1);
+        }
+      }
+    };
+
+    // 32 keys per step: two 16-key tiles (one, at the end of an odd run) of a
+    // 16-bit cache, or the two halves of one 32-key tile of an 8-bit cache.
+    // One softmax update per step; O rescaled only when a column's maximum grew.
+    for (int kb = cur.kb0; kb < cur.kb1; kb += KV8 ? 1 : 2) {
+      const bool two = KV8 || kb + 1 < cur.kb1;  // warp-uniform
+      produce(consumed + S);
+      uint32_t kt0, vt0, kt1, vt1;
+      bool landed;
+      if constexpr (KV8) {
+        const uint32_t slot = consumed % S;
+        landed = mbar_wait_bounded(smem_u32(&bars[warp][slot]), (consumed / S) & 1u, kWaitTimeoutNs);
+        kt0 = my_ring + slot * T::SLOT_BYTES;
+        vt0 = kt0 + T::TILE_BYTES;
+        kt1 = kt0 + kTileKeys * D;  // rows 16..31
+        vt1 = vt0 + kTileKeys * D;
+      } else {
+        const uint32_t slot0 = consumed % S, slot1 = (consumed + 1) % S;
+        landed = mbar_wait_bounded(smem_u32(&bars[warp][slot0]), (consumed / S) & 1u, kWaitTimeoutNs);
+        if (two && landed)
+          landed = mbar_wait_bounded(smem_u32(&bars[warp][slot1]), ((consumed + 1) / S) & 1u, kWaitTimeoutNs);
+        kt0 = my_ring + slot0 * T::SLOT_BYTES;
+        vt0 = kt0 + T::TILE_BYTES;
+        kt1 = my_ring + slot1 * T::SLOT_BYTES;
+        vt1 = kt1 + T::TILE_BYTES;
+      }
+      if (!__all_sync(0xffffffffu, landed)) {  // leave together, never with a diverged warp
+        if (lane == 0) flag_error(p.status, PA_FLAG_TIMEOUT);
+        return;
+      }
+      // only the unit's last tile can be partial
+      const int last_valid = cur.kv_end - (cur.kb1 - 1) * KT;
+      if constexpr (KV8) {
+        if (last_valid < KT && kb == cur.kb1 - 1) zero_tail(vt0, last_valid);
+      } else {
+        if (last_valid < KT && kb + (two ? 1 : 0) == cur.kb1 - 1) zero_tail(two ? vt1 : vt0, last_valid);
+      }
+
+      float s0[4], s1[4];
+      scores(kt0, s0);
+      if (two) scores(kt1, s1);
+      const int t0 = kb * KT + (lane >> 2), t1 = t0 + 8, t2 = t0 + kTileKeys, t3 = t1 + kTileKeys;
+      const float x0 = t0 < lim[0] ? s0[0] * col_scale[0] : -INFINITY;
+      const float x1 = t0 < lim[1] ? s0[1] * col_scale[1] : -INFINITY;
+      const float x2 = t1 < lim[0] ? s0[2] * col_scale[0] : -INFINITY;
+      const float x3 = t1 < lim[1] ? s0[3] * col_scale[1] : -INFINITY;
+      const float y0 = two && t2 < lim[0] ? s1[0] * col_scale[0] : -INFINITY;
+      const float y1 = two && t2 < lim[1] ? s1[1] * col_scale[1] : -INFINITY;
+      const float y2 = two && t3 < lim[0] ? s1[2] * col_scale[0] : -INFINITY;
+      const float y3 = two && t3 < lim[1] ? s1[3] * col_scale[1] : -INFINITY;
+      float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -736,52 +844,36 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const float al0 = ex2_approx(m[0] - ms0), al1 = ex2_approx(m[1] - ms1);
       const float p0 = ex2_approx(x0 - ms0), p1 = ex2_approx(x1 - ms1);
       const float p2 = ex2_approx(x2 - ms0), p3 = ex2_approx(x3 - ms1);
-      l[0] = l[0] * al0 + p0 + p2;
-      l[1] = l[1] * al1 + p1 + p3;
+      const float q0 = ex2_approx(y0 - ms0), q1 = ex2_approx(y1 - ms1);
+      const float q2 = ex2_approx(y2 - ms0), q3 = ex2_approx(y3 - ms1);
+      l[0] = l[0] * al0 + ((p0 + p2) + (q0 + q2));
+      l[1] = l[1] * al1 + ((p1 + p3) + (q1 + q3));
       m[0] = mn0;
       m[1] = mn1;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-      // P^T (keys x columns) -> B operand by transposition; P as bf16 hi + lo.
-      const uint32_t h01 = E::pack(p0, p1), h23 = E::pack(p2, p3);
-      const uint32_t l01 = E::pack(p0 - E::lo(h01), p1 - E::hi(h01));
-      const uint32_t l23 = E::pack(p2 - E::lo(h23), p3 - E::hi(h23));
-      const uint32_t b0 = movmatrix_t(h01), b1 = movmatrix_t(h23);
-      const uint32_t c0 = movmatrix_t(l01), c1 = movmatrix_t(l23);
-      if constexpr (KV8) {
-        // transposed x4 load of 16 keys x 32 codes: per lane keys (2(lane%4),
-        // +1) (+8) at d = 2(lane/4) and 2(lane/4) + 1 of each 16-d chunk. Row
-        // lane/4 of m tile mt holds d = 16mt + 2(lane/4), row lane/4 + 8 holds
-        // d = 16mt + 2(lane/4) + 1; the epilogue puts d back in order.
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-          uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
-          ldsm_x4_t(vt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
-          E::from_e4m3x4(r0, l0, h0);
-          E::from_e4m3x4(r1, l1, h1);
-          E::mma(o[2 * j], l0, h0, l1, h1, b0, b1);
-          E::mma(o[2 * j], l0, h0, l1, h1, c0, c1);
-          E::from_e4m3x4(r2, l0, h0);
-          E::from_e4m3x4(r3, l1, h1);
-          E::mma(o[2 * j + 1], l0, h0, l1, h1, b0, b1);
-          E::mma(o[2 * j + 1], l0, h0, l1, h1, c0, c1);
-        }
-      } else {
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vt + T::off(vrow, 2 * mt + ((lane >> 3) & 1)), a0, a1, a2, a3);
-          E::mma(o[mt], a0, a1, a2, a3, b0, b1);
-          E::mma(o[mt], a0, a1, a2, a3, c0, c1);
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
         }
       }
-      __syncwarp();  // every lane is done with this slot before it is refilled
-      ++consumed;
+      // P^T (keys x columns) -> B operand by transposition; P as hi + lo pairs.
+      {
+        const uint32_t h01 = M::pack(p0, p1), h23 = M::pack(p2, p3);
+        const uint32_t l01 = M::pack(p0 - M::lo(h01), p1 - M::hi(h01));
+        const uint32_t l23 = M::pack(p2 - M::lo(h23), p3 - M::hi(h23));
+        pv(vt0, movmatrix_t(h01), movmatrix_t(h23), movmatrix_t(l01), movmatrix_t(l23));
+      }
+      if (two) {
+        const uint32_t h01 = M::pack(q0, q1), h23 = M::pack(q2, q3);
+        const uint32_t l01 = M::pack(q0 - M::lo(h01), q1 - M::hi(h01));
+        const uint32_t l23 = M::pack(q2 - M::lo(h23), q3 - M::hi(h23));
+        pv(vt1, movmatrix_t(h01), movmatrix_t(h23), movmatrix_t(l01), movmatrix_t(l23));
+      }
+      __syncwarp();  // every lane is done with these slots before they are refilled
+      consumed += (KV8 || !two) ? 1 : 2;
     }
 
     // ---- unit epilogue: normalise and write the output or the partial ----
@@ -845,7 +937,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     // ---- advance to the next unit (the producer may already be streaming it) ----
     if (p_unit == 0) {
       if (!have_nxt) {
-        nxt = fetch_unit(p, total_units, lane);
+        nxt = fetch_unit<KT>(p, total_units, lane);
         have_nxt = true;
       }
       p_kb = nxt.kb0;
@@ -926,8 +1018,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 3-D view of one cache, [num_blocks * 16 rows][Hkv][D], with a box of
 // 16 rows x 1 head x 64 elements (128 bytes, 128-byte swizzle).
-// 8-bit caches: elements of one byte and a box of 16 rows x 1 head x D codes
-// (128-byte swizzle at D = 128, 64-byte at D = 64).
+// 8-bit caches: elements of one byte and a box of up to 32 rows x 1 head x D
+// codes (128-byte swizzle at D = 128, 64-byte at D = 64).
 static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
                              int32_t head_dim, int32_t block_size, int32_t dtype, bool kv8) {
   auto encode = tensor_map_encoder();
@@ -937,8 +1029,9 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_bl
                               static_cast<cuuint64_t>(num_blocks) * block_size};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * esize,
                                  static_cast<cuuint64_t>(num_kv_heads) * head_dim * esize};
-  // one box per 16-key tile of a 16- or 32-token block, two per tile of 8-token blocks
-  const cuuint32_t rows = static_cast<cuuint32_t>(block_size < kTileKeys ? block_size : kTileKeys);
+  // box rows: min(block_size, keys per tile), the tile being 16 keys (32 for 8-bit caches)
+  const int kt = kv8 ? kTileKeys8 : kTileKeys;
+  const cuuint32_t rows = static_cast<cuuint32_t>(block_size < kt ? block_size : kt);
   const cuuint32_t box[3] = {kv8 ? static_cast<cuuint32_t>(head_dim) : 64u, 1, rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType type = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8

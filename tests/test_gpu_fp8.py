@@ -152,3 +152,13 @@ def test_fp8_host_errors():
         assert e.value.status == -2
     torch.cuda.synchronize()
     assert B.pa_debug_status() == 0
+
+
+@pytest.mark.parametrize("q_scale", [3.0e4, 2.0e9])
+def test_fp8_bf16_queries_beyond_fp16_range(oracle, q_scale):
+    """Over 8-bit caches the tensor cores take fp16 operands: bf16 q columns whose largest |q|
+    reaches 2^15 (here up to ~1e5 and ~1e10) are scaled by a power of two first, so they must
+    still match the oracle (the softmax is then nearly one-hot)."""
+    w = W.make_workload(f"fp8_bigq_{q_scale:g}", context_lens=[40, 900, 3, 2100], query_lens=[1, 2, 1, 1],
+                        num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype=FP8, q_scale=q_scale, seed=12)
+    run_fp8(w, oracle)
