@@ -133,7 +133,7 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
                                    float k_scale, float v_scale, int32_t dtype, void *stream);
 
 /*
- * Bytes of device workspace pa_attention_varlen needs for these host-side
+ * Bytes of device workspace pa_attention_varlen or pa_attention_varlen_fp8 needs for these host-side
  * bounds (0 if the arguments are invalid). Pure host arithmetic; no CUDA call.
  * The workspace holds the work plan and the split-KV partial results.
  */
@@ -143,8 +143,10 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t total_q_tokens,
                                    int32_t head_dim, int32_t block_size);
 
 /*
- * How pa_attention_varlen will split KV for these bounds: the partition size
- * in tokens and the largest number of partitions of one request. Host only.
+ * How pa_attention_varlen (16-bit caches) will split KV for these bounds: the
+ * partition size in tokens and the largest number of partitions of one
+ * request. Host only. (pa_attention_varlen_fp8 runs more warps per SM, so it
+ * may choose smaller partitions; the workspace size covers both.)
  */
 pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len,
                                  int32_t num_heads, int32_t num_kv_heads,

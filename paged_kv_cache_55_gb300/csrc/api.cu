@@ -162,16 +162,18 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int
                                    int32_t head_dim, int32_t block_size) {
   if (max_query_len < 0 || max_seq_len < max_query_len) return 0;
   if (!supported_dims(num_heads, num_kv_heads, head_dim, block_size)) return 0;
-  pa::WorkspaceLayout w;
-  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, w))
+  // one size for either cache type: the larger of the two plans
+  pa::WorkspaceLayout w16, w8;
+  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, false, w16) ||
+      !pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, true, w8))
     return 0;
-  return w.total;
+  return w16.total > w8.total ? w16.total : w8.total;
 }
 
 pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
                                  int32_t num_kv_heads, int32_t *partition_tokens, int32_t *max_partitions) {
   pa::WorkspaceLayout w;
-  if (!pa::workspace_layout(num_seqs, 0, max_seq_len, num_heads, num_kv_heads, 128, w)) return PA_ERR_DIMS;
+  if (!pa::workspace_layout(num_seqs, 0, max_seq_len, num_heads, num_kv_heads, 128, false, w)) return PA_ERR_DIMS;
   if (partition_tokens) *partition_tokens = w.part_tokens;
   if (max_partitions) *max_partitions = w.max_parts;
   return PA_OK;
@@ -215,7 +217,7 @@ pa_status attention_call(const void *q, int64_t q_token_stride, const void *key_
       !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
     return PA_ERR_ALIGN;
   pa::WorkspaceLayout w;
-  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, w))
+  if (!pa::workspace_layout(num_seqs, total_q_tokens, max_seq_len, num_heads, num_kv_heads, head_dim, kv_fp8, w))
     return PA_ERR_DIMS;
   if (!workspace || workspace_bytes < w.total) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_ALIGN;

@@ -956,14 +956,15 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 // long requests cannot leave most SMs idle at the end of the step; each one
 // costs a partial (D + 1 floats per column) written here and read back by
 // the merge. With many (request, KV head) pairs against the decode kernel's
-// warps (152 SMs x 8 on GB300; a fixed figure so that the host-only sizing
-// calls need no device query) 512 keys balance best; with few pairs, about
-// one partition of the longest request per warp, in multiples of 512 keys up
-// to 2048, keeps every warp busy with fewer partials. Measured on GB300 (step
-// time): batch 256 GQA and 64 MHA are fastest at 512; 8 requests of 32768
-// keys at 2048 (8 % faster than at 512).
-int partition_tokens(int32_t num_seqs, int32_t max_seq_len, int32_t num_kv_heads) {
-  constexpr int64_t kWarps = 152 * 8;
+// warps (152 SMs x 8 warps for 16-bit caches, x 12 for 8-bit ones on GB300;
+// fixed figures so that the host-only sizing calls need no device query)
+// 512 keys balance best; with few pairs, about one partition of the longest
+// request per warp, in multiples of 512 keys up to 2048, keeps every warp
+// busy with fewer partials. Measured on GB300 (step time): batch 256 GQA and
+// 64 MHA are fastest at 512; 8 requests of 32768 keys at 2048 (8 % faster
+// than at 512) with 16-bit caches.
+int partition_tokens(int32_t num_seqs, int32_t max_seq_len, int32_t num_kv_heads, bool kv8) {
+  const int64_t kWarps = 152 * (kv8 ? 12 : 8);
   const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
   if (pairs <= 0 || max_seq_len <= 0 || pairs * 2 >= kWarps) return 512;
   const int64_t per_warp = static_cast<int64_t>(max_seq_len) * pairs / kWarps;
@@ -974,14 +975,14 @@ int partition_tokens(int32_t num_seqs, int32_t max_seq_len, int32_t num_kv_heads
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, int32_t num_heads,
-                      int32_t num_kv_heads, int32_t head_dim, WorkspaceLayout &w) {
+                      int32_t num_kv_heads, int32_t head_dim, bool kv8, WorkspaceLayout &w) {
   if (num_seqs < 0 || total_q < 0 || max_seq_len < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
       head_dim <= 0 || num_heads % num_kv_heads != 0)
     return false;
   const int G = num_heads / num_kv_heads;
   if (G > 8) return false;
   w.rows_per_item = 8 / G;
-  w.part_tokens = partition_tokens(num_seqs, max_seq_len, num_kv_heads);
+  w.part_tokens = partition_tokens(num_seqs, max_seq_len, num_kv_heads, kv8);
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.part_tokens - 1) / w.part_tokens : 1;
   const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts;  // decode items: one group per request
   const int64_t tiles = (static_cast<int64_t>(total_q) * G + kPrefillTileRows - 1) / kPrefillTileRows + num_seqs;
@@ -1044,7 +1045,8 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_bl
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kAttnWarps = 8;
+constexpr int kAttnWarps = 8;   // 16-bit caches: two warps per scheduler
+constexpr int kAttnWarps8 = 12; // 8-bit caches: three, to hide the latency of the per-tile widening
 
 template <int D, int G, typename E, bool KV8>
 static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, cudaStream_t stream,
@@ -1108,7 +1110,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
-  auto kern = splitkv_attention_kernel<D, G, kAttnWarps, E, KV8>;
+  constexpr int NW = KV8 ? kAttnWarps8 : kAttnWarps;
+  auto kern = splitkv_attention_kernel<D, G, NW, E, KV8>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -1116,10 +1119,10 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   // one CTA per SM; fewer when there are fewer units than warps
   int64_t grid = a.sm_count;
   const int64_t units_upper = static_cast<int64_t>(w.max_items) * a.num_kv_heads;
-  if (grid * kAttnWarps > units_upper) grid = (units_upper + kAttnWarps - 1) / kAttnWarps;
+  if (grid * NW > units_upper) grid = (units_upper + NW - 1) / NW;
   if (grid < 1) grid = 1;
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kAttnWarps * 32), smem, stream, kmap, vmap, ap);
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, kmap, vmap, ap);
   if (err != cudaSuccess) return err;
   ++*launched;
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
@@ -1172,7 +1175,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
 
 cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *launched) {
   WorkspaceLayout w;
-  if (!workspace_layout(a.num_seqs, a.total_q, a.max_seq_len, a.num_heads, a.num_kv_heads, a.head_dim, w))
+  if (!workspace_layout(a.num_seqs, a.total_q, a.max_seq_len, a.num_heads, a.num_kv_heads, a.head_dim, a.kv_fp8, w))
     return cudaErrorInvalidValue;
   const int G = a.num_heads / a.num_kv_heads;
 #define PA_DISPATCH(DD, GG)                                                                     \

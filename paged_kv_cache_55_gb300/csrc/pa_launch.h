@@ -47,8 +47,10 @@ struct WorkspaceLayout {
   int32_t rows_per_item;  // query rows per item: 8 / group size
 };
 
+// kv8: the plan for 8-bit caches (more decode warps per SM, so partitions
+// can be smaller). pa_attention_workspace_size covers both plans.
 bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, int32_t num_heads,
-                      int32_t num_kv_heads, int32_t head_dim, WorkspaceLayout &w);
+                      int32_t num_kv_heads, int32_t head_dim, bool kv8, WorkspaceLayout &w);
 
 struct AttnLaunch {
   const void *q;
