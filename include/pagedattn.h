@@ -208,10 +208,9 @@ pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
  *                         * (v_scale * Vc[j]) )
  * q and out are `dtype` (bf16 or fp16). k_scale and v_scale must be finite and
  * positive (PA_ERR_DIMS otherwise). Each code is widened exactly and the
- * products accumulate in fp32, as for 16-bit caches.
- * Supported now for query_len <= 8 / (num_heads / num_kv_heads) per request
- * (decode tokens and short drafts); a larger max_query_len returns
- * PA_ERR_UNSUPPORTED.
+ * products accumulate in fp32, as for 16-bit caches: the tensor cores take
+ * fp16 operands (a bf16 q row or column whose largest |q| reaches 2^15 is
+ * scaled by a power of two first, and its scores scaled back).
  */
 pa_status pa_attention_varlen_fp8(const void *q, int64_t q_token_stride,
                                   const void *key_cache, const void *value_cache,

@@ -203,8 +203,6 @@ pa_status attention_call(const void *q, int64_t q_token_stride, const void *key_
     return PA_ERR_UNSUPPORTED;
   }
   if (!std::isfinite(scale)) return PA_ERR_DIMS;
-  // 8-bit caches: decode tokens and short drafts (query_len <= 8 / group size) only, for now
-  if (kv_fp8 && max_query_len > 8 / (num_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
   if (max_query_len == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_DIMS;
   if (num_blocks > INT32_MAX / block_size) return PA_ERR_UNSUPPORTED;  // cache rows are int32 TMA coordinates

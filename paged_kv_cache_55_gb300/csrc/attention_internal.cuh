@@ -25,7 +25,8 @@ struct TileParams {
   int32_t num_heads;
   int32_t num_kv_heads;
   int64_t num_blocks;
-  float scale_log2;
+  float scale_log2;  // softmax scale (times the K cache scale for 8-bit caches) * log2(e)
+  float out_scale;   // 1, or the V cache scale for 8-bit caches
   bf16 *out;
   const int4 *tiles;
   const int32_t *tile_count;
@@ -37,8 +38,10 @@ struct TileParams {
 };
 
 // Enqueue the tensor-core prefill-tile kernel (PDL launch) on `stream`; E is
-// the element type (ElemBf16 or ElemFp16).
-template <int D, int G, typename E>
+// the element type of q and out (ElemBf16 or ElemFp16); KV8: the caches hold
+// 8-bit E4M3 codes (the maps then have one-byte elements and boxes of
+// min(block_size, 32) rows of head_dim codes).
+template <int D, int G, typename E, bool KV8>
 cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp,
                                  int sm_count, cudaStream_t stream);
 

@@ -44,6 +44,8 @@
 // tiles (checked). Waits on mbarriers are bounded (a thread waits out at most
 // one timeout, then runs to the unit barrier); in-flight loads and products
 // are waited for (bounded) and tensor memory is released on every exit path.
+#include <type_traits>
+
 #include "attention_internal.cuh"
 
 namespace pa {
@@ -55,6 +57,10 @@ constexpr int kKeyTile = 128;  // keys per range (UMMA N of S, K of P V)
 constexpr int kMaxSlots = 8;   // K/V ring slots (as many as shared memory holds)
 constexpr int kSoftmaxWarps = 4 * kHalves, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
 constexpr int kTileThreads = 32 * (kTmaWarp + 1);
+// 8-bit caches: two more warps widen each staged range to fp16 in place.
+constexpr int kConvWarp = kTmaWarp + 1, kConvWarps = 2;
+constexpr int kTileThreads8 = kTileThreads + 32 * kConvWarps;
+constexpr int kRawBoxRows = 32;  // 8-bit boxes: min(block_size, 32) rows
 constexpr uint64_t kTcWaitTimeoutNs = 2000000000;
 constexpr uint32_t kTmemCols = 512;
 
@@ -78,8 +84,9 @@ struct TcLayout {
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;             // one K or V range: a ring slot
   static constexpr int TABLE_ENTRIES = 512;  // staged TMA row coordinates: boxes of keys < 8192 (4096 at bs 8)
   // barriers: full[kMaxSlots], empty[kMaxSlots], per half s_full, p_full, o_done,
-  // then q_full and drain (the MMA thread's last commit)
-  static constexpr int NBARS = 2 * kMaxSlots + 3 * kHalves + 2;
+  // then q_full and drain (the MMA thread's last commit), then raw[kMaxSlots]
+  // (8-bit caches: the staged codes of a slot have landed)
+  static constexpr int NBARS = 3 * kMaxSlots + 3 * kHalves + 2;
   static constexpr int FIXED = kHalves * Q_BYTES + TABLE_ENTRIES * 4 + 8 * NBARS + 16;
   static constexpr int FIT = (227 * 1024 - FIXED) / KV_BYTES;
   static constexpr int SLOTS = FIT < kMaxSlots ? FIT : kMaxSlots;
@@ -200,7 +207,12 @@ __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, 
 // P for 32 keys (scores s[0..32), visible while ck0 + i < lim): p =
 // 2^(s * sl2 - ms), summed into *sum and packed as the 32 TMEM columns of two
 // UMMA K steps: [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo 16-31].
-template <typename E>
+// The exponent is one fused multiply-add, whose unrounded product differs
+// from the rounded one ms was taken from by at most half an ulp of ms: below
+// 2^-12 while |ms| <= 2^12. EXACT rows (larger |ms|) round the product first,
+// so the row maximum's exponent is exactly zero and none exceeds the growth
+// the caller allowed.
+template <typename E, bool EXACT>
 __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int lim, float sl2, float ms, float &sum,
                                         uint32_t (&u)[32]) {
   const bool full = ck0 + 32 <= lim;
@@ -213,7 +225,13 @@ __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int li
       x1 = ck0 + 2 * i + 1 < lim ? x1 : -INFINITY;
     }
     float e0, e1;
-    fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
+    if (EXACT) {
+      // scalar round-to-nearest intrinsics, which are never merged into a fused multiply-add
+      e0 = __fsub_rn(__fmul_rn(x0, sl2), ms);
+      e1 = __fsub_rn(__fmul_rn(x1, sl2), ms);
+    } else {
+      fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
+    }
     const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
     add2(acc0, acc1, acc0, acc1, p0, p1);
     const uint32_t hi = E::pack(p0, p1);
@@ -244,20 +262,33 @@ __device__ __forceinline__ void rescale_p32(uint32_t taddr, float alpha) {
   tmem_st32u(taddr, w);
 }
 
-template <int D, int G, typename E>
-// Ten warps: three share two of the SM's four register-file partitions, so a
-// thread gets at most 168 registers.
-__global__ void __launch_bounds__(kTileThreads, 1)
+// 8-bit caches (KV8): the producer stages a range's codes in the back half of
+// its ring slot (kKeyTile x D bytes, the TMA boxes' own 128- or 64-byte
+// swizzle); two converter warps load them, meet at a named barrier (the
+// fp16 rows they then write overlap the codes), widen them exactly to fp16
+// in the layout the 16-bit path's TMA writes, and arrive on the slot's full
+// barrier. The tensor cores then take fp16 operands whatever q is: a bf16 Q
+// row is stored as fp16, scaled first by a power of two when its largest |q|
+// reaches 2^15, and its thread's softmax factor is scaled back.
+template <int D, int G, typename E, bool KV8>
+// Ten warps (twelve with 8-bit caches): three share each of two (all four) of
+// the SM's register-file partitions, so a thread gets at most 168 registers.
+__global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const TileParams p) {
   using Lay = TcLayout<D>;
   using Tm = TcTmem<D>;
+  using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
+  constexpr int NTHREADS = KV8 ? kTileThreads8 : kTileThreads;
+  constexpr int RAW_BYTES = kKeyTile * D;          // 8-bit codes of one range
+  constexpr uint32_t RAW_OFF = Lay::KV_BYTES / 2;  // staged in the back half of the slot
+  static_assert(RAW_BYTES == Lay::KV_BYTES / 2, "a range's codes fill half of its 16-bit slot");
   constexpr int KSTEPS_S = D / 16;         // UMMA K steps of S = Q K^T
   constexpr int KSTEPS_O = kKeyTile / 16;  // UMMA K steps of O = P V
   constexpr int TILES = kKeyTile / kTileKeys;  // 16-key tiles per range
   constexpr int POS_PER_HALF = kHalfRows / G;
-  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, E::kUmmaFormat);
-  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, E::kUmmaFormat);
+  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, M::kUmmaFormat);
+  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, M::kUmmaFormat);
   // O stays in TMEM and is rescaled only when a row's running maximum grows
   // by more than 2^8 (log2 domain); in between, probabilities are taken
   // against the older maximum and stay below 256.
@@ -277,6 +308,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   // per half h: barrier + 8 * h
   const uint32_t bar_s = bars + 16 * kMaxSlots, bar_p = bar_s + 8 * kHalves, bar_o = bar_p + 8 * kHalves;
   const uint32_t bar_q = bar_o + 8 * kHalves, bar_drain = bar_q + 8;
+  const uint32_t bar_raw = bar_drain + 8;  // per ring slot: barrier + 8 * slot
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS);
   int *unit_s = reinterpret_cast<int *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS + 4);
   int *zbox = reinterpret_cast<int *>(smem_raw + Lay::TABLE_OFF);
@@ -286,7 +318,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 2 * kMaxSlots; ++i) mbar_init(bars + 8 * i, 1);  // full: producer; empty: MMA commits
+    // full: the producer's TMA (16-bit caches) or one arrival per converter warp (8-bit); empty: MMA commits
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_full + 8 * i, KV8 ? kConvWarps : 1);
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_empty + 8 * i, 1);
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_raw + 8 * i, 1);
     for (int h = 0; h < kHalves; ++h) {
       mbar_init(bar_s + 8 * h, 1);
       mbar_init(bar_p + 8 * h, 4);  // the half's four softmax warps
@@ -323,6 +358,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const int u = *unit_s;
     if (u >= total_units) break;
     const int item = u / Hkv, kvh = u - item * Hkv;
+    (void)RAW_OFF;
     const int4 r0 = ld_cg(p.tiles + 2 * item);
     const int4 r1 = ld_cg(p.tiles + 2 * item + 1);
     const int b = r0.x, row0 = r0.y, npos = r0.z, pos0 = r0.w, kv_end = r1.y;
@@ -342,7 +378,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // past the keys, or of a block id out of range, are read at -box_rows
     // (zero fill). All threads compute the unit's coordinates once here, so
     // the producer only reads one from shared memory per box.
-    const int box_rows = bs < kTileKeys ? bs : kTileKeys;
+    constexpr int MAXROWS = KV8 ? kRawBoxRows : kTileKeys;
+    const int box_rows = bs < MAXROWS ? bs : MAXROWS;
     const int nboxes = (kv_end + box_rows - 1) / box_rows;
     auto box_z = [&](int i) {
       const int key = i * box_rows;
@@ -362,7 +399,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       const int last = min(npos, (h + 1) * POS_PER_HALF);  // positions [h * POS_PER_HALF, last)
       nkt_h[h] = last > h * POS_PER_HALF ? (pos0 + last + kKeyTile - 1) / kKeyTile : 0;
     }
-    for (int i = tid; i < min(nboxes, Lay::TABLE_ENTRIES); i += kTileThreads) zbox[i] = box_z(i);
+    for (int i = tid; i < min(nboxes, Lay::TABLE_ENTRIES); i += NTHREADS) zbox[i] = box_z(i);
     __syncthreads();
 
     if (warp == kTmaWarp) {
@@ -374,9 +411,22 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           if (use > 0) wait_or_fail(bar_empty + 8 * slot, (use - 1) & 1u, failed);
           if (failed) return;
           issued = g + 1;
+          const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+          if constexpr (KV8) {
+            // the range's codes: kKeyTile / box_rows boxes of box_rows x D bytes
+            const uint32_t bar = bar_raw + 8 * slot;
+            const uint32_t dst = sRing + slot * Lay::KV_BYTES + RAW_OFF;
+            mbar_arrive_expect_tx(bar, RAW_BYTES);
+            const int nb = kKeyTile / box_rows;
+            for (int j = 0; j < nb; ++j) {
+              const int i = kt * nb + j;
+              const int z = i < nboxes ? (i < Lay::TABLE_ENTRIES ? zbox[i] : box_z(i)) : -box_rows;
+              tma_load_3d(dst + j * box_rows * D, map, bar, 0, kvh, z);
+            }
+            return;
+          }
           const uint32_t bar = bar_full + 8 * slot;
           const uint32_t dst = sRing + slot * Lay::KV_BYTES;
-          const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
           mbar_arrive_expect_tx(bar, Lay::KV_BYTES);
           // a 16-key tile is one 16-row box (16- or 32-token blocks) or two
           // 8-row boxes of consecutive 8-token blocks
@@ -394,15 +444,75 @@ __global__ void __launch_bounds__(kTileThreads, 1)
               }
             }
           };
-          if (bs < kTileKeys)
-            boxes(std::integral_constant<int, 2>());
-          else
-            boxes(std::integral_constant<int, 1>());
+          if constexpr (!KV8) {
+            if (bs < kTileKeys)
+              boxes(std::integral_constant<int, 2>());
+            else
+              boxes(std::integral_constant<int, 1>());
+          }
         };
         // the order the products consume them: S(j) needs K(j) before P V(j) needs V(j)
         for (int j = 0; j < nkt; ++j) {
           load(j, false);
           load(j, true);
+        }
+      }
+    } else if (warp >= kConvWarp) {
+      // ---------------- 8-bit caches: widen staged codes to fp16 in place ----------------
+      if constexpr (KV8) {
+        // Lane l of converter warp w takes 16-byte code chunk c of rows
+        // r0 + l % 8, so the eight lanes of one shared-memory phase touch eight
+        // rows at one chunk: distinct bank groups in both swizzled layouts.
+        constexpr int CPR = D / 16;            // code chunks per row
+        constexpr int ROWS_PASS = 8 * (8 / CPR);  // rows per pass of the 64 threads
+        constexpr int PASSES = kKeyTile / ROWS_PASS;
+        const int ct = (warp - kConvWarp) * 32 + lane;
+        const int q8 = ct >> 3, c = q8 % CPR, rsub = (q8 / CPR) * 8 + (ct & 7);
+        for (int j = 0; j < 2 * nkt; ++j) {
+          const uint32_t g = ring0 + j;
+          const uint32_t slot = g % SLOTS, use = g / SLOTS;
+          wait_or_fail(bar_raw + 8 * slot, use & 1u, failed);
+          const uint32_t sbase = sRing + slot * Lay::KV_BYTES;
+          uint4 codes[PASSES];
+          if (!failed) {
+#pragma unroll
+            for (int i = 0; i < PASSES; ++i) {
+              const int r = i * ROWS_PASS + rsub;
+              const uint32_t a = sbase + RAW_OFF +
+                                 (D == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4));
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                           : "=r"(codes[i].x), "=r"(codes[i].y), "=r"(codes[i].z), "=r"(codes[i].w)
+                           : "r"(a));
+            }
+          }
+          // every code of the slot is in registers before any fp16 row overwrites them
+          asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kConvWarps) : "memory");
+          if (!failed) {
+#pragma unroll
+            for (int i = 0; i < PASSES; ++i) {
+              const int r = i * ROWS_PASS + rsub;
+              const uint32_t w[4] = {codes[i].x, codes[i].y, codes[i].z, codes[i].w};
+              uint32_t h[8];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+                    " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
+                    : "=r"(h[2 * k]), "=r"(h[2 * k + 1])
+                    : "r"(w[k]));
+              }
+              // codes d = 16c .. 16c + 15 -> fp16 chunks 2c (d .. d + 7) and 2c + 1
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sbase + Lay::off(r, 2 * c, Lay::KV_ATOM)),
+                           "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                               sbase + Lay::off(r, 2 * c + 1, Lay::KV_ATOM)),
+                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                           : "memory");
+            }
+            fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+          }
+          __syncwarp();
+          if (lane == 0 && !failed) mbar_arrive(bar_full + 8 * slot);
         }
       }
     } else if (warp == kMmaWarp) {
@@ -505,14 +615,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       const int qi = h * POS_PER_HALF + r / G, g = r % G;
       const bool row_valid = qi < npos;
       const int nk = nkt_h[h];
+      float sl2 = p.scale_log2;  // > 0: the max of raw scores gives the max of scaled ones
       {  // Q of the half: row r = (position, head), K-major, swizzled
         const uint32_t sQ = sQ0 + h * Lay::Q_BYTES;
         const bf16 *qrow =
             p.q + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.q_stride + static_cast<int64_t>(kvh * G + g) * D;
         // q is only required to be 4-byte aligned: 16-byte loads when rows allow them
         const bool q16 = (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 && (p.q_stride & 7) == 0;
-#pragma unroll 4
-        for (int c = 0; c < D / 8; ++c) {
+        auto load_q = [&](int c) {
           uint4 w = make_uint4(0u, 0u, 0u, 0u);
           if (row_valid) {
             if (q16) {
@@ -522,6 +632,34 @@ __global__ void __launch_bounds__(kTileThreads, 1)
               w = make_uint4(__ldg(q32), __ldg(q32 + 1), __ldg(q32 + 2), __ldg(q32 + 3));
             }
           }
+          return w;
+        };
+        // bf16 rows over 8-bit caches: 2^-e, e > 0 only when the row's largest |q| reaches 2^15
+        float qmul = 1.f;
+        if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+          float amax = 0.f;
+#pragma unroll 4
+          for (int c = 0; c < D / 8; ++c) {
+            const uint4 w = load_q(c);
+            const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(v[k])), fabsf(ElemBf16::hi(v[k]))));
+          }
+          const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // floor(log2(amax))
+          const int e = ex >= 15 ? min(ex - 14, 120) : 0;
+          qmul = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+          sl2 *= __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        }
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 w = load_q(c);
+          if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+            w = make_uint4(ElemFp16::pack(ElemBf16::lo(w.x) * qmul, ElemBf16::hi(w.x) * qmul),
+                           ElemFp16::pack(ElemBf16::lo(w.y) * qmul, ElemBf16::hi(w.y) * qmul),
+                           ElemFp16::pack(ElemBf16::lo(w.z) * qmul, ElemBf16::hi(w.z) * qmul),
+                           ElemFp16::pack(ElemBf16::lo(w.w) * qmul, ElemBf16::hi(w.w) * qmul));
+          }
           asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + Lay::off(r, c, Lay::Q_ATOM)),
                        "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
                        : "memory");
@@ -530,7 +668,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q);
       }
-      const float sl2 = p.scale_log2;  // > 0: the max of raw scores gives the max of scaled ones
       float m_used = -INFINITY, l = 0.f;
       const int lim = row_valid ? pos0 + qi + 1 : 0;  // keys j < lim are visible to this row
       for (int kt = 0; kt < nk; ++kt) {
@@ -549,25 +686,32 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           const int ck0 = key0 + 32 * c;
           uint32_t sv[32], u[32];
           tmem_ld32_wait(sp + 32 * c, sv);
-          const float cm = sl2 * masked_max32(sv, ck0, lim);
-          const bool grow = cm > -INFINITY && (m_used == -INFINITY || cm > m_used + kRescaleLog2);
+          // The chunk's maximum, rounded, and its growth over m_used, as separately
+          // rounded operations (no contraction into one fused multiply-add): the
+          // exponents below are bounded by exactly this difference.
+          const float cm = __fmul_rn(sl2, masked_max32(sv, ck0, lim));
+          const bool grow = cm > -INFINITY && (m_used == -INFINITY || __fsub_rn(cm, m_used) > kRescaleLog2);
           if (__any_sync(0xffffffffu, grow)) {
             // The row's maximum grew past the threshold (always in a row's
             // first visible chunk, rarely after): what was taken against the
             // old maximum (this range's sum and stored chunks, and O and l)
             // is scaled by 2^(old - new). TMEM accesses are warp-wide, so the
             // warp does it together (factor 1 in rows that did not grow).
-            const float a = grow && m_used > -INFINITY ? ex2_approx(m_used - cm) : 1.f;
+            const float a = grow && m_used > -INFINITY ? ex2_approx(__fsub_rn(m_used, cm)) : 1.f;
             if (grow) m_used = cm;
             sum *= a;
             alpha *= a;
             if (c > 0) {
               tmem_wait_st();  // the chunks stored so far are read back
 #pragma unroll 1
-              for (int cc = 0; cc < c; ++cc) rescale_p32<E>(sp + 32 * cc, a);
+              for (int cc = 0; cc < c; ++cc) rescale_p32<M>(sp + 32 * cc, a);
             }
           }
-          probs32<E>(sv, ck0, lim, sl2, m_used == -INFINITY ? 0.f : m_used, sum, u);
+          const float ms = m_used == -INFINITY ? 0.f : m_used;
+          if (__any_sync(0xffffffffu, fabsf(ms) > 4096.f))
+            probs32<M, true>(sv, ck0, lim, sl2, ms, sum, u);
+          else
+            probs32<M, false>(sv, ck0, lim, sl2, ms, sum, u);
           tmem_st32u(sp + 32 * c, u);  // P over the scores it came from
         }
         // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
@@ -592,7 +736,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // epilogue: the half's last P V product, normalised
         wait_or_fail(bar_o + 8 * h, (ph[h] + nk - 1) & 1u, failed);
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? p.out_scale / l : 0.f;
         bf16 *dst = p.out + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.num_heads * D +
                     static_cast<int64_t>(kvh * G + g) * D;
 #pragma unroll
@@ -628,8 +772,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (!mbar_wait_bounded(bar_drain, 0, kTcWaitTimeoutNs)) failed = true;
   }
   if (warp == kTmaWarp && lane == 0) {
+    const uint32_t landed = KV8 ? bar_raw : bar_full;  // where the loads' completion is counted
     for (uint32_t g = issued > SLOTS ? issued - SLOTS : 0; g < issued; ++g)
-      if (!mbar_wait_bounded(bar_full + 8 * (g % SLOTS), (g / SLOTS) & 1u, kTcWaitTimeoutNs)) failed = true;
+      if (!mbar_wait_bounded(landed + 8 * (g % SLOTS), (g / SLOTS) & 1u, kTcWaitTimeoutNs)) failed = true;
   }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
   tc_fence_before();
@@ -638,11 +783,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, int G, typename E>
+template <int D, int G, typename E, bool KV8>
 cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp, int sm_count,
                                  cudaStream_t stream) {
   constexpr int smem = TcLayout<D>::REQUEST;
-  auto kern = prefill_tile_kernel<D, G, E>;
+  auto kern = prefill_tile_kernel<D, G, E, KV8>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -651,14 +796,18 @@ cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vma
   const int64_t units = static_cast<int64_t>(tp.max_tiles) * tp.num_kv_heads;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTileThreads), smem, stream, kmap, vmap, tp);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? kTileThreads8 : kTileThreads), smem, stream,
+                    kmap, vmap, tp);
 }
 
-#define PA_TILE_INST(DD, GG)                                                                               \
-  template cudaError_t launch_prefill_tiles<DD, GG, ElemBf16>(const CUtensorMap &, const CUtensorMap &,     \
-                                                              const TileParams &, int, cudaStream_t);      \
-  template cudaError_t launch_prefill_tiles<DD, GG, ElemFp16>(const CUtensorMap &, const CUtensorMap &,     \
-                                                              const TileParams &, int, cudaStream_t);
+#define PA_TILE_INST1(DD, GG, EE, K8)                                                                   \
+  template cudaError_t launch_prefill_tiles<DD, GG, EE, K8>(const CUtensorMap &, const CUtensorMap &,     \
+                                                            const TileParams &, int, cudaStream_t);
+#define PA_TILE_INST(DD, GG)                                                                              \
+  PA_TILE_INST1(DD, GG, ElemBf16, false)                                                                  \
+  PA_TILE_INST1(DD, GG, ElemFp16, false)                                                                  \
+  PA_TILE_INST1(DD, GG, ElemBf16, true)                                                                   \
+  PA_TILE_INST1(DD, GG, ElemFp16, true)
 PA_TILE_INST(128, 1)
 PA_TILE_INST(128, 2)
 PA_TILE_INST(128, 4)
@@ -668,5 +817,6 @@ PA_TILE_INST(64, 2)
 PA_TILE_INST(64, 4)
 PA_TILE_INST(64, 8)
 #undef PA_TILE_INST
+#undef PA_TILE_INST1
 
 }  // namespace pa

@@ -824,14 +824,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       scores(kt0, s0);
       if (two) scores(kt1, s1);
       const int t0 = kb * KT + (lane >> 2), t1 = t0 + 8, t2 = t0 + kTileKeys, t3 = t1 + kTileKeys;
-      const float x0 = t0 < lim[0] ? s0[0] * col_scale[0] : -INFINITY;
-      const float x1 = t0 < lim[1] ? s0[1] * col_scale[1] : -INFINITY;
-      const float x2 = t1 < lim[0] ? s0[2] * col_scale[0] : -INFINITY;
-      const float x3 = t1 < lim[1] ? s0[3] * col_scale[1] : -INFINITY;
-      const float y0 = two && t2 < lim[0] ? s1[0] * col_scale[0] : -INFINITY;
-      const float y1 = two && t2 < lim[1] ? s1[1] * col_scale[1] : -INFINITY;
-      const float y2 = two && t3 < lim[0] ? s1[2] * col_scale[0] : -INFINITY;
-      const float y3 = two && t3 < lim[1] ? s1[3] * col_scale[1] : -INFINITY;
+      const float x0 = t0 < lim[0] ? __fmul_rn(s0[0], col_scale[0]) : -INFINITY;
+      const float x1 = t0 < lim[1] ? __fmul_rn(s0[1], col_scale[1]) : -INFINITY;
+      const float x2 = t1 < lim[0] ? __fmul_rn(s0[2], col_scale[0]) : -INFINITY;
+      const float x3 = t1 < lim[1] ? __fmul_rn(s0[3], col_scale[1]) : -INFINITY;
+      const float y0 = two && t2 < lim[0] ? __fmul_rn(s1[0], col_scale[0]) : -INFINITY;
+      const float y1 = two && t2 < lim[1] ? __fmul_rn(s1[1], col_scale[1]) : -INFINITY;
+      const float y2 = two && t3 < lim[0] ? __fmul_rn(s1[2], col_scale[0]) : -INFINITY;
+      const float y3 = two && t3 < lim[1] ? __fmul_rn(s1[3], col_scale[1]) : -INFINITY;
+      // rounded products (never contracted into the subtractions below), so the
+      // maximum's exponent is exactly zero whatever the magnitude of the scores
       float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -1128,7 +1130,6 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
 
   if (a.max_query_len > w.rows_per_item) {  // some request may be a prefill chunk
-    if (KV8) return cudaErrorNotSupported;    // rejected by the caller
     TileParams tp;
     tp.q = ap.q;
     tp.q_stride = a.q_stride;
@@ -1140,6 +1141,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.num_kv_heads = a.num_kv_heads;
     tp.num_blocks = a.num_blocks;
     tp.scale_log2 = ap.scale_log2;
+    tp.out_scale = ap.out_scale;
     tp.out = ap.out;
     tp.tiles = pp.tiles;
     tp.tile_count = pp.tile_count;
@@ -1148,7 +1150,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.total_q = a.total_q;
     tp.max_tiles = w.max_tiles;
     tp.status = a.status;
-    err = launch_prefill_tiles<D, G, E>(kmap, vmap, tp, a.sm_count, stream);
+    err = launch_prefill_tiles<D, G, E, KV8>(kmap, vmap, tp, a.sm_count, stream);
     if (err != cudaSuccess) return err;
     ++*launched;
   }

@@ -53,6 +53,15 @@ CASES = {
     "g8_d64": dict(context_lens=[1030, 3], query_lens=[1, 1], num_heads=16, num_kv_heads=2, head_dim=64),
     "g4_d128_sharp": dict(context_lens=[300, 2500, 17], query_lens=[1, 2, 1], num_heads=32, num_kv_heads=8,
                           head_dim=128, q_scale=8.0),
+    # chunked-prefill chunks (tensor-core tiles over 8-bit caches) mixed with decode tokens
+    "g4_d128_chunks": dict(context_lens=[0, 37, 600, 20, 1000, 5, 0], query_lens=[40, 2, 1, 129, 1, 7, 300],
+                           num_heads=32, num_kv_heads=8, head_dim=128),
+    "g1_d64_chunks": dict(context_lens=[0, 1000, 5], query_lens=[300, 260, 129], num_heads=4, num_kv_heads=4,
+                          head_dim=64),
+    "g8_d64_chunks": dict(context_lens=[10, 800, 0], query_lens=[5, 1, 24], num_heads=16, num_kv_heads=2,
+                          head_dim=64),
+    "g2_d128_sharp_chunks": dict(context_lens=[700, 3000], query_lens=[200, 77], num_heads=8, num_kv_heads=4,
+                                 head_dim=128, q_scale=8.0),
 }
 
 
@@ -91,9 +100,10 @@ def test_fp8_every_code_round_trips_exactly(dtype, head_dim):
     assert np.array_equal(got, want), "seq_len 1 over an 8-bit cache must return the V row exactly"
 
 
-@pytest.mark.parametrize("name", ["gqa_decode", "mha_decode", "long_decode"])
-def test_fp8_named_full_size_sampled(oracle, name):
-    w = W.by_name(name, seed=0, kv_dtype=FP8)
+@pytest.mark.parametrize("name,dtype", [("gqa_decode", "bf16"), ("mha_decode", "bf16"), ("long_decode", "bf16"),
+                                        ("mixed_step", "bf16"), ("mixed_step", "fp16")])
+def test_fp8_named_full_size_sampled(oracle, name, dtype):
+    w = W.by_name(name, seed=0, kv_dtype=FP8, dtype=dtype)
     st = DeviceStep(w)
     st.run()
     torch.cuda.synchronize()
@@ -156,9 +166,9 @@ def test_fp8_host_errors():
 
 @pytest.mark.parametrize("q_scale", [3.0e4, 2.0e9])
 def test_fp8_bf16_queries_beyond_fp16_range(oracle, q_scale):
-    """Over 8-bit caches the tensor cores take fp16 operands: bf16 q columns whose largest |q|
+    """Over 8-bit caches the tensor cores take fp16 operands: bf16 q rows whose largest |q|
     reaches 2^15 (here up to ~1e5 and ~1e10) are scaled by a power of two first, so they must
-    still match the oracle (the softmax is then nearly one-hot)."""
-    w = W.make_workload(f"fp8_bigq_{q_scale:g}", context_lens=[40, 900, 3, 2100], query_lens=[1, 2, 1, 1],
+    still match the oracle (the softmax is then nearly one-hot); decode tokens and a chunk."""
+    w = W.make_workload(f"fp8_bigq_{q_scale:g}", context_lens=[40, 900, 3, 2100], query_lens=[1, 2, 1, 150],
                         num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype=FP8, q_scale=q_scale, seed=12)
     run_fp8(w, oracle)

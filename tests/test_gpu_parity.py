@@ -371,3 +371,19 @@ def test_named_full_size_sampled(oracle, name, dtype):
     ref = oracle.attention_sampled(w.q, kc_full, vc_full, w.block_tables, w.seq_lens, w.query_start_loc,
                                    w.num_heads, w.scale, tokens, heads, dtype=w.dtype)
     assert_attention_close(out[tokens, heads], ref, f"{name} {dtype}")
+
+
+def test_huge_scores_in_prefill_tiles(oracle):
+    """Scores of order 1e10 (log2 domain) in the tensor-core tiles: the softmax exponent must
+    stay bounded although the products are far beyond fp32's integer precision. (bf16 q of
+    order 1e10: the softmax is one-hot, so fp32 accumulation error, which grows with |q.k|,
+    cannot move a near tie; fp16 q is limited to 65504.)"""
+    w = W.make_workload("huge_scores", context_lens=[900, 0, 2100], query_lens=[150, 300, 1],
+                        num_heads=32, num_kv_heads=8, head_dim=128, q_scale=2.0e9, seed=21)
+    run_and_check(w, oracle)
+
+
+def test_large_fp16_scores_in_prefill_tiles(oracle):
+    w = W.make_workload("large_scores_fp16", context_lens=[900, 0, 2100], query_lens=[150, 300, 1],
+                        num_heads=32, num_kv_heads=8, head_dim=128, q_scale=300.0, seed=21, dtype="fp16")
+    run_and_check(w, oracle)

@@ -111,14 +111,14 @@ def test_fp8_validation_rejects_before_any_cuda_call(lib):
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, float("inf"), 0, None) == -2
     assert r(None, None, 0, 0, None, None, None, 1, 1, 96, 16, 1, 1.0, 1.0, 0, None) == -3   # head_dim
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, 1.0, 1, None) == -1   # fp16: null pointers
-    # pa_attention_varlen_fp8: scales, and query_len limited to 8 / G for now
+    # pa_attention_varlen_fp8: scales and element type
     a = lib.pa_attention_varlen_fp8
     base = [None, 0, None, None, None, 1, None, None, 1, 1, 1, 1, 8, 2, 64, 16, 1, 1.0]
     assert a(*base, 1.0, 1.0, None, None, 0, 0, None) == -1                 # passes to the null check
     assert a(*base, -1.0, 1.0, None, None, 0, 0, None) == -2
     assert a(*base, 1.0, float("nan"), None, None, 0, 0, None) == -2
     assert a(*base, 1.0, 1.0, None, None, 0, 2, None) == -3                 # q must be bf16 or fp16
-    long_q = [None, 0, None, None, None, 0, None, None, 1, 8, 8, 8, 8, 2, 64, 16, 1, 1.0]
-    assert a(*long_q, 1.0, 1.0, None, None, 0, 0, None) == -3               # query_len 8 > 8 / 4
+    long_q = [None, 0, None, None, None, 1, None, None, 1, 8, 8, 8, 8, 2, 64, 16, 1, 1.0]
+    assert a(*long_q, 1.0, 1.0, None, None, 0, 0, None) == -1               # chunks pass to the null check
     assert lib.pa_gather_kv(None, None, None, 4, 2, 64, 16, 10, None, None, 2, None) == -1
     assert lib.pa_launch_count() == 0
