@@ -429,7 +429,9 @@ def run_ours(args, world, rank, local_rank) -> None:
 
     peaks = load_peaks()
     kern_achieved = acct["attention_bytes"] / (kern_ms * 1e-3) / 1e9
-    traffic = committed_traffic(args.workload) if args.dtype == "bf16" and not args.kv_dtype else None
+    # committed counters exist for the default bf16 line and its 8-bit-cache variant
+    traffic = (committed_traffic(args.workload + ("+" + args.kv_dtype if args.kv_dtype else ""))
+               if args.dtype == "bf16" and args.block_size == 16 and not args.rope and not args.batch else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
