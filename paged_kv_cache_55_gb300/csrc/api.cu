@@ -55,13 +55,17 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool valid_cache_scale(float s) { return std::isfinite(s) && s > 0.0f; }
 
+// Head dims with built kernels: 64 and 128, and 80 and 96 (rows padded to
+// whole 64-element swizzle atoms in shared memory).
+bool supported_head_dim(int32_t d) { return d == 64 || d == 80 || d == 96 || d == 128; }
+
 // Bytes of one cache element: 2 for the 16-bit types, 1 for E4M3 codes; 0 if unknown.
 int cache_elem_bytes(int32_t dtype) {
   return (dtype == PA_BF16 || dtype == PA_FP16) ? 2 : (dtype == PA_FP8_E4M3 ? 1 : 0);
 }
 
 bool supported_dims(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
-  if (head_dim != 64 && head_dim != 128) return false;
+  if (!supported_head_dim(head_dim)) return false;
   if (block_size != 8 && block_size != 16 && block_size != 32) return false;
   if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return false;
   const int G = num_heads / num_kv_heads;
@@ -106,7 +110,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
   if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
     return PA_ERR_DIMS;
-  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
   if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
@@ -136,7 +140,7 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t k
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
     return PA_ERR_DIMS;
   if (!valid_cache_scale(k_scale) || !valid_cache_scale(v_scale)) return PA_ERR_DIMS;
-  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
   if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
@@ -349,7 +353,7 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   const int esize = cache_elem_bytes(dtype);
   if (!esize) return PA_ERR_UNSUPPORTED;
   if (seq_len < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_DIMS;
-  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
   if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (seq_len == 0) return PA_OK;
   if (!key_cache || !value_cache || !block_table_row || !key_out || !value_out) return PA_ERR_NULL;

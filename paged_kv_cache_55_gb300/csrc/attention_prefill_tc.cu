@@ -77,7 +77,9 @@ struct TcTmem {
 
 template <int D>
 struct TcLayout {
-  static constexpr int ATOMS = D / 64;             // 64-element swizzle atoms along D
+  // 64-element swizzle atoms along D; head_dim 80 or 96 is padded to two, the
+  // columns past it zero-filled by TMA (K, V) and never read (Q)
+  static constexpr int ATOMS = (D + 63) / 64;
   static constexpr int Q_ATOM = kHalfRows * 128;   // 128 rows x 128 B
   static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
@@ -280,7 +282,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   using Tm = TcTmem<D>;
   using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
   constexpr int NTHREADS = KV8 ? kTileThreads8 : kTileThreads;
-  constexpr int RAW_BYTES = kKeyTile * D;          // 8-bit codes of one range
+  constexpr int RAW_ROW = D <= 64 ? 64 : 128;      // bytes per staged row of codes (padded past head_dim)
+  constexpr int RAW_BYTES = kKeyTile * RAW_ROW;    // 8-bit codes of one range
   constexpr uint32_t RAW_OFF = Lay::KV_BYTES / 2;  // staged in the back half of the slot
   static_assert(RAW_BYTES == Lay::KV_BYTES / 2, "a range's codes fill half of its 16-bit slot");
   constexpr int KSTEPS_S = D / 16;         // UMMA K steps of S = Q K^T
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             for (int j = 0; j < nb; ++j) {
               const int i = kt * nb + j;
               const int z = i < nboxes ? (i < Lay::TABLE_ENTRIES ? zbox[i] : box_z(i)) : -box_rows;
-              tma_load_3d(dst + j * box_rows * D, map, bar, 0, kvh, z);
+              tma_load_3d(dst + j * box_rows * RAW_ROW, map, bar, 0, kvh, z);
             }
             return;
           }
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         // Lane l of converter warp w takes 16-byte code chunk c of rows
         // r0 + l % 8, so the eight lanes of one shared-memory phase touch eight
         // rows at one chunk: distinct bank groups in both swizzled layouts.
-        constexpr int CPR = D / 16;            // code chunks per row
+        constexpr int CPR = RAW_ROW / 16;      // code chunks per staged row (zeros past head_dim)
         constexpr int ROWS_PASS = 8 * (8 / CPR);  // rows per pass of the 64 threads
         constexpr int PASSES = kKeyTile / ROWS_PASS;
         const int ct = (warp - kConvWarp) * 32 + lane;
@@ -478,8 +481,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
 #pragma unroll
             for (int i = 0; i < PASSES; ++i) {
               const int r = i * ROWS_PASS + rsub;
-              const uint32_t a = sbase + RAW_OFF +
-                                 (D == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4));
+              const uint32_t a = sbase + RAW_OFF + (RAW_ROW == 128 ? r * 128 + (((c ^ r) & 7) << 4)
+                                                                     : r * 64 + (((c ^ (r >> 1)) & 3) << 4));
               asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
                            : "=r"(codes[i].x), "=r"(codes[i].y), "=r"(codes[i].z), "=r"(codes[i].w)
                            : "r"(a));
@@ -718,7 +721,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         // last of them finished).
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
+          for (int ch = 0; ch < (D + 31) / 32; ++ch) {  // head_dim 80: also 16 unused columns
             uint32_t t[32];
             tmem_ld32_wait(t_lane + Tm::O + ch * 32, t);
 #pragma unroll
@@ -740,16 +743,17 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         bf16 *dst = p.out + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.num_heads * D +
                     static_cast<int64_t>(kvh * G + g) * D;
 #pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) {
-          uint32_t t[64];
-          tmem_ld64_wait(t_lane + Tm::O + ch * 64, t);
+        for (int ch = 0; ch < (D + 31) / 32; ++ch) {
+          uint32_t t[32];
+          tmem_ld32_wait(t_lane + Tm::O + ch * 32, t);
           if (row_valid && !failed) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
+              if (32 * ch + 8 * c >= D) continue;  // head_dim 80: the last 16 columns are padding
               const float *f = reinterpret_cast<const float *>(&t[8 * c]);
               const uint4 v = make_uint4(E::pack(f[0] * inv, f[1] * inv), E::pack(f[2] * inv, f[3] * inv),
                                          E::pack(f[4] * inv, f[5] * inv), E::pack(f[6] * inv, f[7] * inv));
-              *reinterpret_cast<uint4 *>(dst + ch * 64 + 8 * c) = v;
+              *reinterpret_cast<uint4 *>(dst + ch * 32 + 8 * c) = v;
             }
           }
         }
@@ -816,6 +820,14 @@ PA_TILE_INST(64, 1)
 PA_TILE_INST(64, 2)
 PA_TILE_INST(64, 4)
 PA_TILE_INST(64, 8)
+PA_TILE_INST(96, 1)
+PA_TILE_INST(96, 2)
+PA_TILE_INST(96, 4)
+PA_TILE_INST(96, 8)
+PA_TILE_INST(80, 1)
+PA_TILE_INST(80, 2)
+PA_TILE_INST(80, 4)
+PA_TILE_INST(80, 8)
 #undef PA_TILE_INST
 #undef PA_TILE_INST1
 

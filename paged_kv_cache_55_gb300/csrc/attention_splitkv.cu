@@ -389,7 +389,10 @@ struct MergeParams {
 
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams p) {
-  constexpr int EPL = D / 32;  // outputs per lane: 4 (D=128) or 2 (D=64)
+  // outputs per lane: 4 (D=128), 2 (D=64), else ceil(D / 32) consecutive
+  // elements with the lane's last ones past D unused (D = 80, 96)
+  constexpr int EPL = (D + 31) / 32;
+  constexpr bool VEC = D % 64 == 0;
   griddep_wait();
   const int b = blockIdx.x / p.num_kv_heads, kvh = blockIdx.x - b * p.num_kv_heads;
   const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -413,7 +416,10 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
       const int k = min(k0 + j, np - 1);
       lv[j] = ld_cg(p.part_lse + base + k * kCols);
       const float *src = p.part_o + (base + k * kCols) * D + lane * EPL;
-      if constexpr (EPL == 4) {
+      if constexpr (!VEC) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) ov[j][e] = lane * EPL + e < D ? ld_cg(src + e) : 0.f;
+      } else if constexpr (EPL == 4) {
         const float4 v = ld_cg(reinterpret_cast<const float4 *>(src));
         ov[j][0] = v.x;
         ov[j][1] = v.y;
@@ -448,7 +454,14 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   bf16 *dst = p.out + static_cast<int64_t>(q0 + qi) * p.num_heads * D + static_cast<int64_t>(kvh * G + g) * D +
               lane * EPL;
-  if constexpr (EPL == 4) {
+  if constexpr (!VEC) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if (lane * EPL + e < D) {
+        const uint32_t v = E::pack(acc[e] * inv, 0.f);
+        *reinterpret_cast<unsigned short *>(dst + e) = static_cast<unsigned short>(v & 0xffffu);
+      }
+  } else if constexpr (EPL == 4) {
     *reinterpret_cast<uint2 *>(dst) =
         make_uint2(E::pack(acc[0] * inv, acc[1] * inv), E::pack(acc[2] * inv, acc[3] * inv));
   } else {
@@ -502,9 +515,11 @@ __device__ __forceinline__ Unit fetch_unit(const AttnParams &p, int total_units,
 template <int D, bool KV8>
 struct TileGeom;
 // 16-bit caches: a 16-key tile is D / 64 boxes of 16 rows x 128 bytes (128-byte swizzle).
+// head_dim 80 or 96: rows padded to whole atoms; the box columns past
+// head_dim lie outside the tensor, so TMA fills them with zeros (no HBM read).
 template <int D>
 struct TileGeom<D, false> {
-  static constexpr int HALVES = D / 64;                // 64-element (128-byte) swizzle atoms per row
+  static constexpr int HALVES = (D + 63) / 64;         // 64-element (128-byte) swizzle atoms per row
   static constexpr int HALF_BYTES = kTileKeys * 128;  // 16 rows x 128 B
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;  // K tile then V tile
@@ -518,15 +533,16 @@ struct TileGeom<D, false> {
 // swizzle at D = 128 (16-byte chunk c of row r at c ^ (r % 8)) and 64-byte
 // swizzle at D = 64 (chunk c of row r at c ^ (r / 2 % 4)); either way eight
 // consecutive rows read at one chunk hit eight different bank groups, and
-// rows 16..31 have the layout of rows 0..15 shifted by 16 * D bytes.
+// rows 16..31 have the layout of rows 0..15 shifted by 16 * ROW bytes.
 constexpr int kTileKeys8 = 32;
 template <int D>
 struct TileGeom<D, true> {
-  static_assert(D == 64 || D == 128, "8-bit tiles are one swizzle span wide");
-  static constexpr int TILE_BYTES = kTileKeys8 * D;
+  static_assert(D <= 128, "8-bit tiles are one swizzle span wide");
+  static constexpr int ROW = D <= 64 ? 64 : 128;  // row bytes (head_dim 80, 96: padded, zero-filled by TMA)
+  static constexpr int TILE_BYTES = kTileKeys8 * ROW;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static __device__ __forceinline__ uint32_t off(int r, int c) {
-    return D == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
+    return ROW == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
   }
 };
 
@@ -542,7 +558,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   constexpr int KT = KV8 ? kTileKeys8 : kTileKeys;            // keys per ring tile
   constexpr int S = kSmemBudget / (NWARPS * T::SLOT_BYTES);  // ring slots per warp
   static_assert(S >= 2, "ring needs at least two slots");
-  constexpr int MT = D / 16;
+  constexpr int MT = D / 16;  // k steps of S, m tiles of O
+  // 8-bit caches: an ldmatrix.x4 covers 32 d, so fragments come in pairs; a
+  // head_dim of 80 computes one more (all-zero) k step and m tile
+  constexpr int MQ = KV8 ? 2 * ((D + 31) / 32) : MT;
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[NWARPS][S];
@@ -589,8 +608,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             z = (phys << p.block_shift) + (key & (bs - 1));
         }
         if constexpr (KV8) {
-          tma_load_3d(dst + j * box_rows * D, &kmap, bar, 0, U.kvh, z);
-          tma_load_3d(dst + T::TILE_BYTES + j * box_rows * D, &vmap, bar, 0, U.kvh, z);
+          tma_load_3d(dst + j * box_rows * T::ROW, &kmap, bar, 0, U.kvh, z);
+          tma_load_3d(dst + T::TILE_BYTES + j * box_rows * T::ROW, &vmap, bar, 0, U.kvh, z);
         } else {
 #pragma unroll
           for (int h = 0; h < T::HALVES; ++h) {
@@ -641,7 +660,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 
   while (cur.valid) {
     // ---- per-unit set-up: q fragments (B operand of S^T = K Q^T), causal limits ----
-    uint32_t qf[MT][2];
+    uint32_t qf[MQ][2];
     float col_scale[2] = {p.scale_log2, p.scale_log2};  // log2-domain score factor of accumulator columns
     {
       const int n = lane >> 2, qi = n / G, g = n % G;
@@ -653,9 +672,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         // in which the 8-bit K fragments below hold d
         qp += 4 * (lane & 3);
 #pragma unroll
-        for (int kk = 0; kk < MT; ++kk) {
-          const uint32_t x = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
-          const uint32_t y = ok ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 2)) : 0u;
+        for (int kk = 0; kk < MQ; ++kk) {
+          const bool in = ok && kk < MT;  // k steps past head_dim multiply zero-filled codes: q is 0 there
+          const uint32_t x = in ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk)) : 0u;
+          const uint32_t y = in ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * kk + 2)) : 0u;
           qf[kk][0] = __byte_perm(x, y, 0x5410);
           qf[kk][1] = __byte_perm(x, y, 0x7632);
         }
@@ -667,7 +687,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           // converts exactly (fp16 keeps 11 significant bits, bf16 has 8).
           float amax = 0.f;
 #pragma unroll
-          for (int kk = 0; kk < MT; ++kk)
+          for (int kk = 0; kk < MQ; ++kk)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(qf[kk][h])), fabsf(ElemBf16::hi(qf[kk][h]))));
@@ -677,7 +697,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           const int e = ex >= 15 ? min(ex - 14, 120) : 0;
           const float f = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
 #pragma unroll
-          for (int kk = 0; kk < MT; ++kk)
+          for (int kk = 0; kk < MQ; ++kk)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               qf[kk][h] = ElemFp16::pack(ElemBf16::lo(qf[kk][h]) * f, ElemBf16::hi(qf[kk][h]) * f);
@@ -703,9 +723,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const int qi = (2 * (lane & 3) + e) / G;
       lim[e] = qi < cur.nrows ? min(cur.pos0 + qi + 1, cur.kv_end) : cur.kv_begin;
     }
-    float o[MT][4];
+    float o[MQ][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int mt = 0; mt < MQ; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
 
@@ -728,7 +748,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         // lane/4 and lane/4 + 8 in each of two 16-d chunks, widened exactly
         // into the A fragments of two k steps (d paired as q is above)
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
+        for (int j = 0; j < MQ / 2; ++j) {
           uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
           ldsm_x4(kt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
           M::from_e4m3x4(r0, l0, h0);
@@ -760,7 +780,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         // lane/4 of m tile mt holds d = 16mt + 2(lane/4), row lane/4 + 8 holds
         // d = 16mt + 2(lane/4) + 1; the epilogue puts d back in order.
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
+        for (int j = 0; j < MQ / 2; ++j) {
           uint32_t r0, r1, r2, r3, l0, h0, l1, h1;
           ldsm_x4_t(vt + T::off(arow, 2 * j + (lane >> 4)), r0, r1, r2, r3);
           M::from_e4m3x4(r0, l0, h0);
@@ -796,8 +816,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         landed = mbar_wait_bounded(smem_u32(&bars[warp][slot]), (consumed / S) & 1u, kWaitTimeoutNs);
         kt0 = my_ring + slot * T::SLOT_BYTES;
         vt0 = kt0 + T::TILE_BYTES;
-        kt1 = kt0 + kTileKeys * D;  // rows 16..31
-        vt1 = vt0 + kTileKeys * D;
+        kt1 = kt0 + kTileKeys * T::ROW;  // rows 16..31
+        vt1 = vt0 + kTileKeys * T::ROW;
       } else {
         const uint32_t slot0 = consumed % S, slot1 = (consumed + 1) % S;
         landed = mbar_wait_bounded(smem_u32(&bars[warp][slot0]), (consumed / S) & 1u, kWaitTimeoutNs);
@@ -854,7 +874,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       m[1] = mn1;
       if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+        for (int mt = 0; mt < MQ; ++mt) {
           o[mt][0] *= al0;
           o[mt][1] *= al1;
           o[mt][2] *= al0;
@@ -1035,13 +1055,14 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_bl
   // box rows: min(block_size, keys per tile), the tile being 16 keys (32 for 8-bit caches)
   const int kt = kv8 ? kTileKeys8 : kTileKeys;
   const cuuint32_t rows = static_cast<cuuint32_t>(block_size < kt ? block_size : kt);
-  const cuuint32_t box[3] = {kv8 ? static_cast<cuuint32_t>(head_dim) : 64u, 1, rows};
+  // 8-bit rows: one box of 64 or 128 codes (head_dim 80, 96: the columns past it are zero-filled)
+  const cuuint32_t box[3] = {kv8 ? (head_dim <= 64 ? 64u : 128u) : 64u, 1, rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType type = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                        : (dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   const CUtensorMapSwizzle swz =
-      kv8 && head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+      kv8 && head_dim <= 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return encode(map, type, 3, const_cast<void *>(cache), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1190,6 +1211,8 @@ cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *laun
   }
   PA_DISPATCH(128, 1) PA_DISPATCH(128, 2) PA_DISPATCH(128, 4) PA_DISPATCH(128, 8)
   PA_DISPATCH(64, 1) PA_DISPATCH(64, 2) PA_DISPATCH(64, 4) PA_DISPATCH(64, 8)
+  PA_DISPATCH(96, 1) PA_DISPATCH(96, 2) PA_DISPATCH(96, 4) PA_DISPATCH(96, 8)
+  PA_DISPATCH(80, 1) PA_DISPATCH(80, 2) PA_DISPATCH(80, 4) PA_DISPATCH(80, 8)
 #undef PA_DISPATCH
   return cudaErrorInvalidValue;
 }

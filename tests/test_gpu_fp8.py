@@ -58,6 +58,10 @@ CASES = {
                            num_heads=32, num_kv_heads=8, head_dim=128),
     "g1_d64_chunks": dict(context_lens=[0, 1000, 5], query_lens=[300, 260, 129], num_heads=4, num_kv_heads=4,
                           head_dim=64),
+    "g4_d80_mixed": dict(context_lens=[0, 700, 33, 1500, 20], query_lens=[1, 1, 2, 1, 150], num_heads=16,
+                         num_kv_heads=4, head_dim=80),
+    "g2_d96_mixed": dict(context_lens=[1030, 3, 260, 0], query_lens=[1, 4, 1, 300], num_heads=8, num_kv_heads=4,
+                         head_dim=96),
     "g8_d64_chunks": dict(context_lens=[10, 800, 0], query_lens=[5, 1, 24], num_heads=16, num_kv_heads=2,
                           head_dim=64),
     "g2_d128_sharp_chunks": dict(context_lens=[700, 3000], query_lens=[200, 77], num_heads=8, num_kv_heads=4,
@@ -75,7 +79,7 @@ def test_fp8_cases(oracle, name, bs):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("head_dim", [64, 80, 96, 128])
 def test_fp8_every_code_round_trips_exactly(dtype, head_dim):
     """seq_len 1: the output is the token's own V row. With v_scale = 2^-4 and V made of
     code values times 2^-4 (exact in bf16 and fp16), the scatter stores those codes and the

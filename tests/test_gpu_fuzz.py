@@ -17,7 +17,7 @@ def random_case(seed: int) -> W.Workload:
     rng = np.random.default_rng(1000 + seed)
     G = int(rng.choice([1, 2, 4, 8]))
     Hkv = int(rng.choice([1, 2, 4]))
-    D = int(rng.choice([64, 128]))
+    D = int(rng.choice([64, 80, 96, 128]))
     bs = int(rng.choice([8, 16, 32]))
     dtype = str(rng.choice(["bf16", "fp16"]))
     B = int(rng.integers(1, 13))
@@ -26,7 +26,8 @@ def random_case(seed: int) -> W.Workload:
     ql = np.where(kind == "empty", 0, np.where(kind == "decode", 1, np.where(
         kind == "draft", rng.integers(2, 10, size=B), rng.integers(10, 300, size=B))))
     q_scale = float(rng.choice([1.0, 4.0]))
-    return W.make_workload(f"fuzz{seed}", context_lens=ctx, query_lens=ql, num_heads=Hkv * G, num_kv_heads=Hkv,
+    name = f"fuzz{seed}_g{G}_hkv{Hkv}_d{D}_bs{bs}_{dtype}_q{q_scale:g}"
+    return W.make_workload(name, context_lens=ctx, query_lens=ql, num_heads=Hkv * G, num_kv_heads=Hkv,
                            head_dim=D, block_size=bs, seed=seed, dtype=dtype, q_scale=q_scale)
 
 

@@ -63,6 +63,17 @@ SMALL_CASES = {
                                  num_heads=32, num_kv_heads=8, head_dim=128),
     "mixed_chunks_g1_d128": dict(context_lens=[0, 300, 64], query_lens=[17, 1, 33],
                                  num_heads=4, num_kv_heads=4, head_dim=128),
+    # head dims 80 and 96: rows padded to two 64-element atoms, zero-filled past head_dim
+    "decode_g4_d80": dict(context_lens=[0, 700, 33, 1500], query_lens=[1, 1, 2, 1], num_heads=16, num_kv_heads=4,
+                          head_dim=80),
+    "decode_g8_d96": dict(context_lens=[1030, 3, 260], query_lens=[1, 1, 1], num_heads=16, num_kv_heads=2,
+                          head_dim=96),
+    "chunks_g4_d80": dict(context_lens=[0, 37, 600, 20], query_lens=[40, 2, 1, 300], num_heads=16, num_kv_heads=4,
+                          head_dim=80),
+    "chunks_g1_d96": dict(context_lens=[0, 1000, 5], query_lens=[300, 260, 129], num_heads=4, num_kv_heads=4,
+                          head_dim=96),
+    "chunks_g2_d96": dict(context_lens=[500, 0], query_lens=[77, 200], num_heads=8, num_kv_heads=4, head_dim=96,
+                          q_scale=8.0),
     "mixed_chunks_g8_d64": dict(context_lens=[10, 800, 0], query_lens=[5, 1, 24],
                                 num_heads=16, num_kv_heads=2, head_dim=64),
     # chunks that fill both 128-row halves of a tile, several tiles and a ragged tail
@@ -314,7 +325,7 @@ def test_host_side_errors():
 
     assert call() == 0
     assert call(q=None) == -1
-    assert call(D=96) == -3
+    assert call(D=112) == -3
     assert call(bs=64) == -3
     assert call(Hkv=3) == -2
     assert call(dtype=2) == -3  # 0 = bf16, 1 = fp16

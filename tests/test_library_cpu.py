@@ -57,7 +57,9 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert n > 256 * 8 * 16 * 8 * 128 * 4
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 16) > 0
     # unsupported or inconsistent sizes give 0
-    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 96, 16) == 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 112, 16) == 0  # head dims 64, 80, 96, 128
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 96, 16) > 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 80, 16) > 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 3, 64, 16) == 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 64) == 0  # block sizes 8, 16, 32 only
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 32) > 0
@@ -109,7 +111,8 @@ def test_fp8_validation_rejects_before_any_cuda_call(lib):
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, 1.0, 2, None) == -3   # 8-bit inputs
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 0.0, 1.0, 0, None) == -2   # zero scale
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, float("inf"), 0, None) == -2
-    assert r(None, None, 0, 0, None, None, None, 1, 1, 96, 16, 1, 1.0, 1.0, 0, None) == -3   # head_dim
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 112, 16, 1, 1.0, 1.0, 0, None) == -3  # head_dim
+    assert r(None, None, 0, 0, None, None, None, 1, 1, 80, 16, 1, 1.0, 1.0, 0, None) == -1   # 80: null pointers
     assert r(None, None, 0, 0, None, None, None, 1, 1, 64, 16, 1, 1.0, 1.0, 1, None) == -1   # fp16: null pointers
     # pa_attention_varlen_fp8: scales and element type
     a = lib.pa_attention_varlen_fp8
