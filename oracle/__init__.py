@@ -101,6 +101,9 @@ class Oracle:
         L.oracle_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32,
                                                    ctypes.c_float, ctypes.c_float]
         L.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+        L.oracle_rope_reshape_and_cache_fp8.argtypes = L.oracle_rope_reshape_and_cache.argtypes + [ctypes.c_float,
+                                                                                                   ctypes.c_float]
+        L.oracle_rope_reshape_and_cache_fp8.restype = ctypes.c_int
 
     @staticmethod
     def _check(rc: int, what: str) -> None:
@@ -162,6 +165,28 @@ class Oracle:
             _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slots), _ptr(pos), _ptr(cs),
             int(cs.shape[0]), int(cs.shape[1]), int(bool(is_neox)), T, H, hkv, D, bs, nb, DTYPES[dtype])
         self._check(rc, "rope_reshape_and_cache")
+
+    def rope_reshape_and_cache_fp8(self, q, key, value, key_cache, value_cache, slot_mapping, positions,
+                                   cos_sin_cache, is_neox: bool, block_size: int, k_scale: float, v_scale: float,
+                                   dtype: str = "bf16"):
+        """As rope_reshape_and_cache into 8-bit caches (uint8): the rotated key and the value rows
+        are stored as E4M3 codes of x / k_scale and x / v_scale."""
+        assert q.flags.c_contiguous and q.dtype == np.uint16
+        assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+        assert key_cache.dtype == np.uint8 and value_cache.dtype == np.uint8
+        key = np.ascontiguousarray(key, dtype=np.uint16)
+        value = np.ascontiguousarray(value, dtype=np.uint16)
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        pos = np.ascontiguousarray(positions, dtype=np.int64)
+        cs = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+        T, H, D = q.shape
+        nb, bs, hkv, d = key_cache.shape
+        assert bs == block_size and d == D
+        rc = self.lib.oracle_rope_reshape_and_cache_fp8(
+            _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slots), _ptr(pos), _ptr(cs),
+            int(cs.shape[0]), int(cs.shape[1]), int(bool(is_neox)), T, H, hkv, D, bs, nb, DTYPES[dtype],
+            float(k_scale), float(v_scale))
+        self._check(rc, "rope_reshape_and_cache_fp8")
 
     def decode_elements(self, bits, dtype: str = "bf16") -> np.ndarray:
         """The oracle's widening of 16-bit element bit patterns to float64."""

@@ -467,6 +467,60 @@ int oracle_rope_reshape_and_cache(uint16_t *q, const uint16_t *key, const uint16
     return ORACLE_OK;
 }
 
+/*
+ * The same rotation into 8-bit caches: q is rotated in place as above; the
+ * rotated key row (rounded once to the element type, as above) and the value
+ * row are stored as E4M3 codes of x / k_scale and x / v_scale, i.e. exactly
+ * the rotation followed by oracle_reshape_and_cache_fp8's quantisation.
+ */
+int oracle_rope_reshape_and_cache_fp8(uint16_t *q, const uint16_t *key, const uint16_t *value,
+                                      uint8_t *key_cache, uint8_t *value_cache, const int64_t *slot_mapping,
+                                      const int64_t *positions, const float *cos_sin_cache, int32_t max_position,
+                                      int32_t rotary_dim, int32_t is_neox, int64_t num_tokens, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                      int32_t dtype, float k_scale, float v_scale)
+{
+    if (num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        rotary_dim <= 0 || rotary_dim % 2 || rotary_dim > head_dim || max_position <= 0 ||
+        (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) || !(k_scale > 0.0f) || !(v_scale > 0.0f) ||
+        isinf(k_scale) || isinf(v_scale))
+        return ORACLE_ERR_ARG;
+    const int64_t D = head_dim;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)D);
+    if (!tmp)
+        return ORACLE_ERR_NOMEM;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t pos = positions[t];
+        if (pos < 0 || pos >= max_position) {
+            free(tmp);
+            return ORACLE_ERR_ARG;
+        }
+        const float *cs = cos_sin_cache + pos * rotary_dim;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            uint16_t *row = q + (t * num_heads + h) * D;
+            rotate_row(tmp, row, head_dim, cs, rotary_dim, is_neox, dtype);
+            memcpy(row, tmp, sizeof(uint16_t) * (size_t)D);
+        }
+        const int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= num_blocks * block_size) {
+            free(tmp);
+            return ORACLE_ERR_SLOT_RANGE;
+        }
+        const int64_t row = (int64_t)num_kv_heads * D;
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            rotate_row(tmp, key + (t * num_kv_heads + h) * D, head_dim, cs, rotary_dim, is_neox, dtype);
+            for (int64_t d = 0; d < D; ++d) {
+                key_cache[s * row + h * D + d] = quantize_elem(dtype, tmp[d], k_scale);
+                value_cache[s * row + h * D + d] = quantize_elem(dtype, value[(t * num_kv_heads + h) * D + d], v_scale);
+            }
+        }
+    }
+    free(tmp);
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step 2: attention over the paged cache                                    */
 /* ------------------------------------------------------------------------ */

@@ -610,7 +610,40 @@ def pin_fp8_attention_vs_sdpa(oracle):
         assert err <= 1e-12, f"8-bit cache attention vs SDPA max |diff| {err} for {(ctx, ql, H, Hkv, D, bs)}"
 
 
+def pin_rope_fp8_identity_and_quarter_turn(oracle):
+    """The rotary scatter into 8-bit caches: at position 0 the codes are PyTorch's cast of
+    k / k_scale and v / v_scale; with a row (cos 0, sin 1) K's rotated pairs become
+    (-x2, x1) exactly, so their codes are the cast of those over k_scale."""
+    rng = np.random.default_rng(45)
+    ks, vs = np.float32(0.07), np.float32(0.05)
+    D, rot, half = 32, 16, 8
+    quarter = np.zeros((2, rot), dtype=np.float32)
+    quarter[0, :half] = 1.0
+    quarter[1, half:] = 1.0
+    for dtype in ("bf16", "fp16"):
+        for table, pos in ((rope_cos_sin_cache(64, rot), [0] * 6), (quarter, [1] * 6)):
+            p = RopeProblem(rng, D=D, rot=rot, dtype=dtype, table=table, positions=pos)
+            q = p.q.copy()
+            kc = np.full((p.nb, p.bs, p.k.shape[1], D), 0x7F, dtype=np.uint8)
+            vc = kc.copy()
+            oracle.rope_reshape_and_cache_fp8(q, p.k, p.v, kc, vc, p.slots, p.pos, p.table, True, p.bs,
+                                              float(ks), float(vs), dtype)
+            kx = bits_to_f32(p.k, dtype)
+            if pos[0] == 1:  # neox pairs (i, i + half), i < half: (x1, x2) -> (-x2, x1)
+                kr = kx.copy()
+                kr[..., :half] = -kx[..., half:rot]
+                kr[..., half:rot] = kx[..., :half]
+                kx = kr
+            want_k = _torch_e4m3_codes(kx / ks)
+            want_v = _torch_e4m3_codes(bits_to_f32(p.v, dtype) / vs)
+            got_k = kc.reshape(-1, p.k.shape[1], D)[p.slots]
+            got_v = vc.reshape(-1, p.k.shape[1], D)[p.slots]
+            assert np.array_equal(got_k, want_k), f"8-bit rotary K codes ({dtype}, position {pos[0]})"
+            assert np.array_equal(got_v, want_v), f"8-bit rotary V codes ({dtype})"
+
+
 PINS += [
+    pin_rope_fp8_identity_and_quarter_turn,
     pin_fp8_decode_matches_torch,
     pin_fp8_round_matches_torch,
     pin_fp8_round_saturates_and_specials,

@@ -36,6 +36,10 @@ MUTANTS = {
                           "return e4m3_to_double(((const uint8_t *)cache)[idx]) / scale;"),
     "fp8_v_scale_for_k": ("K[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->k_scale);",
                           "K[(int64_t)j * D + d] = cache_value(p, p->key_cache, base + d, p->v_scale);"),
+    "rope_fp8_key_unrotated": ("key_cache[s * row + h * D + d] = quantize_elem(dtype, tmp[d], k_scale);",
+                               "key_cache[s * row + h * D + d] = quantize_elem(dtype, key[(t * num_kv_heads + h) * D + d], k_scale);"),
+    "rope_fp8_v_scale_for_k": ("key_cache[s * row + h * D + d] = quantize_elem(dtype, tmp[d], k_scale);",
+                               "key_cache[s * row + h * D + d] = quantize_elem(dtype, tmp[d], v_scale);"),
     "fp8_quotient_in_double": ("float qf = xf / scale;                      /* binary32 division, correctly rounded */",
                                "double qf = (double)xf / (double)scale;"),
     "fp16_exponent_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
