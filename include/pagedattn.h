@@ -260,6 +260,24 @@ pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void 
                                     int32_t dtype, void *stream);
 
 /*
+ * The same rotation into 8-bit caches: q is rotated in place as above; the
+ * rotated key row (rounded once to `dtype`, exactly as above) and the value
+ * row are stored as the E4M3 codes of x / k_scale and x / v_scale, as
+ * pa_reshape_and_cache_fp8 stores them. key_cache, value_cache: (device)
+ * uint8 [num_blocks, block_size, num_kv_heads, head_dim], 16-byte aligned;
+ * head_dim a multiple of 16; k_scale and v_scale finite and positive
+ * (PA_ERR_DIMS otherwise). Other arguments and errors as above.
+ */
+pa_status pa_rope_reshape_and_cache_fp8(void *q, int64_t q_token_stride, const void *key, const void *value,
+                                        int64_t key_token_stride, int64_t value_token_stride,
+                                        void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                                        const int64_t *positions, const float *cos_sin_cache,
+                                        int32_t max_position, int32_t rotary_dim, int32_t is_neox,
+                                        int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                        float k_scale, float v_scale, int32_t dtype, void *stream);
+
+/*
  * Copy-on-write block copy (LLM-infra reading map, §2.2: a physical block
  * shared by several requests is copied before one of them writes into it).
  * For each pair i < num_pairs, copy physical block block_mapping[2*i] to

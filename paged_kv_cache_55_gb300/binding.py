@@ -56,6 +56,9 @@ SIGNATURES = {
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
+    "pa_rope_reshape_and_cache_fp8": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                       _I32, _I32, _I32, _I32, _I64, ctypes.c_float, ctypes.c_float, _I32, _P],
+                                      ctypes.c_int32),
     "pa_reshape_and_cache_fp8": ([_P, _P, _I64, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, ctypes.c_float,
                                   ctypes.c_float, _I32, _P], ctypes.c_int),
     "pa_attention_varlen_fp8": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -279,6 +282,36 @@ def pa_rope_reshape_and_cache(q: torch.Tensor, key: torch.Tensor, value: torch.T
                                             value_cache.data_ptr(), slot_mapping.data_ptr(), positions.data_ptr(),
                                             cos_sin_cache.data_ptr(), max_pos, rot, int(bool(is_neox)), T, H, hkv, D,
                                             bs, nb, dt, _stream(stream)), "pa_rope_reshape_and_cache")
+
+
+def pa_rope_reshape_and_cache_fp8(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                                  key_cache: torch.Tensor, value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                                  positions: torch.Tensor, cos_sin_cache: torch.Tensor, k_scale: float,
+                                  v_scale: float, is_neox: bool = True, stream=None) -> None:
+    """pa_rope_reshape_and_cache into 8-bit caches (uint8 [NB, bs, Hkv, D] of E4M3 codes): the rotated
+    key and the value rows are stored as codes of x / k_scale and x / v_scale."""
+    dt = _elem_code((q, "q"), (key, "key"), (value, "value"))
+    _need(key_cache, "key_cache", torch.uint8)
+    _need(value_cache, "value_cache", torch.uint8)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(positions, "positions", torch.int64)
+    _need(cos_sin_cache, "cos_sin_cache", torch.float32)
+    T, H, D = q.shape
+    _, hkv, d = key.shape
+    for t, n in ((q, "q"), (key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"each token row of {n} must be [heads, D] contiguous")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous() and cos_sin_cache.is_contiguous()
+            and slot_mapping.is_contiguous() and positions.is_contiguous()):
+        raise ValueError("caches, cos_sin_cache, slot_mapping and positions must be contiguous")
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    max_pos, rot = cos_sin_cache.shape
+    _check(_lib().pa_rope_reshape_and_cache_fp8(q.data_ptr(), q.stride(0), key.data_ptr(), value.data_ptr(),
+                                                key.stride(0), value.stride(0), key_cache.data_ptr(),
+                                                value_cache.data_ptr(), slot_mapping.data_ptr(), positions.data_ptr(),
+                                                cos_sin_cache.data_ptr(), max_pos, rot, int(bool(is_neox)), T, H,
+                                                hkv, D, bs, nb, float(k_scale), float(v_scale), dt, _stream(stream)),
+           "pa_rope_reshape_and_cache_fp8")
 
 
 def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,

@@ -292,18 +292,23 @@ pa_status pa_attention_varlen_fp8(const void *q, int64_t q_token_stride, const v
                         workspace, workspace_bytes, dtype, stream);
 }
 
-pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void *key, const void *value,
-                                    int64_t key_token_stride, int64_t value_token_stride, void *key_cache,
-                                    void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
-                                    const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
-                                    int32_t is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
-                                    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
-                                    void *stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status rope_call(void *q, int64_t q_token_stride, const void *key, const void *value, int64_t key_token_stride,
+                    int64_t value_token_stride, void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                    const int64_t *positions, const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
+                    int32_t is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int64_t num_blocks, bool kv8, float k_scale, float v_scale, int32_t dtype,
+                    void *stream) {
   if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_blocks < 0 || max_position <= 0 || rotary_dim <= 0 || rotary_dim > head_dim)
     return PA_ERR_DIMS;
-  if (head_dim % 8 || rotary_dim % 16) return PA_ERR_ALIGN;
+  if (kv8 && (!valid_cache_scale(k_scale) || !valid_cache_scale(v_scale))) return PA_ERR_DIMS;
+  // 16-byte vectors of elements; 8-bit caches: 8-byte vectors of codes, rows of whole 16-byte vectors
+  if (head_dim % (kv8 ? 16 : 8) || rotary_dim % 16) return PA_ERR_ALIGN;
   if (rotary_dim > 512) return PA_ERR_UNSUPPORTED;  // the table row is staged in shared memory
   if (num_tokens == 0) return PA_OK;
   if (!q || !key || !value || !key_cache || !value_cache || !slot_mapping || !positions || !cos_sin_cache)
@@ -321,10 +326,40 @@ pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void 
   cudaError_t err = pa::launch_rope_reshape_and_cache(
       q, q_token_stride, key, value, key_token_stride, value_token_stride, key_cache, value_cache, slot_mapping,
       positions, cos_sin_cache, max_position, rotary_dim, is_neox != 0, num_tokens, num_heads, num_kv_heads,
-      head_dim, num_blocks * block_size, dtype, ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
+      head_dim, num_blocks * block_size, dtype, kv8, k_scale, v_scale, ds->status, ds->sm_count,
+      static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_rope_reshape_and_cache(void *q, int64_t q_token_stride, const void *key, const void *value,
+                                    int64_t key_token_stride, int64_t value_token_stride, void *key_cache,
+                                    void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
+                                    const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
+                                    int32_t is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t dtype,
+                                    void *stream) {
+  return rope_call(q, q_token_stride, key, value, key_token_stride, value_token_stride, key_cache, value_cache,
+                   slot_mapping, positions, cos_sin_cache, max_position, rotary_dim, is_neox, num_tokens, num_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, false, 1.0f, 1.0f, dtype, stream);
+}
+
+pa_status pa_rope_reshape_and_cache_fp8(void *q, int64_t q_token_stride, const void *key, const void *value,
+                                        int64_t key_token_stride, int64_t value_token_stride, void *key_cache,
+                                        void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
+                                        const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
+                                        int32_t is_neox, int32_t num_tokens, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                        int64_t num_blocks, float k_scale, float v_scale, int32_t dtype,
+                                        void *stream) {
+  return rope_call(q, q_token_stride, key, value, key_token_stride, value_token_stride, key_cache, value_cache,
+                   slot_mapping, positions, cos_sin_cache, max_position, rotary_dim, is_neox, num_tokens, num_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, true, k_scale, v_scale, dtype, stream);
 }
 
 pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping, int32_t num_pairs,

@@ -190,13 +190,34 @@ __device__ __forceinline__ void rope_adjacent8(uint4 &a, const float *c, const f
 
 constexpr int kRopeMaxRot = 512;  // largest rotary_dim (the table row is staged in shared memory)
 
-template <typename E, bool NEOX>
+// Eight elements -> eight E4M3 codes of x / scale (the quantiser of reshape_and_cache_fp8).
+template <typename E>
+__device__ __forceinline__ uint2 quantize8(uint4 a, float scale) {
+  const uint32_t x[4] = {a.x, a.y, a.z, a.w};
+  uint32_t c[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t p0 = e4m3x2_from_f32(__fdiv_rn(E::lo(x[2 * k]), scale), __fdiv_rn(E::hi(x[2 * k]), scale));
+    const uint32_t p1 =
+        e4m3x2_from_f32(__fdiv_rn(E::lo(x[2 * k + 1]), scale), __fdiv_rn(E::hi(x[2 * k + 1]), scale));
+    c[k] = p0 | (p1 << 16);
+  }
+  return make_uint2(c[0], c[1]);
+}
+
+// KV8: the caches hold E4M3 codes; the rotated key row (rounded to the
+// element type, as for 16-bit caches) and the value row are quantised by the
+// cache scales on their way in, eight elements to one 8-byte store.
+template <typename E, bool NEOX, bool KV8>
 __global__ void __launch_bounds__(256) rope_reshape_and_cache_kernel(
     uint4 *q, int64_t q_stride16, const uint4 *__restrict__ key, const uint4 *__restrict__ value,
-    int64_t key_stride16, int64_t value_stride16, uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+    int64_t key_stride16, int64_t value_stride16, void *__restrict__ key_cache_v, void *__restrict__ value_cache_v,
     const int64_t *__restrict__ slot_mapping, const int64_t *__restrict__ positions,
     const float *__restrict__ cos_sin, int32_t max_position, int32_t rot, int32_t num_tokens, int32_t num_heads,
-    int32_t num_kv_heads, int32_t d16, int64_t num_slots, unsigned int *status) {
+    int32_t num_kv_heads, int32_t d16, int64_t num_slots, float k_scale, float v_scale, unsigned int *status) {
+  // 16-bit caches: one 16-byte vector per 8-element chunk; 8-bit: one 8-byte vector
+  uint4 *key_cache = static_cast<uint4 *>(key_cache_v), *value_cache = static_cast<uint4 *>(value_cache_v);
+  uint2 *key_cache8 = static_cast<uint2 *>(key_cache_v), *value_cache8 = static_cast<uint2 *>(value_cache_v);
   // One CTA per token at a time: the position, slot and table row are read
   // once and shared, so the chunks of the token's rows need no dependent
   // global loads.
@@ -261,22 +282,31 @@ __global__ void __launch_bounds__(256) rope_reshape_and_cache_kernel(
           if (partner) continue;
           const int32_t h = r - num_heads;
           const uint4 *src = key + static_cast<int64_t>(t) * key_stride16 + static_cast<int64_t>(h) * d16;
-          uint4 *dst = key_cache + slot * row16 + static_cast<int64_t>(h) * d16;
+          const int64_t dofs = slot * row16 + static_cast<int64_t>(h) * d16;
           uint4 x = ld_cg(src + c);
           if (rotates) {
             if (NEOX) {
               uint4 y = ld_cg(src + c + half16);
               rope_pair8<E>(x, y, cf, sf);
-              dst[c + half16] = y;
+              if constexpr (KV8)
+                key_cache8[dofs + c + half16] = quantize8<E>(y, k_scale);
+              else
+                key_cache[dofs + c + half16] = y;
             } else {
               rope_adjacent8<E>(x, cf, sf);
             }
           }
-          dst[c] = x;
+          if constexpr (KV8)
+            key_cache8[dofs + c] = quantize8<E>(x, k_scale);
+          else
+            key_cache[dofs + c] = x;
         } else {  // V head: copied
           const int32_t h = r - num_heads - num_kv_heads;
-          value_cache[slot * row16 + static_cast<int64_t>(h) * d16 + c] =
-              ld_cg(value + static_cast<int64_t>(t) * value_stride16 + static_cast<int64_t>(h) * d16 + c);
+          const uint4 x = ld_cg(value + static_cast<int64_t>(t) * value_stride16 + static_cast<int64_t>(h) * d16 + c);
+          if constexpr (KV8)
+            value_cache8[slot * row16 + static_cast<int64_t>(h) * d16 + c] = quantize8<E>(x, v_scale);
+          else
+            value_cache[slot * row16 + static_cast<int64_t>(h) * d16 + c] = x;
         }
       }
     }
@@ -335,24 +365,26 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
                                           void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
                                           const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
                                           bool is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
-                                          int32_t head_dim, int64_t num_slots, int32_t dtype, unsigned int *status,
-                                          int sm_count, cudaStream_t stream) {
+                                          int32_t head_dim, int64_t num_slots, int32_t dtype, bool kv8, float k_scale,
+                                          float v_scale, unsigned int *status, int sm_count, cudaStream_t stream) {
   const int32_t d16 = head_dim / 8;
   int64_t g = static_cast<int64_t>(sm_count) * 8;  // CTAs (tokens in flight): 8 per SM
   if (g > num_tokens) g = num_tokens;
   const int grid = static_cast<int>(g < 1 ? 1 : g);
-#define PA_ROPE_LAUNCH(EE, NN)                                                                                    \
-  return launch_pdl(rope_reshape_and_cache_kernel<EE, NN>, dim3(grid), dim3(256), 0, stream,                      \
+#define PA_ROPE_LAUNCH(EE, NN, K8)                                                                                \
+  return launch_pdl(rope_reshape_and_cache_kernel<EE, NN, K8>, dim3(grid), dim3(256), 0, stream,                  \
                     static_cast<uint4 *>(q), q_stride / 8, static_cast<const uint4 *>(key),                        \
-                    static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8,                            \
-                    static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping, positions,     \
-                    cos_sin_cache, max_position, rotary_dim, num_tokens, num_heads, num_kv_heads, d16, num_slots,  \
-                    status);
+                    static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8, key_cache, value_cache,    \
+                    slot_mapping, positions, cos_sin_cache, max_position, rotary_dim, num_tokens, num_heads,        \
+                    num_kv_heads, d16, num_slots, k_scale, v_scale, status);
+#define PA_ROPE_KV(EE, NN) \
+  if (kv8) PA_ROPE_LAUNCH(EE, NN, true) else PA_ROPE_LAUNCH(EE, NN, false)
   if (dtype == PA_FP16) {
-    if (is_neox) PA_ROPE_LAUNCH(ElemFp16, true) else PA_ROPE_LAUNCH(ElemFp16, false)
+    if (is_neox) PA_ROPE_KV(ElemFp16, true) else PA_ROPE_KV(ElemFp16, false)
   } else {
-    if (is_neox) PA_ROPE_LAUNCH(ElemBf16, true) else PA_ROPE_LAUNCH(ElemBf16, false)
+    if (is_neox) PA_ROPE_KV(ElemBf16, true) else PA_ROPE_KV(ElemBf16, false)
   }
+#undef PA_ROPE_KV
 #undef PA_ROPE_LAUNCH
 }
 

@@ -30,8 +30,8 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
                                           void *value_cache, const int64_t *slot_mapping, const int64_t *positions,
                                           const float *cos_sin_cache, int32_t max_position, int32_t rotary_dim,
                                           bool is_neox, int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
-                                          int32_t head_dim, int64_t num_slots, int32_t dtype, unsigned int *status,
-                                          int sm_count, cudaStream_t stream);
+                                          int32_t head_dim, int64_t num_slots, int32_t dtype, bool kv8, float k_scale,
+                                          float v_scale, unsigned int *status, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_gather_kv(const void *key_cache, const void *value_cache, const int32_t *table_row,
                              int32_t seq_len, int32_t row_bytes, int32_t block_size, int64_t num_blocks, void *key_out,

@@ -62,8 +62,6 @@ class DeviceStep:
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.rope = None
         if rope is not None:
-            if self.kv_fp8:
-                raise ValueError("the fused rotary scatter writes 16-bit caches only")
             table, positions, is_neox = rope
             self.rope = (torch.from_numpy(np.ascontiguousarray(table, dtype=np.float32)).to(dev),
                          torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int64)).to(dev), bool(is_neox))
@@ -76,8 +74,13 @@ class DeviceStep:
     def reshape_and_cache(self, stream=None) -> None:
         if self.rope is not None:
             table, positions, is_neox = self.rope
-            B.pa_rope_reshape_and_cache(self.q, self.key, self.value, self.key_cache, self.value_cache,
-                                        self.slot_mapping, positions, table, is_neox=is_neox, stream=stream)
+            if self.kv_fp8:
+                B.pa_rope_reshape_and_cache_fp8(self.q, self.key, self.value, self.key_cache, self.value_cache,
+                                                self.slot_mapping, positions, table, self.w.k_scale, self.w.v_scale,
+                                                is_neox=is_neox, stream=stream)
+            else:
+                B.pa_rope_reshape_and_cache(self.q, self.key, self.value, self.key_cache, self.value_cache,
+                                            self.slot_mapping, positions, table, is_neox=is_neox, stream=stream)
             return
         if self.kv_fp8:
             B.pa_reshape_and_cache_fp8(self.key, self.value, self.key_cache, self.value_cache, self.slot_mapping,

@@ -116,3 +116,67 @@ def test_rope_q_with_token_stride_and_bad_position(oracle):
     assert within_one_ulp(gq[keep], q).all() and within_one_ulp(gk.reshape(kc.shape), kc).all()
     assert np.array_equal(bf16_to_numpy_bits(fused[:, H:]), np.zeros((w.total_q, 2 * Hkv, D), np.uint16)), \
         "the rest of the fused buffer is not touched"
+
+
+def within_one_code(g: np.ndarray, o: np.ndarray) -> np.ndarray:
+    """E4M3 codes: equal, or neighbours of the same sign (the rotated element they quantise may
+    differ by one unit in the last place between the fp32 kernel and the fp64 oracle)."""
+    gi, oi = g.astype(np.int64), o.astype(np.int64)
+    return (gi == oi) | (((gi >> 7) == (oi >> 7)) & (np.abs((gi & 0x7F) - (oi & 0x7F)) <= 1))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("case", CASES)
+def test_rope_fp8_matches_oracle(oracle, dtype, neox, case):
+    D, rot, H, Hkv = case
+    w = W.make_workload("rope_fp8", context_lens=[0, 30, 900, 5], query_lens=[40, 1, 3, 17], num_heads=H,
+                        num_kv_heads=Hkv, head_dim=D, seed=5, dtype=dtype, kv_dtype=W.FP8_E4M3)
+    table = W.rope_cos_sin_cache(int(w.max_seq_len) + 8, rot)
+    pos = positions_of(w)
+    st = DeviceStep(w)
+    B.pa_rope_reshape_and_cache_fp8(st.q, st.key, st.value, st.key_cache, st.value_cache, st.slot_mapping,
+                                    torch.from_numpy(pos).cuda(), torch.from_numpy(table).cuda(), w.k_scale,
+                                    w.v_scale, is_neox=neox)
+    torch.cuda.synchronize()
+    assert B.pa_debug_status() == 0
+    q = w.q.copy()
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    oracle.rope_reshape_and_cache_fp8(q, w.key, w.value, kc, vc, w.slot_mapping, pos, table, neox, w.block_size,
+                                      w.k_scale, w.v_scale, w.dtype)
+    assert within_one_ulp(bf16_to_numpy_bits(st.q), q).all(), "rotated q"
+    assert np.array_equal(st.value_cache.cpu().numpy(), vc), "V codes must match bit for bit"
+    gk = st.key_cache.cpu().numpy()
+    assert within_one_code(gk, kc).all(), "rotated K codes within one step"
+    rows = w.slot_mapping
+    gk_rows = gk.reshape(-1, Hkv, D)[rows]
+    ok_rows = kc.reshape(-1, Hkv, D)[rows]
+    assert np.array_equal(gk_rows[..., rot:], ok_rows[..., rot:]), "K past rotary_dim must match bit for bit"
+    assert (gk_rows == ok_rows).mean() > 0.99
+    # everything outside the written slots is untouched
+    untouched = np.ones(gk.reshape(-1, Hkv, D).shape[0], dtype=bool)
+    untouched[rows] = False
+    assert np.array_equal(gk.reshape(-1, Hkv, D)[untouched], w.key_cache.reshape(-1, Hkv, D)[untouched])
+
+
+def test_rope_fp8_step_matches_oracle(oracle):
+    """A whole step over 8-bit caches: rotary scatter, then attention, against the oracle's."""
+    w = W.make_workload("rope_fp8_step", context_lens=[0, 37, 600, 20, 1000], query_lens=[40, 2, 1, 129, 1],
+                        num_heads=32, num_kv_heads=8, head_dim=128, seed=6, kv_dtype=W.FP8_E4M3)
+    table = W.rope_cos_sin_cache(int(w.max_seq_len) + 8, 128)
+    pos = positions_of(w)
+    st = DeviceStep(w, rope=(table, pos, True))
+    st.run()
+    torch.cuda.synchronize()
+    assert B.pa_debug_status() == 0
+    q = w.q.copy()
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    oracle.rope_reshape_and_cache_fp8(q, w.key, w.value, kc, vc, w.slot_mapping, pos, table, True, w.block_size,
+                                      w.k_scale, w.v_scale, w.dtype)
+    # attention on the GPU's own caches and rotated q (isolates the attention step from 1-ulp rotations)
+    gq = bf16_to_numpy_bits(st.q)
+    gk, gv = st.key_cache.cpu().numpy(), st.value_cache.cpu().numpy()
+    ref = oracle.attention(gq, gk, gv, w.block_tables, w.seq_lens, w.query_start_loc, w.num_heads, w.scale,
+                           dtype=w.dtype, k_scale=w.k_scale, v_scale=w.v_scale)
+    assert_attention_close(bf16_to_float64(st.out), ref, w.name)
+    assert within_one_code(gk, kc).all() and np.array_equal(gv, vc)
