@@ -40,6 +40,7 @@ if ROOT not in sys.path:
 METRIC = "paged-attn KV GB/s & fraction of GB300 HBM peak; decode tokens/s per layer"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 WORKLOAD_TEXT = {
     "tiny_decode": "tiny decode: 4 requests, seq_lens {1,7,16,33}, H=4, Hkv=1, D=64, bs=16",
@@ -74,13 +75,30 @@ def step_accounting(w, rope: bool = False) -> dict:
     if rope:  # q rotated in place (read + write), positions, one table row per token
         reshape += 2 * T * H * D * 2 + T * 8 + T * D * 4
     kv_bytes = uniq * kv_tok
-    flops = 0
+    flops = tile_flops = 0
     ql = w.query_lens
+    rows_per_item = 8 // (H // Hkv)  # longer requests go to the tensor-core tiles
+    decode_reqs = []
     for b in range(w.num_seqs):
         L, n = int(w.seq_lens[b]), int(ql[b])
         visible = n * (L - n) + n * (n + 1) // 2
         flops += 4 * H * D * visible
+        if n > rows_per_item:
+            tile_flops += 4 * H * D * visible
+        elif n > 0:
+            decode_reqs.append(b)
+    # bytes the split-KV decode kernel must move: unique KV of its requests, their q and out
+    seen = {}
+    for b in decode_reqs:
+        L = int(w.seq_lens[b])
+        for i in range(-(-L // bs)):
+            blk = int(w.block_tables[b, i])
+            seen[blk] = max(seen.get(blk, 0), min(bs, L - i * bs))
+    dec_q = int(sum(int(ql[b]) for b in decode_reqs))
+    decode_bytes = (sum(seen.values()) * kv_tok + 2 * dec_q * H * D * 2 + tables + meta)
     return {
+        "tile_flops": tile_flops,
+        "decode_bytes": decode_bytes,
         "kv_bytes": kv_bytes,
         "kv_bytes_logical": logical * kv_tok,
         "attention_bytes": kv_bytes + q_out + tables + meta,
@@ -268,8 +286,8 @@ def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 def run_reference(args, world, rank) -> None:
@@ -356,9 +374,12 @@ def run_ours(args, world, rank, local_rank) -> None:
     # warm-up (the first call also creates the timing events)
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)]
-    for a, b in ev_pairs:
+    tile_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    for a, b in ev_pairs + tile_pairs:
         a.record(stream)
         b.record(stream)
+    has_tiles = acct["tile_flops"] > 0
     for _ in range(max(args.warmup, 1)):
         st.run()
     torch.cuda.synchronize()
@@ -383,15 +404,18 @@ def run_ours(args, world, rank, local_rank) -> None:
     if world > 1:
         dist.barrier()
     step_ms = t0.elapsed_time(t1) / args.steps
-    # Second pass of the same steps, with events around the attention kernel
-    # alone (they serialise it against its neighbours, so the step time above
-    # is taken without them).
+    # Second pass of the same steps, with events around the split-KV kernel
+    # and the prefill-tile kernel alone (they serialise the kernels against
+    # their neighbours, so the step time above is taken without them).
     for k in range(args.steps):
         B.pa_attention_set_timing_events(*ev_pairs[k])
+        if has_tiles:
+            B.pa_attention_set_tile_timing_events(*tile_pairs[k])
         st.run()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs)
+    tile_ms = statistics.mean(a.elapsed_time(b) for a, b in tile_pairs) if has_tiles else 0.0
 
     max_ms = reduce_max(step_ms, device)
     total_bytes = reduce_sum(float(acct["step_bytes"]), device)
@@ -457,10 +481,26 @@ def run_ours(args, world, rank, local_rank) -> None:
     e2e_value = aggregate_rate(total_bytes, e2e_ms * 1e-3) / 1e9
 
     peaks = load_peaks()
-    kern_achieved = acct["attention_bytes"] / (kern_ms * 1e-3) / 1e9
+    # the split-KV kernel against HBM: the bytes of the requests it serves
+    dec_bytes = acct["attention_bytes"] if not has_tiles else acct["decode_bytes"]
+    kern_achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
     # committed counters exist for the default bf16 line and its 8-bit-cache variant
     traffic = (committed_traffic(args.workload + ("+" + args.kv_dtype if args.kv_dtype else ""))
                if args.dtype == "bf16" and args.block_size == 16 and not args.rope and not args.batch else None)
+    roof_decode = {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
+                   "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kern_achieved / peaks["hbm_gbs"],
+                   "peak_source": peaks["source"], "kernel_ms": kern_ms,
+                   "algorithmic_bytes_per_launch": dec_bytes, "traffic": traffic}
+    roof = roof_decode
+    if has_tiles:
+        # a step with prefill chunks: the dominant kernel is the tensor-core tile kernel
+        # (algorithmic FLOPs: 4 H D per visible (query, key) pair of the chunks; the bf16
+        # burst peak, the fp16 rate being the same)
+        tile_achieved = acct["tile_flops"] / (tile_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill_tile_kernel", "achieved": tile_achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tile_achieved / peaks["bf16_tflops"],
+                "peak_source": peaks["source"], "kernel_ms": tile_ms,
+                "algorithmic_flops_per_launch": acct["tile_flops"], "traffic": None}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
@@ -476,10 +516,8 @@ def run_ours(args, world, rank, local_rank) -> None:
                    "kv_cache": args.kv_dtype or args.dtype,
                    "step_bytes": acct["step_bytes"], "kv_bytes": acct["kv_bytes"],
                    "kv_bytes_logical": acct["kv_bytes_logical"], "flops": acct["flops"]},
-        "roofline": {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kern_achieved / peaks["hbm_gbs"],
-                     "peak_source": peaks["source"], "kernel_ms": kern_ms,
-                     "algorithmic_bytes_per_launch": acct["attention_bytes"], "traffic": traffic},
+        "roofline": roof,
+        "roofline_decode_kernel": roof_decode if has_tiles else None,
         "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers; two device buffer sets, uploads and downloads on their own "

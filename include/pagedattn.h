@@ -341,6 +341,14 @@ const char *pa_last_cuda_error(void);
 pa_status pa_attention_set_timing_events(void *start, void *stop);
 
 /*
+ * The same for the prefill-tile (tensor-core) kernel of the next
+ * pa_attention_varlen / pa_attention_varlen_fp8 call by this host thread; the
+ * events are not recorded if that call launches no tile kernel (no request
+ * has more than 8 / (num_heads / num_kv_heads) query tokens).
+ */
+pa_status pa_attention_set_tile_timing_events(void *start, void *stop);
+
+/*
  * Attention without a caller-provided workspace, for callers that cannot
  * allocate device memory: code running inside a CUDA graph capture that
  * forbids allocation, plugins of a host framework that owns every allocation,

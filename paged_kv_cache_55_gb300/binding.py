@@ -54,6 +54,7 @@ SIGNATURES = {
     "pa_rope_reshape_and_cache": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
                                    _I32, _I32, _I32, _I64, _I32, _P], ctypes.c_int32),
     "pa_attention_set_timing_events": ([_P, _P], ctypes.c_int),
+    "pa_attention_set_tile_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
     "pa_rope_reshape_and_cache_fp8": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
@@ -360,6 +361,13 @@ def pa_attention_set_timing_events(start: Optional[torch.cuda.Event], stop: Opti
     s = start.cuda_event if start is not None else None
     e = stop.cuda_event if stop is not None else None
     _check(_lib().pa_attention_set_timing_events(s, e), "pa_attention_set_timing_events")
+
+
+def pa_attention_set_tile_timing_events(start: Optional[torch.cuda.Event],
+                                        stop: Optional[torch.cuda.Event]) -> None:
+    s = start.cuda_event if start is not None else None
+    e = stop.cuda_event if stop is not None else None
+    _check(_lib().pa_attention_set_tile_timing_events(s, e), "pa_attention_set_tile_timing_events")
 
 
 def pa_status_string(status: int) -> str:

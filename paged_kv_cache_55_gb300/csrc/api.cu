@@ -27,6 +27,8 @@ DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_launches{0};
 thread_local cudaEvent_t t_ev_start = nullptr;
 thread_local cudaEvent_t t_ev_stop = nullptr;
+thread_local cudaEvent_t t_tile_start = nullptr;
+thread_local cudaEvent_t t_tile_stop = nullptr;
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 
 // Record the CUDA error behind a PA_ERR_LAUNCH / PA_ERR_CUDA return.
@@ -99,6 +101,13 @@ pa_status pa_attention_set_timing_events(void *start, void *stop) {
   if ((start == nullptr) != (stop == nullptr)) return PA_ERR_NULL;
   t_ev_start = static_cast<cudaEvent_t>(start);
   t_ev_stop = static_cast<cudaEvent_t>(stop);
+  return PA_OK;
+}
+
+pa_status pa_attention_set_tile_timing_events(void *start, void *stop) {
+  if ((start == nullptr) != (stop == nullptr)) return PA_ERR_NULL;
+  t_tile_start = static_cast<cudaEvent_t>(start);
+  t_tile_stop = static_cast<cudaEvent_t>(stop);
   return PA_OK;
 }
 
@@ -195,8 +204,8 @@ pa_status attention_call(const void *q, int64_t q_token_stride, const void *key_
                          int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale, bool kv_fp8,
                          float k_scale, float v_scale, void *out, void *workspace, size_t workspace_bytes,
                          int32_t dtype, void *stream) {
-  cudaEvent_t ev_start = t_ev_start, ev_stop = t_ev_stop;
-  t_ev_start = t_ev_stop = nullptr;
+  cudaEvent_t ev_start = t_ev_start, ev_stop = t_ev_stop, tile_start = t_tile_start, tile_stop = t_tile_stop;
+  t_ev_start = t_ev_stop = t_tile_start = t_tile_stop = nullptr;
   if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && (!valid_cache_scale(k_scale) || !valid_cache_scale(v_scale))) return PA_ERR_DIMS;
   if (num_seqs < 0 || total_q_tokens < 0 || max_query_len < 0 || max_seq_len < max_query_len ||
@@ -255,6 +264,8 @@ pa_status attention_call(const void *q, int64_t q_token_stride, const void *key_
   a.sm_count = ds->sm_count;
   a.ev_start = ev_start;
   a.ev_stop = ev_stop;
+  a.tile_start = tile_start;
+  a.tile_stop = tile_stop;
   int launched = 0;
   cudaError_t err = pa::launch_attention(a, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(static_cast<uint64_t>(launched));

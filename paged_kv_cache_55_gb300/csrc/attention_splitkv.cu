@@ -1171,7 +1171,9 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.total_q = a.total_q;
     tp.max_tiles = w.max_tiles;
     tp.status = a.status;
+    if (a.tile_start) cudaEventRecord(a.tile_start, stream);
     err = launch_prefill_tiles<D, G, E, KV8>(kmap, vmap, tp, a.sm_count, stream);
+    if (err == cudaSuccess && a.tile_stop) cudaEventRecord(a.tile_stop, stream);
     if (err != cudaSuccess) return err;
     ++*launched;
   }

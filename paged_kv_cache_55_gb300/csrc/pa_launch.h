@@ -70,7 +70,8 @@ struct AttnLaunch {
   void *workspace;
   unsigned int *status;
   int sm_count;
-  cudaEvent_t ev_start, ev_stop;
+  cudaEvent_t ev_start, ev_stop;      // around the split-KV decode kernel, if set
+  cudaEvent_t tile_start, tile_stop;  // around the prefill-tile kernel, if set and launched
 };
 
 // Enqueue planning, split-KV attention and (when a request can be split) the
