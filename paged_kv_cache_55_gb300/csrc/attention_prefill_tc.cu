@@ -168,6 +168,16 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
+// The same for 16 columns.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Packed pairs of fp32 operations (one instruction for two lanes of data).
 __device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0, float c1) {
   asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
@@ -197,8 +207,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, int lim) {
   float m = -INFINITY;
   if (ck0 + 32 <= lim) {
+    // a tree of depth 4 (a chain of 16 three-input maxima would be 16 deep)
+    float t[8];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(s[i]), __uint_as_float(s[i + 1]));
+    for (int i = 0; i < 8; ++i)
+      t[i] = max3(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]),
+                  fmaxf(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])));
+    m = max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i) m = ck0 + i < lim ? fmaxf(m, __uint_as_float(s[i])) : m;
@@ -207,14 +222,17 @@ __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, 
 }
 
 // P for 32 keys (scores s[0..32), visible while ck0 + i < lim): p =
-// 2^(s * sl2 - ms), summed into *sum and packed as the 32 TMEM columns of two
-// UMMA K steps: [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo 16-31].
+// 2^(s * sl2 - ms), summed into *sum and packed as the TMEM columns of two
+// UMMA K steps. SPLIT (bf16 operands, 8 significant bits): P as a hi + lo
+// pair, 32 columns [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo
+// 16-31]; otherwise (fp16, 11 bits: a weight's rounding error of 2^-12
+// keeps the output within the tolerance) one pair per two keys, 16 columns.
 // The exponent is one fused multiply-add, whose unrounded product differs
 // from the rounded one ms was taken from by at most half an ulp of ms: below
 // 2^-12 while |ms| <= 2^12. EXACT rows (larger |ms|) round the product first,
 // so the row maximum's exponent is exactly zero and none exceeds the growth
 // the caller allowed.
-template <typename E, bool EXACT>
+template <typename E, bool EXACT, bool SPLIT>
 __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int lim, float sl2, float ms, float &sum,
                                         uint32_t (&u)[32]) {
   const bool full = ck0 + 32 <= lim;
@@ -237,17 +255,31 @@ __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int li
     const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
     add2(acc0, acc1, acc0, acc1, p0, p1);
     const uint32_t hi = E::pack(p0, p1);
-    float l0, l1;
-    sub2(l0, l1, p0, p1, E::lo(hi), E::hi(hi));
-    const int step = i >> 3, k = i & 7;
-    u[16 * step + k] = hi;
-    u[16 * step + 8 + k] = E::pack(l0, l1);
+    if (SPLIT) {
+      float l0, l1;
+      sub2(l0, l1, p0, p1, E::lo(hi), E::hi(hi));
+      const int step = i >> 3, k = i & 7;
+      u[16 * step + k] = hi;
+      u[16 * step + 8 + k] = E::pack(l0, l1);
+    } else {
+      u[i] = hi;
+    }
   }
   sum += acc0 + acc1;
 }
 
 // Multiply the probabilities already stored in a 32-column chunk of P (the
 // layout probs32 writes) by alpha, re-splitting each into hi + lo.
+// The same for a chunk of single pairs (16 columns).
+template <typename E>
+__device__ __forceinline__ void rescale_p16(uint32_t taddr, float alpha) {
+  uint32_t w[16];
+  tmem_ld16_wait(taddr, w);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = E::pack(E::lo(w[i]) * alpha, E::hi(w[i]) * alpha);
+  tmem_st16u(taddr, w);
+}
+
 template <typename E>
 __device__ __forceinline__ void rescale_p32(uint32_t taddr, float alpha) {
   uint32_t w[32];
@@ -281,6 +313,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   using Lay = TcLayout<D>;
   using Tm = TcTmem<D>;
   using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
+  constexpr bool SPLIT = std::is_same<M, ElemBf16>::value;      // P as a hi + lo pair (bf16 operands only)
+  constexpr int PCOLS = SPLIT ? 32 : 16;                        // TMEM columns of P per 32 keys
   constexpr int NTHREADS = KV8 ? kTileThreads8 : kTileThreads;
   constexpr int RAW_ROW = D <= 64 ? 64 : 128;      // bytes per staged row of codes (padded past head_dim)
   constexpr int RAW_BYTES = kKeyTile * RAW_ROW;    // 8-bit codes of one range
@@ -587,16 +621,17 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             tc_fence_after();
             const uint32_t vlo = v_lo + vslot * SLOT_STEP;
             const uint32_t t = tmem + h * Tm::HALF;
+            // K step ks reads P at columns PCOLS / 2 * ks (+ 8 for the lo half of a pair)
             if (kt == 0)
               mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);  // the unit's first product overwrites O
             else
               mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);
-            mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, DHI, IDESC_O);
+            if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, DHI, IDESC_O);
 #pragma unroll
             for (int ks = 1; ks < KSTEPS_O; ++ks) {
               const uint32_t vo = (ks * 2048) >> 4;  // 16 keys x 128 B per K step
-              mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks, vlo + vo, DHI, IDESC_O);
-              mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vo, DHI, IDESC_O);
+              mma_ts<1>(t + Tm::O, t + Tm::SP + (PCOLS / 2) * ks, vlo + vo, DHI, IDESC_O);
+              if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vo, DHI, IDESC_O);
             }
             tc_commit(bar_o + 8 * h);
             if (h == last_reader(kt)) tc_commit(bar_empty + 8 * vslot);
@@ -707,15 +742,29 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             if (c > 0) {
               tmem_wait_st();  // the chunks stored so far are read back
 #pragma unroll 1
-              for (int cc = 0; cc < c; ++cc) rescale_p32<M>(sp + 32 * cc, a);
+              for (int cc = 0; cc < c; ++cc) {
+                if constexpr (SPLIT)
+                  rescale_p32<M>(sp + 32 * cc, a);
+                else
+                  rescale_p16<M>(sp + 16 * cc, a);
+              }
             }
           }
           const float ms = m_used == -INFINITY ? 0.f : m_used;
           if (__any_sync(0xffffffffu, fabsf(ms) > 4096.f))
-            probs32<M, true>(sv, ck0, lim, sl2, ms, sum, u);
+            probs32<M, true, SPLIT>(sv, ck0, lim, sl2, ms, sum, u);
           else
-            probs32<M, false>(sv, ck0, lim, sl2, ms, sum, u);
-          tmem_st32u(sp + 32 * c, u);  // P over the scores it came from
+            probs32<M, false, SPLIT>(sv, ck0, lim, sl2, ms, sum, u);
+          // P over the scores it came from (single pairs: chunk c at columns 16c, over
+          // scores of chunks <= c that have been read already)
+          if constexpr (SPLIT) {
+            tmem_st32u(sp + 32 * c, u);
+          } else {
+            uint32_t u16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u16[i] = u[i];
+            tmem_st16u(sp + 16 * c, u16);
+          }
         }
         // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
         // last of them finished).
