@@ -375,6 +375,17 @@ pa_status pa_attention_set_tile_timing_events(void *start, void *stop);
  */
 #define PA_STATIC_WORKSPACE_BYTES (32u << 20)
 
+/* The same over 8-bit caches (arguments as pa_attention_varlen_fp8, minus the workspace). */
+pa_status pa_attention_varlen_fp8_static(const void *q, int64_t q_token_stride,
+                                         const void *key_cache, const void *value_cache,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *seq_lens, const int32_t *query_start_loc,
+                                         int32_t num_seqs, int32_t total_q_tokens,
+                                         int32_t max_query_len, int32_t max_seq_len,
+                                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int64_t num_blocks, float scale,
+                                         float k_scale, float v_scale, void *out, int32_t dtype, void *stream);
+
 pa_status pa_attention_varlen_static(const void *q, int64_t q_token_stride,
                                      const void *key_cache, const void *value_cache,
                                      const int32_t *block_tables, int32_t max_blocks_per_seq,

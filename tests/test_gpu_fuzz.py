@@ -8,6 +8,7 @@ import pytest
 
 from paged_kv_cache_55_gb300 import workloads as W
 
+from test_gpu_fp8 import run_fp8
 from test_gpu_parity import run_and_check
 
 pytestmark = pytest.mark.gpu
@@ -26,12 +27,16 @@ def random_case(seed: int) -> W.Workload:
     ql = np.where(kind == "empty", 0, np.where(kind == "decode", 1, np.where(
         kind == "draft", rng.integers(2, 10, size=B), rng.integers(10, 300, size=B))))
     q_scale = float(rng.choice([1.0, 4.0]))
-    name = f"fuzz{seed}_g{G}_hkv{Hkv}_d{D}_bs{bs}_{dtype}_q{q_scale:g}"
+    kv = W.FP8_E4M3 if seed % 3 == 2 else ""  # every third case over 8-bit caches
+    name = f"fuzz{seed}_g{G}_hkv{Hkv}_d{D}_bs{bs}_{dtype}_q{q_scale:g}{'_fp8' if kv else ''}"
     return W.make_workload(name, context_lens=ctx, query_lens=ql, num_heads=Hkv * G, num_kv_heads=Hkv,
-                           head_dim=D, block_size=bs, seed=seed, dtype=dtype, q_scale=q_scale)
+                           head_dim=D, block_size=bs, seed=seed, dtype=dtype, q_scale=q_scale, kv_dtype=kv)
 
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_problem_matches_oracle(oracle, seed):
     w = random_case(seed)
-    run_and_check(w, oracle)
+    if w.kv_fp8:
+        run_fp8(w, oracle)
+    else:
+        run_and_check(w, oracle)
