@@ -2,11 +2,13 @@
 """Benchmark of one paged-attention step (reshape_and_cache + attention) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gqa_decode] [--seed 0]
+                    [--workload gqa_decode] [--seed 0] [--dtype bf16|fp16]
+                    [--kv-dtype fp8_e4m3] [--block-size 8|16|32] [--rope]
 
 A step is one pass of the whole path over one batch: pa_reshape_and_cache of
 the step's new K/V rows, then pa_attention_varlen (planning, split-KV
-attention, log-sum-exp merge). Inputs are seeded synthetic data resident in
+attention, prefill tiles when the batch has chunks, log-sum-exp merge); with
+--kv-dtype fp8_e4m3 the 8-bit-cache calls, with --rope the rotary scatter. Inputs are seeded synthetic data resident in
 HBM before timing starts. The KV working set (1.7 GB for the default
 workload) is far larger than the 126 MB L2, so no L2 flush is needed between
 steps. Prints one JSON line (rank 0).
