@@ -66,6 +66,12 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert lib.pa_attention_workspace_size(4, 4, 40, 33, 4, 1, 64, 16) == 0
     pt, mp = B.pa_attention_plan_info(8, 32768, 64, 8)
     assert pt % 16 == 0 and mp == -(-32768 // pt)
+    # one size serves both cache types: 8-bit caches run 12 decode warps per SM and split 8 x 32768
+    # keys into 1536-key partitions (22 per request) where 16-bit caches use 2048 (16)
+    assert pt == 2048
+    n = lib.pa_attention_workspace_size(8, 8, 1, 32768, 64, 8, 128, 16)
+    partials_8bit = 8 * 8 * 22 * 8 * (128 + 1) * 4
+    assert n >= partials_8bit
 
 
 def test_validation_rejects_before_any_cuda_call(lib):
