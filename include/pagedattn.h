@@ -95,12 +95,12 @@ enum {
  * A negative slot means "padding token, write nothing". Two tokens of one
  * call must not name the same slot (which write wins is then unspecified).
  *
- *   key, value         (device) bf16, token t starts at key + t * key_token_stride
+ *   key, value         (device) `dtype`, token t starts at key + t * key_token_stride
  *                      elements and holds [num_kv_heads, head_dim] contiguous
  *                      elements (so key may be a slice of a fused QKV output).
  *   key_token_stride,  elements between consecutive tokens (>= num_kv_heads * head_dim,
  *   value_token_stride a multiple of 8).
- *   key_cache,         (device) bf16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *   key_cache,         (device) `dtype` [num_blocks, block_size, num_kv_heads, head_dim],
  *   value_cache        contiguous, updated in place.
  *   slot_mapping       (device) int64 [num_tokens].
  * All data pointers must be 16-byte aligned (PA_ERR_ALIGN otherwise).
@@ -166,11 +166,11 @@ pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len,
  * h / (num_heads / num_kv_heads). Logical key j of request b lives at
  * block_tables[b * max_blocks_per_seq + j / block_size], row j % block_size.
  *
- *   out[t][h][:] = bf16( sum_j softmax_j(scale * q[t][h] . K[j]) * V[j] )
+ *   out[t][h][:] = round_dtype( sum_j softmax_j(scale * q[t][h] . K[j]) * V[j] )
  *
- *   q                (device) bf16; token t at q + t * q_token_stride elements,
+ *   q                (device) `dtype`; token t at q + t * q_token_stride elements,
  *                    [num_heads, head_dim] contiguous; q_token_stride even.
- *   key_cache,       (device) bf16 [num_blocks, block_size, num_kv_heads, head_dim].
+ *   key_cache,       (device) `dtype` [num_blocks, block_size, num_kv_heads, head_dim].
  *   value_cache
  *   block_tables     (device) int32 [num_seqs, max_blocks_per_seq]; entries past
  *                    ceil(seq_len / block_size) are never read.
@@ -180,13 +180,15 @@ pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len,
  *   max_query_len,   (host) upper bounds of query_len and seq_len over the batch;
  *   max_seq_len      they size the launch and the workspace without a device read.
  *   scale            softmax scale (usually 1/sqrt(head_dim)).
- *   out              (device) bf16 [total_q_tokens, num_heads, head_dim], contiguous.
+ *   out              (device) `dtype` [total_q_tokens, num_heads, head_dim], contiguous.
  *   workspace        (device) at least pa_attention_workspace_size(...) bytes,
  *                    256-byte aligned; contents need no initialisation and are
  *                    scratch after the call.
  * Requests with query_len 0 are allowed and produce nothing. All work is
- * enqueued on `stream`: a planning kernel, the split-KV attention kernel and,
- * when some request is split, the log-sum-exp merge kernel.
+ * enqueued on `stream`: a planning kernel, the split-KV attention kernel (for
+ * requests of at most 8 / (num_heads / num_kv_heads) query tokens), the
+ * tensor-core prefill-tile kernel when some request is longer, and the
+ * log-sum-exp merge kernel when some request is split.
  */
 pa_status pa_attention_varlen(const void *q, int64_t q_token_stride,
                               const void *key_cache, const void *value_cache,
