@@ -352,9 +352,10 @@ pa_status pa_attention_set_tile_timing_events(void *start, void *stop);
 
 /*
  * Attention without a caller-provided workspace, for callers that cannot
- * allocate device memory: code running inside a CUDA graph capture that
- * forbids allocation, plugins of a host framework that owns every allocation,
- * or allocators that are locked down in production. The pages describe no
+ * call cudaMalloc: a plugin inside a host framework that owns every device
+ * allocation and hands the plugin only its inputs and outputs, or a serving
+ * process whose device memory is all reserved up front by its own pool, so
+ * that a further allocation would fail or fragment it. The pages describe no
  * such call; it exists only for these callers.
  *
  * Same arguments and result as pa_attention_varlen, minus `workspace` and
@@ -376,17 +377,6 @@ pa_status pa_attention_set_tile_timing_events(void *start, void *stop);
  *     on the array and produce garbage. Order such calls on one stream.
  */
 #define PA_STATIC_WORKSPACE_BYTES (32u << 20)
-
-/* The same over 8-bit caches (arguments as pa_attention_varlen_fp8, minus the workspace). */
-pa_status pa_attention_varlen_fp8_static(const void *q, int64_t q_token_stride,
-                                         const void *key_cache, const void *value_cache,
-                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                         const int32_t *seq_lens, const int32_t *query_start_loc,
-                                         int32_t num_seqs, int32_t total_q_tokens,
-                                         int32_t max_query_len, int32_t max_seq_len,
-                                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                                         int32_t block_size, int64_t num_blocks, float scale,
-                                         float k_scale, float v_scale, void *out, int32_t dtype, void *stream);
 
 pa_status pa_attention_varlen_static(const void *q, int64_t q_token_stride,
                                      const void *key_cache, const void *value_cache,

@@ -57,9 +57,6 @@ SIGNATURES = {
     "pa_attention_set_tile_timing_events": ([_P, _P], ctypes.c_int),
     "pa_attention_varlen_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _I64, ctypes.c_float, _P, _I32, _P], ctypes.c_int),
-    "pa_attention_varlen_fp8_static": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
-                                        _I32, _I32, _I64, ctypes.c_float, ctypes.c_float, ctypes.c_float, _P, _I32,
-                                        _P], ctypes.c_int),
     "pa_rope_reshape_and_cache_fp8": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                        _I32, _I32, _I32, _I32, _I64, ctypes.c_float, ctypes.c_float, _I32, _P],
                                       ctypes.c_int32),
@@ -259,26 +256,6 @@ def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_c
                                              seq_lens.data_ptr(), query_start_loc.data_ptr(), B, T, max_query_len,
                                              max_seq_len, H, hkv, D, bs, nb, float(scale), out.data_ptr(), dt,
                                              _stream(stream)), "pa_attention_varlen_static")
-
-
-def pa_attention_varlen_fp8_static(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
-                                   block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
-                                   max_query_len: int, max_seq_len: int, scale: float, k_scale: float,
-                                   v_scale: float, out: torch.Tensor, stream=None) -> None:
-    """pa_attention_varlen_fp8 on the library's built-in scratch array (see pa_attention_varlen_static)."""
-    dt = _elem_code((q, "q"), (out, "out"))
-    _need(key_cache, "key_cache", torch.uint8)
-    _need(value_cache, "value_cache", torch.uint8)
-    T, H, D = q.shape
-    nb, bs, hkv, _ = key_cache.shape
-    B_ = seq_lens.shape[0]
-    _check(_lib().pa_attention_varlen_fp8_static(q.data_ptr(), q.stride(0), key_cache.data_ptr(),
-                                                 value_cache.data_ptr(), block_tables.data_ptr(),
-                                                 block_tables.shape[1], seq_lens.data_ptr(),
-                                                 query_start_loc.data_ptr(), B_, T, max_query_len, max_seq_len, H,
-                                                 hkv, D, bs, nb, float(scale), float(k_scale), float(v_scale),
-                                                 out.data_ptr(), dt, _stream(stream)),
-           "pa_attention_varlen_fp8_static")
 
 
 def pa_rope_reshape_and_cache(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,

@@ -60,26 +60,3 @@ extern "C" pa_status pa_attention_varlen_static(const void *q, int64_t q_token_s
                              num_kv_heads, head_dim, block_size, num_blocks, scale, out, scratch,
                              scratch ? PA_STATIC_WORKSPACE_BYTES : 0, dtype, stream);
 }
-
-extern "C" pa_status pa_attention_varlen_fp8_static(const void *q, int64_t q_token_stride, const void *key_cache,
-                                                    const void *value_cache, const int32_t *block_tables,
-                                                    int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                                                    const int32_t *query_start_loc, int32_t num_seqs,
-                                                    int32_t total_q_tokens, int32_t max_query_len,
-                                                    int32_t max_seq_len, int32_t num_heads, int32_t num_kv_heads,
-                                                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                                                    float scale, float k_scale, float v_scale, void *out,
-                                                    int32_t dtype, void *stream) {
-  const size_t need = pa_attention_workspace_size(num_seqs, total_q_tokens, max_query_len, max_seq_len, num_heads,
-                                                  num_kv_heads, head_dim, block_size);
-  if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
-  void *scratch = nullptr;
-  if (num_seqs > 0 && total_q_tokens > 0 && need > 0) {
-    scratch = static_scratch();
-    if (!scratch) return PA_ERR_CUDA;
-  }
-  return pa_attention_varlen_fp8(q, q_token_stride, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                                 seq_lens, query_start_loc, num_seqs, total_q_tokens, max_query_len, max_seq_len,
-                                 num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_scale, v_scale,
-                                 out, scratch, scratch ? PA_STATIC_WORKSPACE_BYTES : 0, dtype, stream);
-}
