@@ -325,8 +325,9 @@ def run_reference(args, world, rank) -> None:
         "decode_tokens_per_s": float(np.mean(toks)),
         "config": {"workload": workload_text(args), "seed": args.seed},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"per step: random requests of the workload (mean {np.mean(reqs):.1f} of "
-                                   f"{w.num_seqs}) for about {per_step:.1f} s of fp64 oracle work"},
+                         "sample": f"per step: {np.mean(reqs):.0f} request evaluations drawn in random order "
+                                   f"from the workload's {w.num_seqs} requests (wrapping around), about "
+                                   f"{per_step:.1f} s of fp64 oracle work"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
