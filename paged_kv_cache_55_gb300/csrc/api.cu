@@ -124,6 +124,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_t
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > INT32_MAX) return PA_ERR_UNSUPPORTED;  // a token row's element count is an int32 in the kernel
   if (key_token_stride < row || value_token_stride < row) return PA_ERR_DIMS;
   if (key_token_stride % 8 || value_token_stride % 8) return PA_ERR_ALIGN;
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
@@ -154,6 +155,7 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t k
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_NULL;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row > INT32_MAX) return PA_ERR_UNSUPPORTED;  // a token row's element count is an int32 in the kernel
   if (key_token_stride < row || value_token_stride < row) return PA_ERR_DIMS;
   if (key_token_stride % 8 || value_token_stride % 8) return PA_ERR_ALIGN;
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
@@ -321,6 +323,9 @@ pa_status rope_call(void *q, int64_t q_token_stride, const void *key, const void
   // 16-byte vectors of elements; 8-bit caches: 8-byte vectors of codes, rows of whole 16-byte vectors
   if (head_dim % (kv8 ? 16 : 8) || rotary_dim % 16) return PA_ERR_ALIGN;
   if (rotary_dim > 512) return PA_ERR_UNSUPPORTED;  // the table row is staged in shared memory
+  // a token's q, K and V rows, counted in 16-byte chunks, are an int32 in the kernel
+  if ((static_cast<int64_t>(num_heads) + 2 * static_cast<int64_t>(num_kv_heads)) * (head_dim / 8) > INT32_MAX)
+    return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!q || !key || !value || !key_cache || !value_cache || !slot_mapping || !positions || !cos_sin_cache)
     return PA_ERR_NULL;
@@ -406,10 +411,12 @@ pa_status pa_gather_kv(const void *key_cache, const void *value_cache, const int
   if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(key_out, 16) || !aligned(value_out, 16) ||
       !aligned(block_table_row, 4))
     return PA_ERR_ALIGN;
+  const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * esize;
+  if (row_bytes > INT32_MAX) return PA_ERR_UNSUPPORTED;  // a cache row's byte count is an int32 in the kernel
   DeviceState *ds = device_state();
   if (!ds) return PA_ERR_CUDA;
   cudaError_t err = pa::launch_gather_kv(key_cache, value_cache, block_table_row, seq_len,
-                                         num_kv_heads * head_dim * esize, block_size, num_blocks, key_out,
+                                         static_cast<int32_t>(row_bytes), block_size, num_blocks, key_out,
                                          value_out, ds->status, ds->sm_count, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(PA_ERR_LAUNCH, err);
   g_launches.fetch_add(1);

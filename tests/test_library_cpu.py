@@ -131,3 +131,18 @@ def test_fp8_validation_rejects_before_any_cuda_call(lib):
     assert a(*long_q, 1.0, 1.0, None, None, 0, 0, None) == -1               # chunks pass to the null check
     assert lib.pa_gather_kv(None, None, None, 4, 2, 64, 16, 10, None, None, 2, None) == -1
     assert lib.pa_launch_count() == 0
+
+
+def test_row_sizes_beyond_int32_are_refused_before_any_cuda_call(lib):
+    # num_kv_heads * head_dim elements (or bytes) per token row is an int32 inside the kernels
+    huge = 1 << 25  # x 128 elements = 2^32
+    assert lib.pa_reshape_and_cache(1, 1, 1 << 33, 1 << 33, 1, 1, 1, 1, huge, 128, 16, 1, 0, None) == -3
+    assert lib.pa_reshape_and_cache(1, 1, 1 << 33, 1 << 33, 1, 1, 1, 1, 1 << 20, 128, 16, 1, 0, None) != -3
+    assert lib.pa_reshape_and_cache_fp8(1, 1, 1 << 33, 1 << 33, 1, 1, 1, 1, huge, 128, 16, 1, 1.0, 1.0, 0,
+                                        None) == -3
+    assert lib.pa_gather_kv(16, 16, 4, 4, huge // 2, 128, 16, 10, 16, 16, 0, None) == -3
+    # rotary scatter: q, K and V rows of one token in 16-byte chunks
+    r = lib.pa_rope_reshape_and_cache
+    assert r(16, 1 << 40, 16, 16, 1 << 40, 1 << 40, 16, 16, 8, 8, 16, 4096, 128, 1, 1, 1 << 28, 8, 128, 16, 10, 0,
+             None) == -3
+    assert lib.pa_launch_count() == 0
