@@ -225,8 +225,9 @@ __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, 
 // 2^(s * sl2 - ms), summed into *sum and packed as the TMEM columns of two
 // UMMA K steps. SPLIT (bf16 operands, 8 significant bits): P as a hi + lo
 // pair, 32 columns [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo
-// 16-31]; otherwise (fp16, 11 bits: a weight's rounding error of 2^-12
-// keeps the output within the tolerance) one pair per two keys, 16 columns.
+// 16-31]; otherwise (fp16, 11 bits: a weight's relative rounding error of
+// at most 2^-11 moves the output by at most 2^-11 max|V|, and far less when
+// the roundings are independent) one pair per two keys, 16 columns.
 // The exponent is one fused multiply-add, whose unrounded product differs
 // from the rounded one ms was taken from by at most half an ulp of ms: below
 // 2^-12 while |ms| <= 2^12. EXACT rows (larger |ms|) round the product first,
