@@ -132,12 +132,102 @@ def _cache_code(*named) -> int:
     return _CACHE_CODES[first.dtype]
 
 
+# Shape checks. The C ABI receives plain pointers, so a tensor of the wrong
+# size would be read or written past its end on the device; these checks use
+# only .shape and run before any library call.
+def _dims(t: torch.Tensor, n: int, name: str) -> None:
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+
+
+def _cache_pair_shapes(key_cache: torch.Tensor, value_cache: torch.Tensor) -> None:
+    _dims(key_cache, 4, "key_cache")
+    if value_cache.shape != key_cache.shape:
+        raise ValueError(f"value_cache {tuple(value_cache.shape)} must have key_cache's shape "
+                         f"{tuple(key_cache.shape)} [num_blocks, block_size, num_kv_heads, head_dim]")
+
+
+def _scatter_shapes(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                    slot_mapping: torch.Tensor) -> None:
+    """key/value [T, Hkv, D], caches [NB, bs, Hkv, D], slot_mapping [T]."""
+    _dims(key, 3, "key")
+    if value.shape != key.shape:
+        raise ValueError(f"value {tuple(value.shape)} must have key's shape {tuple(key.shape)}")
+    _cache_pair_shapes(key_cache, value_cache)
+    if tuple(key_cache.shape[2:]) != tuple(key.shape[1:]):
+        raise ValueError(f"cache rows {tuple(key_cache.shape[2:])} must be key's [Hkv, D] {tuple(key.shape[1:])}")
+    _dims(slot_mapping, 1, "slot_mapping")
+    if slot_mapping.shape[0] != key.shape[0]:
+        raise ValueError(f"slot_mapping has {slot_mapping.shape[0]} entries for {key.shape[0]} tokens")
+
+
+def _attention_shapes(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                      out: torch.Tensor) -> None:
+    """q and out [T, H, D], caches [NB, bs, Hkv, D], block_tables [B, M], seq_lens [B], query_start_loc [B+1]."""
+    _dims(q, 3, "q")
+    if out.shape != q.shape:
+        raise ValueError(f"out {tuple(out.shape)} must have q's shape {tuple(q.shape)}")
+    _cache_pair_shapes(key_cache, value_cache)
+    if key_cache.shape[3] != q.shape[2]:
+        raise ValueError(f"head_dim of the caches ({key_cache.shape[3]}) and of q ({q.shape[2]}) differ")
+    _dims(seq_lens, 1, "seq_lens")
+    _dims(block_tables, 2, "block_tables")
+    _dims(query_start_loc, 1, "query_start_loc")
+    b = seq_lens.shape[0]
+    if block_tables.shape[0] != b or query_start_loc.shape[0] != b + 1:
+        raise ValueError(f"{b} requests need block_tables [{b}, M] and query_start_loc [{b + 1}], got "
+                         f"{tuple(block_tables.shape)} and {tuple(query_start_loc.shape)}")
+
+
+def _rope_shapes(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                 value_cache: torch.Tensor, slot_mapping: torch.Tensor, positions: torch.Tensor,
+                 cos_sin_cache: torch.Tensor) -> None:
+    """q [T, H, D], key/value [T, Hkv, D], caches [NB, bs, Hkv, D], slot_mapping and positions [T],
+    cos_sin_cache [max_position, rotary_dim]."""
+    _scatter_shapes(key, value, key_cache, value_cache, slot_mapping)
+    _dims(q, 3, "q")
+    if q.shape[0] != key.shape[0] or q.shape[2] != key.shape[2]:
+        raise ValueError(f"q {tuple(q.shape)} must be [T, H, D] for key {tuple(key.shape)}")
+    _dims(positions, 1, "positions")
+    if positions.shape[0] != q.shape[0]:
+        raise ValueError(f"positions has {positions.shape[0]} entries for {q.shape[0]} tokens")
+    _dims(cos_sin_cache, 2, "cos_sin_cache")
+
+
+def _gather_shapes(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_row: torch.Tensor, seq_len: int,
+                   key_out: torch.Tensor, value_out: torch.Tensor) -> None:
+    """caches [NB, bs, Hkv, D], block_table_row [>= ceil(seq_len / bs)], outputs [seq_len, Hkv, D]."""
+    _cache_pair_shapes(key_cache, value_cache)
+    _dims(block_table_row, 1, "block_table_row")
+    bs = key_cache.shape[1]
+    if block_table_row.shape[0] * bs < seq_len:
+        raise ValueError(f"block_table_row has {block_table_row.shape[0]} blocks of {bs} for {seq_len} tokens")
+    want = (seq_len, key_cache.shape[2], key_cache.shape[3])
+    if tuple(key_out.shape) != want or tuple(value_out.shape) != want:
+        raise ValueError(f"key_out and value_out must be {want}, got {tuple(key_out.shape)} and "
+                         f"{tuple(value_out.shape)}")
+
+
+def _index_tensors(*named) -> None:
+    for t, n in named:
+        _need(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+
+
+def _workspace(workspace: torch.Tensor) -> None:
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+
+
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
                          value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
     """key/value [T, Hkv, D] (token stride free), caches [NB, bs, Hkv, D], all bf16 or all fp16;
     slots int64 [T]."""
     dt = _elem_code((key, "key"), (value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache"))
     _need(slot_mapping, "slot_mapping", torch.int64)
+    _scatter_shapes(key, value, key_cache, value_cache, slot_mapping)
     T, hkv, d = key.shape
     if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
         raise ValueError("each token row of key/value must be [Hkv, D] contiguous")
@@ -158,6 +248,7 @@ def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: 
     _need(key_cache, "key_cache", torch.uint8)
     _need(value_cache, "value_cache", torch.uint8)
     _need(slot_mapping, "slot_mapping", torch.int64)
+    _scatter_shapes(key, value, key_cache, value_cache, slot_mapping)
     T, hkv, d = key.shape
     if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
         raise ValueError("each token row of key/value must be [Hkv, D] contiguous")
@@ -193,10 +284,9 @@ def pa_attention_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: t
     """q [T, H, D], caches [NB, bs, Hkv, D], out [T, H, D] contiguous (all bf16 or all fp16),
     block_tables [B, M] int32, seq_lens [B] int32, query_start_loc [B+1] int32, workspace uint8 (device)."""
     dt = _elem_code((q, "q"), (out, "out"), (key_cache, "key_cache"), (value_cache, "value_cache"))
-    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
-        _need(t, n, torch.int32)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
+    _index_tensors((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc"))
+    _attention_shapes(q, key_cache, value_cache, block_tables, seq_lens, query_start_loc, out)
+    _workspace(workspace)
     if not out.is_contiguous() or not key_cache.is_contiguous() or not value_cache.is_contiguous():
         raise ValueError("out and the caches must be contiguous")
     T, H, D = q.shape
@@ -221,10 +311,9 @@ def pa_attention_varlen_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cach
     dt = _elem_code((q, "q"), (out, "out"))
     _need(key_cache, "key_cache", torch.uint8)
     _need(value_cache, "value_cache", torch.uint8)
-    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
-        _need(t, n, torch.int32)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
+    _index_tensors((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc"))
+    _attention_shapes(q, key_cache, value_cache, block_tables, seq_lens, query_start_loc, out)
+    _workspace(workspace)
     if not out.is_contiguous() or not key_cache.is_contiguous() or not value_cache.is_contiguous():
         raise ValueError("out and the caches must be contiguous")
     T, H, D = q.shape
@@ -248,7 +337,13 @@ def pa_attention_varlen_static(q: torch.Tensor, key_cache: torch.Tensor, value_c
     library's built-in scratch array (PA_STATIC_WORKSPACE_BYTES) is used instead. Calls on one device
     share that array, so calls on different streams must not overlap."""
     dt = _elem_code((q, "q"), (out, "out"), (key_cache, "key_cache"), (value_cache, "value_cache"))
+    _index_tensors((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc"))
+    _attention_shapes(q, key_cache, value_cache, block_tables, seq_lens, query_start_loc, out)
+    if not out.is_contiguous() or not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("out and the caches must be contiguous")
     T, H, D = q.shape
+    if q.stride(2) != 1 or q.stride(1) != D:
+        raise ValueError("each token row of q must be [H, D] contiguous")
     nb, bs, hkv, _ = key_cache.shape
     B = seq_lens.shape[0]
     _check(_lib().pa_attention_varlen_static(q.data_ptr(), q.stride(0), key_cache.data_ptr(),
@@ -268,9 +363,10 @@ def pa_rope_reshape_and_cache(q: torch.Tensor, key: torch.Tensor, value: torch.T
     _need(slot_mapping, "slot_mapping", torch.int64)
     _need(positions, "positions", torch.int64)
     _need(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _rope_shapes(q, key, value, key_cache, value_cache, slot_mapping, positions, cos_sin_cache)
     T, H, D = q.shape
     _, hkv, d = key.shape
-    for t, n, h in ((q, "q", H), (key, "key", hkv), (value, "value", hkv)):
+    for t, n in ((q, "q"), (key, "key"), (value, "value")):
         if t.stride(2) != 1 or t.stride(1) != D:
             raise ValueError(f"each token row of {n} must be [heads, D] contiguous")
     if not (key_cache.is_contiguous() and value_cache.is_contiguous() and cos_sin_cache.is_contiguous()
@@ -297,6 +393,7 @@ def pa_rope_reshape_and_cache_fp8(q: torch.Tensor, key: torch.Tensor, value: tor
     _need(slot_mapping, "slot_mapping", torch.int64)
     _need(positions, "positions", torch.int64)
     _need(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _rope_shapes(q, key, value, key_cache, value_cache, slot_mapping, positions, cos_sin_cache)
     T, H, D = q.shape
     _, hkv, d = key.shape
     for t, n in ((q, "q"), (key, "key"), (value, "value")):
@@ -325,6 +422,7 @@ def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_map
         raise ValueError("caches and block_mapping must be contiguous")
     if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be [n, 2]")
+    _cache_pair_shapes(key_cache, value_cache)
     nb, bs, hkv, d = key_cache.shape
     _check(_lib().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), block_mapping.data_ptr(),
                                  block_mapping.shape[0], hkv, d, bs, nb, dt, _stream(stream)), "pa_copy_blocks")
@@ -334,6 +432,10 @@ def pa_gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table
                  seq_len: int, key_out: torch.Tensor, value_out: torch.Tensor, stream=None) -> None:
     dt = _cache_code((key_cache, "key_cache"), (value_cache, "value_cache"), (key_out, "key_out"),
                      (value_out, "value_out"))
+    _need(block_table_row, "block_table_row", torch.int32)
+    _gather_shapes(key_cache, value_cache, block_table_row, seq_len, key_out, value_out)
+    if not all(t.is_contiguous() for t in (key_cache, value_cache, block_table_row, key_out, value_out)):
+        raise ValueError("caches, block_table_row and the outputs must be contiguous")
     nb, bs, hkv, d = key_cache.shape
     _check(_lib().pa_gather_kv(key_cache.data_ptr(), value_cache.data_ptr(), block_table_row.data_ptr(), seq_len,
                                hkv, d, bs, nb, key_out.data_ptr(), value_out.data_ptr(), dt,
