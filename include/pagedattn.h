@@ -48,6 +48,9 @@
  *     reading map, §2.3, sweeps page sizes; the kernels stage K/V 16 keys at a
  *     time); num_heads a multiple of num_kv_heads with group size 1, 2, 4 or 8.
  *     pa_rope_reshape_and_cache and pa_copy_blocks take any block_size.
+ *     The elements of one token's cache row (num_kv_heads * head_dim; for
+ *     the rotary calls, its q, K and V rows together) must number fewer than
+ *     2^31 (PA_ERR_UNSUPPORTED otherwise).
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
