@@ -148,6 +148,25 @@ def pin_dense_vs_sdpa_fp16(oracle):
     pin_dense_vs_sdpa(oracle, dtype="fp16")
 
 
+def pin_sampled_equals_full(oracle):
+    """attention_sampled, the reference of the full-size GPU checks, equals attention at every
+    (token, head) pair asked for in any order, bit for bit (the same definition, evaluated the
+    same way), on the dense shapes above (so it inherits their agreement with SDPA)."""
+    rng = np.random.default_rng(15)
+    for k, (ctx, ql, H, Hkv, D, bs) in enumerate(DENSE_CASES):
+        dtype = "fp16" if k % 2 else "bf16"
+        p = DenseProblem(rng, ctx, ql, H, Hkv, D, bs, dtype=dtype)
+        full = p.run(oracle)
+        T = int(p.qsl[-1])
+        if T == 0:
+            continue
+        order = rng.permutation(T * H)
+        tokens, heads = (order // H).astype(np.int64), (order % H).astype(np.int32)
+        got = oracle.attention_sampled(p.q, p.kc, p.vc, p.bt, p.seq_lens, p.qsl, H, p.scale, tokens, heads,
+                                       dtype=dtype)
+        assert np.array_equal(got, full[tokens, heads]), f"sampled != full for case {(ctx, ql, H, Hkv, D, bs)}"
+
+
 def pin_block_permutation_invariance(oracle):
     rng = np.random.default_rng(12)
     p = DenseProblem(rng, [40, 9, 70], [3, 1, 6], 8, 2, 8, bs=16, extra_blocks=5)
@@ -452,6 +471,7 @@ def pin_rope_relative_positions(oracle):
 
 PINS = [
     pin_dense_vs_sdpa,
+    pin_sampled_equals_full,
     pin_dense_vs_sdpa_fp16,
     pin_seq_len_one_is_v_row_fp16,
     pin_fp16_decoding_matches_ieee,

@@ -62,6 +62,9 @@ MUTANTS = {
                              "return bf16_to_double(h);"),
     "first_query_row_only": ("const uint16_t *qrow = p->q + ((int64_t)(q0 + i) * p->num_heads + h) * D;",
                              "const uint16_t *qrow = p->q + ((int64_t)(q0) * p->num_heads + h) * D;"),
+    "sampled_first_row_of_request": ("int32_t i = (int32_t)(t - query_start_loc[b]);", "int32_t i = 0;"),
+    "sampled_kv_head_modulo": ("gather_request(&p, b, h / G, K, V);",
+                               "gather_request(&p, b, h % num_kv_heads, K, V);"),
     "drops_last_token": ("        if (s < 0)\n            continue;\n        int64_t block",
                          "        if (s < 0 || t == num_tokens - 1)\n            continue;\n        int64_t block"),
 }
