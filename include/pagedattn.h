@@ -90,7 +90,10 @@ enum {
 };
 
 /*
- * Step 1 - reshape_and_cache: write this step's new K/V rows into the cache.
+ * Step 1 - reshape_and_cache: write this step's new K/V rows into the cache
+ * (vLLM notes, §Paged Attention: slot_mapping names each new token's slot,
+ * and a slot splits into block = slot / block_size and offset = slot %
+ * block_size, which address the cache).
  *
  * For every token t in [0, num_tokens) with s = slot_mapping[t] >= 0:
  *   key_cache[s / block_size][s % block_size][:][:]   = key[t][:][:]
@@ -157,7 +160,13 @@ pa_status pa_attention_plan_info(int32_t num_seqs, int32_t max_seq_len,
 
 /*
  * Step 2 - attention over the paged cache, for a batch that may mix decode
- * tokens and chunked-prefill chunks.
+ * tokens and chunked-prefill chunks (vLLM notes, §LLM 推理全流程 3: Q of
+ * [query_lens, num_heads, head_dim] against K/V read through the block table
+ * from the paged cache, GQA by index, FlashAttention-style online softmax;
+ * §Continuous Batching: each request's query tokens are the ones between
+ * num_computed_tokens and num_tokens; LLM-infra reading map, §6: long
+ * contexts split over KV partitions whose partial results are merged by
+ * their log-sum-exp, Flash-Decoding).
  *
  * Request b owns query tokens [query_start_loc[b], query_start_loc[b+1]) and
  * has seq_len = seq_lens[b] KV tokens, which include its new tokens (run
@@ -367,12 +376,16 @@ pa_status pa_attention_set_tile_timing_events(void *start, void *stop);
  * memory, held on every GPU that loads the library until the process exits).
  * The call itself allocates nothing.
  *
- *   - A problem whose pa_attention_workspace_size() exceeds
- *     PA_STATIC_WORKSPACE_BYTES is rejected with PA_ERR_WORKSPACE before
- *     anything is launched; use pa_attention_varlen for it.
+ *   - A problem whose workspace exceeds PA_STATIC_WORKSPACE_BYTES is
+ *     rejected with PA_ERR_WORKSPACE before anything is launched; use
+ *     pa_attention_varlen for it. The size checked is that of the plan
+ *     pa_attention_varlen makes for 16-bit caches (at most
+ *     pa_attention_workspace_size(), which also covers 8-bit caches).
  *   - The first call on a device looks up that device's copy of the scratch
  *     array (with the device current); make that first call before any
- *     stream capture. Later calls only read the cached address.
+ *     stream capture. Later calls only read the cached address. A lookup
+ *     that fails returns PA_ERR_CUDA (pa_last_cuda_error() names the
+ *     error) and is tried again by the next call.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind. Nothing in it needs to start at zero (the planning kernel
  *     rewrites every word that later kernels read), but calls whose kernels

@@ -76,6 +76,8 @@ bool supported_dims(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, i
 
 }  // namespace
 
+void pa::set_last_cuda_error(cudaError_t err) { t_last_cuda_error = err; }
+
 extern "C" {
 
 const char *pa_status_string(int32_t status) {

@@ -829,7 +829,14 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         vt1 = kt1 + T::TILE_BYTES;
       }
       if (!__all_sync(0xffffffffu, landed)) {  // leave together, never with a diverged warp
-        if (lane == 0) flag_error(p.status, PA_FLAG_TIMEOUT);
+        if (lane == 0) {
+          flag_error(p.status, PA_FLAG_TIMEOUT);
+          // Loads this warp issued into its ring may still be in flight: wait
+          // for each of them (bounded) before the warp stops using its slots.
+          for (uint32_t g = consumed; g < issued; ++g)
+            (void)mbar_wait_bounded(smem_u32(&bars[warp][g % S]), (g / S) & 1u, kWaitTimeoutNs);
+        }
+        __syncwarp();
         return;
       }
       // only the unit's last tile can be partial

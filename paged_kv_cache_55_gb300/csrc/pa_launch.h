@@ -8,6 +8,10 @@
 
 namespace pa {
 
+// Record the CUDA error behind a PA_ERR_LAUNCH / PA_ERR_CUDA return, for
+// pa_last_cuda_error() on the calling host thread (defined in api.cu).
+void set_last_cuda_error(cudaError_t err);
+
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t key_stride,
                                      int64_t value_stride, void *key_cache, void *value_cache,
                                      const int64_t *slot_mapping, int32_t num_tokens, int32_t row_elems,

@@ -13,7 +13,7 @@ from paged_kv_cache_55_gb300 import binding as B
 from paged_kv_cache_55_gb300 import workloads as W
 from paged_kv_cache_55_gb300.runner import DeviceStep, bf16_to_float64
 
-from test_gpu_parity import _sample_pairs, assert_attention_close
+from test_gpu_parity import NAMED, assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -104,26 +104,13 @@ def test_fp8_every_code_round_trips_exactly(dtype, head_dim):
     assert np.array_equal(got, want), "seq_len 1 over an 8-bit cache must return the V row exactly"
 
 
-@pytest.mark.parametrize("name,dtype", [("gqa_decode", "bf16"), ("mha_decode", "bf16"), ("long_decode", "bf16"),
-                                        ("mixed_step", "bf16"), ("mixed_step", "fp16")])
-def test_fp8_named_full_size_sampled(oracle, name, dtype):
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("name", NAMED)
+def test_fp8_named_full_size(oracle, name, dtype):
+    """Full-size workloads over 8-bit caches: the whole quantised cache bit for bit
+    and every attention output against the oracle."""
     w = W.by_name(name, seed=0, kv_dtype=FP8, dtype=dtype)
-    st = DeviceStep(w)
-    st.run()
-    torch.cuda.synchronize()
-    assert B.pa_debug_status() == 0
-    kc = st.key_cache.cpu().numpy()
-    vc = st.value_cache.cpu().numpy()
-    kref, vref = w.key_cache.copy(), w.value_cache.copy()
-    oracle.reshape_and_cache_fp8(w.key, w.value, kref, vref, w.slot_mapping, w.block_size, w.k_scale, w.v_scale,
-                                 dtype=w.dtype)
-    assert np.array_equal(kc, kref) and np.array_equal(vc, vref), "full-size quantising scatter"
-    tokens, heads = _sample_pairs(w, 64, np.random.default_rng(1))
-    ref = oracle.attention_sampled(w.q, kc, vc, w.block_tables, w.seq_lens, w.query_start_loc, w.num_heads,
-                                   w.scale, tokens, heads, dtype=w.dtype, k_scale=w.k_scale, v_scale=w.v_scale)
-    out = bf16_to_float64(st.out)
-    gpu = out[tokens, heads]
-    assert_attention_close(gpu, ref, f"{name} fp8 sampled")
+    run_fp8(w, oracle)
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])

@@ -146,3 +146,11 @@ def test_row_sizes_beyond_int32_are_refused_before_any_cuda_call(lib):
     assert r(16, 1 << 40, 16, 16, 1 << 40, 1 << 40, 16, 16, 8, 8, 16, 4096, 128, 1, 1, 1 << 28, 8, 128, 16, 10, 0,
              None) == -3
     assert lib.pa_launch_count() == 0
+
+
+def test_static_workspace_size_matches_the_header():
+    """The binding's copy of PA_STATIC_WORKSPACE_BYTES is the header's value."""
+    text = open(os.path.join(ROOT, "include", "pagedattn.h")).read()
+    m = re.search(r"#define\s+PA_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "PA_STATIC_WORKSPACE_BYTES is not a (N u << S) literal any more: update this test"
+    assert B.PA_STATIC_WORKSPACE_BYTES == int(m.group(1)) << int(m.group(2))

@@ -28,21 +28,23 @@ pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-3, 1e-2
 
 
-def _static_call(st: DeviceStep, out: torch.Tensor) -> int:
+def _static_call(st: DeviceStep, out: torch.Tensor, dtype: int = B.PA_BF16) -> int:
     w = st.w
     lib = B._lib()
     return lib.pa_attention_varlen_static(
         st.q.data_ptr(), st.q.stride(0), st.key_cache.data_ptr(), st.value_cache.data_ptr(),
         st.block_tables.data_ptr(), st.block_tables.shape[1], st.seq_lens.data_ptr(), st.query_start_loc.data_ptr(),
         w.num_seqs, w.total_q, st.max_query_len, st.max_seq_len, w.num_heads, w.num_kv_heads, w.head_dim,
-        w.block_size, w.num_blocks, ctypes.c_float(w.scale), out.data_ptr(), B.PA_BF16,
+        w.block_size, w.num_blocks, ctypes.c_float(w.scale), out.data_ptr(), dtype,
         torch.cuda.current_stream().cuda_stream)
 
 
-def test_static_workspace_matches_regular_entry_point_twice():
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_static_workspace_matches_regular_entry_point_twice(dtype):
     # decode requests long enough to be split into partitions, plus causal prefill chunks
     w = W.make_workload("no_alloc", context_lens=[3000, 17, 900, 0, 1500, 64, 2600, 5],
-                        query_lens=[1, 1, 1, 33, 1, 12, 1, 1], num_heads=32, num_kv_heads=8, head_dim=128, seed=13)
+                        query_lens=[1, 1, 1, 33, 1, 12, 1, 1], num_heads=32, num_kv_heads=8, head_dim=128, seed=13,
+                        dtype=dtype)
     st = DeviceStep(w)
     need = B.pa_attention_workspace_size(w.num_seqs, w.total_q, st.max_query_len, st.max_seq_len, w.num_heads,
                                          w.num_kv_heads, w.head_dim)
@@ -53,7 +55,7 @@ def test_static_workspace_matches_regular_entry_point_twice():
     ref_bits = bf16_to_numpy_bits(st.out)
     for _ in range(2):
         out = torch.full_like(st.out, float("nan"))
-        assert _static_call(st, out) == 0
+        assert _static_call(st, out, B.PA_FP16 if dtype == "fp16" else B.PA_BF16) == 0
         torch.cuda.synchronize()
         assert B.pa_debug_status() == 0
         got = bf16_to_float64(out)
