@@ -13,6 +13,12 @@ HBM before timing starts. The KV working set (1.7 GB for the default
 workload) is far larger than the 126 MB L2, so no L2 flush is needed between
 steps. Prints one JSON line (rank 0).
 
+The default run (gqa_decode, bf16, N=1) adds to its line the same step drawn
+from two more seeds ("seed_spread") and one record per other named
+configuration ("configs": tiny, MHA, long-context, mixed), each with its
+step time, the dominant kernel's roofline and the oracle timed on the host
+cores (one thread as well for the tiny, MHA and GQA configurations).
+
 --impl reference times the fp64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload.
 
@@ -346,6 +352,115 @@ def workload_text(args) -> str:
     return text + (f" [batch overridden to {args.batch}]" if args.batch else "")
 
 
+def step_timing(st, acct, steps: int, warmup: int, stream):
+    """Device-timed steps of a built DeviceStep: the mean over `steps` back-to-back
+    steps (one event pair around all of them), then a second pass with an event
+    pair around every step and around its split-KV and prefill-tile kernels
+    (per-step median, kernel durations)."""
+    import torch
+    from paged_kv_cache_55_gb300 import binding as B
+    has_tiles = acct["tile_flops"] > 0
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(ev(), ev()) for _ in range(steps)]
+    kern_ev = [(ev(), ev()) for _ in range(steps)]
+    tile_ev = [(ev(), ev()) for _ in range(steps)]
+    for a, b in step_ev + kern_ev + tile_ev:  # create the events before timing
+        a.record(stream)
+        b.record(stream)
+    for _ in range(max(warmup, 1)):
+        st.run()
+    torch.cuda.synchronize()
+    if B.pa_debug_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+    t0, t1 = ev(), ev()
+    launches0 = B.pa_launch_count()
+    t0.record(stream)
+    for _ in range(steps):
+        st.run()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = B.pa_launch_count() - launches0
+    step_ms = t0.elapsed_time(t1) / steps
+    for k in range(steps):
+        step_ev[k][0].record(stream)
+        B.pa_attention_set_timing_events(*kern_ev[k])
+        if has_tiles:
+            B.pa_attention_set_tile_timing_events(*tile_ev[k])
+        st.run()
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    if B.pa_debug_status() != 0:
+        raise RuntimeError("device status flags set during timing")
+    return {
+        "step_ms": step_ms,
+        "step_ms_median": statistics.median(a.elapsed_time(b) for a, b in step_ev),
+        "kern_ms": statistics.mean(a.elapsed_time(b) for a, b in kern_ev),
+        "tile_ms": statistics.mean(a.elapsed_time(b) for a, b in tile_ev) if has_tiles else 0.0,
+        "launches": launches,
+    }
+
+
+def rooflines(acct, t, peaks):
+    """The split-KV kernel against HBM (bytes of the requests it serves) and, when the
+    step has prefill chunks, the tensor-core tile kernel against the bf16 peak
+    (algorithmic FLOPs: 4 H D per visible (query, key) pair of the chunks)."""
+    has_tiles = acct["tile_flops"] > 0
+    dec_bytes = acct["attention_bytes"] if not has_tiles else acct["decode_bytes"]
+    kern_achieved = dec_bytes / (t["kern_ms"] * 1e-3) / 1e9
+    decode = {"bound": "hbm", "kernel": "splitkv_attention_kernel", "achieved": kern_achieved,
+              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kern_achieved / peaks["hbm_gbs"],
+              "peak_source": peaks["source"], "kernel_ms": t["kern_ms"],
+              "algorithmic_bytes_per_launch": dec_bytes, "traffic": None}
+    tile = None
+    if has_tiles:
+        tile_achieved = acct["tile_flops"] / (t["tile_ms"] * 1e-3) / 1e12
+        tile = {"bound": "tensor", "kernel": "prefill_tile_kernel", "achieved": tile_achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tile_achieved / peaks["bf16_tflops"],
+                "peak_source": peaks["source"], "kernel_ms": t["tile_ms"],
+                "algorithmic_flops_per_launch": acct["tile_flops"], "traffic": None}
+    return decode, tile
+
+
+EXTRA_CONFIGS = ["tiny_decode", "mha_decode", "long_decode", "mixed_step"]
+SINGLE_THREAD_ORACLE = {"tiny_decode", "mha_decode", "gqa_decode"}
+
+
+def config_record(name, seed, steps, warmup, device, stream, peaks, cpu_seconds):
+    """One named configuration on one GPU: device-timed steps, the dominant kernel's
+    roofline, and the oracle on the host cores (all of them, and one thread for the
+    small and decode configurations) on a bounded sample of the same workload."""
+    import torch
+    from paged_kv_cache_55_gb300 import workloads as W
+    from paged_kv_cache_55_gb300.runner import DeviceStep
+    w = W.by_name(name, seed=seed)
+    acct = step_accounting(w)
+    st = DeviceStep(w, device=str(device))
+    t = step_timing(st, acct, steps, warmup, stream)
+    del st
+    torch.cuda.empty_cache()
+    peaks_d, tile = rooflines(acct, t, peaks)
+    value = acct["step_bytes"] / (t["step_ms"] * 1e-3) / 1e9
+    rec = {"workload": WORKLOAD_TEXT[name], "seed": seed, "steps": steps, "warmup": warmup,
+           "ms_per_step": t["step_ms"], "ms_per_step_median": t["step_ms_median"], "value": value, "unit": UNIT,
+           "hbm_frac": value / peaks["hbm_gbs"], "query_tokens_per_s": acct["query_tokens"] / (t["step_ms"] * 1e-3),
+           "step_bytes": acct["step_bytes"], "flops": acct["flops"], "gpu_launches_per_step": t["launches"] / steps,
+           "roofline": tile if tile is not None else peaks_d,
+           "roofline_decode_kernel": peaks_d if tile is not None else None}
+    if name == "tiny_decode":
+        rec["roofline"]["bound"] = "launch latency (15 KB of work: the bytes are not the limit)"
+    kc, vc = scattered_caches(w)
+    rng = np.random.default_rng(1)
+    r, _, secs, n, threads = oracle_rate(w, kc, vc, cpu_seconds, rng, host_threads())
+    rec["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
+                           "sample": f"{n} request evaluations drawn in random order from the workload's "
+                                     f"{w.num_seqs} requests, {secs:.1f} s of fp64 oracle attention"}
+    if name in SINGLE_THREAD_ORACLE:
+        r1, _, secs1, n1, _ = oracle_rate(w, kc, vc, cpu_seconds / 2, np.random.default_rng(2), 1)
+        rec["cpu_baseline_single_thread"] = {"value": r1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                             "sample": f"{n1} request evaluations, {secs1:.1f} s on one thread"}
+    return rec
+
+
 def run_ours(args, world, rank, local_rank) -> None:
     import torch
     import torch.distributed as dist
@@ -410,13 +525,18 @@ def run_ours(args, world, rank, local_rank) -> None:
     # Second pass of the same steps, with events around the split-KV kernel
     # and the prefill-tile kernel alone (they serialise the kernels against
     # their neighbours, so the step time above is taken without them).
+    step_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
     for k in range(args.steps):
+        step_pairs[k][0].record(stream)
         B.pa_attention_set_timing_events(*ev_pairs[k])
         if has_tiles:
             B.pa_attention_set_tile_timing_events(*tile_pairs[k])
         st.run()
+        step_pairs[k][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    step_ms_median = statistics.median(a.elapsed_time(b) for a, b in step_pairs)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs)
     tile_ms = statistics.mean(a.elapsed_time(b) for a, b in tile_pairs) if has_tiles else 0.0
 
@@ -508,6 +628,7 @@ def run_ours(args, world, rank, local_rank) -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "ms_per_step_median": step_ms_median,
         "hbm_frac": value / peaks["hbm_gbs"],
         "decode_tokens_per_s": total_tok / (max_ms * 1e-3),
         "config": {"workload": workload_text(args), "seed": args.seed,
@@ -535,6 +656,38 @@ def run_ours(args, world, rank, local_rank) -> None:
                                 "sample": f"{n} request evaluations drawn in random order from the workload's "
                                           f"{w.num_seqs} requests, {secs:.1f} s of fp64 oracle attention "
                                           f"(KV bytes of the evaluated requests / time)"}
+        if args.workload in SINGLE_THREAD_ORACLE:
+            r1, _, secs1, n1, _ = oracle_rate(w, kc, vc, args.cpu_seconds / 3, np.random.default_rng(2), 1)
+            line["cpu_baseline_single_thread"] = {"value": r1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                                  "sample": f"{n1} request evaluations, {secs1:.1f} s on one thread"}
+        del kc, vc
+    default_line = (args.workload == "gqa_decode" and args.dtype == "bf16" and not args.kv_dtype and
+                    args.block_size == 16 and not args.rope and not args.batch)
+    if rank == 0 and world == 1 and default_line and not args.no_extra_configs:
+        # the other named configurations and two more seeds of this one, each timed
+        # on its own (outside the headline's timed region)
+        del sets
+        torch.cuda.empty_cache()
+        n_extra = max(3, min(args.steps, 20))
+        spread = {"seeds": [args.seed], "value": [value], "kernel_frac": [roof_decode["frac"]],
+                  "ms_per_step": [max_ms]}
+        for sd in (args.seed + 1, args.seed + 2):
+            w2 = W.by_name(args.workload, seed=sd)
+            a2 = step_accounting(w2)
+            st2 = DeviceStep(w2, device=str(device))
+            t2 = step_timing(st2, a2, n_extra, max(args.warmup, 3), stream)
+            del st2
+            torch.cuda.empty_cache()
+            d2, _ = rooflines(a2, t2, peaks)
+            spread["seeds"].append(sd)
+            spread["value"].append(a2["step_bytes"] / (t2["step_ms"] * 1e-3) / 1e9)
+            spread["kernel_frac"].append(d2["frac"])
+            spread["ms_per_step"].append(t2["step_ms"])
+        line["seed_spread"] = spread
+        line["configs"] = {}
+        for name in EXTRA_CONFIGS:
+            line["configs"][name] = config_record(name, args.seed, n_extra, max(args.warmup, 3), device, stream,
+                                                  peaks, args.extra_cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -714,6 +867,10 @@ def main() -> None:
                     help="override the workload's number of requests (small profiling cases only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip the records of the other named configurations and seeds")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=4.0,
+                    help="oracle seconds per extra configuration record")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
