@@ -41,8 +41,10 @@ struct TileParams {
 // the element type of q and out (ElemBf16 or ElemFp16); KV8: the caches hold
 // 8-bit E4M3 codes (the maps then have one-byte elements and boxes of
 // min(block_size, 32) rows of head_dim codes).
+// vmapb: at head_dim 128 over 16-bit caches, the value cache as whole-block
+// boxes (block_size rows x both 64-element atoms; unused otherwise).
 template <int D, int G, typename E, bool KV8>
-cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp,
-                                 int sm_count, cudaStream_t stream);
+cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &vmapb,
+                                 const TileParams &tp, int sm_count, cudaStream_t stream);
 
 }  // namespace pa

@@ -9,41 +9,46 @@
 //     position (chunked prefill, named in the LLM-infra reading map,
 //     "lpnh.cn/news/2436702", §2.3).
 //
-// One CTA handles one tile of 256 "packed rows" = (query position, head of
-// the GQA group) pairs of one request and one KV head, as two halves A and B
-// of 128 rows (the UMMA M) that share every K/V range staged for the tile, so
-// each K/V byte serves 2 x 128 rows. The keys are walked in ranges of 128 (an
-// M128 x N128 product runs at close to the tensor cores' peak; N64 at half)
-// by three kinds of warps that hand work over through mbarriers only:
-//   * a producer warp issues TMA loads of the (block, KV head) tiles of K and
-//     V through the block table into 128-byte-swizzled shared memory (the
-//     decode path's boxes), into one ring of K(0), V(0), K(1), V(1), ...
-//     (as many 128-key slots as shared memory holds: five at D = 128), each
-//     slot with full/empty barriers, so loads run two ranges ahead;
+// One CTA per SM runs a stream of units. A unit is a tile of 256 "packed
+// rows" = (query position, head of the GQA group) pairs of one request and
+// one KV head, as two halves A and B of 128 rows (the UMMA M) that share
+// every K/V range staged for the tile, so each K/V byte serves 2 x 128 rows.
+// The keys are walked in ranges of 128 (an M128 x N128 product runs at close
+// to the tensor cores' peak; N64 at half) by warps that hand work over
+// through mbarriers only (every wait bounded):
+//   * a producer warp claims units from the global queue and publishes each
+//     in a two-slot record ring, then issues TMA loads of its K and V ranges
+//     through the block table into one ring of K(0), V(0), K(1), V(1), ...
+//     (five 32 KB slots at D = 128), running on into the next unit while the
+//     current one finishes: a unit's first loads are in flight before the
+//     previous unit's last products. K arrives as per-atom boxes of 16 rows
+//     (the K-major operand wants rows 128 bytes apart); at head_dim 128, V
+//     arrives one box per cache block holding both 64-element atoms (4-D
+//     tensor map), fewer and larger boxes, which the TMA engine moves faster;
 //   * an MMA warp issues tcgen05.mma. Each half owns one score buffer in
 //     tensor memory: S(r) = Q K(r)^T lands there, the softmax overwrites it
-//     in place with P(r), and O += P_hi(r) V(r) + P_lo(r) V(r) reads P from
-//     there (V an MN-major shared-memory operand). The order is P V_A(r),
-//     S_A(r+1) once that product has completed, P V_B(r), S_B(r+1): while one
-//     half's softmax runs, the tensor cores work on the other half. The warp
-//     zeroes V rows past the last key before the first product reads them;
-//   * eight softmax warps, four per half, own one row each per thread (its
-//     TMEM lane). Per range they read the 128 scores once, 32 at a time,
-//     apply the causal limit, keep the running max and sum (log2 domain) and
-//     write P as bf16 hi + lo pairs over the scores they came from. O
-//     accumulates in tensor memory; O, the row sum and the probabilities
-//     already written are rescaled (by the whole warp, each row by its own
-//     factor) only when a row's running maximum grows by more than 2^8; no
-//     product is in flight then. The softmax warps of TMEM lanes 0-31 share
-//     a scheduler with the MMA warp, whose issue rate the tensor cores depend
-//     on, so their arithmetic is kept lean (paired fp32 instructions).
+//     in place with P(r), and O += P(r) V(r) reads P from there (V an
+//     MN-major shared-memory operand). The order is P V_A(r), S_A(r+1) once
+//     that product has completed, P V_B(r), S_B(r+1): while one half's
+//     softmax runs, the tensor cores work on the other half. The warp zeroes
+//     V rows past the last key before the first product reads them;
+//   * sixteen softmax warps, two per TMEM lane quadrant and half: each thread
+//     owns one row (its TMEM lane) and 64 of the 128 keys of every range. The
+//     two warps of a row exchange their maxima through shared memory (an
+//     mbarrier pair), so both take the range's probabilities against the
+//     same running maximum; each keeps its own partial row sum, rescales its
+//     own half of O, and writes its own half of the output. O accumulates in
+//     tensor memory and is rescaled only when a row's maximum grows by more
+//     than 2^8. At the end of a unit the warps load the next unit's Q (its
+//     record is already published) before they write the current output, so
+//     the next unit's first product overlaps this unit's epilogue.
 // Half A holds the earlier positions, so it may stop some ranges before half
 // B (its keys end sooner); a half without valid rows does no work at all.
 // One CTA per SM (all 512 TMEM columns, 256 per half). All shared state is in
 // the dynamic segment, whose start must be 1024-byte aligned for the swizzled
-// tiles (checked). Waits on mbarriers are bounded (a thread waits out at most
-// one timeout, then runs to the unit barrier); in-flight loads and products
-// are waited for (bounded) and tensor memory is released on every exit path.
+// tiles (checked). On a timeout the warp records it, stops, and the kernel
+// waits (bounded) for its loads and products in flight before it releases
+// tensor memory.
 #include <type_traits>
 
 #include "attention_internal.cuh"
@@ -53,9 +58,11 @@ namespace pa {
 constexpr int kHalfRows = 128;  // UMMA M: rows per half
 constexpr int kHalves = kPrefillTileRows / kHalfRows;
 static_assert(kHalves == 2, "the pipeline interleaves exactly two halves");
-constexpr int kKeyTile = 128;  // keys per range (UMMA N of S, K of P V)
-constexpr int kMaxSlots = 8;   // K/V ring slots (as many as shared memory holds)
-constexpr int kSoftmaxWarps = 4 * kHalves, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
+constexpr int kParts = 2;        // softmax warps per TMEM lane quadrant and half (64 keys of a range each)
+constexpr int kKeyTile = 128;    // keys per range (UMMA N of S, K of P V)
+constexpr int kMaxSlots = 8;     // K/V ring slots (as many as shared memory holds)
+constexpr int kUnitSlots = 2;    // published unit records
+constexpr int kSoftmaxWarps = 4 * kHalves * kParts, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
 constexpr int kTileThreads = 32 * (kTmaWarp + 1);
 // 8-bit caches: two more warps widen each staged range to fp16 in place.
 constexpr int kConvWarp = kTmaWarp + 1, kConvWarps = 2;
@@ -66,8 +73,12 @@ constexpr uint32_t kTmemCols = 512;
 
 // Tensor memory columns of half A: the score buffer SP [0, 128) and O
 // [128, 128 + D); half B's are the same plus HALF. SP holds S (fp32, column
-// = key) and then P: the 16 keys of UMMA K step k occupy columns [16k, 16k+16)
-// of either, as 8 columns of P_hi pairs followed by 8 of P_lo pairs.
+// = key) and then P. With P as a bf16 hi + lo pair, the 16 keys of UMMA K
+// step k occupy columns [16k, 16k + 16) (8 columns of hi pairs, then 8 of lo
+// pairs); with one 16-bit P per key, K step k occupies 8 columns at 8k for
+// k < 4 and at 8k + 32 for k >= 4, so that each softmax warp's probabilities
+// stay inside the 64 score columns it reads (the other warp of its row may
+// still be reading its own).
 template <int D>
 struct TcTmem {
   static constexpr uint32_t SP = 0, O = kKeyTile;
@@ -84,20 +95,28 @@ struct TcLayout {
   static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;             // one K or V range: a ring slot
-  static constexpr int TABLE_ENTRIES = 512;  // staged TMA row coordinates: boxes of keys < 8192 (4096 at bs 8)
-  // barriers: full[kMaxSlots], empty[kMaxSlots], per half s_full, p_full, o_done,
-  // then q_full and drain (the MMA thread's last commit), then raw[kMaxSlots]
-  // (8-bit caches: the staged codes of a slot have landed)
-  static constexpr int NBARS = 3 * kMaxSlots + 3 * kHalves + 2;
-  static constexpr int FIXED = kHalves * Q_BYTES + TABLE_ENTRIES * 4 + 8 * NBARS + 16;
+  // mbarriers (8 bytes each): per ring slot full, empty, raw (8-bit codes
+  // landed) and conv (both converter warps hold a slot's codes); per half s
+  // (S complete), p (P written), o (P V complete), qf (Q stored), qe (the MMA
+  // warp has seen qf); per unit slot uf (record published), ue (record read);
+  // per (half, lane quadrant) the softmax pair's exchange; drain
+  static constexpr int B_FULL = 0, B_EMPTY = kMaxSlots, B_RAW = 2 * kMaxSlots, B_CONV = 3 * kMaxSlots;
+  static constexpr int B_S = 4 * kMaxSlots, B_P = B_S + kHalves, B_O = B_P + kHalves, B_QF = B_O + kHalves;
+  static constexpr int B_QE = B_QF + kHalves, B_UF = B_QE + kHalves, B_UE = B_UF + kUnitSlots;
+  static constexpr int B_X = B_UE + kUnitSlots, B_DRAIN = B_X + 4 * kHalves, NBARS = B_DRAIN + 1;
+  static constexpr int XCH_BYTES = kHalves * kParts * kHalfRows * 4;  // one float per (half, part, row)
+  static constexpr int UNIT_BYTES = kUnitSlots * 32;                  // records of eight ints
+  static constexpr int FIXED = kHalves * Q_BYTES + XCH_BYTES + UNIT_BYTES + 8 * NBARS + 16;
   static constexpr int FIT = (227 * 1024 - FIXED) / KV_BYTES;
   static constexpr int SLOTS = FIT < kMaxSlots ? FIT : kMaxSlots;
   static_assert(SLOTS >= 4, "the ring holds at least K and V of two ranges");
   static constexpr int Q_OFF = 0;                                // Q of halves A and B
   static constexpr int RING_OFF = Q_OFF + kHalves * Q_BYTES;     // K(0), V(0), K(1), V(1), ... in SLOTS slots
-  static constexpr int TABLE_OFF = RING_OFF + SLOTS * KV_BYTES;  // the unit's box coordinates
-  static constexpr int BAR_OFF = TABLE_OFF + TABLE_ENTRIES * 4;
-  static constexpr int BYTES = BAR_OFF + 8 * NBARS + 16;
+  static constexpr int XCH_OFF = RING_OFF + SLOTS * KV_BYTES;    // the softmax pairs' exchange
+  static constexpr int UNIT_OFF = XCH_OFF + XCH_BYTES;           // unit records
+  static constexpr int BAR_OFF = UNIT_OFF + UNIT_BYTES;
+  static constexpr int TMEM_OFF = BAR_OFF + 8 * NBARS;
+  static constexpr int BYTES = TMEM_OFF + 16;
   // Shared memory requested per CTA: more than half an SM's, so that a second
   // CTA (which would wait for TMEM) never lands on the same SM.
   static constexpr int REQUEST = BYTES > 116 * 1024 ? BYTES : 116 * 1024;
@@ -107,11 +126,14 @@ struct TcLayout {
   }
 };
 static_assert(TcLayout<128>::BYTES <= 227 * 1024, "shared memory of one CTA");
+static_assert(TcLayout<128>::SLOTS >= 5, "loads run two ranges ahead at head_dim 128");
 
-// Bounded wait that is skipped once this thread has given up: a thread waits
-// out at most one timeout, then runs to the next unit barrier.
-__device__ __forceinline__ void wait_or_fail(uint32_t bar, uint32_t parity, bool &failed) {
+// Bounded wait by a whole warp; the outcome is made warp-uniform, so a warp
+// that gives up leaves its loops together (no lane is left inside a
+// warp-collective instruction). A warp waits out at most one timeout.
+__device__ __forceinline__ void wait_warp(uint32_t bar, uint32_t parity, bool &failed) {
   if (!failed) failed = !mbar_wait_bounded(bar, parity, kTcWaitTimeoutNs);
+  failed = __any_sync(0xffffffffu, failed);
 }
 
 // The two 32-bit words of a 128-byte-swizzle shared-memory descriptor (the
@@ -269,53 +291,91 @@ __device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int li
   sum += acc0 + acc1;
 }
 
-// Multiply the probabilities already stored in a 32-column chunk of P (the
-// layout probs32 writes) by alpha, re-splitting each into hi + lo.
-// The same for a chunk of single pairs (16 columns).
-template <typename E>
-__device__ __forceinline__ void rescale_p16(uint32_t taddr, float alpha) {
-  uint32_t w[16];
-  tmem_ld16_wait(taddr, w);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = E::pack(E::lo(w[i]) * alpha, E::hi(w[i]) * alpha);
-  tmem_st16u(taddr, w);
+// Store 8 32-bit columns (raw bits) of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr), "r"(v[0]),
+      "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
 }
 
-template <typename E>
-__device__ __forceinline__ void rescale_p32(uint32_t taddr, float alpha) {
-  uint32_t w[32];
-  tmem_ld32_wait(taddr, w);
+// P for the 16 keys of one UMMA K step (scores s[0..16), key k0 + i visible
+// while k0 + i < lim), summed into *sum and stored at TMEM column `col` of
+// this thread's lane: SPLIT as 8 hi pairs then 8 lo pairs (16 columns),
+// otherwise 8 pairs. Same arithmetic as probs32.
+template <typename E, bool EXACT, bool SPLIT>
+__device__ __forceinline__ void probs16_store(const uint32_t *s, int k0, int lim, float sl2, float ms, float &sum,
+                                              uint32_t col) {
+  const bool full = k0 + 16 <= lim;
+  float acc0 = 0.f, acc1 = 0.f;
+  uint32_t hv[8], lv[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int hk = 16 * (i >> 3) + (i & 7);
-    const float p0 = (E::lo(w[hk]) + E::lo(w[hk + 8])) * alpha;
-    const float p1 = (E::hi(w[hk]) + E::hi(w[hk + 8])) * alpha;
-    const uint32_t hi = E::pack(p0, p1);
-    w[hk] = hi;
-    w[hk + 8] = E::pack(p0 - E::lo(hi), p1 - E::hi(hi));
+  for (int i = 0; i < 8; ++i) {
+    float x0 = __uint_as_float(s[2 * i]), x1 = __uint_as_float(s[2 * i + 1]);
+    if (!full) {
+      x0 = k0 + 2 * i < lim ? x0 : -INFINITY;
+      x1 = k0 + 2 * i + 1 < lim ? x1 : -INFINITY;
+    }
+    float e0, e1;
+    if (EXACT) {
+      e0 = __fsub_rn(__fmul_rn(x0, sl2), ms);
+      e1 = __fsub_rn(__fmul_rn(x1, sl2), ms);
+    } else {
+      fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
+    }
+    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+    add2(acc0, acc1, acc0, acc1, p0, p1);
+    hv[i] = E::pack(p0, p1);
+    if (SPLIT) {
+      float l0, l1;
+      sub2(l0, l1, p0, p1, E::lo(hv[i]), E::hi(hv[i]));
+      lv[i] = E::pack(l0, l1);
+    }
   }
-  tmem_st32u(taddr, w);
+  sum += acc0 + acc1;
+  tmem_st8u(col, hv);
+  if (SPLIT) tmem_st8u(col + 8, lv);
 }
+
+// Two 32-column loads of this thread's TMEM lane, then one wait.
+__device__ __forceinline__ void tmem_ld32x2_wait(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(taddr + 32)
+      : "memory");
+}
+
+// A published unit: a tile of one request and one KV head, or the end of the stream.
+struct TileUnit {
+  int b, row0, npos, pos0, kv_end, kvh, stop;
+};
 
 // 8-bit caches (KV8): the producer stages a range's codes in the back half of
 // its ring slot (kKeyTile x D bytes, the TMA boxes' own 128- or 64-byte
-// swizzle); two converter warps load them, meet at a named barrier (the
-// fp16 rows they then write overlap the codes), widen them exactly to fp16
-// in the layout the 16-bit path's TMA writes, and arrive on the slot's full
-// barrier. The tensor cores then take fp16 operands whatever q is: a bf16 Q
-// row is stored as fp16, scaled first by a power of two when its largest |q|
-// reaches 2^15, and its thread's softmax factor is scaled back.
+// swizzle); two converter warps load them, meet at the slot's conv barrier
+// (the fp16 rows they then write overlap the codes), widen them exactly to
+// fp16 in the layout the 16-bit path's TMA writes, and arrive on the slot's
+// full barrier. The tensor cores then take fp16 operands whatever q is: a
+// bf16 Q row is stored as fp16, scaled first by a power of two when its
+// largest |q| reaches 2^15, and its row's softmax factor is scaled back.
 template <int D, int G, typename E, bool KV8>
-// Ten warps (twelve with 8-bit caches): three share each of two (all four) of
-// the SM's register-file partitions, so a thread gets at most 168 registers.
+// Eighteen warps (twenty with 8-bit caches), one CTA per SM.
 __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const TileParams p) {
+                        const __grid_constant__ CUtensorMap vmapb, const TileParams p) {
   using Lay = TcLayout<D>;
   using Tm = TcTmem<D>;
   using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
   constexpr bool SPLIT = std::is_same<M, ElemBf16>::value;      // P as a hi + lo pair (bf16 operands only)
-  constexpr int PCOLS = SPLIT ? 32 : 16;                        // TMEM columns of P per 32 keys
+  // V staged one cache block per box, both atoms (4-D map): 16-bit caches at head_dim 128
+  constexpr bool VBLK = D == 128 && !KV8;
   constexpr int NTHREADS = KV8 ? kTileThreads8 : kTileThreads;
   constexpr int RAW_ROW = D <= 64 ? 64 : 128;      // bytes per staged row of codes (padded past head_dim)
   constexpr int RAW_BYTES = kKeyTile * RAW_ROW;    // 8-bit codes of one range
@@ -323,14 +383,17 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   static_assert(RAW_BYTES == Lay::KV_BYTES / 2, "a range's codes fill half of its 16-bit slot");
   constexpr int KSTEPS_S = D / 16;         // UMMA K steps of S = Q K^T
   constexpr int KSTEPS_O = kKeyTile / 16;  // UMMA K steps of O = P V
-  constexpr int TILES = kKeyTile / kTileKeys;  // 16-key tiles per range
   constexpr int POS_PER_HALF = kHalfRows / G;
+  constexpr int PART_KEYS = kKeyTile / kParts;  // keys of a range per softmax warp
+  constexpr int NCH = (D + 31) / 32;            // 32-column chunks of O (head_dim 80: 16 padding columns)
   constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, M::kUmmaFormat);
   constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, M::kUmmaFormat);
   // O stays in TMEM and is rescaled only when a row's running maximum grows
   // by more than 2^8 (log2 domain); in between, probabilities are taken
   // against the older maximum and stay below 256.
   constexpr float kRescaleLog2 = 8.f;
+  constexpr unsigned FULL = 0xffffffffu;
+  (void)NTHREADS;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -341,34 +404,39 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   }
   constexpr int SLOTS = Lay::SLOTS;
   const uint32_t sQ0 = base + Lay::Q_OFF, sRing = base + Lay::RING_OFF;
-  const uint32_t bars = base + Lay::BAR_OFF;
-  const uint32_t bar_full = bars, bar_empty = bars + 8 * kMaxSlots;  // per ring slot: barrier + 8 * slot
-  // per half h: barrier + 8 * h
-  const uint32_t bar_s = bars + 16 * kMaxSlots, bar_p = bar_s + 8 * kHalves, bar_o = bar_p + 8 * kHalves;
-  const uint32_t bar_q = bar_o + 8 * kHalves, bar_drain = bar_q + 8;
-  const uint32_t bar_raw = bar_drain + 8;  // per ring slot: barrier + 8 * slot
-  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS);
-  int *unit_s = reinterpret_cast<int *>(smem_raw + Lay::BAR_OFF + 8 * Lay::NBARS + 4);
-  int *zbox = reinterpret_cast<int *>(smem_raw + Lay::TABLE_OFF);
+  auto bar = [&](int i) { return base + Lay::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::TMEM_OFF);
+  volatile int *units = reinterpret_cast<volatile int *>(smem_raw + Lay::UNIT_OFF);
+  volatile float *xch = reinterpret_cast<volatile float *>(smem_raw + Lay::XCH_OFF);
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    // full: the producer's TMA (16-bit caches) or one arrival per converter warp (8-bit); empty: MMA commits
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_full + 8 * i, KV8 ? kConvWarps : 1);
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_empty + 8 * i, 1);
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(bar_raw + 8 * i, 1);
-    for (int h = 0; h < kHalves; ++h) {
-      mbar_init(bar_s + 8 * h, 1);
-      mbar_init(bar_p + 8 * h, 4);  // the half's four softmax warps
-      mbar_init(bar_o + 8 * h, 1);
+    for (int i = 0; i < kMaxSlots; ++i) {
+      // full: the producer's TMA (16-bit caches) or one arrival per converter warp (8-bit)
+      mbar_init(bar(Lay::B_FULL + i), KV8 ? kConvWarps : 1);
+      mbar_init(bar(Lay::B_EMPTY + i), 1);  // the MMA warp's commit after the range's last product
+      mbar_init(bar(Lay::B_RAW + i), 1);
+      mbar_init(bar(Lay::B_CONV + i), 32 * kConvWarps);
     }
-    mbar_init(bar_q, kSoftmaxWarps);
-    mbar_init(bar_drain, 1);
+    for (int h = 0; h < kHalves; ++h) {
+      mbar_init(bar(Lay::B_S + h), 1);
+      mbar_init(bar(Lay::B_P + h), 4 * kParts);  // the half's softmax warps
+      mbar_init(bar(Lay::B_O + h), 1);
+      mbar_init(bar(Lay::B_QF + h), 4 * kParts);
+      mbar_init(bar(Lay::B_QE + h), 1);
+    }
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(bar(Lay::B_UF + i), 1);
+      mbar_init(bar(Lay::B_UE + i), 1 + kSoftmaxWarps + (KV8 ? kConvWarps : 0));
+    }
+    for (int i = 0; i < 4 * kHalves; ++i) mbar_init(bar(Lay::B_X + i), 32 * kParts);
+    mbar_init(bar(Lay::B_DRAIN), 1);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
+    if (VBLK) prefetch_tmap(&vmapb);
   }
   fence_mbar_init();
   tc_fence_before();
@@ -378,199 +446,253 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   griddep_wait();
 
   const int Hkv = p.num_kv_heads;
-  const int total_units = min(max(ld_cg(p.tile_count), 0), p.max_tiles) * Hkv;
-  // Phase bookkeeping (it runs on across units, like the barriers). Each
-  // half's s_full, p_full and o_done complete once per range of that half,
-  // so range r of a unit is phase ph[h] + r. The ring carries K(0), V(0),
-  // K(1), V(1), ... of every unit in turn: load number g = ring0 + 2 r (+1
-  // for V) sits in slot g % SLOTS as that slot's use g / SLOTS.
-  uint32_t ph[kHalves] = {0, 0};
-  uint32_t ring0 = 0;
-  uint32_t issued = 0;  // producer: loads actually issued
-  uint32_t n_q = 0;
+  const int bs = p.block_size;
   bool failed = false;
+  uint32_t issued = 0;  // producer: loads issued (the final drain waits for them)
 
-  for (;;) {
-    if (tid == 0) *unit_s = atomicAdd(p.tile_counter, 1);
-    if (__syncthreads_or(failed)) break;  // unit barrier: every role is done with the last unit
-    const int u = *unit_s;
-    if (u >= total_units) break;
-    const int item = u / Hkv, kvh = u - item * Hkv;
-    (void)RAW_OFF;
-    const int4 r0 = ld_cg(p.tiles + 2 * item);
-    const int4 r1 = ld_cg(p.tiles + 2 * item + 1);
-    const int b = r0.x, row0 = r0.y, npos = r0.z, pos0 = r0.w, kv_end = r1.y;
-    const bool sane = b >= 0 && b < p.num_seqs && npos >= 1 && npos <= kPrefillTileRows / G && row0 >= 0 &&
-                      row0 + npos <= p.total_q && pos0 >= 0 && kv_end == pos0 + npos &&
-                      kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
-    if (!sane) {
-      if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
-      __syncthreads();  // unit_s is rewritten next iteration
-      continue;
+  // Record j of the stream sits in slot j % kUnitSlots; every consumer warp
+  // reads each record once and releases the slot.
+  auto read_unit = [&](uint32_t j, TileUnit &r) {
+    const uint32_t s = j % kUnitSlots;
+    wait_warp(bar(Lay::B_UF + s), (j / kUnitSlots) & 1u, failed);
+    r.stop = 1;
+    if (!failed) {
+      const volatile int *u = units + 8 * s;
+      r.b = u[0];
+      r.row0 = u[1];
+      r.npos = u[2];
+      r.pos0 = u[3];
+      r.kv_end = u[4];
+      r.kvh = u[5];
+      r.stop = u[6];
     }
-    const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    const int bs = p.block_size;
-    // A TMA box is box_rows consecutive keys of one block (16, or 8 with
-    // 8-token blocks). The cache row of box i's first key, k = i * box_rows,
-    // is table[k / bs] * bs + k % bs (powers of two: shift and mask); boxes
-    // past the keys, or of a block id out of range, are read at -box_rows
-    // (zero fill). All threads compute the unit's coordinates once here, so
-    // the producer only reads one from shared memory per box.
-    constexpr int MAXROWS = KV8 ? kRawBoxRows : kTileKeys;
-    const int box_rows = bs < MAXROWS ? bs : MAXROWS;
-    const int nboxes = (kv_end + box_rows - 1) / box_rows;
-    auto box_z = [&](int i) {
-      const int key = i * box_rows;
-      if (key >= kv_end) return -box_rows;
-      const int phys = __ldg(table + (key >> p.block_shift));
-      if (phys < 0 || phys >= p.num_blocks) {
-        flag_error(p.status, PA_FLAG_BLOCK_RANGE);
-        return -box_rows;
-      }
-      return (phys << p.block_shift) + (key & (bs - 1));
-    };
-    const int nkt = (kv_end + kKeyTile - 1) / kKeyTile;
-    // key ranges each half needs: up to its last valid position (0 = no valid rows)
-    int nkt_h[kHalves];
+    __syncwarp();
+    if (lane == 0 && !failed) mbar_arrive(bar(Lay::B_UE + s));
+  };
+  // key ranges of the unit, and of each half: up to its last valid position (0 = no valid rows)
+  auto ranges = [&](const TileUnit &r, int (&nh)[kHalves]) {
 #pragma unroll
     for (int h = 0; h < kHalves; ++h) {
-      const int last = min(npos, (h + 1) * POS_PER_HALF);  // positions [h * POS_PER_HALF, last)
-      nkt_h[h] = last > h * POS_PER_HALF ? (pos0 + last + kKeyTile - 1) / kKeyTile : 0;
+      const int last = min(r.npos, (h + 1) * POS_PER_HALF);  // positions [h * POS_PER_HALF, last)
+      nh[h] = last > h * POS_PER_HALF ? (r.pos0 + last + kKeyTile - 1) / kKeyTile : 0;
     }
-    for (int i = tid; i < min(nboxes, Lay::TABLE_ENTRIES); i += NTHREADS) zbox[i] = box_z(i);
-    __syncthreads();
+    return (r.kv_end + kKeyTile - 1) / kKeyTile;
+  };
+  // V in shared memory. VBLK: block after block of R = block_size rows, each
+  // [atom][R rows][128 B]; else [atom][128 keys][128 B] (per-atom boxes).
+  const int vshift = p.block_shift;  // log2(R)
+  auto v_off = [&](int rr, int c) -> uint32_t {  // 16-byte chunk c of key row rr of a range
+    if constexpr (VBLK) {
+      const int blk = rr >> vshift, r = rr & (bs - 1);
+      return static_cast<uint32_t>(blk * bs * 256 + (c >> 3) * bs * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    } else {
+      return Lay::off(rr, c, Lay::KV_ATOM);
+    }
+  };
 
-    if (warp == kTmaWarp) {
-      // ---------------- producer: K(j+1) ahead of V(j) ----------------
-      if (lane == 0) {
-        auto load = [&](int kt, bool is_v) {
-          const uint32_t g = ring0 + 2 * kt + (is_v ? 1 : 0);
-          const uint32_t slot = g % SLOTS, use = g / SLOTS;
-          if (use > 0) wait_or_fail(bar_empty + 8 * slot, (use - 1) & 1u, failed);
-          if (failed) return;
-          issued = g + 1;
-          const void *map = is_v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
-          if constexpr (KV8) {
-            // the range's codes: kKeyTile / box_rows boxes of box_rows x D bytes
-            const uint32_t bar = bar_raw + 8 * slot;
-            const uint32_t dst = sRing + slot * Lay::KV_BYTES + RAW_OFF;
-            mbar_arrive_expect_tx(bar, RAW_BYTES);
-            const int nb = kKeyTile / box_rows;
-            for (int j = 0; j < nb; ++j) {
-              const int i = kt * nb + j;
-              const int z = i < nboxes ? (i < Lay::TABLE_ENTRIES ? zbox[i] : box_z(i)) : -box_rows;
-              tma_load_3d(dst + j * box_rows * RAW_ROW, map, bar, 0, kvh, z);
-            }
-            return;
-          }
-          const uint32_t bar = bar_full + 8 * slot;
-          const uint32_t dst = sRing + slot * Lay::KV_BYTES;
-          mbar_arrive_expect_tx(bar, Lay::KV_BYTES);
-          // a 16-key tile is one 16-row box (16- or 32-token blocks) or two
-          // 8-row boxes of consecutive 8-token blocks
-          auto boxes = [&](auto nbox_c) {
-            constexpr int NBOX = decltype(nbox_c)::value, ROWS = kTileKeys / NBOX;
-#pragma unroll
-            for (int tile = 0; tile < TILES; ++tile) {
-#pragma unroll
-              for (int j = 0; j < NBOX; ++j) {
-                const int i = (kt * TILES + tile) * NBOX + j;
-                const int z = i < nboxes ? (i < Lay::TABLE_ENTRIES ? zbox[i] : box_z(i)) : -ROWS;
-#pragma unroll
-                for (int a = 0; a < Lay::ATOMS; ++a)
-                  tma_load_3d(dst + a * Lay::KV_ATOM + tile * 2048 + j * ROWS * 128, map, bar, a * 64, kvh, z);
-              }
-            }
-          };
-          if constexpr (!KV8) {
-            if (bs < kTileKeys)
-              boxes(std::integral_constant<int, 2>());
-            else
-              boxes(std::integral_constant<int, 1>());
-          }
-        };
-        // the order the products consume them: S(j) needs K(j) before P V(j) needs V(j)
-        for (int j = 0; j < nkt; ++j) {
-          load(j, false);
-          load(j, true);
+  if (warp == kTmaWarp) {
+    // ---------------- producer: unit records, then K(j), V(j) of each range ----------------
+    const int total_units = min(max(ld_cg(p.tile_count), 0), p.max_tiles) * Hkv;
+    constexpr int MAXROWS = KV8 ? kRawBoxRows : kTileKeys;
+    const int box_rows = bs < MAXROWS ? bs : MAXROWS;  // K boxes (and V boxes unless VBLK)
+    const int nbk = kKeyTile / box_rows;                // 4 .. 16
+    const int nbv = VBLK ? kKeyTile / bs : nbk;         // VBLK: one box per block
+    uint32_t j = 0, g = 0;
+    for (;;) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.tile_counter, 1);
+      u = __shfl_sync(FULL, u, 0);
+      TileUnit r{0, 0, 0, 0, 0, 0, u >= total_units ? 1 : 0};
+      if (!r.stop) {
+        const int item = u / Hkv;
+        r.kvh = u - item * Hkv;
+        const int4 r0 = ld_cg(p.tiles + 2 * item);
+        const int4 r1 = ld_cg(p.tiles + 2 * item + 1);
+        r.b = r0.x;
+        r.row0 = r0.y;
+        r.npos = r0.z;
+        r.pos0 = r0.w;
+        r.kv_end = r1.y;
+        const bool sane = r.b >= 0 && r.b < p.num_seqs && r.npos >= 1 && r.npos <= kPrefillTileRows / G &&
+                          r.row0 >= 0 && r.row0 + r.npos <= p.total_q && r.pos0 >= 0 &&
+                          r.kv_end == r.pos0 + r.npos &&
+                          r.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * bs;
+        if (!sane) {
+          if (lane == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+          continue;
         }
       }
-    } else if (warp >= kConvWarp) {
-      // ---------------- 8-bit caches: widen staged codes to fp16 in place ----------------
-      if constexpr (KV8) {
-        // Lane l of converter warp w takes 16-byte code chunk c of rows
-        // r0 + l % 8, so the eight lanes of one shared-memory phase touch eight
-        // rows at one chunk: distinct bank groups in both swizzled layouts.
-        constexpr int CPR = RAW_ROW / 16;      // code chunks per staged row (zeros past head_dim)
-        constexpr int ROWS_PASS = 8 * (8 / CPR);  // rows per pass of the 64 threads
-        constexpr int PASSES = kKeyTile / ROWS_PASS;
-        const int ct = (warp - kConvWarp) * 32 + lane;
-        const int q8 = ct >> 3, c = q8 % CPR, rsub = (q8 / CPR) * 8 + (ct & 7);
-        for (int j = 0; j < 2 * nkt; ++j) {
-          const uint32_t g = ring0 + j;
+      const uint32_t s = j % kUnitSlots;
+      if (j >= kUnitSlots) wait_warp(bar(Lay::B_UE + s), (j / kUnitSlots - 1) & 1u, failed);
+      if (failed) break;
+      if (lane == 0) {
+        volatile int *d = units + 8 * s;
+        d[0] = r.b;
+        d[1] = r.row0;
+        d[2] = r.npos;
+        d[3] = r.pos0;
+        d[4] = r.kv_end;
+        d[5] = r.kvh;
+        d[6] = r.stop;
+        mbar_arrive(bar(Lay::B_UF + s));  // release: the record is visible to whoever sees the phase
+      }
+      __syncwarp();
+      ++j;
+      if (r.stop) break;
+      const int32_t *table = p.block_tables + static_cast<int64_t>(r.b) * p.max_blocks_per_seq;
+      // First cache row of the box of `rows` keys starting at `key`: a block-table
+      // lookup (block sizes are powers of two); keys past the end, or a block id
+      // out of range, read at -rows (zero fill).
+      auto box_z = [&](int key, int rows) {
+        if (key >= r.kv_end) return -rows;
+        const int phys = __ldg(table + (key >> p.block_shift));
+        if (phys < 0 || phys >= p.num_blocks) {
+          flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+          return -rows;
+        }
+        return (phys << p.block_shift) + (key & (bs - 1));
+      };
+      int dummy[kHalves];
+      const int nkt = ranges(r, dummy);
+      for (int kt = 0; kt < nkt && !failed; ++kt) {
+        // lane i computes the row coordinate of K box i and V box i of this
+        // range, and issues those boxes itself once lane 0 has set the byte count
+        const int zk = lane < nbk ? box_z(kt * kKeyTile + lane * box_rows, box_rows) : 0;
+        const int zv = VBLK ? (lane < nbv ? box_z(kt * kKeyTile + lane * bs, bs) : 0) : zk;
+        for (int v = 0; v < 2 && !failed; ++v) {
           const uint32_t slot = g % SLOTS, use = g / SLOTS;
-          wait_or_fail(bar_raw + 8 * slot, use & 1u, failed);
-          const uint32_t sbase = sRing + slot * Lay::KV_BYTES;
-          uint4 codes[PASSES];
-          if (!failed) {
+          if (use > 0) wait_warp(bar(Lay::B_EMPTY + slot), (use - 1) & 1u, failed);
+          if (failed) break;
+          const void *map = v ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+          const uint32_t dst = sRing + slot * Lay::KV_BYTES;
+          if constexpr (KV8) {
+            // the range's codes: boxes of box_rows x D bytes into the back half of the slot
+            const uint32_t b8 = bar(Lay::B_RAW + slot);
+            if (lane == 0) mbar_arrive_expect_tx(b8, RAW_BYTES);
+            __syncwarp();
+            if (lane < nbk) tma_load_3d(dst + RAW_OFF + lane * box_rows * RAW_ROW, map, b8, 0, r.kvh, zk);
+          } else {
+            const uint32_t bf = bar(Lay::B_FULL + slot);
+            if (lane == 0) mbar_arrive_expect_tx(bf, Lay::KV_BYTES);
+            __syncwarp();
+            if (VBLK && v) {
+              // one box per block: both atoms of bs rows, [atom][rows][128 B]
+              if (lane < nbv) tma_load_4d(dst + lane * bs * 256, &vmapb, bf, 0, zv, 0, r.kvh);
+            } else if (lane < nbk) {
+              // per-atom boxes of box_rows rows: [atom][128 keys][128 B]
 #pragma unroll
-            for (int i = 0; i < PASSES; ++i) {
-              const int r = i * ROWS_PASS + rsub;
-              const uint32_t a = sbase + RAW_OFF + (RAW_ROW == 128 ? r * 128 + (((c ^ r) & 7) << 4)
-                                                                     : r * 64 + (((c ^ (r >> 1)) & 3) << 4));
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-                           : "=r"(codes[i].x), "=r"(codes[i].y), "=r"(codes[i].z), "=r"(codes[i].w)
-                           : "r"(a));
+              for (int a = 0; a < Lay::ATOMS; ++a)
+                tma_load_3d(dst + a * Lay::KV_ATOM + lane * box_rows * 128, map, bf, a * 64, r.kvh, v ? zv : zk);
             }
-          }
-          // every code of the slot is in registers before any fp16 row overwrites them
-          asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kConvWarps) : "memory");
-          if (!failed) {
-#pragma unroll
-            for (int i = 0; i < PASSES; ++i) {
-              const int r = i * ROWS_PASS + rsub;
-              const uint32_t w[4] = {codes[i].x, codes[i].y, codes[i].z, codes[i].w};
-              uint32_t h[8];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
-                    " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
-                    : "=r"(h[2 * k]), "=r"(h[2 * k + 1])
-                    : "r"(w[k]));
-              }
-              // codes d = 16c .. 16c + 15 -> fp16 chunks 2c (d .. d + 7) and 2c + 1
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sbase + Lay::off(r, 2 * c, Lay::KV_ATOM)),
-                           "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                           : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                               sbase + Lay::off(r, 2 * c + 1, Lay::KV_ATOM)),
-                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                           : "memory");
-            }
-            fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
           }
           __syncwarp();
-          if (lane == 0 && !failed) mbar_arrive(bar_full + 8 * slot);
+          issued = ++g;
         }
       }
-    } else if (warp == kMmaWarp) {
-      // ---------------- MMA issue ----------------
-      // The whole warp follows the loop (it zeroes the tail of the last V
-      // range); lane 0 alone issues tensor-core work and commits. Range r is
-      // read by the halves with r < nkt_h: the first of them waits for the
-      // K/V loads, the last one's commit releases the buffers.
+      if (failed) break;
+    }
+  } else if (warp >= kConvWarp) {
+    // ---------------- 8-bit caches: widen staged codes to fp16 in place ----------------
+    if constexpr (KV8) {
+      // Lane l of converter warp w takes 16-byte code chunk c of rows
+      // r0 + l % 8, so the eight lanes of one shared-memory phase touch eight
+      // rows at one chunk: distinct bank groups in both swizzled layouts.
+      constexpr int CPR = RAW_ROW / 16;         // code chunks per staged row (zeros past head_dim)
+      constexpr int ROWS_PASS = 8 * (8 / CPR);  // rows per pass of the 64 threads
+      constexpr int PASSES = kKeyTile / ROWS_PASS;
+      const int ct = (warp - kConvWarp) * 32 + lane;
+      const int q8 = ct >> 3, c = q8 % CPR, rsub = (q8 / CPR) * 8 + (ct & 7);
+      uint32_t j = 0, g = 0;
+      for (;;) {
+        TileUnit r;
+        read_unit(j++, r);
+        if (failed || r.stop) break;
+        int dummy[kHalves];
+        const int nkt = ranges(r, dummy);
+        for (int i = 0; i < 2 * nkt && !failed; ++i, ++g) {
+          const uint32_t slot = g % SLOTS, use = g / SLOTS;
+          wait_warp(bar(Lay::B_RAW + slot), use & 1u, failed);
+          if (failed) break;
+          const uint32_t sbase = sRing + slot * Lay::KV_BYTES;
+          uint4 codes[PASSES];
+#pragma unroll
+          for (int i2 = 0; i2 < PASSES; ++i2) {
+            const int rr = i2 * ROWS_PASS + rsub;
+            const uint32_t a = sbase + RAW_OFF + (RAW_ROW == 128 ? rr * 128 + (((c ^ rr) & 7) << 4)
+                                                                  : rr * 64 + (((c ^ (rr >> 1)) & 3) << 4));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                         : "=r"(codes[i2].x), "=r"(codes[i2].y), "=r"(codes[i2].z), "=r"(codes[i2].w)
+                         : "r"(a));
+          }
+          // every code of the slot is in registers (both warps) before any fp16 row overwrites them
+          mbar_arrive(bar(Lay::B_CONV + slot));
+          wait_warp(bar(Lay::B_CONV + slot), use & 1u, failed);
+          if (failed) break;
+#pragma unroll
+          for (int i2 = 0; i2 < PASSES; ++i2) {
+            const int rr = i2 * ROWS_PASS + rsub;
+            const uint32_t w[4] = {codes[i2].x, codes[i2].y, codes[i2].z, codes[i2].w};
+            uint32_t hh[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+                  " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
+                  : "=r"(hh[2 * k]), "=r"(hh[2 * k + 1])
+                  : "r"(w[k]));
+            }
+            // codes d = 16c .. 16c + 15 -> fp16 chunks 2c (d .. d + 7) and 2c + 1
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sbase + Lay::off(rr, 2 * c, Lay::KV_ATOM)),
+                         "r"(hh[0]), "r"(hh[1]), "r"(hh[2]), "r"(hh[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                             sbase + Lay::off(rr, 2 * c + 1, Lay::KV_ATOM)),
+                         "r"(hh[4]), "r"(hh[5]), "r"(hh[6]), "r"(hh[7])
+                         : "memory");
+          }
+          fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Lay::B_FULL + slot));
+        }
+        if (failed) break;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue ----------------
+    // The whole warp follows the loops (it zeroes the tail of the last V
+    // range); lane 0 alone issues tensor-core work and commits. Range r of a
+    // unit is read by the halves with r < nkt_h: the first of them waits for
+    // the K/V loads, the last one's commit releases the buffers.
+    constexpr uint32_t DHI = desc_hi(1024);
+    const uint32_t q_lo0 = desc_lo(sQ0, 16), q_lo1 = desc_lo(sQ0 + Lay::Q_BYTES, 16);
+    const uint32_t k_lo = desc_lo(sRing, 16);  // slot 0
+    // V (MN-major): LBO = distance between the two 64-element atoms along d,
+    // SBO = distance between 8-key groups along K; VBLK blocks of 8 rows put
+    // consecutive 8-key groups in consecutive blocks
+    const uint32_t v_lo = VBLK ? desc_lo(sRing, static_cast<uint32_t>(bs) * 128u) : desc_lo(sRing, Lay::KV_ATOM);
+    const uint32_t v_hi = VBLK && bs == 8 ? desc_hi(2048) : DHI;
+    constexpr uint32_t SLOT_STEP = Lay::KV_BYTES >> 4;  // per slot
+    uint32_t vks[KSTEPS_O];                              // byte offset >> 4 of V's K step ks
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS_O; ++ks) {
+      const int k16 = ks * 16;
+      vks[ks] = VBLK ? static_cast<uint32_t>(((k16 >> vshift) * bs * 256 + (k16 & (bs - 1)) * 128) >> 4)
+                     : static_cast<uint32_t>((ks * 2048) >> 4);
+    }
+    uint32_t ph[kHalves] = {0, 0};  // ranges each half has run so far (phases of its s, p, o barriers)
+    uint32_t ring0 = 0;             // loads of earlier units
+    for (uint32_t j = 0;; ++j) {
+      TileUnit r;
+      read_unit(j, r);
+      if (failed || r.stop) break;
+      int nkt_h[kHalves];
+      const int nkt = ranges(r, nkt_h);
       auto first_reader = [&](int kt) { return kt < nkt_h[0] ? 0 : 1; };
       auto last_reader = [&](int kt) { return kt < nkt_h[1] ? 1 : 0; };
       // ring slot of K(kt) (v = 0) or V(kt) (v = 1), and the parity of its full barrier
       auto slot_of = [&](int kt, int v) { return (ring0 + 2 * kt + v) % SLOTS; };
       auto full_parity = [&](int kt, int v) { return ((ring0 + 2 * kt + v) / SLOTS) & 1u; };
-      constexpr uint32_t DHI = desc_hi(1024);
-      const uint32_t q_lo0 = desc_lo(sQ0, 16), q_lo1 = desc_lo(sQ0 + Lay::Q_BYTES, 16);
-      const uint32_t k_lo = desc_lo(sRing, 16), v_lo = desc_lo(sRing, Lay::KV_ATOM);  // slot 0
-      constexpr uint32_t SLOT_STEP = Lay::KV_BYTES >> 4;                            // per slot
-      static_assert(kHalves == 2, "descriptor words are kept for two halves");
       auto mma_s = [&](int kt, int h) {
-        if (lane == 0 && !failed) {
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t klo = k_lo + slot_of(kt, 0) * SLOT_STEP, qlo = h ? q_lo1 : q_lo0;
           const uint32_t d = tmem + h * Tm::HALF + Tm::SP;
@@ -581,197 +703,239 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             const uint32_t ko = ((ks >> 2) * Lay::KV_ATOM + (ks & 3) * 32) >> 4;
             mma_ss<1>(d, qlo + qo, DHI, klo + ko, DHI, IDESC_S);
           }
-          tc_commit(bar_s + 8 * h);
-          if (h == last_reader(kt)) tc_commit(bar_empty + 8 * slot_of(kt, 0));
+          tc_commit(bar(Lay::B_S + h));
+          if (h == last_reader(kt)) tc_commit(bar(Lay::B_EMPTY + slot_of(kt, 0)));
         }
         __syncwarp();
       };
-      wait_or_fail(bar_q, n_q & 1u, failed);
-      ++n_q;
-      if (nkt > 0) {
-        wait_or_fail(bar_full + 8 * slot_of(0, 0), full_parity(0, 0), failed);
+      // this unit's Q in both halves (the softmax warps store it); qe lets them store the next one
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          if (nkt_h[h] > 0) mma_s(0, h);
+      for (int h = 0; h < kHalves; ++h) {
+        wait_warp(bar(Lay::B_QF + h), j & 1u, failed);
+        if (lane == 0 && !failed) mbar_arrive(bar(Lay::B_QE + h));
       }
-      for (int kt = 0; kt < nkt; ++kt) {
+      if (failed) break;
+      if (nkt > 0) {
+        wait_warp(bar(Lay::B_FULL + slot_of(0, 0)), full_parity(0, 0), failed);
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h) {
+          if (nkt_h[h] == 0) continue;
+          // the score buffer is free once the half's last product of the previous unit completed
+          if (ph[h] > 0) wait_warp(bar(Lay::B_O + h), (ph[h] - 1) & 1u, failed);
+          if (!failed) mma_s(0, h);
+        }
+      }
+      for (int kt = 0; kt < nkt && !failed; ++kt) {
         const uint32_t vslot = slot_of(kt, 1);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
           if (kt >= nkt_h[h]) continue;
-          wait_or_fail(bar_p + 8 * h, (ph[h] + kt) & 1u, failed);  // P(kt) is in place
+          wait_warp(bar(Lay::B_P + h), (ph[h] + kt) & 1u, failed);  // P(kt) is in place
+          if (failed) break;
           if (h == first_reader(kt)) {
-            wait_or_fail(bar_full + 8 * vslot, full_parity(kt, 1), failed);
+            wait_warp(bar(Lay::B_FULL + vslot), full_parity(kt, 1), failed);
+            if (failed) break;
             const int key0 = kt * kKeyTile;
-            if (!failed && key0 + kKeyTile > kv_end) {
+            if (key0 + kKeyTile > r.kv_end) {
               // rows of keys past kv_end may hold anything (even NaN): zero them in V
               const uint32_t sV = sRing + vslot * Lay::KV_BYTES;
-              const int vr0 = kv_end - key0;
+              const int vr0 = r.kv_end - key0;
               const int n = (kKeyTile - vr0) * (D / 8);
               for (int i = lane; i < n; i += 32) {
                 const int rr = vr0 + i / (D / 8), c = i % (D / 8);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sV + Lay::off(rr, c, Lay::KV_ATOM)),
-                             "r"(0u)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sV + v_off(rr, c)), "r"(0u)
                              : "memory");
               }
               fence_proxy_async_smem();
             }
             __syncwarp();
           }
-          if (lane == 0 && !failed) {
+          if (lane == 0) {
             tc_fence_after();
             const uint32_t vlo = v_lo + vslot * SLOT_STEP;
             const uint32_t t = tmem + h * Tm::HALF;
-            // K step ks reads P at columns PCOLS / 2 * ks (+ 8 for the lo half of a pair)
+            // P of K step ks: SPLIT hi at 16 ks, lo at 16 ks + 8; else 8 ks (+ 32 for the second part's keys)
+            auto pcol = [](int ks) { return SPLIT ? 16 * ks : 8 * ks + (ks >= 4 ? 32 : 0); };
             if (kt == 0)
-              mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);  // the unit's first product overwrites O
+              mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);  // the unit's first product overwrites O
             else
-              mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, DHI, IDESC_O);
-            if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, DHI, IDESC_O);
+              mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);
+            if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, v_hi, IDESC_O);
 #pragma unroll
             for (int ks = 1; ks < KSTEPS_O; ++ks) {
-              const uint32_t vo = (ks * 2048) >> 4;  // 16 keys x 128 B per K step
-              mma_ts<1>(t + Tm::O, t + Tm::SP + (PCOLS / 2) * ks, vlo + vo, DHI, IDESC_O);
-              if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vo, DHI, IDESC_O);
+              mma_ts<1>(t + Tm::O, t + Tm::SP + pcol(ks), vlo + vks[ks], v_hi, IDESC_O);
+              if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + pcol(ks) + 8, vlo + vks[ks], v_hi, IDESC_O);
             }
-            tc_commit(bar_o + 8 * h);
-            if (h == last_reader(kt)) tc_commit(bar_empty + 8 * vslot);
+            tc_commit(bar(Lay::B_O + h));
+            if (h == last_reader(kt)) tc_commit(bar(Lay::B_EMPTY + vslot));
           }
           __syncwarp();
           if (kt + 1 < nkt_h[h]) {
             if (h == first_reader(kt + 1))
-              wait_or_fail(bar_full + 8 * slot_of(kt + 1, 0), full_parity(kt + 1, 0), failed);
-            wait_or_fail(bar_o + 8 * h, (ph[h] + kt) & 1u, failed);  // P V(kt) has read P(kt)
+              wait_warp(bar(Lay::B_FULL + slot_of(kt + 1, 0)), full_parity(kt + 1, 0), failed);
+            wait_warp(bar(Lay::B_O + h), (ph[h] + kt) & 1u, failed);  // P V(kt) has read P(kt)
+            if (failed) break;
             mma_s(kt + 1, h);
           }
         }
       }
-    } else {
-      // ---------------- softmax: one row per thread (its TMEM lane) ----------------
-      const int h = warp / 4;
-      const int r = tid % kHalfRows;  // row within the half = TMEM lane
-      const uint32_t t_lane = tmem + h * Tm::HALF + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-      const int qi = h * POS_PER_HALF + r / G, g = r % G;
-      const bool row_valid = qi < npos;
-      const int nk = nkt_h[h];
-      float sl2 = p.scale_log2;  // > 0: the max of raw scores gives the max of scaled ones
-      {  // Q of the half: row r = (position, head), K-major, swizzled
-        const uint32_t sQ = sQ0 + h * Lay::Q_BYTES;
-        const bf16 *qrow =
-            p.q + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.q_stride + static_cast<int64_t>(kvh * G + g) * D;
-        // q is only required to be 4-byte aligned: 16-byte loads when rows allow them
-        const bool q16 = (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 && (p.q_stride & 7) == 0;
-        auto load_q = [&](int c) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (row_valid) {
-            if (q16) {
-              w = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
-            } else {
-              const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow) + 4 * c;
-              w = make_uint4(__ldg(q32), __ldg(q32 + 1), __ldg(q32 + 2), __ldg(q32 + 3));
-            }
-          }
-          return w;
-        };
-        // bf16 rows over 8-bit caches: 2^-e, e > 0 only when the row's largest |q| reaches 2^15
-        float qmul = 1.f;
-        if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
-          float amax = 0.f;
-#pragma unroll 4
-          for (int c = 0; c < D / 8; ++c) {
-            const uint4 w = load_q(c);
-            const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+      if (failed) break;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(v[k])), fabsf(ElemBf16::hi(v[k]))));
+      for (int h = 0; h < kHalves; ++h) ph[h] += nkt_h[h];
+      ring0 += 2 * nkt;
+    }
+  } else {
+    // ---------------- softmax: one row per thread (its TMEM lane), 64 keys per range ----------------
+    const int quad = warp & 3, h = (warp >> 2) & 1, part = warp / (4 * kHalves);
+    const int r = quad * 32 + lane;  // row within the half = TMEM lane
+    const uint32_t t_lane = tmem + h * Tm::HALF + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t bx = bar(Lay::B_X + h * 4 + quad);  // exchange with the other warp of these rows
+    volatile float *x_mine = xch + (h * kParts + part) * kHalfRows + r;
+    volatile float *x_other = xch + (h * kParts + (kParts - 1 - part)) * kHalfRows + r;
+    uint32_t nx = 0;  // exchanges so far
+    // my value out, the other warp's value in (both warps of the rows call it alike)
+    auto exchange = [&](float v) -> float {
+      *x_mine = v;
+      mbar_arrive(bx);  // every thread: release of its own store
+      wait_warp(bx, nx & 1u, failed);
+      ++nx;
+      return failed ? v : *x_other;
+    };
+    // both warps of the rows have reached this point (no data)
+    auto pair_sync = [&]() {
+      mbar_arrive(bx);
+      wait_warp(bx, nx & 1u, failed);
+      ++nx;
+    };
+    const int ch0 = part ? (NCH + 1) / 2 : 0, ch1 = part ? NCH : (NCH + 1) / 2;  // this warp's O chunks
+    const int g = r % G;
+    uint32_t phh = 0;  // ranges this half has run so far
+
+    // Q of the half for unit `u`: this warp stores its half of the row's 16-byte
+    // chunks (row r = (position, head), K-major, swizzled); returns the row's
+    // softmax factor (log2 domain, times 2^e for a scaled bf16 row over 8-bit caches)
+    auto load_q = [&](const TileUnit &u) -> float {
+      const int qi = h * POS_PER_HALF + r / G;
+      const bool valid = qi < u.npos;
+      const uint32_t sQ = sQ0 + h * Lay::Q_BYTES;
+      const bf16 *qrow =
+          p.q + static_cast<int64_t>(u.row0 + (valid ? qi : 0)) * p.q_stride + static_cast<int64_t>(u.kvh * G + g) * D;
+      // q is only required to be 4-byte aligned: 16-byte loads when rows allow them
+      const bool q16 = (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 && (p.q_stride & 7) == 0;
+      auto ldq = [&](int c) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          if (q16) {
+            w = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+          } else {
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow) + 4 * c;
+            w = make_uint4(__ldg(q32), __ldg(q32 + 1), __ldg(q32 + 2), __ldg(q32 + 3));
           }
-          const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // floor(log2(amax))
-          const int e = ex >= 15 ? min(ex - 14, 120) : 0;
-          qmul = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-          sl2 *= __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
         }
+        return w;
+      };
+      float sl2 = p.scale_log2;  // > 0: the max of raw scores gives the max of scaled ones
+      float qmul = 1.f;
+      if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+        // bf16 rows over 8-bit caches: 2^-e, e > 0 only when the row's largest |q| reaches 2^15
+        float amax = 0.f;
 #pragma unroll 4
         for (int c = 0; c < D / 8; ++c) {
-          uint4 w = load_q(c);
-          if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
-            w = make_uint4(ElemFp16::pack(ElemBf16::lo(w.x) * qmul, ElemBf16::hi(w.x) * qmul),
-                           ElemFp16::pack(ElemBf16::lo(w.y) * qmul, ElemBf16::hi(w.y) * qmul),
-                           ElemFp16::pack(ElemBf16::lo(w.z) * qmul, ElemBf16::hi(w.z) * qmul),
-                           ElemFp16::pack(ElemBf16::lo(w.w) * qmul, ElemBf16::hi(w.w) * qmul));
-          }
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + Lay::off(r, c, Lay::Q_ATOM)),
-                       "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
-                       : "memory");
-        }
-        fence_proxy_async_smem();  // the MMA reads Q through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_q);
-      }
-      float m_used = -INFINITY, l = 0.f;
-      const int lim = row_valid ? pos0 + qi + 1 : 0;  // keys j < lim are visible to this row
-      for (int kt = 0; kt < nk; ++kt) {
-        const int key0 = kt * kKeyTile;
-        const uint32_t sp = t_lane + Tm::SP;
-        wait_or_fail(bar_s + 8 * h, (ph[h] + kt) & 1u, failed);
-        tc_fence_after();
-        // One pass over the range, 32 keys at a time: each chunk's maximum is
-        // checked against the running one before its probabilities are taken.
-        // One pass over the range, 32 keys at a time: each chunk's maximum is
-        // checked against the running one before its probabilities are taken.
-        float sum = 0.f;     // this range's probabilities, against m_used
-        float alpha = 1.f;   // factor owed by O and l for growth within this range
-#pragma unroll 1
-        for (int c = 0; c < kKeyTile / 32; ++c) {
-          const int ck0 = key0 + 32 * c;
-          uint32_t sv[32], u[32];
-          tmem_ld32_wait(sp + 32 * c, sv);
-          // The chunk's maximum, rounded, and its growth over m_used, as separately
-          // rounded operations (no contraction into one fused multiply-add): the
-          // exponents below are bounded by exactly this difference.
-          const float cm = __fmul_rn(sl2, masked_max32(sv, ck0, lim));
-          const bool grow = cm > -INFINITY && (m_used == -INFINITY || __fsub_rn(cm, m_used) > kRescaleLog2);
-          if (__any_sync(0xffffffffu, grow)) {
-            // The row's maximum grew past the threshold (always in a row's
-            // first visible chunk, rarely after): what was taken against the
-            // old maximum (this range's sum and stored chunks, and O and l)
-            // is scaled by 2^(old - new). TMEM accesses are warp-wide, so the
-            // warp does it together (factor 1 in rows that did not grow).
-            const float a = grow && m_used > -INFINITY ? ex2_approx(__fsub_rn(m_used, cm)) : 1.f;
-            if (grow) m_used = cm;
-            sum *= a;
-            alpha *= a;
-            if (c > 0) {
-              tmem_wait_st();  // the chunks stored so far are read back
-#pragma unroll 1
-              for (int cc = 0; cc < c; ++cc) {
-                if constexpr (SPLIT)
-                  rescale_p32<M>(sp + 32 * cc, a);
-                else
-                  rescale_p16<M>(sp + 16 * cc, a);
-              }
-            }
-          }
-          const float ms = m_used == -INFINITY ? 0.f : m_used;
-          if (__any_sync(0xffffffffu, fabsf(ms) > 4096.f))
-            probs32<M, true, SPLIT>(sv, ck0, lim, sl2, ms, sum, u);
-          else
-            probs32<M, false, SPLIT>(sv, ck0, lim, sl2, ms, sum, u);
-          // P over the scores it came from (single pairs: chunk c at columns 16c, over
-          // scores of chunks <= c that have been read already)
-          if constexpr (SPLIT) {
-            tmem_st32u(sp + 32 * c, u);
-          } else {
-            uint32_t u16[16];
+          const uint4 w = ldq(c);
+          const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) u16[i] = u[i];
-            tmem_st16u(sp + 16 * c, u16);
-          }
+          for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(v[k])), fabsf(ElemBf16::hi(v[k]))));
+        }
+        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // floor(log2(amax))
+        const int e = ex >= 15 ? min(ex - 14, 120) : 0;
+        qmul = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        sl2 *= __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+      }
+      constexpr int CQ = D / 16;  // chunks per warp (D / 8 per row)
+#pragma unroll 4
+      for (int c = part * CQ; c < (part + 1) * CQ; ++c) {
+        uint4 w = ldq(c);
+        if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+          w = make_uint4(ElemFp16::pack(ElemBf16::lo(w.x) * qmul, ElemBf16::hi(w.x) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.y) * qmul, ElemBf16::hi(w.y) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.z) * qmul, ElemBf16::hi(w.z) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.w) * qmul, ElemBf16::hi(w.w) * qmul));
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + Lay::off(r, c, Lay::Q_ATOM)), "r"(w.x),
+                     "r"(w.y), "r"(w.z), "r"(w.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // the MMA reads Q through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Lay::B_QF + h));
+      return sl2;
+    };
+
+    TileUnit cur;
+    read_unit(0, cur);
+    float sl2 = 0.f;
+    if (!failed && !cur.stop) sl2 = load_q(cur);
+    for (uint32_t j = 0; !failed && !cur.stop; ++j) {
+      int nkt_h[kHalves];
+      ranges(cur, nkt_h);
+      const int nk = nkt_h[h];
+      const int qi = h * POS_PER_HALF + r / G;
+      const bool row_valid = qi < cur.npos;
+      const int lim = row_valid ? cur.pos0 + qi + 1 : 0;  // keys j < lim are visible to this row
+      float m_used = -INFINITY, l = 0.f;
+      for (int kt = 0; kt < nk; ++kt) {
+        const int ck0 = kt * kKeyTile + part * PART_KEYS;  // this warp's first key of the range
+        const uint32_t sp = t_lane + Tm::SP + part * PART_KEYS;
+        wait_warp(bar(Lay::B_S + h), (phh + kt) & 1u, failed);
+        if (failed) break;
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32x2_wait(sp, s0, s1);
+        // The range's maximum over both warps' keys, then its growth over
+        // m_used, as separately rounded operations (no contraction into one
+        // fused multiply-add): the exponents below are bounded by exactly this
+        // difference. The other warp reads its scores before either writes P.
+        const float mx = fmaxf(masked_max32(s0, ck0, lim), masked_max32(s1, ck0 + 32, lim));
+        const float mo = exchange(mx);
+        if (failed) break;
+        const float cm = __fmul_rn(sl2, fmaxf(mx, mo));
+        const bool grow = cm > -INFINITY && (m_used == -INFINITY || __fsub_rn(cm, m_used) > kRescaleLog2);
+        float alpha = 1.f;  // factor owed by O and l for the growth
+        if (grow) {
+          alpha = m_used > -INFINITY ? ex2_approx(__fsub_rn(m_used, cm)) : 1.f;
+          m_used = cm;
+        }
+        const float ms = m_used == -INFINITY ? 0.f : m_used;
+        float sum = 0.f;
+        const bool exact = __any_sync(FULL, fabsf(ms) > 4096.f);
+        // P over the scores it came from, one UMMA K step (16 keys) at a time:
+        // SPLIT, 16 columns per step in place; single pairs, 8 columns per step
+        // from the start of this warp's columns
+        // (the second 32 scores are read again after the first 32 probabilities
+        // are stored, which keeps a thread's live registers within budget; P of
+        // the first 32 keys never covers the columns of the second)
+        constexpr uint32_t PSTEP = SPLIT ? 16 : 8;
+        if (exact) {
+          probs16_store<M, true, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
+          probs16_store<M, true, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+        } else {
+          probs16_store<M, false, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
+          probs16_store<M, false, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+        }
+        tmem_ld32_wait(sp + 32, s1);
+        if (exact) {
+          probs16_store<M, true, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+          probs16_store<M, true, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
+        } else {
+          probs16_store<M, false, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+          probs16_store<M, false, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
         }
         // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
-        // last of them finished).
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // last of them finished); each warp rescales its own columns.
+        if (kt > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
-          for (int ch = 0; ch < (D + 31) / 32; ++ch) {  // head_dim 80: also 16 unused columns
+          for (int ch = ch0; ch < ch1; ++ch) {
             uint32_t t[32];
             tmem_ld32_wait(t_lane + Tm::O + ch * 32, t);
 #pragma unroll
@@ -783,20 +947,35 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p + 8 * h);
+        if (lane == 0) mbar_arrive(bar(Lay::B_P + h));
       }
+      if (failed) break;
+      // the next unit's record and Q (overlapping this unit's last products)
+      TileUnit nxt;
+      read_unit(j + 1, nxt);
+      float nsl2 = sl2;
+      if (!failed && !nxt.stop) {
+        wait_warp(bar(Lay::B_QE + h), j & 1u, failed);  // the MMA warp has taken this unit's Q
+        if (!failed) nsl2 = load_q(nxt);
+      }
+      if (failed) break;
       if (nk > 0) {
-        // epilogue: the half's last P V product, normalised
-        wait_or_fail(bar_o + 8 * h, (ph[h] + nk - 1) & 1u, failed);
+        // epilogue: the row sum over both warps' keys, then this warp's columns
+        // of the half's last P V product, normalised
+        pair_sync();  // both warps are past their last read of the maxima
+        const float lt = l + exchange(l);
+        pair_sync();  // both have read the sums
+        wait_warp(bar(Lay::B_O + h), (phh + nk - 1) & 1u, failed);
+        if (failed) break;
         tc_fence_after();
-        const float inv = l > 0.f ? p.out_scale / l : 0.f;
-        bf16 *dst = p.out + static_cast<int64_t>(row0 + (row_valid ? qi : 0)) * p.num_heads * D +
-                    static_cast<int64_t>(kvh * G + g) * D;
-#pragma unroll
-        for (int ch = 0; ch < (D + 31) / 32; ++ch) {
+        const float inv = lt > 0.f ? p.out_scale / lt : 0.f;
+        bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (row_valid ? qi : 0)) * p.num_heads * D +
+                    static_cast<int64_t>(cur.kvh * G + g) * D;
+#pragma unroll 1
+        for (int ch = ch0; ch < ch1; ++ch) {
           uint32_t t[32];
           tmem_ld32_wait(t_lane + Tm::O + ch * 32, t);
-          if (row_valid && !failed) {
+          if (row_valid) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               if (32 * ch + 8 * c >= D) continue;  // head_dim 80: the last 16 columns are padding
@@ -807,28 +986,28 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             }
           }
         }
+        tc_fence_before();  // O is overwritten by a later unit's first product
       }
-      tc_fence_before();  // O is overwritten by the next unit's first product after the unit barrier
+      phh += nk;
+      cur = nxt;
+      sl2 = nsl2;
     }
-    // every role advances the phase bookkeeping alike
-#pragma unroll
-    for (int hh = 0; hh < kHalves; ++hh) ph[hh] += nkt_h[hh];
-    ring0 += 2 * nkt;
   }
 
-  // Every thread left the loop at the same unit barrier. Before tensor memory
-  // and shared memory go away, wait (bounded) for work still in flight: the
-  // MMA thread's products (one last commit) and, after a timeout, the
-  // producer's loads that no product consumed (loads into a buffer complete
-  // in order, so waiting for the last one issued suffices).
+  // Every warp has left its loop (normally at the end of the stream, or after
+  // a timeout). Before tensor memory and shared memory go away, wait (bounded)
+  // for work still in flight: the MMA thread's products (one last commit)
+  // and the producer's loads (loads into a buffer complete in order, so
+  // waiting for the last SLOTS issued suffices).
   if (warp == kMmaWarp && lane == 0) {
-    tc_commit(bar_drain);
-    if (!mbar_wait_bounded(bar_drain, 0, kTcWaitTimeoutNs)) failed = true;
+    tc_commit(bar(Lay::B_DRAIN));
+    if (!mbar_wait_bounded(bar(Lay::B_DRAIN), 0, kTcWaitTimeoutNs)) failed = true;
   }
   if (warp == kTmaWarp && lane == 0) {
-    const uint32_t landed = KV8 ? bar_raw : bar_full;  // where the loads' completion is counted
+    const int landed = KV8 ? Lay::B_RAW : Lay::B_FULL;  // where the loads' completion is counted
     for (uint32_t g = issued > SLOTS ? issued - SLOTS : 0; g < issued; ++g)
-      if (!mbar_wait_bounded(landed + 8 * (g % SLOTS), (g / SLOTS) & 1u, kTcWaitTimeoutNs)) failed = true;
+      if (!mbar_wait_bounded(bar(landed + static_cast<int>(g % SLOTS)), (g / SLOTS) & 1u, kTcWaitTimeoutNs))
+        failed = true;
   }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
   tc_fence_before();
@@ -838,8 +1017,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
 }
 
 template <int D, int G, typename E, bool KV8>
-cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const TileParams &tp, int sm_count,
-                                 cudaStream_t stream) {
+cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &vmapb,
+                                 const TileParams &tp, int sm_count, cudaStream_t stream) {
   constexpr int smem = TcLayout<D>::REQUEST;
   auto kern = prefill_tile_kernel<D, G, E, KV8>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -851,12 +1030,13 @@ cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vma
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? kTileThreads8 : kTileThreads), smem, stream,
-                    kmap, vmap, tp);
+                    kmap, vmap, vmapb, tp);
 }
 
 #define PA_TILE_INST1(DD, GG, EE, K8)                                                                   \
   template cudaError_t launch_prefill_tiles<DD, GG, EE, K8>(const CUtensorMap &, const CUtensorMap &,     \
-                                                            const TileParams &, int, cudaStream_t);
+                                                            const CUtensorMap &, const TileParams &, int, \
+                                                            cudaStream_t);
 #define PA_TILE_INST(DD, GG)                                                                              \
   PA_TILE_INST1(DD, GG, ElemBf16, false)                                                                  \
   PA_TILE_INST1(DD, GG, ElemFp16, false)                                                                  \

@@ -103,6 +103,7 @@ struct AttnParams {
   int32_t max_parts;
   float *part_o;    // [num_seqs][Hkv][max_parts][8][D]
   float *part_lse;  // [num_seqs][Hkv][max_parts][8]
+  int32_t block_boxes;  // 1: 16-bit caches, head_dim 128, blocks of >= 16 tokens: one 4-D box per tile
   unsigned int *status;
 };
 
@@ -549,6 +550,7 @@ struct TileGeom<D, true> {
 template <int D, int G, int NWARPS, typename E, bool KV8>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     splitkv_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4,
                              const AttnParams p) {
   using T = TileGeom<D, KV8>;
   // Tensor-core operand type: E, except over 8-bit caches, where K, V and P
@@ -572,6 +574,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
+    if (p.block_boxes) {
+      prefetch_tmap(&kmap4);
+      prefetch_tmap(&vmap4);
+    }
   }
   fence_mbar_init();
   __syncthreads();
@@ -610,6 +616,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         if constexpr (KV8) {
           tma_load_3d(dst + j * box_rows * T::ROW, &kmap, bar, 0, U.kvh, z);
           tma_load_3d(dst + T::TILE_BYTES + j * box_rows * T::ROW, &vmap, bar, 0, U.kvh, z);
+        } else if (D == 128 && p.block_boxes) {
+          // one box per cache holds both 64-element atoms of the tile's 16 rows,
+          // atom after atom: the layout T::off addresses (one TMA instruction
+          // instead of two; the engine moves larger boxes at a higher rate)
+          tma_load_4d(dst, &kmap4, bar, 0, z, 0, U.kvh);
+          tma_load_4d(dst + T::TILE_BYTES, &vmap4, bar, 0, z, 0, U.kvh);
         } else {
 #pragma unroll
           for (int h = 0; h < T::HALVES; ++h) {
@@ -1075,6 +1087,30 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_bl
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D view of one 16-bit cache at head_dim 128, [Hkv][2 atoms][num_blocks *
+// block_size rows][64 elements] from the outermost dimension in (strides:
+// head D * 2 bytes, atom 128 bytes, row Hkv * D * 2 bytes), with a box of
+// `rows` rows x both atoms x 1 head: a whole (block, KV head) tile of up to
+// 32 rows in one TMA instruction, landing atom after atom (128-byte swizzle).
+// Every coordinate the kernels use lies inside the cache; a negative row
+// coordinate reads zeros.
+static bool encode_block_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int32_t num_kv_heads,
+                             int32_t block_size, int32_t rows, int32_t dtype) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  constexpr int D = 128;
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(num_blocks) * block_size, 2,
+                              static_cast<cuuint64_t>(num_kv_heads)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(num_kv_heads) * D * 2, 128, D * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), 2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType type =
+      dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode(map, type, 4, const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kAttnWarps = 8;   // 16-bit caches: two warps per scheduler
 constexpr int kAttnWarps8 = 12; // 8-bit caches: three, to hide the latency of the per-tile widening
 
@@ -1110,6 +1146,14 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (!encode_cache_map(&kmap, a.key_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype, KV8) ||
       !encode_cache_map(&vmap, a.value_cache, a.num_blocks, a.num_kv_heads, D, a.block_size, a.dtype, KV8))
     return cudaErrorInvalidValue;
+  // whole-block boxes (16-bit caches at head_dim 128): 16-row tiles for the
+  // decode kernel when blocks hold at least 16 tokens
+  const bool block_boxes = !KV8 && D == 128 && a.block_size >= kTileKeys;
+  CUtensorMap kmap4 = kmap, vmap4 = vmap;
+  if (block_boxes &&
+      (!encode_block_map(&kmap4, a.key_cache, a.num_blocks, a.num_kv_heads, a.block_size, kTileKeys, a.dtype) ||
+       !encode_block_map(&vmap4, a.value_cache, a.num_blocks, a.num_kv_heads, a.block_size, kTileKeys, a.dtype)))
+    return cudaErrorInvalidValue;
 
   cudaError_t err = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
   if (err != cudaSuccess) return err;
@@ -1137,6 +1181,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.max_parts = w.max_parts;
   ap.part_o = reinterpret_cast<float *>(ws + w.part_o);
   ap.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+  ap.block_boxes = block_boxes ? 1 : 0;
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
@@ -1152,7 +1197,8 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   if (grid * NW > units_upper) grid = (units_upper + NW - 1) / NW;
   if (grid < 1) grid = 1;
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, kmap, vmap, ap);
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, kmap, vmap, kmap4, vmap4,
+                   ap);
   if (err != cudaSuccess) return err;
   ++*launched;
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
@@ -1178,8 +1224,13 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     tp.total_q = a.total_q;
     tp.max_tiles = w.max_tiles;
     tp.status = a.status;
+    // value cache in whole-block boxes for the tile kernel (block_size rows)
+    CUtensorMap vmapb = vmap;
+    if (!KV8 && D == 128 &&
+        !encode_block_map(&vmapb, a.value_cache, a.num_blocks, a.num_kv_heads, a.block_size, a.block_size, a.dtype))
+      return cudaErrorInvalidValue;
     if (a.tile_start) cudaEventRecord(a.tile_start, stream);
-    err = launch_prefill_tiles<D, G, E, KV8>(kmap, vmap, tp, a.sm_count, stream);
+    err = launch_prefill_tiles<D, G, E, KV8>(kmap, vmap, vmapb, tp, a.sm_count, stream);
     if (err == cudaSuccess && a.tile_stop) cudaEventRecord(a.tile_stop, stream);
     if (err != cudaSuccess) return err;
     ++*launched;
