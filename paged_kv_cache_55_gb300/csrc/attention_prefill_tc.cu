@@ -28,10 +28,13 @@
 //   * an MMA warp issues tcgen05.mma. Each half owns one score buffer in
 //     tensor memory: S(r) = Q K(r)^T lands there, the softmax overwrites it
 //     in place with P(r), and O += P(r) V(r) reads P from there (V an
-//     MN-major shared-memory operand). The order is P V_A(r), S_A(r+1) once
-//     that product has completed, P V_B(r), S_B(r+1): while one half's
-//     softmax runs, the tensor cores work on the other half. The warp zeroes
-//     V rows past the last key before the first product reads them;
+//     MN-major shared-memory operand). The order is P V_A(r), S_A(r+1),
+//     P V_B(r), S_B(r+1): while one half's softmax runs, the tensor cores
+//     work on the other half. S_A(r+1) is issued right behind P V_A(r),
+//     whose operand it overwrites: the products one thread issues execute in
+//     issue order, and the commit that signals S_A(r+1) complete also covers
+//     every product issued before it. The warp zeroes V rows past the last
+//     key before the first product reads them;
 //   * sixteen softmax warps, two per TMEM lane quadrant and half: each thread
 //     owns one row (its TMEM lane) and 64 of the 128 keys of every range. The
 //     two warps of a row exchange their maxima through shared memory (an
@@ -718,12 +721,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
       if (nkt > 0) {
         wait_warp(bar(Lay::B_FULL + slot_of(0, 0)), full_parity(0, 0), failed);
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h) {
-          if (nkt_h[h] == 0) continue;
-          // the score buffer is free once the half's last product of the previous unit completed
-          if (ph[h] > 0) wait_warp(bar(Lay::B_O + h), (ph[h] - 1) & 1u, failed);
-          if (!failed) mma_s(0, h);
-        }
+        for (int h = 0; h < kHalves; ++h)
+          if (nkt_h[h] > 0 && !failed) mma_s(0, h);
       }
       for (int kt = 0; kt < nkt && !failed; ++kt) {
         const uint32_t vslot = slot_of(kt, 1);
@@ -773,7 +772,6 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
           if (kt + 1 < nkt_h[h]) {
             if (h == first_reader(kt + 1))
               wait_warp(bar(Lay::B_FULL + slot_of(kt + 1, 0)), full_parity(kt + 1, 0), failed);
-            wait_warp(bar(Lay::B_O + h), (ph[h] + kt) & 1u, failed);  // P V(kt) has read P(kt)
             if (failed) break;
             mma_s(kt + 1, h);
           }
@@ -931,8 +929,9 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
           probs16_store<M, false, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
           probs16_store<M, false, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
         }
-        // O holds P V(0 .. kt-1), all complete (S(kt) was issued after the
-        // last of them finished); each warp rescales its own columns.
+        // O holds P V(0 .. kt-1), all complete (they were issued before S(kt),
+        // whose completion the wait above observed); each warp rescales its
+        // own columns.
         if (kt > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
           for (int ch = ch0; ch < ch1; ++ch) {
