@@ -65,11 +65,16 @@ constexpr int kParts = 2;        // softmax warps per TMEM lane quadrant and hal
 constexpr int kKeyTile = 128;    // keys per range (UMMA N of S, K of P V)
 constexpr int kMaxSlots = 8;     // K/V ring slots (as many as shared memory holds)
 constexpr int kUnitSlots = 2;    // published unit records
-constexpr int kSoftmaxWarps = 4 * kHalves * kParts, kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
-constexpr int kTileThreads = 32 * (kTmaWarp + 1);
+// Warp roles. The MMA warp is warp 0: its issue rate sets the tensor cores'
+// (they queue only a couple of products) and it shares a scheduler with
+// softmax warps; the schedulers favour lower-numbered warps when several are
+// ready. Warp 1 loads K/V; warps 2 and 3 widen 8-bit codes (idle otherwise);
+// warps 4 .. 19 run the softmax (warp % 4 is their TMEM lane quadrant).
+constexpr int kSoftmaxWarps = 4 * kHalves * kParts, kMmaWarp = 0, kTmaWarp = 1, kSoftmaxWarp0 = 4;
+constexpr int kTileThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
 // 8-bit caches: two more warps widen each staged range to fp16 in place.
-constexpr int kConvWarp = kTmaWarp + 1, kConvWarps = 2;
-constexpr int kTileThreads8 = kTileThreads + 32 * kConvWarps;
+constexpr int kConvWarp = 2, kConvWarps = 2;
+constexpr int kTileThreads8 = kTileThreads;
 constexpr int kRawBoxRows = 32;  // 8-bit boxes: min(block_size, 32) rows
 constexpr uint64_t kTcWaitTimeoutNs = 2000000000;
 constexpr uint32_t kTmemCols = 512;
@@ -369,7 +374,7 @@ struct TileUnit {
 // bf16 Q row is stored as fp16, scaled first by a power of two when its
 // largest |q| reaches 2^15, and its row's softmax factor is scaled back.
 template <int D, int G, typename E, bool KV8>
-// Eighteen warps (twenty with 8-bit caches), one CTA per SM.
+// Twenty warps (two of them idle over 16-bit caches), one CTA per SM.
 __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const __grid_constant__ CUtensorMap vmapb, const TileParams p) {
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
       }
       if (failed) break;
     }
-  } else if (warp >= kConvWarp) {
+  } else if (warp >= kConvWarp && warp < kSoftmaxWarp0) {
     // ---------------- 8-bit caches: widen staged codes to fp16 in place ----------------
     if constexpr (KV8) {
       // Lane l of converter warp w takes 16-byte code chunk c of rows
@@ -784,7 +789,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     }
   } else {
     // ---------------- softmax: one row per thread (its TMEM lane), 64 keys per range ----------------
-    const int quad = warp & 3, h = (warp >> 2) & 1, part = warp / (4 * kHalves);
+    const int sw = warp - kSoftmaxWarp0;  // softmax warp index
+    const int quad = sw & 3, h = (sw >> 2) & 1, part = sw / (4 * kHalves);
     const int r = quad * 32 + lane;  // row within the half = TMEM lane
     const uint32_t t_lane = tmem + h * Tm::HALF + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t bx = bar(Lay::B_X + h * 4 + quad);  // exchange with the other warp of these rows
