@@ -44,7 +44,7 @@
  *     quotient in binary32 (correctly rounded), then rounded to the nearest
  *     code, ties to even, magnitudes beyond 448 saturating to 448. Reading
  *     uses code * scale. q, key, value and out stay bf16 or fp16.
- *   - Supported now: head_dim 64, 80, 96 or 128; block_size 8, 16 or 32 (the
+ *   - Supported now: head_dim 64, 80, 96, 128 or 256; block_size 8, 16 or 32 (the
  *     reading map, §2.3, sweeps page sizes; the kernels stage K/V 16 keys at a
  *     time); num_heads a multiple of num_kv_heads with group size 1, 2, 4 or 8.
  *     pa_rope_reshape_and_cache and pa_copy_blocks take any block_size.

@@ -57,9 +57,9 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool valid_cache_scale(float s) { return std::isfinite(s) && s > 0.0f; }
 
-// Head dims with built kernels: 64 and 128, and 80 and 96 (rows padded to
-// whole 64-element swizzle atoms in shared memory).
-bool supported_head_dim(int32_t d) { return d == 64 || d == 80 || d == 96 || d == 128; }
+// Head dims with built kernels: 64 and 128, 80 and 96 (rows padded to whole
+// 64-element swizzle atoms in shared memory), and 256.
+bool supported_head_dim(int32_t d) { return d == 64 || d == 80 || d == 96 || d == 128 || d == 256; }
 
 // Bytes of one cache element: 2 for the 16-bit types, 1 for E4M3 codes; 0 if unknown.
 int cache_elem_bytes(int32_t dtype) {

@@ -14,6 +14,12 @@ using bf16 = __nv_bfloat16;
 // kPrefillTileRows / G positions per tile. Records: {b, first query token,
 // positions, absolute position of the first}, {0, key end, -1, 1}.
 constexpr int kPrefillTileRows = 256;
+// head_dim 256 tiles are one 128-row half (S and O of one half fill the
+// tensor memory): kPrefillTileRows128 rows
+constexpr int kPrefillTileRows128 = 128;
+__host__ __device__ constexpr int prefill_tile_rows(int head_dim) {
+  return head_dim == 256 ? kPrefillTileRows128 : kPrefillTileRows;
+}
 
 struct TileParams {
   const bf16 *q;

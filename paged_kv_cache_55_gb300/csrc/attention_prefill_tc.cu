@@ -1021,21 +1021,635 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// head_dim 256: one 128-row half per tile. S (128 columns) and O (256) of a
+// half take 384 of the 512 TMEM columns, so the tile has one half and two
+// score buffers: S(r + 1) is computed while the softmax works on S(r), and
+// the tensor cores run P V(r) and S(r + 2) behind it. A K or V range is
+// staged as two units of 128 keys x 128 elements (d 0..127 and 128..255),
+// each laid out like a head_dim-128 ring slot (so 8-bit codes are widened
+// unit by unit exactly as there), four loads per range; S takes its first
+// eight K steps from the first K unit and the rest from the second, and
+// P V is two N = 128 products per K step, one per V unit, into O's two
+// column halves. The roles, the record ring, the bounded waits and the exit
+// path are those of the kernel above; eight softmax warps (two per TMEM lane
+// quadrant, 64 keys of a range each).
+// ---------------------------------------------------------------------------
+constexpr int kWideD = 256;
+constexpr int kWideSoftmaxWarps = 8;
+constexpr int kWideThreads = 32 * (kSoftmaxWarp0 + kWideSoftmaxWarps);
+
+struct WideTmem {
+  static constexpr uint32_t SP0 = 0, O = 2 * kKeyTile;  // score buffers at 0 and 128, O at [256, 512)
+};
+
+struct WideLayout {
+  static constexpr int Q_ATOM = kHalfRows * 128;   // 128 rows x 128 B
+  static constexpr int Q_BYTES = 4 * Q_ATOM;       // one half, four 64-element atoms
+  static constexpr int KV_ATOM = kKeyTile * 128;   // 128 keys x 128 B
+  static constexpr int UNIT_BYTES = 2 * KV_ATOM;   // 128 keys x 128 elements: a ring slot
+  // mbarriers: per ring slot full, empty, raw, conv; per score buffer s, p;
+  // o, qf, qe; per record slot uf, ue; per lane quadrant x1 (values
+  // written), x2 (values read); drain
+  static constexpr int B_FULL = 0, B_EMPTY = kMaxSlots, B_RAW = 2 * kMaxSlots, B_CONV = 3 * kMaxSlots;
+  static constexpr int B_S = 4 * kMaxSlots, B_P = B_S + 2, B_O = B_P + 2, B_QF = B_O + 1, B_QE = B_QF + 1;
+  static constexpr int B_UF = B_QE + 1, B_UE = B_UF + kUnitSlots, B_X1 = B_UE + kUnitSlots, B_X2 = B_X1 + 4;
+  static constexpr int B_DRAIN = B_X2 + 4, NBARS = B_DRAIN + 1;
+  static constexpr int XCH_BYTES = kWideSoftmaxWarps * 32 * 4;
+  static constexpr int REC_BYTES = kUnitSlots * 32;
+  static constexpr int FIXED = Q_BYTES + XCH_BYTES + REC_BYTES + 8 * NBARS + 16;
+  static constexpr int FIT = (227 * 1024 - FIXED) / UNIT_BYTES;
+  static constexpr int SLOTS = FIT < kMaxSlots ? FIT : kMaxSlots;
+  static_assert(SLOTS >= 5, "the ring holds a range's four loads and the next one's first");
+  static constexpr int RING_OFF = Q_BYTES;
+  static constexpr int XCH_OFF = RING_OFF + SLOTS * UNIT_BYTES;
+  static constexpr int REC_OFF = XCH_OFF + XCH_BYTES;
+  static constexpr int BAR_OFF = REC_OFF + REC_BYTES;
+  static constexpr int TMEM_OFF = BAR_OFF + 8 * NBARS;
+  static constexpr int BYTES = TMEM_OFF + 16;
+};
+static_assert(WideLayout::BYTES <= 227 * 1024, "shared memory of one CTA");
+
+template <int G, typename E, bool KV8>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    prefill_tile_wide_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const TileParams p) {
+  using Lay = WideLayout;
+  using Tm = WideTmem;
+  using TL = TcLayout<128>;  // a ring slot: the layout of a head_dim-128 range
+  constexpr int D = kWideD;
+  using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
+  constexpr bool SPLIT = std::is_same<M, ElemBf16>::value;      // P as a hi + lo pair (bf16 operands only)
+  constexpr int RAW_ROW = 128;
+  constexpr int RAW_BYTES = kKeyTile * RAW_ROW;    // 8-bit codes of one unit
+  constexpr uint32_t RAW_OFF = Lay::UNIT_BYTES / 2;
+  constexpr int LPR = 4;                           // loads per range: K lo, K hi, V lo, V hi
+  constexpr int KSTEPS_S = D / 16;
+  constexpr int KSTEPS_O = kKeyTile / 16;
+  constexpr int POS = kHalfRows / G;               // positions per tile
+  constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, M::kUmmaFormat);
+  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, 128, 1, M::kUmmaFormat);
+  constexpr float kRescaleLog2 = 8.f;
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int SLOTS = Lay::SLOTS;
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+    return;
+  }
+  const uint32_t sQ = base, sRing = base + Lay::RING_OFF;
+  auto bar = [&](int i) { return base + Lay::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::TMEM_OFF);
+  volatile int *units = reinterpret_cast<volatile int *>(smem_raw + Lay::REC_OFF);
+  volatile float *xch = reinterpret_cast<volatile float *>(smem_raw + Lay::XCH_OFF);
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kMaxSlots; ++i) {
+      mbar_init(bar(Lay::B_FULL + i), KV8 ? kConvWarps : 1);
+      mbar_init(bar(Lay::B_EMPTY + i), 1);
+      mbar_init(bar(Lay::B_RAW + i), 1);
+      mbar_init(bar(Lay::B_CONV + i), 32 * kConvWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(Lay::B_S + b), 1);
+      mbar_init(bar(Lay::B_P + b), kWideSoftmaxWarps);
+    }
+    mbar_init(bar(Lay::B_O), 1);
+    mbar_init(bar(Lay::B_QF), kWideSoftmaxWarps);
+    mbar_init(bar(Lay::B_QE), 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(bar(Lay::B_UF + i), 1);
+      mbar_init(bar(Lay::B_UE + i), 1 + kWideSoftmaxWarps + (KV8 ? kConvWarps : 0));
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(bar(Lay::B_X1 + q), 64);  // the two softmax warps of a lane quadrant
+      mbar_init(bar(Lay::B_X2 + q), 64);
+    }
+    mbar_init(bar(Lay::B_DRAIN), 1);
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+  fence_mbar_init();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  griddep_wait();
+
+  const int Hkv = p.num_kv_heads;
+  const int bs = p.block_size;
+  bool failed = false;
+  uint32_t issued = 0;
+
+  auto read_unit = [&](uint32_t j, TileUnit &r) {
+    const uint32_t s = j % kUnitSlots;
+    wait_warp(bar(Lay::B_UF + s), (j / kUnitSlots) & 1u, failed);
+    r.stop = 1;
+    if (!failed) {
+      const volatile int *u = units + 8 * s;
+      r.b = u[0];
+      r.row0 = u[1];
+      r.npos = u[2];
+      r.pos0 = u[3];
+      r.kv_end = u[4];
+      r.kvh = u[5];
+      r.stop = u[6];
+    }
+    __syncwarp();
+    if (lane == 0 && !failed) mbar_arrive(bar(Lay::B_UE + s));
+  };
+  auto nranges = [&](const TileUnit &r) { return (r.kv_end + kKeyTile - 1) / kKeyTile; };
+
+  if (warp == kTmaWarp) {
+    // ---------------- producer ----------------
+    const int total_units = min(max(ld_cg(p.tile_count), 0), p.max_tiles) * Hkv;
+    constexpr int MAXROWS = KV8 ? kRawBoxRows : kTileKeys;
+    const int box_rows = bs < MAXROWS ? bs : MAXROWS;
+    const int nbk = kKeyTile / box_rows;
+    uint32_t j = 0, g = 0;
+    for (;;) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.tile_counter, 1);
+      u = __shfl_sync(FULL, u, 0);
+      TileUnit r{0, 0, 0, 0, 0, 0, u >= total_units ? 1 : 0};
+      if (!r.stop) {
+        const int item = u / Hkv;
+        r.kvh = u - item * Hkv;
+        const int4 r0 = ld_cg(p.tiles + 2 * item);
+        const int4 r1 = ld_cg(p.tiles + 2 * item + 1);
+        r.b = r0.x;
+        r.row0 = r0.y;
+        r.npos = r0.z;
+        r.pos0 = r0.w;
+        r.kv_end = r1.y;
+        const bool sane = r.b >= 0 && r.b < p.num_seqs && r.npos >= 1 && r.npos <= POS && r.row0 >= 0 &&
+                          r.row0 + r.npos <= p.total_q && r.pos0 >= 0 && r.kv_end == r.pos0 + r.npos &&
+                          r.kv_end <= static_cast<int64_t>(p.max_blocks_per_seq) * bs;
+        if (!sane) {
+          if (lane == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+          continue;
+        }
+      }
+      const uint32_t s = j % kUnitSlots;
+      if (j >= kUnitSlots) wait_warp(bar(Lay::B_UE + s), (j / kUnitSlots - 1) & 1u, failed);
+      if (failed) break;
+      if (lane == 0) {
+        volatile int *d = units + 8 * s;
+        d[0] = r.b;
+        d[1] = r.row0;
+        d[2] = r.npos;
+        d[3] = r.pos0;
+        d[4] = r.kv_end;
+        d[5] = r.kvh;
+        d[6] = r.stop;
+        mbar_arrive(bar(Lay::B_UF + s));
+      }
+      __syncwarp();
+      ++j;
+      if (r.stop) break;
+      const int32_t *table = p.block_tables + static_cast<int64_t>(r.b) * p.max_blocks_per_seq;
+      auto box_z = [&](int key, int rows) {
+        if (key >= r.kv_end) return -rows;
+        const int phys = __ldg(table + (key >> p.block_shift));
+        if (phys < 0 || phys >= p.num_blocks) {
+          flag_error(p.status, PA_FLAG_BLOCK_RANGE);
+          return -rows;
+        }
+        return (phys << p.block_shift) + (key & (bs - 1));
+      };
+      const int nkt = nranges(r);
+      for (int kt = 0; kt < nkt && !failed; ++kt) {
+        const int z = lane < nbk ? box_z(kt * kKeyTile + lane * box_rows, box_rows) : 0;
+        for (int v = 0; v < LPR && !failed; ++v) {
+          const uint32_t slot = g % SLOTS, use = g / SLOTS;
+          if (use > 0) wait_warp(bar(Lay::B_EMPTY + slot), (use - 1) & 1u, failed);
+          if (failed) break;
+          const void *map = v >= 2 ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+          const int x0 = (v & 1) * 128;  // first element of the unit's half of d
+          const uint32_t dst = sRing + slot * Lay::UNIT_BYTES;
+          if constexpr (KV8) {
+            const uint32_t b8 = bar(Lay::B_RAW + slot);
+            if (lane == 0) mbar_arrive_expect_tx(b8, RAW_BYTES);
+            __syncwarp();
+            if (lane < nbk) tma_load_3d(dst + RAW_OFF + lane * box_rows * RAW_ROW, map, b8, x0, r.kvh, z);
+          } else {
+            const uint32_t bf = bar(Lay::B_FULL + slot);
+            if (lane == 0) mbar_arrive_expect_tx(bf, Lay::UNIT_BYTES);
+            __syncwarp();
+            if (lane < nbk) {
+#pragma unroll
+              for (int a = 0; a < 2; ++a)
+                tma_load_3d(dst + a * Lay::KV_ATOM + lane * box_rows * 128, map, bf, x0 + a * 64, r.kvh, z);
+            }
+          }
+          __syncwarp();
+          issued = ++g;
+        }
+      }
+      if (failed) break;
+    }
+  } else if (warp >= kConvWarp && warp < kSoftmaxWarp0) {
+    // ---------------- 8-bit caches: widen staged codes to fp16 in place (unit by unit) ----------------
+    if constexpr (KV8) {
+      constexpr int CPR = RAW_ROW / 16;
+      constexpr int ROWS_PASS = 8 * (8 / CPR);
+      constexpr int PASSES = kKeyTile / ROWS_PASS;
+      const int ct = (warp - kConvWarp) * 32 + lane;
+      const int q8 = ct >> 3, c = q8 % CPR, rsub = (q8 / CPR) * 8 + (ct & 7);
+      uint32_t j = 0, g = 0;
+      for (;;) {
+        TileUnit r;
+        read_unit(j++, r);
+        if (failed || r.stop) break;
+        const int nkt = nranges(r);
+        for (int i = 0; i < LPR * nkt && !failed; ++i, ++g) {
+          const uint32_t slot = g % SLOTS, use = g / SLOTS;
+          wait_warp(bar(Lay::B_RAW + slot), use & 1u, failed);
+          if (failed) break;
+          const uint32_t sbase = sRing + slot * Lay::UNIT_BYTES;
+          uint4 codes[PASSES];
+#pragma unroll
+          for (int i2 = 0; i2 < PASSES; ++i2) {
+            const int rr = i2 * ROWS_PASS + rsub;
+            const uint32_t a = sbase + RAW_OFF + rr * 128 + (((c ^ rr) & 7) << 4);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                         : "=r"(codes[i2].x), "=r"(codes[i2].y), "=r"(codes[i2].z), "=r"(codes[i2].w)
+                         : "r"(a));
+          }
+          mbar_arrive(bar(Lay::B_CONV + slot));
+          wait_warp(bar(Lay::B_CONV + slot), use & 1u, failed);
+          if (failed) break;
+#pragma unroll
+          for (int i2 = 0; i2 < PASSES; ++i2) {
+            const int rr = i2 * ROWS_PASS + rsub;
+            const uint32_t w[4] = {codes[i2].x, codes[i2].y, codes[i2].z, codes[i2].w};
+            uint32_t hh[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+                  " cvt.rn.f16x2.e4m3x2 %1, u;\n}\n"
+                  : "=r"(hh[2 * k]), "=r"(hh[2 * k + 1])
+                  : "r"(w[k]));
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sbase + TL::off(rr, 2 * c, TL::KV_ATOM)),
+                         "r"(hh[0]), "r"(hh[1]), "r"(hh[2]), "r"(hh[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                             sbase + TL::off(rr, 2 * c + 1, TL::KV_ATOM)),
+                         "r"(hh[4]), "r"(hh[5]), "r"(hh[6]), "r"(hh[7])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Lay::B_FULL + slot));
+        }
+        if (failed) break;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue ----------------
+    // Ranges run S(0), S(1), then per range r: P V(r) (once P(r) is written)
+    // and S(r + 2) into the score buffer P V(r) read (the products one thread
+    // issues execute in issue order). Range number gr = (ranges of earlier
+    // units) + r counts across units: its score buffer is gr % 2 and that
+    // buffer's barriers complete once per use, phase gr / 2.
+    constexpr uint32_t DHI = desc_hi(1024);
+    const uint32_t q_lo = desc_lo(sQ, 16);
+    const uint32_t k_lo = desc_lo(sRing, 16), v_lo = desc_lo(sRing, Lay::KV_ATOM);
+    constexpr uint32_t SLOT_STEP = Lay::UNIT_BYTES >> 4;
+    uint32_t ph = 0, ring0 = 0;
+    for (uint32_t j = 0;; ++j) {
+      TileUnit r;
+      read_unit(j, r);
+      if (failed || r.stop) break;
+      const int nkt = nranges(r);
+      auto slot_of = [&](int kt, int u) { return (ring0 + LPR * kt + u) % SLOTS; };
+      auto full_parity = [&](int kt, int u) { return ((ring0 + LPR * kt + u) / SLOTS) & 1u; };
+      auto mma_s = [&](int kt) {
+        wait_warp(bar(Lay::B_FULL + slot_of(kt, 0)), full_parity(kt, 0), failed);
+        wait_warp(bar(Lay::B_FULL + slot_of(kt, 1)), full_parity(kt, 1), failed);
+        if (failed) return;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t gr = ph + kt;
+          const uint32_t d = tmem + Tm::SP0 + (gr & 1u) * kKeyTile;
+          const uint32_t klo0 = k_lo + slot_of(kt, 0) * SLOT_STEP, klo1 = k_lo + slot_of(kt, 1) * SLOT_STEP;
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS_S; ++ks) {
+            const uint32_t qo = ((ks >> 2) * Lay::Q_ATOM + (ks & 3) * 32) >> 4;
+            const uint32_t ko = (((ks >> 2) & 1) * Lay::KV_ATOM + (ks & 3) * 32) >> 4;
+            const uint32_t kb = ks < 8 ? klo0 : klo1;
+            if (ks == 0)
+              mma_ss<0>(d, q_lo + qo, DHI, kb + ko, DHI, IDESC_S);
+            else
+              mma_ss<1>(d, q_lo + qo, DHI, kb + ko, DHI, IDESC_S);
+          }
+          tc_commit(bar(Lay::B_S + (gr & 1u)));
+          tc_commit(bar(Lay::B_EMPTY + slot_of(kt, 0)));
+          tc_commit(bar(Lay::B_EMPTY + slot_of(kt, 1)));
+        }
+        __syncwarp();
+      };
+      wait_warp(bar(Lay::B_QF), j & 1u, failed);
+      if (lane == 0 && !failed) mbar_arrive(bar(Lay::B_QE));
+      if (failed) break;
+      if (nkt > 0) mma_s(0);
+      if (nkt > 1) mma_s(1);
+      for (int kt = 0; kt < nkt && !failed; ++kt) {
+        const uint32_t gr = ph + kt;
+        wait_warp(bar(Lay::B_P + (gr & 1u)), (gr >> 1) & 1u, failed);  // P(kt) is in place
+        const uint32_t vs0 = slot_of(kt, 2), vs1 = slot_of(kt, 3);
+        wait_warp(bar(Lay::B_FULL + vs0), full_parity(kt, 2), failed);
+        wait_warp(bar(Lay::B_FULL + vs1), full_parity(kt, 3), failed);
+        if (failed) break;
+        const int key0 = kt * kKeyTile;
+        if (key0 + kKeyTile > r.kv_end) {
+          // rows of keys past kv_end may hold anything (even NaN): zero them in both V units
+          const int vr0 = r.kv_end - key0;
+          const int n = (kKeyTile - vr0) * 16;  // 16 chunks of 16 bytes per row and unit
+          for (int i = lane; i < 2 * n; i += 32) {
+            const int unit = i / n, ii = i - unit * n;
+            const int rr = vr0 + ii / 16, c = ii % 16;
+            const uint32_t sV = sRing + (unit ? vs1 : vs0) * Lay::UNIT_BYTES;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sV + TL::off(rr, c, TL::KV_ATOM)),
+                         "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sp = tmem + Tm::SP0 + (gr & 1u) * kKeyTile;
+          const uint32_t v0 = v_lo + vs0 * SLOT_STEP, v1 = v_lo + vs1 * SLOT_STEP;
+          // P of K step ks: SPLIT hi at 16 ks, lo at 16 ks + 8; else 8 ks (+ 32 for the second warp's keys)
+          auto pcol = [](int ks) { return SPLIT ? 16 * ks : 8 * ks + (ks >= 4 ? 32 : 0); };
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS_O; ++ks) {
+            const uint32_t vo = (ks * 2048) >> 4;
+            const uint32_t a = sp + pcol(ks);
+            if (kt == 0 && ks == 0) {  // the unit's first products overwrite O
+              mma_ts<0>(tmem + Tm::O, a, v0 + vo, DHI, IDESC_O);
+              mma_ts<0>(tmem + Tm::O + 128, a, v1 + vo, DHI, IDESC_O);
+            } else {
+              mma_ts<1>(tmem + Tm::O, a, v0 + vo, DHI, IDESC_O);
+              mma_ts<1>(tmem + Tm::O + 128, a, v1 + vo, DHI, IDESC_O);
+            }
+            if (SPLIT) {
+              mma_ts<1>(tmem + Tm::O, a + 8, v0 + vo, DHI, IDESC_O);
+              mma_ts<1>(tmem + Tm::O + 128, a + 8, v1 + vo, DHI, IDESC_O);
+            }
+          }
+          tc_commit(bar(Lay::B_O));
+          tc_commit(bar(Lay::B_EMPTY + vs0));
+          tc_commit(bar(Lay::B_EMPTY + vs1));
+        }
+        __syncwarp();
+        if (kt + 2 < nkt) mma_s(kt + 2);
+      }
+      if (failed) break;
+      ph += nkt;
+      ring0 += LPR * nkt;
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------- softmax: one row per thread, 64 keys of each range per warp ----------------
+    const int sw = warp - kSoftmaxWarp0;
+    const int quad = sw & 3, part = sw >> 2;
+    const int r = quad * 32 + lane;  // row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bx1 = bar(Lay::B_X1 + quad), bx2 = bar(Lay::B_X2 + quad);
+    volatile float *x_mine = xch + (part * 4 + quad) * 32 + lane;
+    volatile float *x_other = xch + ((1 - part) * 4 + quad) * 32 + lane;
+    uint32_t nx = 0;
+    // my value out, the other warp's value in; x2 (its read of the last
+    // exchange) is waited for only before the next write
+    auto exchange = [&](float v) -> float {
+      if (nx > 0) wait_warp(bx2, (nx - 1) & 1u, failed);
+      *x_mine = v;
+      mbar_arrive(bx1);
+      wait_warp(bx1, nx & 1u, failed);
+      const float o = failed ? v : *x_other;
+      mbar_arrive(bx2);
+      ++nx;
+      return o;
+    };
+    const int g = r % G;
+    const int qi = r / G;
+    auto load_q = [&](const TileUnit &u) -> float {
+      const bool valid = qi < u.npos;
+      const bf16 *qrow = p.q + static_cast<int64_t>(u.row0 + (valid ? qi : 0)) * p.q_stride +
+                         static_cast<int64_t>(u.kvh * G + g) * D;
+      const bool q16 = (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 && (p.q_stride & 7) == 0;
+      auto ldq = [&](int c) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          if (q16) {
+            w = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+          } else {
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow) + 4 * c;
+            w = make_uint4(__ldg(q32), __ldg(q32 + 1), __ldg(q32 + 2), __ldg(q32 + 3));
+          }
+        }
+        return w;
+      };
+      float sl2 = p.scale_log2;
+      float qmul = 1.f;
+      if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+        float amax = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 w = ldq(c);
+          const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(ElemBf16::lo(v[k])), fabsf(ElemBf16::hi(v[k]))));
+        }
+        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+        const int e = ex >= 15 ? min(ex - 14, 120) : 0;
+        qmul = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        sl2 *= __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+      }
+      constexpr int CQ = D / 16;  // this warp's half of the row's 16-byte chunks
+#pragma unroll 4
+      for (int c = part * CQ; c < (part + 1) * CQ; ++c) {
+        uint4 w = ldq(c);
+        if constexpr (KV8 && std::is_same<E, ElemBf16>::value) {
+          w = make_uint4(ElemFp16::pack(ElemBf16::lo(w.x) * qmul, ElemBf16::hi(w.x) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.y) * qmul, ElemBf16::hi(w.y) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.z) * qmul, ElemBf16::hi(w.z) * qmul),
+                         ElemFp16::pack(ElemBf16::lo(w.w) * qmul, ElemBf16::hi(w.w) * qmul));
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sQ + TL::off(r, c, Lay::Q_ATOM)),
+                     "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Lay::B_QF));
+      return sl2;
+    };
+
+    uint32_t ph = 0;
+    TileUnit cur;
+    read_unit(0, cur);
+    float sl2 = 0.f;
+    if (!failed && !cur.stop) sl2 = load_q(cur);
+    for (uint32_t j = 0; !failed && !cur.stop; ++j) {
+      const int nk = nranges(cur);
+      const bool row_valid = qi < cur.npos;
+      const int lim = row_valid ? cur.pos0 + qi + 1 : 0;
+      float m_used = -INFINITY, l = 0.f;
+      for (int kt = 0; kt < nk; ++kt) {
+        const uint32_t gr = ph + kt;
+        const int ck0 = kt * kKeyTile + part * 64;
+        const uint32_t sp = tmem + lane_off + Tm::SP0 + (gr & 1u) * kKeyTile + part * 64;
+        wait_warp(bar(Lay::B_S + (gr & 1u)), (gr >> 1) & 1u, failed);
+        if (failed) break;
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32x2_wait(sp, s0, s1);
+        const float mx = fmaxf(masked_max32(s0, ck0, lim), masked_max32(s1, ck0 + 32, lim));
+        const float mo = exchange(mx);
+        if (failed) break;
+        const float cm = __fmul_rn(sl2, fmaxf(mx, mo));
+        const bool grow = cm > -INFINITY && (m_used == -INFINITY || __fsub_rn(cm, m_used) > kRescaleLog2);
+        float alpha = 1.f;
+        if (grow) {
+          alpha = m_used > -INFINITY ? ex2_approx(__fsub_rn(m_used, cm)) : 1.f;
+          m_used = cm;
+        }
+        const float ms = m_used == -INFINITY ? 0.f : m_used;
+        float sum = 0.f;
+        constexpr uint32_t PSTEP = SPLIT ? 16 : 8;
+        if (__any_sync(FULL, fabsf(ms) > 4096.f)) {
+          probs16_store<M, true, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
+          probs16_store<M, true, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+        } else {
+          probs16_store<M, false, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
+          probs16_store<M, false, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+        }
+        tmem_ld32_wait(sp + 32, s1);
+        if (__any_sync(FULL, fabsf(ms) > 4096.f)) {
+          probs16_store<M, true, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+          probs16_store<M, true, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
+        } else {
+          probs16_store<M, false, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+          probs16_store<M, false, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
+        }
+        // O holds P V(0 .. kt-1) once P V(kt-1) completes (S(kt) may have been
+        // issued before it): wait for it only when O must be rescaled
+        if (kt > 0 && __any_sync(FULL, alpha != 1.f)) {
+          wait_warp(bar(Lay::B_O), (gr - 1) & 1u, failed);
+          if (failed) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int ch = part * 4; ch < part * 4 + 4; ++ch) {
+            uint32_t t[32];
+            tmem_ld32_wait(tmem + lane_off + Tm::O + ch * 32, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st32u(tmem + lane_off + Tm::O + ch * 32, t);
+          }
+        }
+        l = l * alpha + sum;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Lay::B_P + (gr & 1u)));
+      }
+      if (failed) break;
+      TileUnit nxt;
+      read_unit(j + 1, nxt);
+      float nsl2 = sl2;
+      if (!failed && !nxt.stop) {
+        wait_warp(bar(Lay::B_QE), j & 1u, failed);
+        if (!failed) nsl2 = load_q(nxt);
+      }
+      if (failed) break;
+      if (nk > 0) {
+        const float lt = l + exchange(l);
+        wait_warp(bar(Lay::B_O), (ph + nk - 1) & 1u, failed);
+        if (failed) break;
+        tc_fence_after();
+        const float inv = lt > 0.f ? p.out_scale / lt : 0.f;
+        bf16 *dst = p.out + static_cast<int64_t>(cur.row0 + (row_valid ? qi : 0)) * p.num_heads * D +
+                    static_cast<int64_t>(cur.kvh * G + g) * D;
+#pragma unroll 1
+        for (int ch = part * 4; ch < part * 4 + 4; ++ch) {
+          uint32_t t[32];
+          tmem_ld32_wait(tmem + lane_off + Tm::O + ch * 32, t);
+          if (row_valid) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float *f = reinterpret_cast<const float *>(&t[8 * c]);
+              const uint4 v = make_uint4(E::pack(f[0] * inv, f[1] * inv), E::pack(f[2] * inv, f[3] * inv),
+                                         E::pack(f[4] * inv, f[5] * inv), E::pack(f[6] * inv, f[7] * inv));
+              *reinterpret_cast<uint4 *>(dst + ch * 32 + 8 * c) = v;
+            }
+          }
+        }
+        tc_fence_before();
+      }
+      ph += nk;
+      cur = nxt;
+      sl2 = nsl2;
+    }
+  }
+
+  if (warp == kMmaWarp && lane == 0) {
+    tc_commit(bar(Lay::B_DRAIN));
+    if (!mbar_wait_bounded(bar(Lay::B_DRAIN), 0, kTcWaitTimeoutNs)) failed = true;
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    const int landed = KV8 ? Lay::B_RAW : Lay::B_FULL;
+    for (uint32_t g = issued > SLOTS ? issued - SLOTS : 0; g < issued; ++g)
+      if (!mbar_wait_bounded(bar(landed + static_cast<int>(g % SLOTS)), (g / SLOTS) & 1u, kTcWaitTimeoutNs))
+        failed = true;
+  }
+  if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 template <int D, int G, typename E, bool KV8>
 cudaError_t launch_prefill_tiles(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &vmapb,
                                  const TileParams &tp, int sm_count, cudaStream_t stream) {
-  constexpr int smem = TcLayout<D>::REQUEST;
-  auto kern = prefill_tile_kernel<D, G, E, KV8>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (err != cudaSuccess) return err;
-  int64_t grid = sm_count;  // one CTA per SM: it holds all of the SM's tensor memory
-  const int64_t units = static_cast<int64_t>(tp.max_tiles) * tp.num_kv_heads;
-  if (grid > units) grid = units;
-  if (grid < 1) grid = 1;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? kTileThreads8 : kTileThreads), smem, stream,
-                    kmap, vmap, vmapb, tp);
+  if constexpr (D == kWideD) {
+    (void)vmapb;
+    constexpr int smem = WideLayout::BYTES;
+    auto kern = prefill_tile_wide_kernel<G, E, KV8>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+    int64_t grid = sm_count;
+    const int64_t units = static_cast<int64_t>(tp.max_tiles) * tp.num_kv_heads;
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kWideThreads), smem, stream, kmap, vmap, tp);
+  } else {
+    constexpr int smem = TcLayout<D>::REQUEST;
+    auto kern = prefill_tile_kernel<D, G, E, KV8>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+    int64_t grid = sm_count;  // one CTA per SM: it holds all of the SM's tensor memory
+    const int64_t units = static_cast<int64_t>(tp.max_tiles) * tp.num_kv_heads;
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? kTileThreads8 : kTileThreads), smem,
+                      stream, kmap, vmap, vmapb, tp);
+  }
 }
 
 #define PA_TILE_INST1(DD, GG, EE, K8)                                                                   \
@@ -1063,6 +1677,10 @@ PA_TILE_INST(80, 1)
 PA_TILE_INST(80, 2)
 PA_TILE_INST(80, 4)
 PA_TILE_INST(80, 8)
+PA_TILE_INST(256, 1)
+PA_TILE_INST(256, 2)
+PA_TILE_INST(256, 4)
+PA_TILE_INST(256, 8)
 #undef PA_TILE_INST
 #undef PA_TILE_INST1
 

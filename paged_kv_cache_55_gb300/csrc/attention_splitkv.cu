@@ -77,7 +77,7 @@ struct PlanParams {
   int32_t *tile_count;    // [1]
   int32_t *tile_counter;  // [1], zeroed here, consumed by the tile kernel
   int32_t max_tiles;
-  int32_t tile_pos;       // query positions per tile: kPrefillTileRows / G
+  int32_t tile_pos;       // query positions per tile: prefill_tile_rows(D) / G
   unsigned int *status;
 };
 
@@ -120,7 +120,7 @@ struct AttnParams {
 // ---------------------------------------------------------------------------
 // A request whose query rows fit one column group (query_len <= 8 / G: decode
 // tokens, speculative drafts) becomes split-KV decode items; a longer one
-// (a chunked-prefill chunk) becomes tensor-core tiles of kPrefillTileRows / G
+// (a chunked-prefill chunk) becomes tensor-core tiles of prefill_tile_rows / G
 // positions.
 // Returns the number of decode items; *ntiles receives the number of tiles.
 __device__ __forceinline__ int request_shape(const PlanParams &p, int b, int &q0, int &ql, int &L, int &np,
@@ -390,7 +390,7 @@ struct MergeParams {
 
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams p) {
-  // outputs per lane: 4 (D=128), 2 (D=64), else ceil(D / 32) consecutive
+  // outputs per lane: 8 (D=256), 4 (D=128), 2 (D=64), else ceil(D / 32) consecutive
   // elements with the lane's last ones past D unused (D = 80, 96)
   constexpr int EPL = (D + 31) / 32;
   constexpr bool VEC = D % 64 == 0;
@@ -420,12 +420,15 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
       if constexpr (!VEC) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) ov[j][e] = lane * EPL + e < D ? ld_cg(src + e) : 0.f;
-      } else if constexpr (EPL == 4) {
-        const float4 v = ld_cg(reinterpret_cast<const float4 *>(src));
-        ov[j][0] = v.x;
-        ov[j][1] = v.y;
-        ov[j][2] = v.z;
-        ov[j][3] = v.w;
+      } else if constexpr (EPL >= 4) {
+#pragma unroll
+        for (int e = 0; e < EPL; e += 4) {
+          const float4 v = ld_cg(reinterpret_cast<const float4 *>(src + e));
+          ov[j][e] = v.x;
+          ov[j][e + 1] = v.y;
+          ov[j][e + 2] = v.z;
+          ov[j][e + 3] = v.w;
+        }
       } else {
         const float2 v = ld_cg(reinterpret_cast<const float2 *>(src));
         ov[j][0] = v.x;
@@ -462,9 +465,11 @@ __global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams
         const uint32_t v = E::pack(acc[e] * inv, 0.f);
         *reinterpret_cast<unsigned short *>(dst + e) = static_cast<unsigned short>(v & 0xffffu);
       }
-  } else if constexpr (EPL == 4) {
-    *reinterpret_cast<uint2 *>(dst) =
-        make_uint2(E::pack(acc[0] * inv, acc[1] * inv), E::pack(acc[2] * inv, acc[3] * inv));
+  } else if constexpr (EPL >= 4) {
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4)
+      *reinterpret_cast<uint2 *>(dst + e) =
+          make_uint2(E::pack(acc[e] * inv, acc[e + 1] * inv), E::pack(acc[e + 2] * inv, acc[e + 3] * inv));
   } else {
     *reinterpret_cast<uint32_t *>(dst) = E::pack(acc[0] * inv, acc[1] * inv);
   }
@@ -536,14 +541,19 @@ struct TileGeom<D, false> {
 // consecutive rows read at one chunk hit eight different bank groups, and
 // rows 16..31 have the layout of rows 0..15 shifted by 16 * ROW bytes.
 constexpr int kTileKeys8 = 32;
+// head_dim 256: rows of two 128-code atoms, stored atom after atom (32 rows x
+// 128 bytes each), so chunk c of row r sits in atom c / 8.
 template <int D>
 struct TileGeom<D, true> {
-  static_assert(D <= 128, "8-bit tiles are one swizzle span wide");
-  static constexpr int ROW = D <= 64 ? 64 : 128;  // row bytes (head_dim 80, 96: padded, zero-filled by TMA)
-  static constexpr int TILE_BYTES = kTileKeys8 * ROW;
+  static_assert(D <= 256, "head dims up to 256");
+  static constexpr int ROW = D <= 64 ? 64 : 128;  // row bytes per atom (head_dim 80, 96: padded, zero-filled by TMA)
+  static constexpr int ATOMS = D > 128 ? D / 128 : 1;
+  static constexpr int ATOM_BYTES = kTileKeys8 * ROW;
+  static constexpr int TILE_BYTES = ATOMS * ATOM_BYTES;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static __device__ __forceinline__ uint32_t off(int r, int c) {
-    return ROW == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
+    return ROW == 128 ? (c >> 3) * ATOM_BYTES + r * 128 + (((c ^ r) & 7) << 4)
+                      : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
   }
 };
 
@@ -614,8 +624,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             z = (phys << p.block_shift) + (key & (bs - 1));
         }
         if constexpr (KV8) {
-          tma_load_3d(dst + j * box_rows * T::ROW, &kmap, bar, 0, U.kvh, z);
-          tma_load_3d(dst + T::TILE_BYTES + j * box_rows * T::ROW, &vmap, bar, 0, U.kvh, z);
+#pragma unroll
+          for (int a = 0; a < T::ATOMS; ++a) {
+            tma_load_3d(dst + a * T::ATOM_BYTES + j * box_rows * T::ROW, &kmap, bar, a * 128, U.kvh, z);
+            tma_load_3d(dst + T::TILE_BYTES + a * T::ATOM_BYTES + j * box_rows * T::ROW, &vmap, bar, a * 128,
+                        U.kvh, z);
+          }
         } else if (D == 128 && p.block_boxes) {
           // one box per cache holds both 64-element atoms of the tile's 16 rows,
           // atom after atom: the layout T::off addresses (one TMA instruction
@@ -1026,7 +1040,8 @@ bool workspace_layout(int32_t num_seqs, int32_t total_q, int32_t max_seq_len, in
   w.part_tokens = partition_tokens(num_seqs, max_seq_len, num_kv_heads, kv8);
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.part_tokens - 1) / w.part_tokens : 1;
   const int64_t items = static_cast<int64_t>(num_seqs) * w.max_parts;  // decode items: one group per request
-  const int64_t tiles = (static_cast<int64_t>(total_q) * G + kPrefillTileRows - 1) / kPrefillTileRows + num_seqs;
+  const int tile_rows = prefill_tile_rows(head_dim);
+  const int64_t tiles = (static_cast<int64_t>(total_q) * G + tile_rows - 1) / tile_rows + num_seqs;
   if (items * num_kv_heads > (1LL << 30) || tiles * num_kv_heads > (1LL << 30)) return false;
   w.max_items = static_cast<int32_t>(items > 0 ? items : 1);
   w.max_tiles = static_cast<int32_t>(tiles > 0 ? tiles : 1);
@@ -1113,6 +1128,12 @@ static bool encode_block_map(CUtensorMap *map, const void *cache, int64_t num_bl
 
 constexpr int kAttnWarps = 8;   // 16-bit caches: two warps per scheduler
 constexpr int kAttnWarps8 = 12; // 8-bit caches: three, to hide the latency of the per-tile widening
+// head_dim 256: a ring slot (K and V of one tile) is 16 KB, so four warps of
+// three slots fill the ring budget (192 KB in flight per SM, as at 128)
+template <int D, bool KV8>
+constexpr int decode_warps() {
+  return D == 256 ? 4 : (KV8 ? kAttnWarps8 : kAttnWarps);
+}
 
 template <int D, int G, typename E, bool KV8>
 static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, cudaStream_t stream,
@@ -1139,7 +1160,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   pp.tile_counter = pp.item_count + 3;
   pp.tiles = reinterpret_cast<int4 *>(ws + w.tiles);
   pp.max_tiles = w.max_tiles;
-  pp.tile_pos = kPrefillTileRows / G;
+  pp.tile_pos = prefill_tile_rows(D) / G;
   pp.status = a.status;
 
   CUtensorMap kmap, vmap;
@@ -1185,7 +1206,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
-  constexpr int NW = KV8 ? kAttnWarps8 : kAttnWarps;
+  constexpr int NW = decode_warps<D, KV8>();
   auto kern = splitkv_attention_kernel<D, G, NW, E, KV8>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -1273,6 +1294,7 @@ cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, int *laun
   PA_DISPATCH(64, 1) PA_DISPATCH(64, 2) PA_DISPATCH(64, 4) PA_DISPATCH(64, 8)
   PA_DISPATCH(96, 1) PA_DISPATCH(96, 2) PA_DISPATCH(96, 4) PA_DISPATCH(96, 8)
   PA_DISPATCH(80, 1) PA_DISPATCH(80, 2) PA_DISPATCH(80, 4) PA_DISPATCH(80, 8)
+  PA_DISPATCH(256, 1) PA_DISPATCH(256, 2) PA_DISPATCH(256, 4) PA_DISPATCH(256, 8)
 #undef PA_DISPATCH
   return cudaErrorInvalidValue;
 }

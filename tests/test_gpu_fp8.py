@@ -66,6 +66,11 @@ CASES = {
                           head_dim=64),
     "g2_d128_sharp_chunks": dict(context_lens=[700, 3000], query_lens=[200, 77], num_heads=8, num_kv_heads=4,
                                  head_dim=128, q_scale=8.0),
+    # head_dim 256: rows of two 128-code atoms (decode), units of half a row (tiles)
+    "g4_d256_mixed": dict(context_lens=[0, 700, 33, 1500, 20], query_lens=[1, 1, 2, 1, 150], num_heads=16,
+                          num_kv_heads=4, head_dim=256),
+    "g1_d256_chunks": dict(context_lens=[0, 1000, 5000], query_lens=[300, 130, 1], num_heads=4, num_kv_heads=4,
+                           head_dim=256),
 }
 
 
@@ -79,7 +84,7 @@ def test_fp8_cases(oracle, name, bs):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("head_dim", [64, 80, 96, 128])
+@pytest.mark.parametrize("head_dim", [64, 80, 96, 128, 256])
 def test_fp8_every_code_round_trips_exactly(dtype, head_dim):
     """seq_len 1: the output is the token's own V row. With v_scale = 2^-4 and V made of
     code values times 2^-4 (exact in bf16 and fp16), the scatter stores those codes and the

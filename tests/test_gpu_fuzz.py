@@ -18,7 +18,7 @@ def random_case(seed: int) -> W.Workload:
     rng = np.random.default_rng(1000 + seed)
     G = int(rng.choice([1, 2, 4, 8]))
     Hkv = int(rng.choice([1, 2, 4]))
-    D = int(rng.choice([64, 80, 96, 128]))
+    D = int(rng.choice([64, 80, 96, 128, 256]))
     bs = int(rng.choice([8, 16, 32]))
     dtype = str(rng.choice(["bf16", "fp16"]))
     B = int(rng.integers(1, 13))

@@ -100,6 +100,25 @@ SMALL_CASES = {
     "sharp_scores": dict(context_lens=[300, 1800, 4], query_lens=[1, 1, 9], num_heads=32, num_kv_heads=8,
                          head_dim=128, q_scale=8.0),
     "seq_len_one": dict(context_lens=[0, 0, 0], query_lens=[1, 1, 1], num_heads=8, num_kv_heads=2, head_dim=64),
+    # head_dim 256: decode (four warps per SM, 16 KB ring slots), split requests (merge of
+    # 8 outputs per lane), and the one-half tile kernel (128-row tiles, two score buffers)
+    "decode_g4_d256": dict(context_lens=[0, 700, 33, 1500, 2047], query_lens=[1] * 5, num_heads=16,
+                           num_kv_heads=4, head_dim=256),
+    "decode_g8_d256_long": dict(context_lens=[5000, 31, 0], query_lens=[1, 1, 1], num_heads=16, num_kv_heads=2,
+                                head_dim=256),
+    "chunks_g2_d256": dict(context_lens=[0, 300, 1000, 7], query_lens=[200, 1, 130, 3], num_heads=8,
+                           num_kv_heads=4, head_dim=256),
+    "chunks_g1_d256_sharp": dict(context_lens=[500, 0], query_lens=[140, 300], num_heads=4, num_kv_heads=4,
+                                 head_dim=256, q_scale=8.0),
+    "chunks_g8_d256": dict(context_lens=[10, 2000, 0], query_lens=[40, 1, 17], num_heads=16, num_kv_heads=2,
+                           head_dim=256),
+    "chunks_g4_d256": dict(context_lens=[0, 37, 600, 20, 1000], query_lens=[40, 2, 1, 129, 1], num_heads=16,
+                           num_kv_heads=4, head_dim=256),
+    "block8_chunks_g4_d256": dict(context_lens=[0, 37, 600, 20], query_lens=[40, 2, 1, 129], num_heads=8,
+                                  num_kv_heads=2, head_dim=256, block_size=8),
+    "block32_mixed_g2_d256": dict(context_lens=[130, 0, 999, 3000], query_lens=[389, 1, 70, 1], num_heads=8,
+                                  num_kv_heads=4, head_dim=256, block_size=32),
+    "seq_len_one_d256": dict(context_lens=[0, 0], query_lens=[1, 1], num_heads=4, num_kv_heads=2, head_dim=256),
 }
 
 
@@ -108,7 +127,7 @@ def test_growing_key_norms_rescale_within_ranges(oracle):
     # jump by more than 2^8 inside a 128-key range again and again, so the
     # probabilities already written for the range, O and the row sum are
     # rescaled mid-range (the prefill tile path; G = 4 and G = 1).
-    for heads, kv_heads, d in ((8, 2, 128), (4, 4, 64)):
+    for heads, kv_heads, d in ((8, 2, 128), (4, 4, 64), (8, 4, 256)):
         w = W.make_workload("growing_keys", context_lens=[0, 37], query_lens=[256, 200], num_heads=heads,
                             num_kv_heads=kv_heads, head_dim=d, seed=11, q_scale=2.0)
         k = W.bf16_bits_to_f32(w.key)
@@ -132,7 +151,7 @@ def test_small_cases(oracle, name):
 
 FP16_CASES = ["block8_mixed_chunks_g4_d128", "block32_decode_g8_d64", "ragged_decode_g4_d128", "decode_g8_d64", "decode_g1_d64", "mixed_chunks_g4_d128",
               "mixed_chunks_g1_d128", "mixed_chunks_g8_d64", "long_chunks_g2_d128", "sharp_long_chunks_g4_d128",
-              "empty_requests", "seq_len_one"]
+              "empty_requests", "seq_len_one", "chunks_g2_d256", "decode_g8_d256_long", "block32_mixed_g2_d256"]
 
 
 @pytest.mark.parametrize("name", FP16_CASES)
@@ -177,8 +196,9 @@ def test_shared_prefix_step(oracle):
     run_and_check(w, oracle)
 
 
-def test_seq_len_one_returns_v_row_exactly():
-    w = W.make_workload("one", seed=9, **SMALL_CASES["seq_len_one"])
+@pytest.mark.parametrize("case", ["seq_len_one", "seq_len_one_d256"])
+def test_seq_len_one_returns_v_row_exactly(case):
+    w = W.make_workload("one", seed=9, **SMALL_CASES[case])
     st = DeviceStep(w)
     st.run()
     out = bf16_to_numpy_bits(st.out)
