@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   const uint32_t base = smem_u32(smem_raw);
   if (base & 1023u) {  // the swizzled tiles need 1024-byte alignment; never touch misaligned tiles
     if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+    griddep_wait();  // completion still implies the decode kernel's
     return;
   }
   constexpr int SLOTS = Lay::SLOTS;
@@ -450,8 +451,12 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // No griddepcontrol.wait here: this kernel follows the split-KV decode
+  // kernel, which lets it start as its CTAs exit; it reads only what the
+  // kernels before that one wrote (the plan's tiles, q, the caches), all
+  // complete before the decode kernel let it start. It waits for the decode
+  // kernel at its end, so its own completion still orders later work.
   const uint32_t tmem = *tmem_base_s;
-  griddep_wait();
 
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;
@@ -1015,6 +1020,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         failed = true;
   }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
+  griddep_wait();  // the decode kernel before this one has completed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1098,6 +1104,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t base = smem_u32(smem_raw);
   if (base & 1023u) {
     if (tid == 0) flag_error(p.status, PA_FLAG_LENGTHS);
+    griddep_wait();
     return;
   }
   const uint32_t sQ = base, sRing = base + Lay::RING_OFF;
@@ -1140,8 +1147,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // No griddepcontrol.wait here: this kernel follows the split-KV decode
+  // kernel, which lets it start as its CTAs exit; it reads only what the
+  // kernels before that one wrote (the plan's tiles, q, the caches), all
+  // complete before the decode kernel let it start. It waits for the decode
+  // kernel at its end, so its own completion still orders later work.
   const uint32_t tmem = *tmem_base_s;
-  griddep_wait();
 
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;
@@ -1614,6 +1625,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         failed = true;
   }
   if (failed) flag_error(p.status, PA_FLAG_TIMEOUT);
+  griddep_wait();  // the decode kernel before this one has completed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

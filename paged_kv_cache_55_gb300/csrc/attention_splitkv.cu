@@ -104,6 +104,7 @@ struct AttnParams {
   float *part_o;    // [num_seqs][Hkv][max_parts][8][D]
   float *part_lse;  // [num_seqs][Hkv][max_parts][8]
   int32_t block_boxes;  // 1: 16-bit caches, head_dim 128, blocks of >= 16 tokens: one 4-D box per tile
+  int32_t tiles_follow; // 1: the prefill-tile kernel is launched after this one
   unsigned int *status;
 };
 
@@ -552,8 +553,8 @@ struct TileGeom<D, true> {
   static constexpr int TILE_BYTES = ATOMS * ATOM_BYTES;
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static __device__ __forceinline__ uint32_t off(int r, int c) {
-    return ROW == 128 ? (c >> 3) * ATOM_BYTES + r * 128 + (((c ^ r) & 7) << 4)
-                      : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
+    const uint32_t in_atom = ROW == 128 ? r * 128 + (((c ^ r) & 7) << 4) : r * 64 + (((c ^ (r >> 1)) & 3) << 4);
+    return ATOMS == 1 ? in_atom : (c >> 3) * ATOM_BYTES + in_atom;  // one atom: no atom term at all
   }
 };
 
@@ -592,6 +593,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   fence_mbar_init();
   __syncthreads();
   griddep_wait();  // the plan (and the cache scatter before it) must be complete
+  // When prefill tiles follow, they may be scheduled from now on: tile CTAs
+  // take over SMs as this kernel's CTAs exit, and read only what the kernels
+  // before this one wrote. (A merge kernel that follows directly is left to
+  // start after this kernel: resident early, its CTAs slowed the step.)
+  if (p.tiles_follow) griddep_launch_dependents();
 
   const int Hkv = p.num_kv_heads;
   const int total_units = min(max(ld_cg(p.item_count), 0), p.max_items) * Hkv;
@@ -1203,6 +1209,7 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
   ap.part_o = reinterpret_cast<float *>(ws + w.part_o);
   ap.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
   ap.block_boxes = block_boxes ? 1 : 0;
+  ap.tiles_follow = a.max_query_len > w.rows_per_item ? 1 : 0;
   ap.status = a.status;
 
   constexpr int smem = kSmemBudget + 1024;  // ring + alignment slack
