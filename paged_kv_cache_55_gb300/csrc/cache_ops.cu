@@ -188,7 +188,20 @@ __device__ __forceinline__ void rope_adjacent8(uint4 &a, const float *c, const f
   }
 }
 
-constexpr int kRopeMaxRot = 512;  // largest rotary_dim (the table row is staged in shared memory)
+constexpr int kRopeMaxRot = 512;  // largest rotary_dim (a table row is staged in shared memory per warp)
+constexpr int kRopeWarps = 8;     // tokens in flight per CTA (one per warp)
+
+// Four floats of a table written before this kernel (the rotary table may come
+// from an earlier kernel of the stream): a volatile, L1-cached load that the
+// compiler cannot hoist above griddep_wait (as it may an invariant load).
+__device__ __forceinline__ float4 ld_ca4(const float *p) {
+  float4 v;
+  asm volatile("ld.global.ca.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 
 // Eight elements -> eight E4M3 codes of x / scale (the quantiser of reshape_and_cache_fp8).
 template <typename E>
@@ -214,103 +227,139 @@ __global__ void __launch_bounds__(256) rope_reshape_and_cache_kernel(
     int64_t key_stride16, int64_t value_stride16, void *__restrict__ key_cache_v, void *__restrict__ value_cache_v,
     const int64_t *__restrict__ slot_mapping, const int64_t *__restrict__ positions,
     const float *__restrict__ cos_sin, int32_t max_position, int32_t rot, int32_t num_tokens, int32_t num_heads,
-    int32_t num_kv_heads, int32_t d16, int64_t num_slots, float k_scale, float v_scale, unsigned int *status) {
+    int32_t num_kv_heads, int32_t d16, int64_t num_slots, float k_scale, float v_scale, int32_t slices,
+    unsigned int *status) {
   // 16-bit caches: one 16-byte vector per 8-element chunk; 8-bit: one 8-byte vector
   uint4 *key_cache = static_cast<uint4 *>(key_cache_v), *value_cache = static_cast<uint4 *>(value_cache_v);
   uint2 *key_cache8 = static_cast<uint2 *>(key_cache_v), *value_cache8 = static_cast<uint2 *>(value_cache_v);
-  // One CTA per token at a time: the position, slot and table row are read
-  // once and shared, so the chunks of the token's rows need no dependent
-  // global loads.
-  __shared__ __align__(16) float tab[kRopeMaxRot];
-  __shared__ int64_t s_pos, s_slot;
   griddep_wait();
   griddep_launch_dependents();
-  const int32_t rows = num_heads + 2 * num_kv_heads;
-  const int32_t items = rows * d16;
   const int32_t half16 = rot / 16;  // chunks in one half of the rotated part (NEOX)
+  // Work items of a token: per q head the rotated chunks (NEOX: chunk c <
+  // half16 with its partner c + half16; GPT-J: chunk c < rot / 8); per K head
+  // those and the chunks past the rotated part; per V head every chunk.
+  const int32_t uq = NEOX ? half16 : rot / 8, uk = NEOX ? d16 - half16 : d16;
+  const int32_t kq = num_heads * uq, kk = kq + num_kv_heads * uk;
+  const int32_t items = kk + num_kv_heads * d16;
   const int64_t row16 = static_cast<int64_t>(num_kv_heads) * d16;
-  for (int32_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
-    if (threadIdx.x == 0) {
-      s_pos = ld_cg(reinterpret_cast<const long long *>(positions) + t);
-      s_slot = ld_cg(reinterpret_cast<const long long *>(slot_mapping) + t);
+
+  // One warp per (token, slice of its chunks), eight per CTA at a time (a
+  // step with few tokens splits each token's chunks into `slices` so that
+  // every SM has work), with no CTA-wide synchronisation: the lanes read the
+  // token's position and slot (one broadcast load each), stage its cos/sin
+  // row in the warp's own shared memory (L1-cached loads, issued after the
+  // wait above), and issue the loads of kBatch chunks each before they
+  // rotate and store any. A rotating chunk's thread also does its partner
+  // chunk, whichever slice that lies in.
+  constexpr int kBatch = 4;
+  __shared__ __align__(16) float tabs[kRopeWarps][kRopeMaxRot];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *tw = tabs[wid];
+  const int64_t units = static_cast<int64_t>(num_tokens) * slices;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kRopeWarps + wid; u < units;
+       u += static_cast<int64_t>(gridDim.x) * kRopeWarps) {
+    const int32_t t = static_cast<int32_t>(u / slices), sl = static_cast<int32_t>(u - static_cast<int64_t>(t) * slices);
+    const int32_t w_begin = static_cast<int32_t>(static_cast<int64_t>(items) * sl / slices);
+    const int32_t w_end = static_cast<int32_t>(static_cast<int64_t>(items) * (sl + 1) / slices);
+    const int64_t pos = ld_cg(reinterpret_cast<const long long *>(positions) + t);
+    const int64_t slot = ld_cg(reinterpret_cast<const long long *>(slot_mapping) + t);
+    if (!(pos >= 0 && pos < max_position)) {
+      if (lane == 0 && sl == 0) flag_error(status, PA_FLAG_POSITION_RANGE);
+      continue;
     }
-    __syncthreads();
-    const int64_t pos = s_pos, slot = s_slot;
-    const bool pos_ok = pos >= 0 && pos < max_position;
-    if (pos_ok) {
-      const float4 *row4 = reinterpret_cast<const float4 *>(cos_sin + pos * rot);
-      for (int32_t i = threadIdx.x; i < rot / 4; i += blockDim.x) reinterpret_cast<float4 *>(tab)[i] = __ldg(row4 + i);
-    } else if (threadIdx.x == 0) {
-      flag_error(status, PA_FLAG_POSITION_RANGE);
-    }
-    if (pos_ok && slot >= num_slots && threadIdx.x == 0) flag_error(status, PA_FLAG_SLOT_RANGE);
-    __syncthreads();
-    if (pos_ok) {
-      const bool cache_ok = slot >= 0 && slot < num_slots;  // slot < 0: padding token, nothing cached
-#pragma unroll 2
-      for (int32_t w = threadIdx.x; w < items; w += blockDim.x) {
-        const int32_t r = w / d16, c = w - r * d16;
-        // which chunks this thread rotates: NEOX chunk c < half16 with c + half16;
-        // GPT-J chunk c < rot / 8 on its own; chunks in [half16, 2 half16) (NEOX)
-        // belong to their partner's thread
-        const bool partner = NEOX && c >= half16 && c < 2 * half16;
-        const bool rotates = NEOX ? c < half16 : c < rot / 8;
-        float cf[8], sf[8];
-        if (rotates) {
-          const int base = NEOX ? 8 * c : 4 * c;  // first frequency index of this chunk
+    if (slot >= num_slots && lane == 0 && sl == 0) flag_error(status, PA_FLAG_SLOT_RANGE);
+    const bool cache_ok = slot >= 0 && slot < num_slots;  // slot < 0: padding token, nothing cached
+    __syncwarp();  // the warp's previous token is done with tw
+    for (int32_t i = lane; i < rot / 4; i += 32)
+      reinterpret_cast<float4 *>(tw)[i] = ld_ca4(cos_sin + pos * rot + 4 * i);
+    __syncwarp();
+    for (int32_t w0 = w_begin + lane; w0 < w_end; w0 += kBatch * 32) {
+      uint4 x[kBatch], y[kBatch];
+      int kind[kBatch];  // 0 nothing, 1 q head, 2 K head, 3 V head
+      // loads
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            cf[k] = (NEOX || k < 4) ? tab[base + k] : 0.f;
-            sf[k] = (NEOX || k < 4) ? tab[rot / 2 + base + k] : 0.f;
-          }
-        }
-        if (r < num_heads) {  // q head: in place
-          if (!rotates) continue;
-          uint4 *qrow = q + static_cast<int64_t>(t) * q_stride16 + static_cast<int64_t>(r) * d16;
-          uint4 x = ld_cg(qrow + c);
-          if (NEOX) {
-            uint4 y = ld_cg(qrow + c + half16);
-            rope_pair8<E>(x, y, cf, sf);
-            qrow[c + half16] = y;
-          } else {
-            rope_adjacent8<E>(x, cf, sf);
-          }
-          qrow[c] = x;
+      for (int k = 0; k < kBatch; ++k) {
+        const int32_t w = w0 + k * 32;
+        kind[k] = 0;
+        if (w >= w_end) continue;
+        // item -> (row kind, head, chunk); NEOX K items past the rotated pairs skip the partner chunks
+        if (w < kq) {  // q head: in place
+          const int32_t h = w / uq, c = w - h * uq;
+          const uint4 *qrow = q + static_cast<int64_t>(t) * q_stride16 + static_cast<int64_t>(h) * d16;
+          x[k] = ld_cg(qrow + c);
+          if (NEOX) y[k] = ld_cg(qrow + c + half16);
+          kind[k] = 1;
         } else if (!cache_ok) {
           continue;
-        } else if (r < num_heads + num_kv_heads) {  // K head: rotated into the cache
-          if (partner) continue;
-          const int32_t h = r - num_heads;
+        } else if (w < kk) {  // K head: rotated into the cache
+          const int32_t h = (w - kq) / uk, j = (w - kq) - h * uk;
+          const int32_t c = NEOX && j >= half16 ? j + half16 : j;
           const uint4 *src = key + static_cast<int64_t>(t) * key_stride16 + static_cast<int64_t>(h) * d16;
+          x[k] = ld_cg(src + c);
+          if (NEOX && c < half16) y[k] = ld_cg(src + c + half16);
+          kind[k] = 2;
+        } else {  // V head: copied
+          const int32_t h = (w - kk) / d16, c = (w - kk) - h * d16;
+          x[k] = ld_cg(value + static_cast<int64_t>(t) * value_stride16 + static_cast<int64_t>(h) * d16 + c);
+          kind[k] = 3;
+        }
+      }
+      // rotations and stores
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (kind[k] == 0) continue;
+        const int32_t w = w0 + k * 32;
+        int32_t h, c;
+        if (kind[k] == 1) {
+          h = w / uq;
+          c = w - h * uq;
+        } else if (kind[k] == 2) {
+          h = (w - kq) / uk;
+          const int32_t j = (w - kq) - h * uk;
+          c = NEOX && j >= half16 ? j + half16 : j;
+        } else {
+          h = (w - kk) / d16;
+          c = (w - kk) - h * d16;
+        }
+        const bool rotates = NEOX ? c < half16 : c < rot / 8;
+        if (rotates && kind[k] != 3) {
+          const int base = NEOX ? 8 * c : 4 * c;  // first frequency index of this chunk
+          float cf[8], sf[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            cf[e] = (NEOX || e < 4) ? tw[base + e] : 0.f;
+            sf[e] = (NEOX || e < 4) ? tw[rot / 2 + base + e] : 0.f;
+          }
+          if (NEOX)
+            rope_pair8<E>(x[k], y[k], cf, sf);
+          else
+            rope_adjacent8<E>(x[k], cf, sf);
+        }
+        if (kind[k] == 1) {
+          uint4 *qrow = q + static_cast<int64_t>(t) * q_stride16 + static_cast<int64_t>(h) * d16;
+          if (NEOX) qrow[c + half16] = y[k];
+          qrow[c] = x[k];
+        } else if (kind[k] == 2) {
           const int64_t dofs = slot * row16 + static_cast<int64_t>(h) * d16;
-          uint4 x = ld_cg(src + c);
-          if (rotates) {
-            if (NEOX) {
-              uint4 y = ld_cg(src + c + half16);
-              rope_pair8<E>(x, y, cf, sf);
-              if constexpr (KV8)
-                key_cache8[dofs + c + half16] = quantize8<E>(y, k_scale);
-              else
-                key_cache[dofs + c + half16] = y;
-            } else {
-              rope_adjacent8<E>(x, cf, sf);
-            }
+          if (NEOX && rotates) {
+            if constexpr (KV8)
+              key_cache8[dofs + c + half16] = quantize8<E>(y[k], k_scale);
+            else
+              key_cache[dofs + c + half16] = y[k];
           }
           if constexpr (KV8)
-            key_cache8[dofs + c] = quantize8<E>(x, k_scale);
+            key_cache8[dofs + c] = quantize8<E>(x[k], k_scale);
           else
-            key_cache[dofs + c] = x;
-        } else {  // V head: copied
-          const int32_t h = r - num_heads - num_kv_heads;
-          const uint4 x = ld_cg(value + static_cast<int64_t>(t) * value_stride16 + static_cast<int64_t>(h) * d16 + c);
+            key_cache[dofs + c] = x[k];
+        } else {
+          const int64_t dofs = slot * row16 + static_cast<int64_t>(h) * d16;
           if constexpr (KV8)
-            value_cache8[slot * row16 + static_cast<int64_t>(h) * d16 + c] = quantize8<E>(x, v_scale);
+            value_cache8[dofs + c] = quantize8<E>(x[k], v_scale);
           else
-            value_cache[slot * row16 + static_cast<int64_t>(h) * d16 + c] = x;
+            value_cache[dofs + c] = x[k];
         }
       }
     }
-    __syncthreads();  // the next token rewrites s_pos, s_slot and tab
   }
 }
 
@@ -368,15 +417,20 @@ cudaError_t launch_rope_reshape_and_cache(void *q, int64_t q_stride, const void 
                                           int32_t head_dim, int64_t num_slots, int32_t dtype, bool kv8, float k_scale,
                                           float v_scale, unsigned int *status, int sm_count, cudaStream_t stream) {
   const int32_t d16 = head_dim / 8;
-  int64_t g = static_cast<int64_t>(sm_count) * 8;  // CTAs (tokens in flight): 8 per SM
-  if (g > num_tokens) g = num_tokens;
+  // slices per token: enough (token, slice) units for about 24 warps per SM, at most 8 per token
+  const int64_t want = static_cast<int64_t>(sm_count) * 24;
+  int32_t slices = static_cast<int32_t>((want + num_tokens - 1) / (num_tokens > 0 ? num_tokens : 1));
+  slices = slices < 1 ? 1 : (slices > 8 ? 8 : slices);
+  int64_t g = static_cast<int64_t>(sm_count) * 4;  // CTAs of kRopeWarps units in flight: 4 per SM at most
+  const int64_t need = (static_cast<int64_t>(num_tokens) * slices + kRopeWarps - 1) / kRopeWarps;
+  if (g > need) g = need;
   const int grid = static_cast<int>(g < 1 ? 1 : g);
 #define PA_ROPE_LAUNCH(EE, NN, K8)                                                                                \
   return launch_pdl(rope_reshape_and_cache_kernel<EE, NN, K8>, dim3(grid), dim3(256), 0, stream,                  \
                     static_cast<uint4 *>(q), q_stride / 8, static_cast<const uint4 *>(key),                        \
                     static_cast<const uint4 *>(value), key_stride / 8, value_stride / 8, key_cache, value_cache,    \
                     slot_mapping, positions, cos_sin_cache, max_position, rotary_dim, num_tokens, num_heads,        \
-                    num_kv_heads, d16, num_slots, k_scale, v_scale, status);
+                    num_kv_heads, d16, num_slots, k_scale, v_scale, slices, status);
 #define PA_ROPE_KV(EE, NN) \
   if (kv8) PA_ROPE_LAUNCH(EE, NN, true) else PA_ROPE_LAUNCH(EE, NN, false)
   if (dtype == PA_FP16) {
