@@ -104,7 +104,9 @@ struct TcLayout {
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;   // Q of one half
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;             // one K or V range: a ring slot
   // mbarriers (8 bytes each): per ring slot full, empty, raw (8-bit codes
-  // landed) and conv (both converter warps hold a slot's codes); per half s
+  // landed; bf16 caches: V range g % kMaxSlots put back to bf16) and conv
+  // (8-bit caches: both converter warps hold a slot's codes; bf16 caches: V
+  // range g % kMaxSlots rewritten); per half s
   // (S complete), p (P written), o (P V complete), qf (Q stored), qe (the MMA
   // warp has seen qf); per unit slot uf (record published), ue (record read);
   // per (half, lane quadrant) the softmax pair's exchange; drain
@@ -114,7 +116,8 @@ struct TcLayout {
   static constexpr int B_X = B_UE + kUnitSlots, B_DRAIN = B_X + 4 * kHalves, NBARS = B_DRAIN + 1;
   static constexpr int XCH_BYTES = kHalves * kParts * kHalfRows * 4;  // one float per (half, part, row)
   static constexpr int UNIT_BYTES = kUnitSlots * 32;                  // records of eight ints
-  static constexpr int FIXED = kHalves * Q_BYTES + XCH_BYTES + UNIT_BYTES + 8 * NBARS + 16;
+  static constexpr int VF_BYTES = kMaxSlots * 8;                      // per V range and converter warp: kept bf16
+  static constexpr int FIXED = kHalves * Q_BYTES + XCH_BYTES + UNIT_BYTES + VF_BYTES + 8 * NBARS + 16;
   static constexpr int FIT = (227 * 1024 - FIXED) / KV_BYTES;
   static constexpr int SLOTS = FIT < kMaxSlots ? FIT : kMaxSlots;
   static_assert(SLOTS >= 4, "the ring holds at least K and V of two ranges");
@@ -122,7 +125,8 @@ struct TcLayout {
   static constexpr int RING_OFF = Q_OFF + kHalves * Q_BYTES;     // K(0), V(0), K(1), V(1), ... in SLOTS slots
   static constexpr int XCH_OFF = RING_OFF + SLOTS * KV_BYTES;    // the softmax pairs' exchange
   static constexpr int UNIT_OFF = XCH_OFF + XCH_BYTES;           // unit records
-  static constexpr int BAR_OFF = UNIT_OFF + UNIT_BYTES;
+  static constexpr int VF_OFF = UNIT_OFF + UNIT_BYTES;           // V range flags (bf16 V rewritten as fp16)
+  static constexpr int BAR_OFF = VF_OFF + VF_BYTES;
   static constexpr int TMEM_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int BYTES = TMEM_OFF + 16;
   // Shared memory requested per CTA: more than half an SM's, so that a second
@@ -345,6 +349,34 @@ __device__ __forceinline__ void probs16_store(const uint32_t *s, int k0, int lim
   if (SPLIT) tmem_st8u(col + 8, lv);
 }
 
+// P of one softmax warp's 64 keys of a range, from column sp of its lane:
+// scores s0 (keys 0-31) in registers, keys 32-63 read again into s1 after
+// the first 32 probabilities are stored (fewer live registers; P of the
+// first 32 keys never covers the columns of the second). PAIR: a bf16 hi +
+// lo pair per key, 16 columns per UMMA K step in place; else one fp16 P per
+// key, 8 columns per K step from sp.
+template <bool PAIR>
+__device__ __forceinline__ void range_probs(const uint32_t (&s0)[32], uint32_t (&s1)[32], uint32_t sp, int ck0,
+                                            int lim, float sl2, float ms, bool exact, float &sum) {
+  using PT = typename std::conditional<PAIR, ElemBf16, ElemFp16>::type;
+  constexpr uint32_t PSTEP = PAIR ? 16 : 8;
+  if (exact) {
+    probs16_store<PT, true, PAIR>(s0, ck0, lim, sl2, ms, sum, sp);
+    probs16_store<PT, true, PAIR>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+  } else {
+    probs16_store<PT, false, PAIR>(s0, ck0, lim, sl2, ms, sum, sp);
+    probs16_store<PT, false, PAIR>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+  }
+  tmem_ld32_wait(sp + 32, s1);
+  if (exact) {
+    probs16_store<PT, true, PAIR>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+    probs16_store<PT, true, PAIR>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
+  } else {
+    probs16_store<PT, false, PAIR>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
+    probs16_store<PT, false, PAIR>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
+  }
+}
+
 // Two 32-column loads of this thread's TMEM lane, then one wait.
 __device__ __forceinline__ void tmem_ld32x2_wait(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
   asm volatile(
@@ -365,6 +397,73 @@ struct TileUnit {
   int b, row0, npos, pos0, kv_end, kvh, stop;
 };
 
+// A bf16 V range in shared memory, rewritten by the two converter warps:
+// converter warp w takes its 16-byte chunks c = w * PER * 32 + lane + 32 i
+// (i < PER); the chunk at byte offset o holds key row key_of(o), and with
+// MASKED rows at or past nvalid are not the request's keys (they are zeroed).
+// A chunk all of whose values have magnitudes below 65536 (bf16 bits
+// 0x4780: no larger bf16 value rounds to a finite fp16 one; inf and NaN come
+// after it) is rewritten as fp16; the others stay bf16. Returns bit i set for
+// each chunk i that stayed bf16.
+template <int PER, bool MASKED, typename Mask, typename KeyOf>
+__device__ __forceinline__ Mask vrange_to_fp16(uint32_t sV, int c0, int nvalid, KeyOf key_of) {
+  constexpr int BATCH = 8;
+  static_assert(PER <= 8 * static_cast<int>(sizeof(Mask)) && PER % BATCH == 0, "a bit per chunk, whole batches");
+  Mask kept = 0;
+  // One batch of code, not unrolled: the twenty warps' hot loops share the
+  // SM's instruction cache, and unrolling this loop four times made the
+  // whole kernel 20 % slower.
+#pragma unroll 1
+  for (int b0 = 0; b0 < PER; b0 += BATCH) {
+    uint4 w[BATCH];
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i)
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                   : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w)
+                   : "r"(sV + 16u * static_cast<uint32_t>(c0 + 32 * (b0 + i))));
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const uint32_t o = 16u * static_cast<uint32_t>(c0 + 32 * (b0 + i));
+      const uint4 v = w[i];
+      const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                  __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu));
+      const bool big = max(m >> 16, m & 0xffffu) >= 0x4780u;
+      const bool zero = MASKED && key_of(o) >= nvalid;
+      uint4 h = make_uint4(0u, 0u, 0u, 0u);
+      if (!zero)
+        h = make_uint4(ElemFp16::pack(bf16_lo(v.x), bf16_hi(v.x)), ElemFp16::pack(bf16_lo(v.y), bf16_hi(v.y)),
+                       ElemFp16::pack(bf16_lo(v.z), bf16_hi(v.z)), ElemFp16::pack(bf16_lo(v.w), bf16_hi(v.w)));
+      if (zero || !big)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sV + o), "r"(h.x), "r"(h.y), "r"(h.z),
+                     "r"(h.w)
+                     : "memory");
+      else
+        kept |= static_cast<Mask>(1) << (b0 + i);
+    }
+  }
+  return kept;
+}
+
+// Back to bf16: the chunks vrange_to_fp16 rewrote (not in `kept`, not
+// zeroed). Exact for every value of magnitude 2^-17 or more (and zero); a
+// smaller one comes back within 2^-25 of the value it was.
+template <int PER, bool MASKED, typename Mask, typename KeyOf>
+__device__ __forceinline__ void vrange_back_to_bf16(uint32_t sV, int c0, int nvalid, Mask kept, KeyOf key_of) {
+#pragma unroll 4
+  for (int i = 0; i < PER; ++i) {
+    const uint32_t o = 16u * static_cast<uint32_t>(c0 + 32 * i);
+    if (((kept >> i) & 1u) || (MASKED && key_of(o) >= nvalid)) continue;
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(sV + o));
+    v = make_uint4(pack_bf16x2(ElemFp16::lo(v.x), ElemFp16::hi(v.x)), pack_bf16x2(ElemFp16::lo(v.y), ElemFp16::hi(v.y)),
+                   pack_bf16x2(ElemFp16::lo(v.z), ElemFp16::hi(v.z)), pack_bf16x2(ElemFp16::lo(v.w), ElemFp16::hi(v.w)));
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(sV + o), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
 // 8-bit caches (KV8): the producer stages a range's codes in the back half of
 // its ring slot (kKeyTile x D bytes, the TMA boxes' own 128- or 64-byte
 // swizzle); two converter warps load them, meet at the slot's conv barrier
@@ -373,15 +472,26 @@ struct TileUnit {
 // full barrier. The tensor cores then take fp16 operands whatever q is: a
 // bf16 Q row is stored as fp16, scaled first by a power of two when its
 // largest |q| reaches 2^15, and its row's softmax factor is scaled back.
+//
+// bf16 caches (VCONV): S takes bf16 Q and K as they are; V is rewritten as
+// fp16 in place, so that P is one fp16 value per key (11 significant bits)
+// instead of a bf16 hi + lo pair, halving the P V products. Each V range is
+// rewritten by both converter warps in one pass: every value of magnitude
+// below 65536 is an fp16 value (exactly so from 2^-17 up, within 2^-25
+// below). A range holding a larger magnitude (or inf, NaN) is put back to
+// bf16 and its flags send the softmax warps and the MMA warp to the hi + lo
+// pair for that range. Either way the rows past the unit's last key are
+// zeroed.
 template <int D, int G, typename E, bool KV8>
-// Twenty warps (two of them idle over 16-bit caches), one CTA per SM.
+// Twenty warps (two of them idle over fp16 caches), one CTA per SM.
 __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     prefill_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const __grid_constant__ CUtensorMap vmapb, const TileParams p) {
   using Lay = TcLayout<D>;
   using Tm = TcTmem<D>;
-  using M = typename std::conditional<KV8, ElemFp16, E>::type;  // tensor-core operand type
-  constexpr bool SPLIT = std::is_same<M, ElemBf16>::value;      // P as a hi + lo pair (bf16 operands only)
+  using M = typename std::conditional<KV8, ElemFp16, E>::type;  // operand type of S = Q K^T
+  constexpr bool VCONV = !KV8 && std::is_same<E, ElemBf16>::value;  // bf16 V rewritten as fp16
+  // P and V are fp16 in every case but a bf16 range that does not fit fp16 (P then a bf16 hi + lo pair)
   // V staged one cache block per box, both atoms (4-D map): 16-bit caches at head_dim 128
   constexpr bool VBLK = D == 128 && !KV8;
   constexpr int NTHREADS = KV8 ? kTileThreads8 : kTileThreads;
@@ -395,7 +505,8 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   constexpr int PART_KEYS = kKeyTile / kParts;  // keys of a range per softmax warp
   constexpr int NCH = (D + 31) / 32;            // 32-column chunks of O (head_dim 80: 16 padding columns)
   constexpr uint32_t IDESC_S = f16_idesc(kHalfRows, kKeyTile, 0, M::kUmmaFormat);
-  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, M::kUmmaFormat);
+  constexpr uint32_t IDESC_O = f16_idesc(kHalfRows, D, 1, ElemFp16::kUmmaFormat);
+  constexpr uint32_t IDESC_OB = f16_idesc(kHalfRows, D, 1, ElemBf16::kUmmaFormat);  // a range kept bf16
   // O stays in TMEM and is rescaled only when a row's running maximum grows
   // by more than 2^8 (log2 domain); in between, probabilities are taken
   // against the older maximum and stay below 256.
@@ -417,6 +528,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem_raw + Lay::TMEM_OFF);
   volatile int *units = reinterpret_cast<volatile int *>(smem_raw + Lay::UNIT_OFF);
   volatile float *xch = reinterpret_cast<volatile float *>(smem_raw + Lay::XCH_OFF);
+  volatile int *vkeep = reinterpret_cast<volatile int *>(smem_raw + Lay::VF_OFF);  // bf16 V range kept bf16
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
@@ -427,8 +539,9 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
       // full: the producer's TMA (16-bit caches) or one arrival per converter warp (8-bit)
       mbar_init(bar(Lay::B_FULL + i), KV8 ? kConvWarps : 1);
       mbar_init(bar(Lay::B_EMPTY + i), 1);  // the MMA warp's commit after the range's last product
-      mbar_init(bar(Lay::B_RAW + i), 1);
-      mbar_init(bar(Lay::B_CONV + i), 32 * kConvWarps);
+      // bf16 caches: conv and raw count one arrival per converter warp
+      mbar_init(bar(Lay::B_RAW + i), KV8 ? 1 : kConvWarps);
+      mbar_init(bar(Lay::B_CONV + i), KV8 ? 32 * kConvWarps : kConvWarps);
     }
     for (int h = 0; h < kHalves; ++h) {
       mbar_init(bar(Lay::B_S + h), 1);
@@ -439,7 +552,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     }
     for (int i = 0; i < kUnitSlots; ++i) {
       mbar_init(bar(Lay::B_UF + i), 1);
-      mbar_init(bar(Lay::B_UE + i), 1 + kSoftmaxWarps + (KV8 ? kConvWarps : 0));
+      mbar_init(bar(Lay::B_UE + i), 1 + kSoftmaxWarps + (KV8 || VCONV ? kConvWarps : 0));
     }
     for (int i = 0; i < 4 * kHalves; ++i) mbar_init(bar(Lay::B_X + i), 32 * kParts);
     mbar_init(bar(Lay::B_DRAIN), 1);
@@ -668,6 +781,64 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         }
         if (failed) break;
       }
+    } else if constexpr (VCONV) {
+      // bf16 V ranges rewritten as fp16 in place, each by both converter
+      // warps (half of its chunks each; one warp per range, the two taking
+      // alternate ranges, measured 5 % slower). Range g (counted over the
+      // CTA's units) uses conv barrier and flags g % kMaxSlots (the ring
+      // keeps the converters fewer ranges ahead): each warp writes its flag
+      // (a chunk stayed bf16) and arrives; the warps then read both flags,
+      // and if either is set they put their fp16 chunks back to bf16 and
+      // arrive on the range's raw barrier, which readers wait for only then.
+      constexpr int PER = Lay::KV_BYTES / 16 / (32 * kConvWarps);  // chunks per lane
+      using Mask = uint32_t;
+      const int cw = warp - kConvWarp;
+      const int c0 = cw * PER * 32 + lane;
+      auto key_of = [&](uint32_t o) -> int {  // key row of the chunk at byte offset o of a V slot
+        if constexpr (VBLK)
+          return static_cast<int>(((o >> (vshift + 8)) << vshift) + ((o >> 7) & static_cast<uint32_t>(bs - 1)));
+        else
+          return static_cast<int>((o >> 7) & static_cast<uint32_t>(kKeyTile - 1));
+      };
+      uint32_t j = 0, ring = 0, gv = 0;
+      for (;;) {
+        TileUnit r;
+        read_unit(j++, r);
+        if (failed || r.stop) break;
+        int dummy[kHalves];
+        const int nkt = ranges(r, dummy);
+        for (int kt = 0; kt < nkt && !failed; ++kt, ++gv) {
+          const uint32_t pos = ring + 2 * kt + 1, slot = pos % SLOTS;  // V(kt) in the load ring
+          wait_warp(bar(Lay::B_FULL + slot), (pos / SLOTS) & 1u, failed);
+          if (failed) break;
+          const uint32_t sV = sRing + slot * Lay::KV_BYTES;
+          const int nvalid = min(r.kv_end - kt * kKeyTile, kKeyTile);
+          const bool masked = nvalid < kKeyTile;
+          const Mask kept = masked ? vrange_to_fp16<PER, true, Mask>(sV, c0, nvalid, key_of)
+                                   : vrange_to_fp16<PER, false, Mask>(sV, c0, nvalid, key_of);
+          const bool any_kept = __any_sync(FULL, kept != 0);
+          const uint32_t fi = gv % kMaxSlots;
+          fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+          __syncwarp();
+          if (lane == 0) {
+            vkeep[2 * fi + cw] = any_kept ? 1 : 0;
+            mbar_arrive(bar(Lay::B_CONV + fi));  // release: the flag and the rows
+          }
+          wait_warp(bar(Lay::B_CONV + fi), (gv / kMaxSlots) & 1u, failed);
+          if (failed) break;
+          if (vkeep[2 * fi] | vkeep[2 * fi + 1]) {
+            if (masked)
+              vrange_back_to_bf16<PER, true>(sV, c0, nvalid, kept, key_of);
+            else
+              vrange_back_to_bf16<PER, false>(sV, c0, nvalid, kept, key_of);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Lay::B_RAW + fi));
+        }
+        ring += 2 * nkt;
+        if (failed) break;
+      }
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue ----------------
@@ -736,12 +907,21 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
       }
       for (int kt = 0; kt < nkt && !failed; ++kt) {
         const uint32_t vslot = slot_of(kt, 1);
+        bool vpair = false;  // this range's V kept bf16: P as a hi + lo pair
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
           if (kt >= nkt_h[h]) continue;
           wait_warp(bar(Lay::B_P + h), (ph[h] + kt) & 1u, failed);  // P(kt) is in place
           if (failed) break;
-          if (h == first_reader(kt)) {
+          if (VCONV && h == first_reader(kt)) {
+            // the converter warp has rewritten V(kt) (and zeroed the rows past the last key)
+            const uint32_t gv = ring0 / 2 + kt, fi = gv % kMaxSlots;
+            wait_warp(bar(Lay::B_CONV + fi), (gv / kMaxSlots) & 1u, failed);
+            if (failed) break;
+            vpair = (vkeep[2 * fi] | vkeep[2 * fi + 1]) != 0;
+            if (vpair) wait_warp(bar(Lay::B_RAW + fi), (gv / kMaxSlots) & 1u, failed);  // back in bf16
+            if (failed) break;
+          } else if (h == first_reader(kt)) {
             wait_warp(bar(Lay::B_FULL + vslot), full_parity(kt, 1), failed);
             if (failed) break;
             const int key0 = kt * kKeyTile;
@@ -763,17 +943,28 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
             tc_fence_after();
             const uint32_t vlo = v_lo + vslot * SLOT_STEP;
             const uint32_t t = tmem + h * Tm::HALF;
-            // P of K step ks: SPLIT hi at 16 ks, lo at 16 ks + 8; else 8 ks (+ 32 for the second part's keys)
-            auto pcol = [](int ks) { return SPLIT ? 16 * ks : 8 * ks + (ks >= 4 ? 32 : 0); };
-            if (kt == 0)
-              mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);  // the unit's first product overwrites O
-            else
-              mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);
-            if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, v_hi, IDESC_O);
+            if (!vpair) {
+              // one fp16 P per key: K step ks at column 8 ks (+ 32 for the second part's keys)
+              auto pcol = [](int ks) { return 8 * ks + (ks >= 4 ? 32 : 0); };
+              if (kt == 0)
+                mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);  // the unit's first product overwrites O
+              else
+                mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_O);
 #pragma unroll
-            for (int ks = 1; ks < KSTEPS_O; ++ks) {
-              mma_ts<1>(t + Tm::O, t + Tm::SP + pcol(ks), vlo + vks[ks], v_hi, IDESC_O);
-              if (SPLIT) mma_ts<1>(t + Tm::O, t + Tm::SP + pcol(ks) + 8, vlo + vks[ks], v_hi, IDESC_O);
+              for (int ks = 1; ks < KSTEPS_O; ++ks)
+                mma_ts<1>(t + Tm::O, t + Tm::SP + pcol(ks), vlo + vks[ks], v_hi, IDESC_O);
+            } else {
+              // a bf16 hi + lo pair per key: K step ks at columns 16 ks (hi) and 16 ks + 8 (lo)
+              if (kt == 0)
+                mma_ts<0>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_OB);
+              else
+                mma_ts<1>(t + Tm::O, t + Tm::SP, vlo, v_hi, IDESC_OB);
+              mma_ts<1>(t + Tm::O, t + Tm::SP + 8, vlo, v_hi, IDESC_OB);
+#pragma unroll
+              for (int ks = 1; ks < KSTEPS_O; ++ks) {
+                mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks, vlo + vks[ks], v_hi, IDESC_OB);
+                mma_ts<1>(t + Tm::O, t + Tm::SP + 16 * ks + 8, vlo + vks[ks], v_hi, IDESC_OB);
+              }
             }
             tc_commit(bar(Lay::B_O + h));
             if (h == last_reader(kt)) tc_commit(bar(Lay::B_EMPTY + vslot));
@@ -819,6 +1010,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     const int ch0 = part ? (NCH + 1) / 2 : 0, ch1 = part ? NCH : (NCH + 1) / 2;  // this warp's O chunks
     const int g = r % G;
     uint32_t phh = 0;  // ranges this half has run so far
+    uint32_t gvs = 0;  // ranges of the CTA's earlier units (both halves)
 
     // Q of the half for unit `u`: this warp stores its half of the row's 16-byte
     // chunks (row r = (position, head), K-major, swizzled); returns the row's
@@ -887,7 +1079,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
     if (!failed && !cur.stop) sl2 = load_q(cur);
     for (uint32_t j = 0; !failed && !cur.stop; ++j) {
       int nkt_h[kHalves];
-      ranges(cur, nkt_h);
+      const int nkt_all = ranges(cur, nkt_h);
       const int nk = nkt_h[h];
       const int qi = h * POS_PER_HALF + r / G;
       const bool row_valid = qi < cur.npos;
@@ -918,28 +1110,18 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         const float ms = m_used == -INFINITY ? 0.f : m_used;
         float sum = 0.f;
         const bool exact = __any_sync(FULL, fabsf(ms) > 4096.f);
-        // P over the scores it came from, one UMMA K step (16 keys) at a time:
-        // SPLIT, 16 columns per step in place; single pairs, 8 columns per step
-        // from the start of this warp's columns
-        // (the second 32 scores are read again after the first 32 probabilities
-        // are stored, which keeps a thread's live registers within budget; P of
-        // the first 32 keys never covers the columns of the second)
-        constexpr uint32_t PSTEP = SPLIT ? 16 : 8;
-        if (exact) {
-          probs16_store<M, true, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
-          probs16_store<M, true, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
-        } else {
-          probs16_store<M, false, SPLIT>(s0, ck0, lim, sl2, ms, sum, sp);
-          probs16_store<M, false, SPLIT>(s0 + 16, ck0 + 16, lim, sl2, ms, sum, sp + PSTEP);
+        bool vpair = false;  // V(kt) kept bf16 (bf16 caches only): P as a hi + lo pair
+        if constexpr (VCONV) {
+          const uint32_t gv = gvs + kt, fi = gv % kMaxSlots;
+          wait_warp(bar(Lay::B_CONV + fi), (gv / kMaxSlots) & 1u, failed);
+          if (failed) break;
+          vpair = (vkeep[2 * fi] | vkeep[2 * fi + 1]) != 0;
         }
-        tmem_ld32_wait(sp + 32, s1);
-        if (exact) {
-          probs16_store<M, true, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
-          probs16_store<M, true, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
-        } else {
-          probs16_store<M, false, SPLIT>(s1, ck0 + 32, lim, sl2, ms, sum, sp + 2 * PSTEP);
-          probs16_store<M, false, SPLIT>(s1 + 16, ck0 + 48, lim, sl2, ms, sum, sp + 3 * PSTEP);
-        }
+        // P over the scores it came from, one UMMA K step (16 keys) at a time
+        if (vpair)
+          range_probs<true>(s0, s1, sp, ck0, lim, sl2, ms, exact, sum);
+        else
+          range_probs<false>(s0, s1, sp, ck0, lim, sl2, ms, exact, sum);
         // O holds P V(0 .. kt-1), all complete (they were issued before S(kt),
         // whose completion the wait above observed); each warp rescales its
         // own columns.
@@ -999,6 +1181,7 @@ __global__ void __launch_bounds__(KV8 ? kTileThreads8 : kTileThreads, 1)
         tc_fence_before();  // O is overwritten by a later unit's first product
       }
       phh += nk;
+      gvs += nkt_all;
       cur = nxt;
       sl2 = nsl2;
     }

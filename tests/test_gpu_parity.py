@@ -395,3 +395,24 @@ def test_large_fp16_scores_in_prefill_tiles(oracle):
     w = W.make_workload("large_scores_fp16", context_lens=[900, 0, 2100], query_lens=[150, 300, 1],
                         num_heads=32, num_kv_heads=8, head_dim=128, q_scale=300.0, seed=21, dtype="fp16")
     run_and_check(w, oracle)
+
+
+@pytest.mark.parametrize("head_dim,block_size", [(128, 16), (128, 8), (128, 32), (96, 16), (64, 16)])
+def test_bf16_values_beyond_fp16_in_prefill_tiles(oracle, head_dim, block_size):
+    """bf16 V rows holding magnitudes that no fp16 value reaches (65536 up to 1e30): the
+    tensor-core tiles keep those key ranges in bf16 (P as a hi + lo pair) and rewrite the
+    other ranges of the same tiles as fp16; 65280, the largest bf16 value below 65504, stays
+    on the fp16 path."""
+    w = W.make_workload("big_v", context_lens=[700, 300, 0], query_lens=[200, 250, 130], num_heads=16,
+                        num_kv_heads=4, head_dim=head_dim, block_size=block_size, seed=23)
+    rng = np.random.default_rng(5)
+    bs, D = w.block_size, w.head_dim
+    vc = w.value_cache.reshape(-1, w.num_kv_heads, D)
+    for pos in (260, 300, 301):  # request 0, its third range of 128 keys
+        slot = int(w.block_tables[0, pos // bs]) * bs + pos % bs
+        vc[slot, 1] = W.f32_to_bf16_bits((rng.standard_normal(D) * 1e5).astype(np.float32))
+    slot = int(w.block_tables[0, 40 // bs]) * bs + 40 % bs  # its first range: 65280 fits fp16
+    vc[slot, 3, :2] = W.f32_to_bf16_bits(np.array([65280.0, -65280.0], np.float32))
+    row = int(w.query_start_loc[1]) + 7  # request 1, a new V row at position 307
+    w.value[row, 2, :5] = W.f32_to_bf16_bits(np.array([7e4, -3e6, 1e30, 65280.0, -65536.0], np.float32))
+    run_and_check(w, oracle)
