@@ -372,10 +372,15 @@ struct Unit {
 
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of the partitions of split requests, after the attention
-// kernel (PDL: launched early, waits for it). One CTA per (request, KV head),
-// one warp per column; each lane owns D/32 outputs and reads the partitions
-// eight at a time with independent loads, keeping a running maximum so one
-// pass suffices. Partitions are summed in order.
+// kernel (PDL: launched early, waits for it). One CTA of four warps per
+// (request, KV head), or of eight when there are few such pairs; warp w
+// merges columns w and w + 4 (a decode request's G columns are the first G,
+// one warp each); the request's partition count
+// and query rows are loaded together, then each lane reads its D/32 outputs
+// of the partitions eight at a time with independent loads, keeping a
+// running maximum so one pass suffices. Partitions are summed in order. (A
+// CTA of eight warps, one per column, holds 60 registers x 256 threads: four
+// CTAs per SM, 3.4 waves at batch 256 x 8 KV heads.)
 // ---------------------------------------------------------------------------
 struct MergeParams {
   const int32_t *query_start_loc;
@@ -389,90 +394,97 @@ struct MergeParams {
   bf16 *out;
 };
 
-template <int D, int G, typename E>
-__global__ void __launch_bounds__(kCols * 32) lse_merge_kernel(const MergeParams p) {
+// NW warps per CTA (columns w, w + NW, ...): four when the (request, KV
+// head) pairs are many (more CTAs per SM), eight when they fit one wave of
+// eight-warp CTAs (the columns in parallel).
+template <int D, int G, typename E, int NW>
+__global__ void __launch_bounds__(NW * 32, (D > 128 ? 4 : 8) * 4 / NW) lse_merge_kernel(const MergeParams p) {
   // outputs per lane: 8 (D=256), 4 (D=128), 2 (D=64), else ceil(D / 32) consecutive
   // elements with the lane's last ones past D unused (D = 80, 96)
   constexpr int EPL = (D + 31) / 32;
   constexpr bool VEC = D % 64 == 0;
   griddep_wait();
   const int b = blockIdx.x / p.num_kv_heads, kvh = blockIdx.x - b * p.num_kv_heads;
-  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // independent loads, one round trip
   const int np = ld_cg(p.nparts + b);
-  if (np <= 1 || np > p.max_parts) return;
   const int q0 = ld_cg(p.query_start_loc + b);
   const int ql = ld_cg(p.query_start_loc + b + 1) - q0;
-  const int qi = col / G, g = col % G;
-  if (qi >= ql) return;
-  const int64_t base = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.max_parts * kCols + col;
-  // one pass with a running maximum (every lane holds the same values)
-  float M = -INFINITY;
-  float acc[EPL];
+  if (np <= 1 || np > p.max_parts) return;
+#pragma unroll 1
+  for (int col = warp; col < kCols; col += NW) {
+    const int qi = col / G, g = col % G;
+    if (qi >= ql) break;  // columns run over query rows in order
+    const int64_t base = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.max_parts * kCols + col;
+    // one pass with a running maximum (every lane holds the same values)
+    float M = -INFINITY;
+    float acc[EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int k0 = 0; k0 < np; k0 += 8) {
-    float lv[8], ov[8][EPL];
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    for (int k0 = 0; k0 < np; k0 += 8) {
+      float lv[8], ov[8][EPL];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int k = min(k0 + j, np - 1);
-      lv[j] = ld_cg(p.part_lse + base + k * kCols);
-      const float *src = p.part_o + (base + k * kCols) * D + lane * EPL;
-      if constexpr (!VEC) {
+      for (int j = 0; j < 8; ++j) {
+        const int k = min(k0 + j, np - 1);
+        lv[j] = ld_cg(p.part_lse + base + k * kCols);
+        const float *src = p.part_o + (base + k * kCols) * D + lane * EPL;
+        if constexpr (!VEC) {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) ov[j][e] = lane * EPL + e < D ? ld_cg(src + e) : 0.f;
-      } else if constexpr (EPL >= 4) {
+          for (int e = 0; e < EPL; ++e) ov[j][e] = lane * EPL + e < D ? ld_cg(src + e) : 0.f;
+        } else if constexpr (EPL >= 4) {
 #pragma unroll
-        for (int e = 0; e < EPL; e += 4) {
-          const float4 v = ld_cg(reinterpret_cast<const float4 *>(src + e));
-          ov[j][e] = v.x;
-          ov[j][e + 1] = v.y;
-          ov[j][e + 2] = v.z;
-          ov[j][e + 3] = v.w;
+          for (int e = 0; e < EPL; e += 4) {
+            const float4 v = ld_cg(reinterpret_cast<const float4 *>(src + e));
+            ov[j][e] = v.x;
+            ov[j][e + 1] = v.y;
+            ov[j][e + 2] = v.z;
+            ov[j][e + 3] = v.w;
+          }
+        } else {
+          const float2 v = ld_cg(reinterpret_cast<const float2 *>(src));
+          ov[j][0] = v.x;
+          ov[j][1] = v.y;
         }
-      } else {
-        const float2 v = ld_cg(reinterpret_cast<const float2 *>(src));
-        ov[j][0] = v.x;
-        ov[j][1] = v.y;
+      }
+      float Mn = M;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (k0 + j < np) Mn = fmaxf(Mn, lv[j]);
+      const float Ms = Mn == -INFINITY ? 0.f : Mn;
+      const float r = ex2_approx(M - Ms);  // rescale what was summed so far (0 on the first pack)
+      wsum *= r;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] *= r;
+      M = Mn;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j < np) {
+          const float w = ex2_approx(lv[j] - Ms);
+          wsum += w;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] += w * ov[j][e];
+        }
       }
     }
-    float Mn = M;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    bf16 *dst = p.out + static_cast<int64_t>(q0 + qi) * p.num_heads * D + static_cast<int64_t>(kvh * G + g) * D +
+                lane * EPL;
+    if constexpr (!VEC) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (k0 + j < np) Mn = fmaxf(Mn, lv[j]);
-    const float Ms = Mn == -INFINITY ? 0.f : Mn;
-    const float r = ex2_approx(M - Ms);  // rescale what was summed so far (0 on the first pack)
-    wsum *= r;
+      for (int e = 0; e < EPL; ++e)
+        if (lane * EPL + e < D) {
+          const uint32_t v = E::pack(acc[e] * inv, 0.f);
+          *reinterpret_cast<unsigned short *>(dst + e) = static_cast<unsigned short>(v & 0xffffu);
+        }
+    } else if constexpr (EPL >= 4) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] *= r;
-    M = Mn;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (k0 + j < np) {
-        const float w = ex2_approx(lv[j] - Ms);
-        wsum += w;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] += w * ov[j][e];
-      }
+      for (int e = 0; e < EPL; e += 4)
+        *reinterpret_cast<uint2 *>(dst + e) =
+            make_uint2(E::pack(acc[e] * inv, acc[e + 1] * inv), E::pack(acc[e + 2] * inv, acc[e + 3] * inv));
+    } else {
+      *reinterpret_cast<uint32_t *>(dst) = E::pack(acc[0] * inv, acc[1] * inv);
     }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  bf16 *dst = p.out + static_cast<int64_t>(q0 + qi) * p.num_heads * D + static_cast<int64_t>(kvh * G + g) * D +
-              lane * EPL;
-  if constexpr (!VEC) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      if (lane * EPL + e < D) {
-        const uint32_t v = E::pack(acc[e] * inv, 0.f);
-        *reinterpret_cast<unsigned short *>(dst + e) = static_cast<unsigned short>(v & 0xffffu);
-      }
-  } else if constexpr (EPL >= 4) {
-#pragma unroll
-    for (int e = 0; e < EPL; e += 4)
-      *reinterpret_cast<uint2 *>(dst + e) =
-          make_uint2(E::pack(acc[e] * inv, acc[e + 1] * inv), E::pack(acc[e + 2] * inv, acc[e + 3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t *>(dst) = E::pack(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -1275,8 +1287,11 @@ static cudaError_t launch_typed(const AttnLaunch &a, const WorkspaceLayout &w, c
     mp.part_o = ap.part_o;
     mp.part_lse = ap.part_lse;
     mp.out = ap.out;
-    err = launch_pdl(lse_merge_kernel<D, G, E>, dim3(static_cast<unsigned>(a.num_seqs * a.num_kv_heads)),
-                     dim3(kCols * 32), 0, stream, mp);
+    const unsigned pairs = static_cast<unsigned>(a.num_seqs * a.num_kv_heads);
+    if (pairs <= 4u * static_cast<unsigned>(a.sm_count))
+      err = launch_pdl(lse_merge_kernel<D, G, E, 8>, dim3(pairs), dim3(8 * 32), 0, stream, mp);
+    else
+      err = launch_pdl(lse_merge_kernel<D, G, E, 4>, dim3(pairs), dim3(4 * 32), 0, stream, mp);
     if (err != cudaSuccess) return err;
     ++*launched;
   }
