@@ -181,18 +181,8 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_
       : "memory");
 }
 
-// 64 consecutive 32-bit columns of this thread's TMEM lane; the wait is in
+// 32 consecutive 32-bit columns of this thread's TMEM lane; the wait is in
 // the same statement, so no use of the registers can be scheduled before it.
-__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
-      : "memory");
-}
-
-// The same for 32 columns.
 __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
@@ -255,54 +245,6 @@ __device__ __forceinline__ float masked_max32(const uint32_t (&s)[32], int ck0, 
   return m;
 }
 
-// P for 32 keys (scores s[0..32), visible while ck0 + i < lim): p =
-// 2^(s * sl2 - ms), summed into *sum and packed as the TMEM columns of two
-// UMMA K steps. SPLIT (bf16 operands, 8 significant bits): P as a hi + lo
-// pair, 32 columns [hi pairs of keys 0-15, lo pairs of 0-15, hi 16-31, lo
-// 16-31]; otherwise (fp16, 11 bits: a weight's relative rounding error of
-// at most 2^-11 moves the output by at most 2^-11 max|V|, and far less when
-// the roundings are independent) one pair per two keys, 16 columns.
-// The exponent is one fused multiply-add, whose unrounded product differs
-// from the rounded one ms was taken from by at most half an ulp of ms: below
-// 2^-12 while |ms| <= 2^12. EXACT rows (larger |ms|) round the product first,
-// so the row maximum's exponent is exactly zero and none exceeds the growth
-// the caller allowed.
-template <typename E, bool EXACT, bool SPLIT>
-__device__ __forceinline__ void probs32(const uint32_t (&s)[32], int ck0, int lim, float sl2, float ms, float &sum,
-                                        uint32_t (&u)[32]) {
-  const bool full = ck0 + 32 <= lim;
-  float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float x0 = __uint_as_float(s[2 * i]), x1 = __uint_as_float(s[2 * i + 1]);
-    if (!full) {
-      x0 = ck0 + 2 * i < lim ? x0 : -INFINITY;
-      x1 = ck0 + 2 * i + 1 < lim ? x1 : -INFINITY;
-    }
-    float e0, e1;
-    if (EXACT) {
-      // scalar round-to-nearest intrinsics, which are never merged into a fused multiply-add
-      e0 = __fsub_rn(__fmul_rn(x0, sl2), ms);
-      e1 = __fsub_rn(__fmul_rn(x1, sl2), ms);
-    } else {
-      fma2(e0, e1, x0, x1, sl2, sl2, -ms, -ms);
-    }
-    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-    add2(acc0, acc1, acc0, acc1, p0, p1);
-    const uint32_t hi = E::pack(p0, p1);
-    if (SPLIT) {
-      float l0, l1;
-      sub2(l0, l1, p0, p1, E::lo(hi), E::hi(hi));
-      const int step = i >> 3, k = i & 7;
-      u[16 * step + k] = hi;
-      u[16 * step + 8 + k] = E::pack(l0, l1);
-    } else {
-      u[i] = hi;
-    }
-  }
-  sum += acc0 + acc1;
-}
-
 // Store 8 32-bit columns (raw bits) of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile(
@@ -312,9 +254,18 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
 }
 
 // P for the 16 keys of one UMMA K step (scores s[0..16), key k0 + i visible
-// while k0 + i < lim), summed into *sum and stored at TMEM column `col` of
-// this thread's lane: SPLIT as 8 hi pairs then 8 lo pairs (16 columns),
-// otherwise 8 pairs. Same arithmetic as probs32.
+// while k0 + i < lim): p = 2^(s * sl2 - ms), summed into *sum and stored at
+// TMEM column `col` of this thread's lane. SPLIT (bf16 P, 8 significant
+// bits): a hi + lo pair per key, 8 columns of hi pairs then 8 of lo pairs;
+// otherwise (fp16, 11 bits: a weight's relative rounding error of at most
+// 2^-11 moves the output by at most 2^-11 max|V|, and far less when the
+// roundings are independent) 8 columns, one pair of keys each. The exponent
+// is one fused multiply-add, whose unrounded product differs from the
+// rounded one ms was taken from by at most half an ulp of ms: below 2^-12
+// while |ms| <= 2^12. EXACT rows (larger |ms|) round the product first (scalar
+// round-to-nearest intrinsics, never merged into a fused multiply-add), so the
+// row maximum's exponent is exactly zero and none exceeds the growth the
+// caller allowed.
 template <typename E, bool EXACT, bool SPLIT>
 __device__ __forceinline__ void probs16_store(const uint32_t *s, int k0, int lim, float sl2, float ms, float &sum,
                                               uint32_t col) {
