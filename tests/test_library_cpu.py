@@ -57,7 +57,9 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert n > 256 * 8 * 16 * 8 * 128 * 4
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 64, 16) > 0
     # unsupported or inconsistent sizes give 0
-    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 112, 16) == 0  # head dims 64, 80, 96, 128
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 112, 16) == 0  # head dims 64, 80, 96, 128, 256
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 256, 16) > 0
+    assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 192, 16) == 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 96, 16) > 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 1, 80, 16) > 0
     assert lib.pa_attention_workspace_size(4, 4, 1, 33, 4, 3, 64, 16) == 0
@@ -154,3 +156,22 @@ def test_static_workspace_size_matches_the_header():
     m = re.search(r"#define\s+PA_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "PA_STATIC_WORKSPACE_BYTES is not a (N u << S) literal any more: update this test"
     assert B.PA_STATIC_WORKSPACE_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_partition_sizes_follow_the_batch(lib):
+    """The split-KV plan's partition size: 512 tokens once the (request, KV head) pairs
+    give every decode warp two or more (batch 256 x 8 KV heads on 1216 warps: 512, the
+    measured best); otherwise the longest request's keys spread over the warps, rounded
+    up to a multiple of 512 and kept within [512, 2048]."""
+    pt, mp = B.pa_attention_plan_info(256, 8192, 32, 8)
+    assert (pt, mp) == (512, 16)
+    pt, mp = B.pa_attention_plan_info(64, 2048, 32, 32)  # MHA batch 64: 2048 pairs
+    assert (pt, mp) == (512, 4)
+    # few pairs: 4 requests x 8 KV heads x 4096 keys over 1216 warps -> 108 -> 512
+    assert B.pa_attention_plan_info(4, 4096, 32, 8)[0] == 512
+    # 16 x 8 pairs of 16384 keys -> 1725 per warp -> 2048
+    assert B.pa_attention_plan_info(16, 16384, 32, 8) == (2048, 8)
+    # 10 x 8 pairs of 8192 keys -> 539 per warp -> 1024
+    assert B.pa_attention_plan_info(10, 8192, 32, 8) == (1024, 8)
+    # an empty batch still plans one partition of the minimum size
+    assert B.pa_attention_plan_info(0, 0, 32, 8)[0] == 512
