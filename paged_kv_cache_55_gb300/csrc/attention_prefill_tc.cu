@@ -34,9 +34,17 @@
 //     whose operand it overwrites: the products one thread issues execute in
 //     issue order, and the commit that signals S_A(r+1) complete also covers
 //     every product issued before it. The warp zeroes V rows past the last
-//     key before the first product reads them;
+//     key before the first product reads them (over bf16 caches the
+//     converter warps do);
+//   * two converter warps rewrite staged ranges in place: 8-bit codes widened
+//     exactly to fp16, and bf16 V rewritten as fp16 so that P can be one
+//     fp16 value per key (a range holding a magnitude of 65536 or more goes
+//     back to bf16 and takes a bf16 hi + lo pair for P);
 //   * sixteen softmax warps, two per TMEM lane quadrant and half: each thread
-//     owns one row (its TMEM lane) and 64 of the 128 keys of every range. The
+//     owns one row (its TMEM lane) and 64 of the 128 keys of every range,
+//     whose probabilities it computes in a loop of K steps that reads 16
+//     scores from TMEM each (a small hot loop: the twenty warps share the
+//     SM's instruction cache). The
 //     two warps of a row exchange their maxima through shared memory (an
 //     mbarrier pair), so both take the range's probabilities against the
 //     same running maximum; each keeps its own partial row sum, rescales its
@@ -51,7 +59,8 @@
 // the dynamic segment, whose start must be 1024-byte aligned for the swizzled
 // tiles (checked). On a timeout the warp records it, stops, and the kernel
 // waits (bounded) for its loads and products in flight before it releases
-// tensor memory.
+// tensor memory. Head dim 256 has its own one-half kernel at the end of the
+// file (S and O of two halves would not fit the 512 TMEM columns).
 #include <type_traits>
 
 #include "attention_internal.cuh"
