@@ -269,11 +269,18 @@ def host_threads() -> int:
 KERNEL_SOURCES = ["paged_kv_cache_55_gb300/csrc/attention_splitkv.cu", "paged_kv_cache_55_gb300/csrc/pa_common.cuh"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(root: str = ROOT) -> str:
+    """Hash of the timed kernel's code: its sources without `//` comments,
+    trailing blanks and empty lines, so that a comment edit keeps the committed
+    counters while any change to the code drops them. (The sources hold no
+    string literal with `//` in it; a CPU test checks that.)"""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(root, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode("utf-8") + b"\n")
     return h.hexdigest()[:16]
 
 

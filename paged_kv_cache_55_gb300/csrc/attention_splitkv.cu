@@ -372,15 +372,15 @@ struct Unit {
 
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of the partitions of split requests, after the attention
-// kernel (PDL: launched early, waits for it). One CTA of four warps per
-// (request, KV head), or of eight when there are few such pairs; warp w
-// merges columns w and w + 4 (a decode request's G columns are the first G,
-// one warp each); the request's partition count
-// and query rows are loaded together, then each lane reads its D/32 outputs
-// of the partitions eight at a time with independent loads, keeping a
-// running maximum so one pass suffices. Partitions are summed in order. (A
-// CTA of eight warps, one per column, holds 60 registers x 256 threads: four
-// CTAs per SM, 3.4 waves at batch 256 x 8 KV heads.)
+// kernel (PDL: launched early, waits for it). One CTA per (request, KV
+// head): four warps, warp w merging columns w and w + 4 (a decode request's
+// G columns are the first G, one warp each), or eight warps, one per
+// column, when the pairs fit one wave of such CTAs. The request's partition
+// count and query rows are loaded together, then each lane reads its D/32
+// outputs of the partitions eight at a time with independent loads, keeping
+// a running maximum so one pass suffices. Partitions are summed in order.
+// (Eight warps for every pair hold 60 registers x 256 threads: four CTAs
+// per SM, 3.4 waves at batch 256 x 8 KV heads.)
 // ---------------------------------------------------------------------------
 struct MergeParams {
   const int32_t *query_start_loc;

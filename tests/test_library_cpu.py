@@ -175,3 +175,31 @@ def test_partition_sizes_follow_the_batch(lib):
     assert B.pa_attention_plan_info(10, 8192, 32, 8) == (1024, 8)
     # an empty batch still plans one partition of the minimum size
     assert B.pa_attention_plan_info(0, 0, 32, 8)[0] == 512
+
+
+def test_kernel_hash_ignores_comments_only(tmp_path):
+    """bench.py keys the committed ncu counters to a hash of the timed kernel's code
+    with `//` comments removed: that is sound only while no string literal in those
+    sources contains `//`, and the hash must move with any change to the code (checked
+    on copies of the sources)."""
+    import shutil
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    for rel in bench.KERNEL_SOURCES:
+        text = open(os.path.join(bench.ROOT, rel), encoding="utf-8").read()
+        code = "\n".join(line.split("//", 1)[0] for line in text.splitlines())
+        assert "/*" not in code, rel
+        for lit in re.findall(r'"(?:[^"\\\n]|\\.)*"', code):
+            assert "//" not in lit, (rel, lit)
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copyfile(os.path.join(bench.ROOT, rel), dst)
+    h0 = bench.kernel_source_hash()
+    assert bench.kernel_source_hash(str(tmp_path)) == h0
+    copy = tmp_path / bench.KERNEL_SOURCES[0]
+    original = copy.read_text(encoding="utf-8")
+    copy.write_text(original.replace("\n", "  // a comment\n", 3) + "\n// another\n\n", encoding="utf-8")
+    assert bench.kernel_source_hash(str(tmp_path)) == h0
+    copy.write_text(original + "\nstatic int unused_marker_for_the_hash_test = 0;\n", encoding="utf-8")
+    assert bench.kernel_source_hash(str(tmp_path)) != h0
